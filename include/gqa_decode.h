@@ -1,0 +1,211 @@
+/*
+ * gqa_decode.h -- C ABI of the GB300 fused GQA decode-attention library (libgqa_decode.so).
+ *
+ * One decode step for one new token per sequence:
+ *   1. prologue: per-head QK RMSNorm, then RoPE at the token's position, on q and k;
+ *      k (post-RoPE) and v (raw) are appended to the bf16 KV cache at that position
+ *      ("Qwen3-14B Optimization", section 2.1 Shape 4 and "Then: buy it" / #796, where
+ *      QK-norm and RoPE are folded into the attention kernel; section 3.3 for the folded
+ *      norm reciprocal and the lo/hi RoPE halves; "ADR-0060: AHBM GQA Fused Attention
+ *      Kernel (Llama3-70B)", section 0.5.1 preconditions P2-P4: K cached post-RoPE,
+ *      V raw, the new row written before attention reads the cache).
+ *   2. split-KV attention: the G = H_q / H_kv query heads that share a KV head are
+ *      stacked into one tile (ADR-0060 section 5.2, M-fold), the KV cache is streamed in
+ *      64-token tiles with an online softmax (ADR-0060 section 3), and each split writes
+ *      an unnormalised (m, l, O) partial (ADR-0060 sections 0.5.4 and 4).
+ *   3. combine: the log-sum-exp merge of the partials, normalised once (ADR-0060
+ *      section 4, merge()).
+ *
+ * Conventions shared by every entry point
+ *   - bf16 tensors are passed as pointers to 16-bit storage (IEEE bfloat16 bits).
+ *   - Device pointers must be device-accessible on the plan's device; all device
+ *     tensors are dense, row-major, with the shapes stated, and 16-byte aligned.
+ *   - The caller owns every tensor.  The library writes only `out` (or the host
+ *     output buffer), the B new cache rows, and its own plan workspace.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and never synchronise, except the functions documented
+ *     as synchronous.  Two calls that share a plan must not run concurrently (they
+ *     share the plan's workspace); order them on one stream.
+ *   - Argument errors are reported before anything is launched.  Index errors that can
+ *     only be seen on the device (a position outside [0, seq_len), a seq_len outside
+ *     [1, max_seq_len], a page id outside the pool) do not fault: the kernels skip the
+ *     offending sequence, write zeros for its output, and set a bit in the plan's
+ *     device error word (gqa_plan_device_errors).
+ *
+ * Supported geometry: head_dim == 128, H_q % H_kv == 0, 1 <= G <= 16, batch <= 1024,
+ * paged cache with 64-token blocks or a contiguous per-sequence cache.
+ */
+#ifndef GQA_DECODE_H_
+#define GQA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_HEAD_DIM 128
+#define GQA_BLOCK_SIZE 64
+#define GQA_MAX_GROUP 16
+#define GQA_MAX_BATCH 1024
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,   /* a NULL pointer, a bad size, or an inconsistent argument */
+    GQA_ERR_UNSUPPORTED = 2,   /* a geometry outside the supported set above */
+    GQA_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed */
+    GQA_ERR_WORKSPACE = 4      /* the plan's workspace could not be allocated */
+} gqa_status_t;
+
+/* Bits of the device error word (gqa_plan_device_errors). */
+#define GQA_DEVERR_POSITION 0x1u  /* positions[b] outside [0, seq_lens[b]) */
+#define GQA_DEVERR_SEQLEN 0x2u    /* seq_lens[b] outside [1, max_seq_len] */
+#define GQA_DEVERR_PAGE 0x4u      /* a page-table entry outside [0, num_cache_blocks) */
+#define GQA_DEVERR_TIMEOUT 0x8u   /* a pipeline wait gave up (the kernel returned early) */
+
+/* Shapes and layout a plan is built for. */
+typedef struct gqa_plan_desc {
+    int batch;            /* B, 1..GQA_MAX_BATCH */
+    int num_q_heads;      /* H_q */
+    int num_kv_heads;     /* H_kv; H_q % H_kv == 0 and G = H_q / H_kv <= 16 */
+    int head_dim;         /* d; must be 128 */
+    int block_size;       /* 64: paged cache [num_cache_blocks, 64, H_kv, d] with a page table;
+                             0: contiguous cache [B, max_seq_len, H_kv, d], no page table */
+    int max_seq_len;      /* per-sequence capacity in tokens (>= 1); the page table has
+                             ceil(max_seq_len / 64) entries per sequence */
+    int num_cache_blocks; /* paged: number of 64-token blocks in each cache pool (>= 1);
+                             ignored (may be 0) when contiguous */
+    int num_workers;      /* CTAs of the split-KV kernel; 0 lets the planner choose */
+    int device;           /* CUDA device ordinal the plan and its calls run on */
+} gqa_plan_desc_t;
+
+typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp32 partials) */
+
+/*
+ * gqa_plan_create -- the split planner.  Validates the geometry, chooses the number of
+ * split-KV workers (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
+ * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
+ * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
+ * workspace once, so no call allocates.
+ *   desc          : geometry (copied).
+ *   seq_lens_host : optional host array [B] of expected lengths used only to size the
+ *                   worker count; NULL plans for B sequences of max_seq_len tokens.
+ *   plan          : receives the new plan.
+ * Errors: GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE.
+ * Synchronous (allocates device memory).
+ */
+gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_lens_host,
+                             gqa_plan_t **plan);
+
+/* Frees the plan and its workspace (synchronous). NULL is accepted. */
+gqa_status_t gqa_plan_destroy(gqa_plan_t *plan);
+
+/* Number of split-KV workers (CTAs) the plan launches; 0 for a NULL plan. */
+int gqa_plan_num_workers(const gqa_plan_t *plan);
+
+/* Bytes of device workspace the plan owns; 0 for a NULL plan. */
+size_t gqa_plan_workspace_bytes(const gqa_plan_t *plan);
+
+/*
+ * gqa_decode_attn -- the whole decode step: prologue, split-KV attention, combine.
+ *   q_new      [B, H_q, d]  bf16 device   new-token queries (pre-norm, pre-RoPE)
+ *   k_new      [B, H_kv, d] bf16 device   new-token keys (pre-norm, pre-RoPE)
+ *   v_new      [B, H_kv, d] bf16 device   new-token values
+ *   k_cache, v_cache        bf16 device   paged [num_cache_blocks, 64, H_kv, d] or
+ *                                         contiguous [B, max_seq_len, H_kv, d]; the row for
+ *                                         token t of sequence b is
+ *                                         page_table[b][t / 64] * 64 + t % 64 (paged) or
+ *                                         b * max_seq_len + t (contiguous).  Modified in
+ *                                         place at token positions[b] only.
+ *   page_table [B, ceil(max_seq_len/64)] int32 device, or NULL when contiguous
+ *   seq_lens   [B] int32 device   L_b = tokens to attend to, including the new one
+ *   positions  [B] int32 device   p_b = RoPE position and cache slot of the new token,
+ *                                 0 <= p_b < L_b (a decode step has p_b = L_b - 1)
+ *   q_norm_w, k_norm_w [d] bf16 device, or NULL for no QK-norm on q / on k
+ *   rope_theta RoPE base (> 0); frequencies theta^(-2i/d), half-split pairs (i, i + d/2)
+ *   eps        RMSNorm epsilon (>= 0)
+ *   out        [B, H_q, d] bf16 device   softmax(q k^T / sqrt(d)) v per query head,
+ *                                        query head h reading KV head h / G
+ *   stream     cudaStream_t as void*
+ * Errors: GQA_ERR_INVALID_ARG (NULL plan or tensor, page_table given for a contiguous
+ * plan or missing for a paged one, rope_theta <= 0, eps < 0 or not finite),
+ * GQA_ERR_CUDA (launch failure).
+ */
+gqa_status_t gqa_decode_attn(const gqa_plan_t *plan,
+                             const void *q_new, const void *k_new, const void *v_new,
+                             void *k_cache, void *v_cache, const int32_t *page_table,
+                             const int32_t *seq_lens, const int32_t *positions,
+                             const void *q_norm_w, const void *k_norm_w,
+                             float rope_theta, float eps, void *out, void *stream);
+
+/*
+ * gqa_decode_attn_host -- the same step with the per-step inputs and the output in host
+ * memory: q_new, k_new, v_new, seq_lens, positions are read from host buffers and `out`
+ * is written to a host buffer, each through one cudaMemcpyAsync on `stream` into or out
+ * of the plan's staging area.  The KV caches, the page table and the norm weights stay
+ * device-resident (model state).  Shapes as for gqa_decode_attn.  The host output is
+ * valid once `stream` has been synchronised; pinned host buffers make the copies
+ * asynchronous.  Errors as for gqa_decode_attn.
+ */
+gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
+                                  const void *q_new_host, const void *k_new_host,
+                                  const void *v_new_host,
+                                  void *k_cache, void *v_cache, const int32_t *page_table,
+                                  const int32_t *seq_lens_host, const int32_t *positions_host,
+                                  const void *q_norm_w, const void *k_norm_w,
+                                  float rope_theta, float eps, void *out_host, void *stream);
+
+/*
+ * The three steps of gqa_decode_attn as separate launches, for callers that schedule
+ * them themselves (and for step-level tests).  They communicate through the plan's
+ * workspace and must be issued in this order on one stream.
+ *   gqa_prologue: QK-norm + RoPE of q into the workspace, k/v rows into the cache.
+ *   gqa_attention_splitkv: reads the rotated q and the cache, writes fp32 partials.
+ *   gqa_combine: merges the partials into `out`.
+ * Arguments and errors as for gqa_decode_attn.
+ */
+gqa_status_t gqa_prologue(const gqa_plan_t *plan,
+                          const void *q_new, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, const int32_t *page_table,
+                          const int32_t *seq_lens, const int32_t *positions,
+                          const void *q_norm_w, const void *k_norm_w,
+                          float rope_theta, float eps, void *stream);
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_cache,
+                                   const void *v_cache, const int32_t *page_table,
+                                   const int32_t *seq_lens, void *stream);
+gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out,
+                         void *stream);
+
+/*
+ * gqa_plan_read_q_rot -- copies the rotated, bf16-rounded queries of the last prologue
+ * out of the workspace into host memory as [B, H_q, d] bf16.  Synchronous (waits for
+ * the device).  For tests and debugging.
+ */
+gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host);
+
+/*
+ * gqa_plan_device_errors -- reads the plan's device error word (GQA_DEVERR_* bits set by
+ * any call since the last clear) into *flags, and clears it when `clear` is non-zero.
+ * Synchronous: waits for all work on the plan's device.
+ */
+gqa_status_t gqa_plan_device_errors(const gqa_plan_t *plan, uint32_t *flags, int clear);
+
+/*
+ * gqa_partition_describe -- host-side view of how the split-KV kernel cuts a batch into
+ * worker ranges (for tests and tooling; no device work).  Given B lengths, H_kv and the
+ * worker count W, writes for every worker w its half-open range of global tile indices
+ * [worker_range[2w], worker_range[2w+1]), where tiles are numbered sequence-major, then
+ * KV head, then 64-token tile.  Returns the total number of tiles, or -1 on bad input.
+ */
+long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int num_kv_heads,
+                                 int max_seq_len, int num_workers, long long *worker_range);
+
+/* Static description of a status code. */
+const char *gqa_status_string(gqa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H_ */

@@ -1,0 +1,181 @@
+"""fp64 CPU oracle for the fused GQA decode-attention step -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  The library (``gqa_decode_attention_fa_gb300``) never does, and the two
+share no code: the oracle is plain C (``gqa_oracle.c``) compiled with gcc, wrapped here with
+ctypes and numpy for argument marshalling only.
+
+Every tensor crosses this boundary as raw bf16 bit patterns (``numpy.uint16``) or int32
+indices, exactly the bits the CUDA path receives.  Results are fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.c")
+_LIB = os.path.join(_HERE, "libgqa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``libgqa_oracle.so`` (gcc, OpenMP, no FP contraction so the
+    result is the same on x86-64 and aarch64)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm",
+        ])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
+        ("block_size", ctypes.c_int), ("max_seq", ctypes.c_int), ("num_rows", ctypes.c_longlong),
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_rmsnorm.argtypes = [P, P, ctypes.c_int, ctypes.c_double, P]
+            lib.oracle_rope.argtypes = [P, ctypes.c_int, ctypes.c_longlong, ctypes.c_double, P]
+            lib.oracle_prologue.argtypes = [ctypes.POINTER(Geom)] + [P] * 10 + [ctypes.c_double, ctypes.c_double, P]
+            lib.oracle_prologue.restype = ctypes.c_int
+            lib.oracle_attention.argtypes = [ctypes.POINTER(Geom), P, P, P, P, P, P, ctypes.c_int, P]
+            lib.oracle_attention.restype = ctypes.c_int
+            lib.oracle_attention_streaming.argtypes = [
+                ctypes.POINTER(Geom), P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, ctypes.c_int, P]
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def geom(B, Hq, Hkv, d, block_size, max_seq, num_rows) -> Geom:
+    return Geom(int(B), int(Hq), int(Hkv), int(d), int(block_size), int(max_seq), int(num_rows))
+
+
+# ----------------------------------------------------------------------------- scalars
+
+def bf16_to_f64(bits) -> np.ndarray:
+    bits = np.asarray(bits, dtype=np.uint16)
+    lib = _load()
+    flat = bits.reshape(-1)
+    return np.array([lib.oracle_bf16_to_double(int(b)) for b in flat], dtype=np.float64).reshape(bits.shape)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round fp64 values to bf16 bit patterns (nearest, ties to even), one at a time."""
+    x = np.asarray(x, dtype=np.float64)
+    lib = _load()
+    flat = x.reshape(-1)
+    return np.array([lib.oracle_round_bf16(float(v)) for v in flat], dtype=np.uint16).reshape(x.shape)
+
+
+def rmsnorm(x, w, eps: float) -> np.ndarray:
+    x = _c(x, np.float64)
+    w = _c(w, np.float64)
+    y = np.empty_like(x)
+    _load().oracle_rmsnorm(_ptr(x), _ptr(w), x.shape[0], float(eps), _ptr(y))
+    return y
+
+
+def rope(y, pos: int, theta: float) -> np.ndarray:
+    y = _c(y, np.float64)
+    z = np.empty_like(y)
+    _load().oracle_rope(_ptr(y), y.shape[0], int(pos), float(theta), _ptr(z))
+    return z
+
+
+# ----------------------------------------------------------------------------- step
+
+def prologue(g: Geom, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+             q_norm_w, k_norm_w, rope_theta: float, eps: float):
+    """Returns (q_rot bits [B,Hq,d], k_cache', v_cache', status).  The input caches are not
+    modified; the returned ones are copies with the new rows written."""
+    q_new, k_new, v_new = (_c(a, np.uint16) for a in (q_new, k_new, v_new))
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    pt = _c(page_table, np.int32)
+    sl, pos = _c(seq_lens, np.int32), _c(positions, np.int32)
+    qw, kw = _c(q_norm_w, np.uint16), _c(k_norm_w, np.uint16)
+    q_rot = np.zeros((g.B, g.Hq, g.d), dtype=np.uint16)
+    st = _load().oracle_prologue(ctypes.byref(g), _ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(kc), _ptr(vc),
+                                 _ptr(pt), _ptr(sl), _ptr(pos), _ptr(qw), _ptr(kw),
+                                 float(rope_theta), float(eps), _ptr(q_rot))
+    return q_rot, kc, vc, st
+
+
+def attention(g: Geom, q_rot, k_cache, v_cache, page_table, seq_lens, pairs=None, threads: int | None = None):
+    """Brute-force attention in fp64.  Returns (out, threads_used); out is [B,Hq,d], or
+    [len(pairs), d] when a list of (b, h) pairs is given."""
+    lib = _load()
+    if threads:
+        lib.oracle_set_threads(int(threads))
+    q_rot, kc, vc = (_c(a, np.uint16) for a in (q_rot, k_cache, v_cache))
+    pt, sl = _c(page_table, np.int32), _c(seq_lens, np.int32)
+    if pairs is not None:
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((pr.shape[0], g.d), dtype=np.float64)
+        used = lib.oracle_attention(ctypes.byref(g), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt), _ptr(sl),
+                                    _ptr(pr), pr.shape[0], _ptr(out))
+    else:
+        out = np.zeros((g.B, g.Hq, g.d), dtype=np.float64)
+        used = lib.oracle_attention(ctypes.byref(g), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt), _ptr(sl),
+                                    None, 0, _ptr(out))
+    return out, used
+
+
+def attention_streaming(g: Geom, q_rot, k_cache, v_cache, page_table, L: int, b: int, h: int,
+                        tile: int, split_bounds) -> np.ndarray:
+    q_rot, kc, vc = (_c(a, np.uint16) for a in (q_rot, k_cache, v_cache))
+    pt = _c(page_table, np.int32)
+    sb = np.ascontiguousarray(np.asarray(split_bounds, dtype=np.int32))
+    out = np.zeros(g.d, dtype=np.float64)
+    _load().oracle_attention_streaming(ctypes.byref(g), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt),
+                                       int(L), int(b), int(h), int(tile), _ptr(sb), len(sb) - 1, _ptr(out))
+    return out
+
+
+def decode_step(g: Geom, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+                q_norm_w, k_norm_w, rope_theta: float, eps: float, pairs=None, threads: int | None = None):
+    """The whole step: prologue (cache append) then attention over the updated cache.
+    Returns dict(out, q_rot, k_cache, v_cache, status, threads)."""
+    q_rot, kc, vc, st = prologue(g, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens,
+                                 positions, q_norm_w, k_norm_w, rope_theta, eps)
+    out, used = attention(g, q_rot, kc, vc, page_table, seq_lens, pairs=pairs, threads=threads)
+    return dict(out=out, q_rot=q_rot, k_cache=kc, v_cache=vc, status=st, threads=used)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))

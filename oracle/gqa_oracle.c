@@ -1,0 +1,321 @@
+/*
+ * Reference oracle for the fused GQA decode-attention step -- TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is a plain, slow, deliberately unoptimised CPU statement of what one decode
+ * step computes.  Only the test suite, the smoke check and the benchmark's CPU-baseline
+ * leg may load it; the library under test never calls it and shares no code with it.
+ *
+ * Arithmetic: IEEE binary64 throughout, over inputs that are bf16 bit patterns widened
+ * exactly to double.  The only roundings to bf16 are the ones the operation defines
+ * (the rotated q and k rows, which are bf16 tensors like every activation on the path).
+ *
+ * What is computed, and where it is stated:
+ *   - QK RMSNorm then RoPE on the new token, folded into one step
+ *     ("Qwen3-14B Optimization", section 2.1 Shape 4 and section 3.3 on folding the
+ *      QK-norm reciprocal into RoPE; the lo/hi RoPE halves there fix the half-split
+ *      pairing (i, i + d/2)).
+ *   - k stored post-RoPE, v stored raw, at the new token's slot before attention reads
+ *     the cache ("ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)", section 0.5.1
+ *     preconditions P2-P4; "Qwen3-14B Optimization", section 2.1 "Then: buy it": the
+ *     paged block-slot-head-dim cache layout).
+ *   - Attention: softmax(q K^T / sqrt(d)) V for every query head h against KV head
+ *     floor(h / G) (ADR-0060, section 0 reference dimensions and section 3).  The
+ *     brute-force form below is the plain definition; the streaming form follows the
+ *     per-tile recurrence of ADR-0060 section 3 and the log-sum-exp merge of section 4,
+ *     so that the two can be checked against each other.
+ *
+ * Parity pins (the tests that tie this file to the pages and to mathematics, not to
+ * itself) live in tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ bf16 <-> double */
+
+double oracle_bf16_to_double(uint16_t bits) {
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 value, ties to even (IEEE 754 roundTiesToEven),
+ * in one step from binary64 (no intermediate binary32 rounding).  bf16 carries 8
+ * significant bits, so the spacing of representable values at magnitude
+ * [2^(e-1), 2^e) is 2^(e-8); below the normal range the spacing stays at 2^-133. */
+uint16_t oracle_round_bf16(double z) {
+    if (isnan(z)) return (uint16_t)0x7fc0;
+    uint16_t sign = signbit(z) ? (uint16_t)0x8000 : (uint16_t)0;
+    double a = fabs(z);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80);
+    int e;
+    (void)frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    int qexp = e - 8;
+    if (qexp < -133) qexp = -133;
+    double n = rint(ldexp(a, -qexp));   /* default rounding mode: nearest, ties to even */
+    double v = ldexp(n, qexp);
+    if (v > 0x1.fep127) return (uint16_t)(sign | 0x7f80);
+    float f = (float)v;                 /* exact: v has at most 8 significant bits */
+    uint32_t w;
+    memcpy(&w, &f, sizeof w);
+    return (uint16_t)(sign | (uint16_t)(w >> 16));
+}
+
+/* ------------------------------------------------------------------ QK-norm, RoPE */
+
+/* RMSNorm of one head vector: y_i = x_i * r * w_i with r = 1 / sqrt(mean(x^2) + eps).
+ * w == NULL means no norm (y = x). */
+void oracle_rmsnorm(const double *x, const double *w, int d, double eps, double *y) {
+    if (!w) {
+        for (int i = 0; i < d; ++i) y[i] = x[i];
+        return;
+    }
+    double ss = 0.0;
+    for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+    double r = 1.0 / sqrt(ss / (double)d + eps);
+    for (int i = 0; i < d; ++i) y[i] = x[i] * r * w[i];
+}
+
+/* Rotary embedding at integer position pos, half-split pairing (i, i + d/2):
+ *   phi_i = pos * theta^(-2i/d)
+ *   z_i       = y_i cos phi_i - y_{i+d/2} sin phi_i
+ *   z_{i+d/2} = y_{i+d/2} cos phi_i + y_i sin phi_i                                     */
+void oracle_rope(const double *y, int d, long long pos, double theta, double *z) {
+    int half = d / 2;
+    for (int i = 0; i < half; ++i) {
+        double inv_freq = pow(theta, -2.0 * (double)i / (double)d);
+        double phi = (double)pos * inv_freq;
+        double c = cos(phi), s = sin(phi);
+        z[i] = y[i] * c - y[i + half] * s;
+        z[i + half] = y[i + half] * c + y[i] * s;
+    }
+}
+
+/* ------------------------------------------------------------------ cache addressing */
+
+/* Cache row that holds token t of sequence b.
+ *   paged (page_table != NULL): [num_blocks, block_size, H_kv, d];
+ *       row = page_table[b][t / block_size] * block_size + t % block_size
+ *   contiguous (page_table == NULL): [B, max_seq, H_kv, d]; row = b * max_seq + t        */
+static long long cache_row(const int32_t *page_table, int max_blocks, int block_size,
+                           int max_seq, int b, int t) {
+    if (page_table) {
+        long long page = page_table[(long long)b * max_blocks + t / block_size];
+        return page * block_size + t % block_size;
+    }
+    return (long long)b * max_seq + t;
+}
+
+typedef struct {
+    int B, Hq, Hkv, d;
+    int block_size;      /* tokens per page when paged */
+    int max_seq;         /* per-sequence capacity in tokens */
+    long long num_rows;  /* rows in the cache pool (num_blocks * block_size, or B * max_seq) */
+} oracle_geom_t;
+
+/* ------------------------------------------------------------------ prologue */
+
+/* One decode step's prologue.  For every sequence b with new-token position p = positions[b]:
+ *   q_rot[b, h]          = bf16(RoPE_p(RMSNorm(q_new[b, h], q_norm_w)))
+ *   k_cache[slot(b, p)]  = bf16(RoPE_p(RMSNorm(k_new[b, kv], k_norm_w)))
+ *   v_cache[slot(b, p)]  = v_new[b, kv]        (bit copy)
+ * Returns 0, or a positive code when an index is out of range (nothing is written for
+ * that sequence): 1 = position outside [0, seq_len), 2 = seq_len outside [1, max_seq],
+ * 3 = page id outside the pool.                                                           */
+int oracle_prologue(const oracle_geom_t *g,
+                    const uint16_t *q_new, const uint16_t *k_new, const uint16_t *v_new,
+                    uint16_t *k_cache, uint16_t *v_cache,
+                    const int32_t *page_table, const int32_t *seq_lens, const int32_t *positions,
+                    const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                    double rope_theta, double eps, uint16_t *q_rot) {
+    const int d = g->d;
+    int status = 0;
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    double *x = malloc(sizeof(double) * d), *y = malloc(sizeof(double) * d);
+    double *z = malloc(sizeof(double) * d);
+    double *qw = malloc(sizeof(double) * d), *kw = malloc(sizeof(double) * d);
+    for (int i = 0; i < d; ++i) {
+        qw[i] = q_norm_w ? oracle_bf16_to_double(q_norm_w[i]) : 1.0;
+        kw[i] = k_norm_w ? oracle_bf16_to_double(k_norm_w[i]) : 1.0;
+    }
+    for (int b = 0; b < g->B; ++b) {
+        int L = seq_lens[b], p = positions[b];
+        if (L < 1 || L > g->max_seq) { status = 2; continue; }
+        if (p < 0 || p >= L) { status = 1; continue; }
+        long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, p);
+        if (row < 0 || row >= g->num_rows) { status = 3; continue; }
+        for (int h = 0; h < g->Hq; ++h) {
+            const uint16_t *src = q_new + ((long long)b * g->Hq + h) * d;
+            for (int i = 0; i < d; ++i) x[i] = oracle_bf16_to_double(src[i]);
+            oracle_rmsnorm(x, q_norm_w ? qw : NULL, d, eps, y);
+            oracle_rope(y, d, p, rope_theta, z);
+            uint16_t *dst = q_rot + ((long long)b * g->Hq + h) * d;
+            for (int i = 0; i < d; ++i) dst[i] = oracle_round_bf16(z[i]);
+        }
+        for (int kv = 0; kv < g->Hkv; ++kv) {
+            const uint16_t *src = k_new + ((long long)b * g->Hkv + kv) * d;
+            for (int i = 0; i < d; ++i) x[i] = oracle_bf16_to_double(src[i]);
+            oracle_rmsnorm(x, k_norm_w ? kw : NULL, d, eps, y);
+            oracle_rope(y, d, p, rope_theta, z);
+            uint16_t *kdst = k_cache + (row * g->Hkv + kv) * d;
+            uint16_t *vdst = v_cache + (row * g->Hkv + kv) * d;
+            const uint16_t *vsrc = v_new + ((long long)b * g->Hkv + kv) * d;
+            for (int i = 0; i < d; ++i) {
+                kdst[i] = oracle_round_bf16(z[i]);
+                vdst[i] = vsrc[i];
+            }
+        }
+    }
+    free(x); free(y); free(z); free(qw); free(kw);
+    return status;
+}
+
+/* ------------------------------------------------------------------ attention */
+
+/* Brute-force attention for one (b, h): the full score vector, max-subtracted softmax,
+ * weighted sum of V.  out has d doubles.                                                 */
+static void attend_one(const oracle_geom_t *g, const uint16_t *q_rot,
+                       const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *page_table, int max_blocks, int L, int b, int h,
+                       double *scores, double *out) {
+    const int d = g->d, G = g->Hq / g->Hkv, kv = h / G;
+    const double scale = 1.0 / sqrt((double)d);
+    const uint16_t *q = q_rot + ((long long)b * g->Hq + h) * d;
+    double m = -INFINITY;
+    for (int t = 0; t < L; ++t) {
+        long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+        const uint16_t *k = k_cache + (row * g->Hkv + kv) * d;
+        double s = 0.0;
+        for (int i = 0; i < d; ++i) s += oracle_bf16_to_double(q[i]) * oracle_bf16_to_double(k[i]);
+        scores[t] = s * scale;
+        if (scores[t] > m) m = scores[t];
+    }
+    double l = 0.0;
+    for (int i = 0; i < d; ++i) out[i] = 0.0;
+    for (int t = 0; t < L; ++t) {
+        double w = exp(scores[t] - m);
+        l += w;
+        long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+        const uint16_t *v = v_cache + (row * g->Hkv + kv) * d;
+        for (int i = 0; i < d; ++i) out[i] += w * oracle_bf16_to_double(v[i]);
+    }
+    for (int i = 0; i < d; ++i) out[i] /= l;
+}
+
+/* out[b, h, :] for every (b, h) -- or, when pairs != NULL, for the n_pairs listed
+ * (b, h) pairs only, written to out[k, :] in list order.  Returns the thread count used. */
+int oracle_attention(const oracle_geom_t *g, const uint16_t *q_rot,
+                     const uint16_t *k_cache, const uint16_t *v_cache,
+                     const int32_t *page_table, const int32_t *seq_lens,
+                     const int32_t *pairs, int n_pairs, double *out) {
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    long long n = pairs ? n_pairs : (long long)g->B * g->Hq;
+    int threads = 1;
+#pragma omp parallel
+    {
+#ifdef _OPENMP
+#pragma omp single
+        threads = omp_get_num_threads();
+#endif
+        double *scores = malloc(sizeof(double) * (size_t)(g->max_seq > 0 ? g->max_seq : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long long k = 0; k < n; ++k) {
+            int b = pairs ? pairs[2 * k] : (int)(k / g->Hq);
+            int h = pairs ? pairs[2 * k + 1] : (int)(k % g->Hq);
+            attend_one(g, q_rot, k_cache, v_cache, page_table, max_blocks, seq_lens[b], b, h,
+                       scores, out + k * g->d);
+        }
+        free(scores);
+    }
+    return threads;
+}
+
+/* Streaming form for one (b, h), used only to check the brute-force form: the token
+ * range [0, L) is cut at split_bounds (n_splits + 1 ascending token indices, first 0,
+ * last L; empty splits allowed).  Each split runs the per-tile online-softmax recurrence
+ * over tiles of `tile` tokens, seeded m = -inf, l = 0, O = 0:
+ *     m' = max(m, max_t s_t);  P_t = exp(s_t - m');  c = exp(m - m')
+ *     l  = l * c + sum_t P_t;  O = O * c + sum_t P_t V_t;  m = m'
+ * and the splits' unnormalised partials are folded left to right with the log-sum-exp
+ * merge  m = max(m_a, m_b); l = l_a e^(m_a - m) + l_b e^(m_b - m);
+ *        O = O_a e^(m_a - m) + O_b e^(m_b - m),  then normalised once: out = O / l.
+ * A split with no tokens keeps m = -inf, l = 0 and is skipped by the merge.            */
+void oracle_attention_streaming(const oracle_geom_t *g, const uint16_t *q_rot,
+                                const uint16_t *k_cache, const uint16_t *v_cache,
+                                const int32_t *page_table, int L, int b, int h, int tile,
+                                const int32_t *split_bounds, int n_splits, double *out) {
+    const int d = g->d, G = g->Hq / g->Hkv, kv = h / G;
+    const double scale = 1.0 / sqrt((double)d);
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    const uint16_t *q = q_rot + ((long long)b * g->Hq + h) * d;
+    double *O = malloc(sizeof(double) * d), *Oacc = malloc(sizeof(double) * d);
+    double *s = malloc(sizeof(double) * (size_t)tile);
+    double m_acc = -INFINITY, l_acc = 0.0;
+    for (int i = 0; i < d; ++i) Oacc[i] = 0.0;
+    for (int sp = 0; sp < n_splits; ++sp) {
+        int lo = split_bounds[sp], hi = split_bounds[sp + 1];
+        double m = -INFINITY, l = 0.0;
+        for (int i = 0; i < d; ++i) O[i] = 0.0;
+        for (int t0 = lo; t0 < hi; t0 += tile) {
+            int n = hi - t0 < tile ? hi - t0 : tile;
+            double mt = -INFINITY;
+            for (int j = 0; j < n; ++j) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t0 + j);
+                const uint16_t *k = k_cache + (row * g->Hkv + kv) * d;
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += oracle_bf16_to_double(q[i]) * oracle_bf16_to_double(k[i]);
+                s[j] = acc * scale;
+                if (s[j] > mt) mt = s[j];
+            }
+            double m_new = m > mt ? m : mt;
+            double c = exp(m - m_new);          /* m = -inf on the first tile: c = 0 */
+            l *= c;
+            for (int i = 0; i < d; ++i) O[i] *= c;
+            for (int j = 0; j < n; ++j) {
+                double P = exp(s[j] - m_new);
+                l += P;
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t0 + j);
+                const uint16_t *v = v_cache + (row * g->Hkv + kv) * d;
+                for (int i = 0; i < d; ++i) O[i] += P * oracle_bf16_to_double(v[i]);
+            }
+            m = m_new;
+        }
+        if (l == 0.0) continue;                 /* empty split */
+        if (l_acc == 0.0) {
+            m_acc = m; l_acc = l;
+            for (int i = 0; i < d; ++i) Oacc[i] = O[i];
+            continue;
+        }
+        double mm = m_acc > m ? m_acc : m;
+        double sa = exp(m_acc - mm), sb = exp(m - mm);
+        l_acc = l_acc * sa + l * sb;
+        for (int i = 0; i < d; ++i) Oacc[i] = Oacc[i] * sa + O[i] * sb;
+        m_acc = mm;
+    }
+    for (int i = 0; i < d; ++i) out[i] = Oacc[i] / l_acc;
+    free(O); free(Oacc); free(s);
+}
+
+/* ------------------------------------------------------------------ threads */
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
