@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GQA decode-attention step on GB300.
+
+One "step" is one pass of the whole hot path -- prologue (QK-norm + RoPE + cache append),
+split-KV attention, log-sum-exp combine -- over one decode batch of synthetic, seeded
+inputs already resident in HBM (for the 40-layer sweep: the 40 layers' calls).
+
+Prints ONE JSON line.  `value` is microseconds per step (lower is better); `roofline`
+reports the split-KV attention kernel's KV-read bandwidth (algorithmic bytes
+sum_b L_b * H_kv * d * 2 * 2 per launch over its CUDA-event duration) against the measured
+HBM copy peak; `e2e` is the same step through the host-buffer entry point with the
+per-step inputs copied in and the output copied out inside the timed region;
+`cpu_baseline` is the fp64 oracle timed on the host cores on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the step
+has no cross-GPU exchange): weak scaling, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "qwen3-14b-4k"
+METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_splitkv_traffic.json")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if k in d:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("attention.cu", "gqa_common.cuh"):
+        with open(os.path.join(ROOT, "gqa_decode_attention_fa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
+    the current kernel source and scales to this workload; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    per_kv_byte = d.get("dram_bytes_per_kv_byte")
+    return per_kv_byte
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.05)
+        return self
+
+    def __exit__(self, *a):
+        self.result = self._collect()
+
+    def _collect(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def build_layers(name: str, device: str, l2_bytes: int):
+    """Per-step list of workloads: the 40 layers for the sweep, else one workload.  Small
+    caches are replicated into enough copies (> 3x L2) that every step reads from HBM; the
+    copies rotate across steps (as a model's layers do)."""
+    import torch
+
+    from gqa_decode_attention_fa_gb300 import workloads as wl
+
+    if name == "qwen3-14b-40layer":
+        return [[wl.named(name, device=device, layer=l) for l in range(wl.LAYERS_40)]], "inputs > L2 (1 GiB KV per layer)"
+    w = wl.named(name, device=device)
+    kvb = w.kv_bytes()
+    if kvb >= 2 * l2_bytes:
+        return [[w]], f"inputs > L2 ({kvb / 2**20:.0f} MiB KV per step)"
+    copies = int(math.ceil(3 * l2_bytes / kvb))
+    sets = [[w]]
+    for _ in range(copies - 1):
+        c = wl.Workload(**{**w.__dict__})
+        c.k_cache = w.k_cache.clone()
+        c.v_cache = w.v_cache.clone()
+        sets.append([c])
+    torch.cuda.synchronize()
+    return sets, f"rotating {copies} cache copies ({copies * kvb / 2**20:.0f} MiB > 3x L2)"
+
+
+def algorithmic_kv_bytes(layers) -> int:
+    return sum(w.kv_bytes() for w in layers)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from gqa_decode_attention_fa_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    free, _ = torch.cuda.mem_get_info(local)
+    need = 48 * 2**30 if args.workload == "qwen3-14b-40layer" else 4 * 2**30
+    if free < need:
+        raise SystemExit(f"bench: {free / 2**30:.1f} GiB free on {dev}, workload needs ~{need / 2**30:.0f} GiB")
+    sets, l2_note = build_layers(args.workload, dev, l2)
+    first = sets[0][0]
+    plan = binding.Plan(first.B, first.Hq, first.Hkv, first.max_seq, block_size=first.block_size,
+                        num_cache_blocks=max(w.num_blocks for s in sets for w in s), device=local,
+                        seq_lens_host=first.seq_lens.cpu().numpy())
+    outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev) for w in sets[0]]
+    stream = torch.cuda.current_stream()
+    kv_per_step = algorithmic_kv_bytes(sets[0])
+    launches_per_step = 3 * len(sets[0])
+
+    def step(k, ev_pairs=None):
+        for li, w in enumerate(sets[k % len(sets)]):
+            plan.prologue(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                          w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, stream)
+            if ev_pairs is not None:
+                ev_pairs[li][0].record(stream)
+            plan.attention_splitkv(w.k_cache, w.v_cache, w.page_table, w.seq_lens, stream)
+            if ev_pairs is not None:
+                ev_pairs[li][1].record(stream)
+            plan.combine(w.seq_lens, outs[li], stream)
+
+    barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
+    K, W = args.steps, args.warmup
+    with ClockSampler(local) as clk:
+        # warm-up: at least W steps and at least ~0.3 s of GPU work so the clock record
+        # covers the loaded state
+        t0 = time.perf_counter()
+        done = 0
+        while done < W or time.perf_counter() - t0 < 0.3:
+            step(done)
+            done += 1
+            if done % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        attn_events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                        for _ in sets[0]] for _ in range(K)]
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for k in range(K):
+            step(k, attn_events[k])
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.result
+    region_ms = e_start.elapsed_time(e_end)
+    attn_ms = [a.elapsed_time(b) for per in attn_events for a, b in per]
+    if plan.device_errors() != 0:
+        raise SystemExit("bench: device error flags set during the timed region")
+
+    # e2e: host buffers through gqa_decode_attn_host, inputs in / output out every step
+    import torch as _t
+    host = []
+    for w in sets[0]:
+        host.append({k: getattr(w, k).cpu().pin_memory() for k in ("q_new", "k_new", "v_new", "seq_lens", "positions")})
+    out_h = [_t.empty((w.B, w.Hq, w.d), dtype=_t.bfloat16).pin_memory() for w in sets[0]]
+    h2d = sum(sum(t.numel() * t.element_size() for t in h.values()) for h in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_h)
+
+    def e2e_step(k):
+        for li, w in enumerate(sets[k % len(sets)]):
+            h = host[li]
+            plan.decode_attn_host(h["q_new"], h["k_new"], h["v_new"], w.k_cache, w.v_cache, w.page_table,
+                                  h["seq_lens"], h["positions"], w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps,
+                                  out_h[li], stream)
+        stream.synchronize()   # the step's result is on the host before the next step
+
+    for k in range(max(3, W)):
+        e2e_step(k)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(K):
+        e2e_step(k)
+    e2e_s = time.perf_counter() - t0
+    barrier()
+
+    us_step = region_ms * 1e3 / K
+    e2e_us = e2e_s * 1e6 / K
+    if world > 1:
+        t = torch.tensor([us_step, e2e_us], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        us_step, e2e_us = float(t[0]), float(t[1])
+
+    peak, peak_src = hbm_peak()
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    kv_per_launch = kv_per_step / len(sets[0])
+    achieved = kv_per_launch / (attn_avg_ms * 1e-3) / 1e9
+    per_kv = recorded_traffic(args.workload)
+    result = {
+        "metric": METRIC,
+        "value": round(us_step, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(us_step / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the named workload)",
+        "config": {"workload": args.workload, "batch": first.B, "q_heads": first.Hq, "kv_heads": first.Hkv,
+                   "head_dim": first.d, "layers": len(sets[0]),
+                   "seq_lens": "ragged U[512,8192]" if first.B > 1 and args.workload == "qwen3-14b-ragged"
+                   else int(first.seq_lens[0].item()),
+                   "cache": "paged-64" if first.paged else "contiguous", "l2": l2_note,
+                   "workers": plan.num_workers, "parallelism": f"replicas x{world}"},
+        "kv_bytes_per_step": kv_per_step,
+        "kv_gbs": round(kv_per_step / (us_step * 1e-6) / 1e9, 1),
+        "roofline": {"bound": "hbm", "kernel": "attn_splitkv_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of_8TBs": round(achieved / 8000.0, 4), "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": int(kv_per_launch),
+                     "traffic": None if per_kv is None else int(per_kv * kv_per_launch)},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    return result, sets
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0):
+    """The fp64 oracle, as it stands, on the host cores: whole decode steps of the workload
+    (for the 40-layer sweep: whole layers, scaled by 40) until ~budget_s of CPU time."""
+    import oracle
+    from gqa_decode_attention_fa_gb300 import workloads as wl
+    from gqa_decode_attention_fa_gb300.workloads import bits, ints
+
+    w = wl.named(name, device="cpu")
+    args = [bits(w.q_new), bits(w.k_new), bits(w.v_new), bits(w.k_cache), bits(w.v_cache), ints(w.page_table),
+            ints(w.seq_lens), ints(w.positions), bits(w.q_norm_w), bits(w.k_norm_w), w.rope_theta, w.eps]
+    g = oracle.geom(w.B, w.Hq, w.Hkv, w.d, w.block_size, w.max_seq, w.num_rows)
+    threads = oracle.max_threads()
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        r = oracle.decode_step(g, *args)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s or len(times) >= 200:
+            break
+    per_unit = statistics.median(times)
+    layers = wl.LAYERS_40 if name == "qwen3-14b-40layer" else 1
+    unit = "layer" if layers > 1 else "step"
+    return {"value": round(per_unit * layers * 1e6, 1), "unit": "us/step", "cores": int(r["threads"]),
+            "kind": "oracle",
+            "sample": f"{len(times)} full {unit}(s) of {name} in fp64 (median), x{layers} per step"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: whole steps of the same workload on the host."""
+    if rank != 0:
+        return None
+    import oracle
+    from gqa_decode_attention_fa_gb300 import workloads as wl
+    from gqa_decode_attention_fa_gb300.workloads import bits, ints
+
+    layers = wl.LAYERS_40 if args.workload == "qwen3-14b-40layer" else 1
+    w = wl.named(args.workload, device="cpu")
+    g = oracle.geom(w.B, w.Hq, w.Hkv, w.d, w.block_size, w.max_seq, w.num_rows)
+    a = [bits(w.q_new), bits(w.k_new), bits(w.v_new), bits(w.k_cache), bits(w.v_cache), ints(w.page_table),
+         ints(w.seq_lens), ints(w.positions), bits(w.q_norm_w), bits(w.k_norm_w), w.rope_theta, w.eps]
+    # bounded sample: one layer stands for each of the 40 identical-shape layers
+    K, W = args.steps, args.warmup
+    budget = 150.0
+    r = None
+    for _ in range(W):
+        r = oracle.decode_step(g, *a)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(K):
+        r = oracle.decode_step(g, *a)
+        done += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    per = (time.perf_counter() - t0) / done
+    us = per * layers * 1e6
+    threads = int(r["threads"]) if r else oracle.max_threads()
+    sample = (f"{done} timed oracle step(s) of {args.workload}" if layers == 1 else
+              f"{done} timed oracle layer(s) of {args.workload}, x{layers} layers per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer",
+                    help="other workloads to time (GPU only) into the line's by_config; '' for none")
+    args = ap.parse_args()
+    rank, world, local = dist_env()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        r = run_reference(args, rank, world)
+        if r is not None:
+            print(json.dumps(r), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    from gqa_decode_attention_fa_gb300 import binding
+    binding.load()
+    result, sets = run_ours(args, rank, world, local)
+    del sets
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.workload)
+    by = {}
+    for name in [n for n in args.by_config.split(",") if n and n != args.workload]:
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50)})
+        r, s = run_ours(sub, rank, world, local)
+        del s
+        torch.cuda.empty_cache()
+        by[name] = {"us_per_step": r["value"], "kv_gbs": r["kv_gbs"], "attn_gbs": r["roofline"]["achieved"],
+                    "frac": r["roofline"]["frac"], "frac_of_8TBs": r["roofline"]["frac_of_8TBs"],
+                    "attn_us": r["roofline"]["avg_launch_us"], "e2e_us": r["e2e"]["value"],
+                    "steps": r["steps"], "l2": r["config"]["l2"], "clocks_sm_mhz": r["clocks"]["sm_mhz"]}
+    if by:
+        result["by_config"] = by
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h).
+
+Argument marshalling only: every step of the decode path runs in the library's CUDA
+kernels.  Device tensors are torch tensors (device memory and streams come from torch);
+host buffers are numpy arrays or CPU torch tensors.  ``load()`` raises if the library
+cannot be loaded -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE = range(5)
+DEVERR_POSITION, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+HEADER = os.path.join(_build.ROOT, "include", "gqa_decode.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "block_size", "max_seq_len",
+        "num_cache_blocks", "num_workers", "device")]
+
+
+def header_functions() -> list:
+    """Names of the functions include/gqa_decode.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(build: bool = True):
+    """Load the library (building it first when stale); raises on failure."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libgqa_decode.so is missing ({path}); build it with "
+                               "gqa_decode_attention_fa_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.gqa_plan_create.argtypes = [ctypes.POINTER(PlanDesc), P, ctypes.POINTER(P)]
+        lib.gqa_plan_destroy.argtypes = [P]
+        lib.gqa_plan_num_workers.argtypes = [P]
+        lib.gqa_plan_num_workers.restype = I
+        lib.gqa_plan_workspace_bytes.argtypes = [P]
+        lib.gqa_plan_workspace_bytes.restype = ctypes.c_size_t
+        step = [P, P, P, P, P, P, P, P, P, P, P, F, F]
+        lib.gqa_decode_attn.argtypes = step + [P, P]
+        lib.gqa_decode_attn_host.argtypes = step + [P, P]
+        lib.gqa_prologue.argtypes = step + [P]
+        lib.gqa_attention_splitkv.argtypes = [P, P, P, P, P, P]
+        lib.gqa_combine.argtypes = [P, P, P, P]
+        lib.gqa_plan_read_q_rot.argtypes = [P, P]
+        lib.gqa_plan_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
+        lib.gqa_partition_describe.argtypes = [P, I, I, I, I, P]
+        lib.gqa_partition_describe.restype = ctypes.c_longlong
+        lib.gqa_status_string.argtypes = [I]
+        lib.gqa_status_string.restype = ctypes.c_char_p
+        for name in ("gqa_plan_create", "gqa_plan_destroy", "gqa_decode_attn", "gqa_decode_attn_host",
+                     "gqa_prologue", "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
+                     "gqa_plan_device_errors"):
+            getattr(lib, name).restype = I
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load(build=False).gqa_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - only used to format an error message
+        return "status"
+
+
+def _check(status: int, what: str):
+    if status != GQA_OK:
+        raise GqaError(status, what)
+
+
+def _dptr(t) -> Optional[int]:
+    """Device pointer of a torch tensor (None passes NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _hptr(a) -> Optional[int]:
+    """Host pointer of a numpy array or CPU torch tensor."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        if not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("expected a C-contiguous array")
+        return a.ctypes.data
+    if a.is_cuda or not a.is_contiguous():
+        raise ValueError("expected a contiguous host tensor")
+    return a.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(stream) if isinstance(stream, int) else stream.cuda_stream
+
+
+def partition_describe(seq_lens, num_kv_heads: int, max_seq_len: int, num_workers: int):
+    """Host view of the split-KV partition: (total tiles, [W, 2] worker ranges)."""
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    rng = np.zeros((num_workers, 2), dtype=np.int64)
+    T = load().gqa_partition_describe(sl.ctypes.data, len(sl), int(num_kv_heads), int(max_seq_len),
+                                      int(num_workers), rng.ctypes.data)
+    if T < 0:
+        raise ValueError("bad partition arguments")
+    return int(T), rng
+
+
+class Plan:
+    """A gqa_plan_t: geometry, split-worker count and the workspace (allocated once)."""
+
+    def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *,
+                 block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128, num_workers: int = 0,
+                 device: int = 0, seq_lens_host=None):
+        self._lib = load()
+        self.desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                             int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device))
+        sl = None
+        if seq_lens_host is not None:
+            sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+        self._h = ctypes.c_void_p()
+        _check(self._lib.gqa_plan_create(ctypes.byref(self.desc), None if sl is None else sl.ctypes.data,
+                                         ctypes.byref(self._h)), "gqa_plan_create")
+
+    @classmethod
+    def for_workload(cls, w, num_workers: int = 0, device: int = 0) -> "Plan":
+        return cls(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
+                   num_workers=num_workers, device=device, seq_lens_host=w.seq_lens.cpu().numpy())
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            _check(self._lib.gqa_plan_destroy(self._h), "gqa_plan_destroy")
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def num_workers(self) -> int:
+        return self._lib.gqa_plan_num_workers(self._h)
+
+    @property
+    def workspace_bytes(self) -> int:
+        return self._lib.gqa_plan_workspace_bytes(self._h)
+
+    # ------------------------------------------------------------------ the step
+    def decode_attn(self, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+                    q_norm_w, k_norm_w, rope_theta: float, eps: float, out, stream=None):
+        _check(self._lib.gqa_decode_attn(
+            self._h, _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
+            _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
+            _dptr(out), _stream(stream)), "gqa_decode_attn")
+
+    def decode_attn_host(self, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+                         q_norm_w, k_norm_w, rope_theta: float, eps: float, out, stream=None):
+        """q/k/v_new, seq_lens, positions and out are host buffers; caches, page table and
+        norm weights are device tensors.  Synchronise the stream before reading `out`."""
+        _check(self._lib.gqa_decode_attn_host(
+            self._h, _hptr(q_new), _hptr(k_new), _hptr(v_new), _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
+            _hptr(seq_lens), _hptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
+            _hptr(out), _stream(stream)), "gqa_decode_attn_host")
+
+    def prologue(self, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w,
+                 k_norm_w, rope_theta: float, eps: float, stream=None):
+        _check(self._lib.gqa_prologue(
+            self._h, _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
+            _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
+            _stream(stream)), "gqa_prologue")
+
+    def attention_splitkv(self, k_cache, v_cache, page_table, seq_lens, stream=None):
+        _check(self._lib.gqa_attention_splitkv(self._h, _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
+                                               _dptr(seq_lens), _stream(stream)), "gqa_attention_splitkv")
+
+    def combine(self, seq_lens, out, stream=None):
+        _check(self._lib.gqa_combine(self._h, _dptr(seq_lens), _dptr(out), _stream(stream)), "gqa_combine")
+
+    def read_q_rot(self) -> np.ndarray:
+        d = self.desc
+        out = np.zeros((d.batch, d.num_q_heads, d.head_dim), dtype=np.uint16)
+        _check(self._lib.gqa_plan_read_q_rot(self._h, out.ctypes.data), "gqa_plan_read_q_rot")
+        return out
+
+    def device_errors(self, clear: bool = True) -> int:
+        f = ctypes.c_uint32(0)
+        _check(self._lib.gqa_plan_device_errors(self._h, ctypes.byref(f), int(bool(clear))), "gqa_plan_device_errors")
+        return int(f.value)
+
+    # ------------------------------------------------------------------ convenience
+    def run(self, w, out, stream=None):
+        """One decode step of a workloads.Workload already on this device."""
+        self.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out, stream)

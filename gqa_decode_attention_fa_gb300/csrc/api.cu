@@ -1,0 +1,429 @@
+// C ABI of libgqa_decode.so: plan (split planner + workspace), argument validation, tensor
+// maps and the launch sequence prologue -> split-KV attention -> combine.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "launch.h"
+
+using namespace gqa;
+
+struct gqa_plan {
+  gqa_plan_desc_t desc;
+  int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0;
+  long long num_rows = 0;
+  void *ws = nullptr;
+  size_t ws_bytes = 0;
+  uint16_t *q_rot = nullptr;
+  float *part_o = nullptr, *part_ml = nullptr;
+  uint32_t *prefix = nullptr, *err = nullptr;
+  uint16_t *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
+  int32_t *st_sl = nullptr, *st_pos = nullptr;
+  // tensor maps of the last cache pair seen (re-encoded when the pointers change)
+  mutable std::mutex tm_mu;
+  mutable const void *tm_k_ptr = nullptr, *tm_v_ptr = nullptr;
+  mutable CUtensorMap tmK, tmV;
+};
+
+namespace {
+
+// Runs the calling thread on `dev` for the guard's lifetime.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      prev = -1;
+      return;
+    }
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// K or V cache viewed as [rows][H_kv][128] bf16; box = 64 dims (128 B, 128-byte swizzle)
+// x 1 head x 64 tokens.
+bool make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(Hkv) * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The split planner: one worker CTA per SM (the kernel holds ~210 KiB of shared memory,
+// so one CTA fits an SM), never more workers than tiles.  Workers take equal contiguous
+// tile ranges, so the count needs no per-length tuning beyond this clamp.
+int plan_workers(int num_sms, long long total_tiles) {
+  long long w = num_sms;
+  if (total_tiles < w) w = total_tiles;
+  return w < 1 ? 1 : static_cast<int>(w);
+}
+
+bool finite_pos(float x) { return isfinite(x) && x > 0.f; }
+
+gqa_status_t check_step_args(const gqa_plan_t *plan, const void *q, const void *k, const void *v, const void *kc,
+                             const void *vc, const int32_t *pt, const int32_t *sl, const int32_t *pos,
+                             float theta, float eps, const void *out) {
+  if (!plan || !q || !k || !v || !kc || !vc || !sl || !pos || !out) return GQA_ERR_INVALID_ARG;
+  const bool paged = plan->desc.block_size > 0;
+  if (paged != (pt != nullptr)) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
+  return GQA_OK;
+}
+
+gqa_status_t cache_maps(const gqa_plan_t *plan, const void *kc, const void *vc, CUtensorMap *tk, CUtensorMap *tv) {
+  std::lock_guard<std::mutex> lk(plan->tm_mu);
+  if (plan->tm_k_ptr != kc || plan->tm_v_ptr != vc) {
+    if (!make_cache_map(&plan->tmK, kc, plan->desc.num_kv_heads, plan->num_rows) ||
+        !make_cache_map(&plan->tmV, vc, plan->desc.num_kv_heads, plan->num_rows)) {
+      plan->tm_k_ptr = plan->tm_v_ptr = nullptr;
+      return GQA_ERR_CUDA;
+    }
+    plan->tm_k_ptr = kc;
+    plan->tm_v_ptr = vc;
+  }
+  *tk = plan->tmK;
+  *tv = plan->tmV;
+  return GQA_OK;
+}
+
+gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
+                          const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                          float theta, float eps, cudaStream_t stream) {
+  PrologueParams p;
+  memset(&p, 0, sizeof p);
+  p.q_new = static_cast<const uint16_t *>(q);
+  p.k_new = static_cast<const uint16_t *>(k);
+  p.v_new = static_cast<const uint16_t *>(v);
+  p.k_cache = static_cast<uint16_t *>(kc);
+  p.v_cache = static_cast<uint16_t *>(vc);
+  p.page_table = pt;
+  p.seq_lens = sl;
+  p.positions = pos;
+  p.q_norm_w = static_cast<const uint16_t *>(qw);
+  p.k_norm_w = static_cast<const uint16_t *>(kw);
+  p.q_rot = plan->q_rot;
+  p.err = plan->err;
+  p.B = plan->desc.batch;
+  p.Hq = plan->desc.num_q_heads;
+  p.Hkv = plan->desc.num_kv_heads;
+  p.G = plan->G;
+  p.npad = plan->npad;
+  p.paged = plan->desc.block_size > 0;
+  p.max_seq = plan->desc.max_seq_len;
+  p.max_blocks = plan->max_blocks;
+  p.num_blocks = plan->desc.num_cache_blocks;
+  p.num_rows = plan->num_rows;
+  p.eps = static_cast<double>(eps);
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    p.inv_freq[i] = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(kHeadDim));
+  return launch_prologue(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_attention(const gqa_plan_t *plan, const void *kc, const void *vc, const int32_t *pt,
+                           const int32_t *sl, cudaStream_t stream) {
+  CUtensorMap tk, tv;
+  gqa_status_t st = cache_maps(plan, kc, vc, &tk, &tv);
+  if (st != GQA_OK) return st;
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.seq_lens = sl;
+  p.page_table = pt;
+  p.q_rot = plan->q_rot;
+  p.part_o = plan->part_o;
+  p.part_ml = plan->part_ml;
+  p.prefix = plan->prefix;
+  p.err = plan->err;
+  p.B = plan->desc.batch;
+  p.Hkv = plan->desc.num_kv_heads;
+  p.G = plan->G;
+  p.paged = plan->desc.block_size > 0;
+  p.max_seq = plan->desc.max_seq_len;
+  p.max_blocks = plan->max_blocks;
+  p.num_blocks = plan->desc.num_cache_blocks;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
+  return launch_attention(tk, tv, p, plan->npad, plan->W, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, cudaStream_t stream) {
+  CombineParams p;
+  memset(&p, 0, sizeof p);
+  p.seq_lens = sl;
+  p.prefix = plan->prefix;
+  p.part_o = plan->part_o;
+  p.part_ml = plan->part_ml;
+  p.out = static_cast<uint16_t *>(out);
+  p.B = plan->desc.batch;
+  p.Hq = plan->desc.num_q_heads;
+  p.Hkv = plan->desc.num_kv_heads;
+  p.G = plan->G;
+  p.W = plan->W;
+  p.max_seq = plan->desc.max_seq_len;
+  return launch_combine(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
+                      const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                      float theta, float eps, void *out, cudaStream_t stream) {
+  gqa_status_t st = run_prologue(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream);
+  if (st != GQA_OK) return st;
+  st = run_attention(plan, kc, vc, pt, sl, stream);
+  if (st != GQA_OK) return st;
+  return run_combine(plan, sl, out, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_lens_host, gqa_plan_t **plan) {
+  if (!desc || !plan) return GQA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const gqa_plan_desc_t &d = *desc;
+  if (d.batch < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.max_seq_len < 1 || d.num_workers < 0 ||
+      d.block_size < 0)
+    return GQA_ERR_INVALID_ARG;
+  if (d.head_dim != GQA_HEAD_DIM || d.num_q_heads % d.num_kv_heads != 0 ||
+      d.num_q_heads / d.num_kv_heads > GQA_MAX_GROUP || d.batch > GQA_MAX_BATCH ||
+      (d.block_size != 0 && d.block_size != GQA_BLOCK_SIZE))
+    return GQA_ERR_UNSUPPORTED;
+  const bool paged = d.block_size > 0;
+  if (paged && d.num_cache_blocks < 1) return GQA_ERR_INVALID_ARG;
+  const long long max_blocks = (d.max_seq_len + kTile - 1) / kTile;
+  const long long num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile
+                                   : static_cast<long long>(d.batch) * d.max_seq_len;
+  if (num_rows > 0x7fffffffLL - kTile) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d.batch) * d.num_kv_heads * max_blocks > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return GQA_ERR_CUDA;
+  if (d.device < 0 || d.device >= ndev) return GQA_ERR_INVALID_ARG;
+
+  DeviceGuard guard(d.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess) return GQA_ERR_CUDA;
+
+  gqa_plan_t *p = new (std::nothrow) gqa_plan_t();
+  if (!p) return GQA_ERR_WORKSPACE;
+  p->desc = d;
+  p->G = d.num_q_heads / d.num_kv_heads;
+  p->npad = p->G <= 8 ? 8 : 16;
+  p->num_sms = sms;
+  p->max_blocks = static_cast<int>(max_blocks);
+  p->num_rows = num_rows;
+  long long total_tiles = 0;
+  for (int b = 0; b < d.batch; ++b) {
+    long long L = seq_lens_host ? seq_lens_host[b] : d.max_seq_len;
+    if (L < 1) L = 1;
+    if (L > d.max_seq_len) L = d.max_seq_len;
+    total_tiles += d.num_kv_heads * ((L + kTile - 1) / kTile);
+  }
+  p->W = d.num_workers > 0 ? d.num_workers : plan_workers(sms, total_tiles);
+
+  const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
+  const long long slots = B * Hkv + p->W;
+  const size_t sz_q = align256(B * Hkv * p->npad * kHeadDim * 2);
+  const size_t sz_o = align256(slots * kConsumerWarps * p->G * kHeadDim * 4);
+  const size_t sz_ml = align256(slots * kConsumerWarps * p->G * 2 * 4);
+  const size_t sz_pre = align256((B + 1) * 4);
+  const size_t sz_err = 256;
+  const size_t sz_sq = align256(B * Hq * kHeadDim * 2), sz_skv = align256(B * Hkv * kHeadDim * 2);
+  const size_t sz_si = align256(B * 4);
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_pre + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si;
+  if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return GQA_ERR_WORKSPACE;
+  }
+  char *c = static_cast<char *>(p->ws);
+  p->q_rot = reinterpret_cast<uint16_t *>(c); c += sz_q;
+  p->part_o = reinterpret_cast<float *>(c); c += sz_o;
+  p->part_ml = reinterpret_cast<float *>(c); c += sz_ml;
+  p->prefix = reinterpret_cast<uint32_t *>(c); c += sz_pre;
+  p->err = reinterpret_cast<uint32_t *>(c); c += sz_err;
+  p->st_q = reinterpret_cast<uint16_t *>(c); c += sz_sq;
+  p->st_out = reinterpret_cast<uint16_t *>(c); c += sz_sq;
+  p->st_k = reinterpret_cast<uint16_t *>(c); c += sz_skv;
+  p->st_v = reinterpret_cast<uint16_t *>(c); c += sz_skv;
+  p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
+  p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad, d.batch) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p->ws);
+    delete p;
+    return GQA_ERR_CUDA;
+  }
+  *plan = p;
+  return GQA_OK;
+}
+
+gqa_status_t gqa_plan_destroy(gqa_plan_t *plan) {
+  if (!plan) return GQA_OK;
+  DeviceGuard guard(plan->desc.device);
+  cudaError_t e = cudaFree(plan->ws);
+  delete plan;
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int gqa_plan_num_workers(const gqa_plan_t *plan) { return plan ? plan->W : 0; }
+
+size_t gqa_plan_workspace_bytes(const gqa_plan_t *plan) { return plan ? plan->ws_bytes : 0; }
+
+gqa_status_t gqa_decode_attn(const gqa_plan_t *plan, const void *q_new, const void *k_new, const void *v_new,
+                             void *k_cache, void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
+                             const int32_t *positions, const void *q_norm_w, const void *k_norm_w, float rope_theta,
+                             float eps, void *out, void *stream) {
+  gqa_status_t st = check_step_args(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+                                    rope_theta, eps, out);
+  if (st != GQA_OK) return st;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_step(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w, k_norm_w,
+                  rope_theta, eps, out, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan, const void *q_new_host, const void *k_new_host,
+                                  const void *v_new_host, void *k_cache, void *v_cache, const int32_t *page_table,
+                                  const int32_t *seq_lens_host, const int32_t *positions_host, const void *q_norm_w,
+                                  const void *k_norm_w, float rope_theta, float eps, void *out_host, void *stream) {
+  gqa_status_t st = check_step_args(plan, q_new_host, k_new_host, v_new_host, k_cache, v_cache, page_table,
+                                    seq_lens_host, positions_host, rope_theta, eps, out_host);
+  if (st != GQA_OK) return st;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t B = plan->desc.batch, Hq = plan->desc.num_q_heads, Hkv = plan->desc.num_kv_heads;
+  const size_t bq = B * Hq * kHeadDim * 2, bkv = B * Hkv * kHeadDim * 2, bi = B * 4;
+  if (cudaMemcpyAsync(plan->st_q, q_new_host, bq, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(plan->st_k, k_new_host, bkv, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(plan->st_v, v_new_host, bkv, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(plan->st_sl, seq_lens_host, bi, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(plan->st_pos, positions_host, bi, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  st = run_step(plan, plan->st_q, plan->st_k, plan->st_v, k_cache, v_cache, page_table, plan->st_sl, plan->st_pos,
+                q_norm_w, k_norm_w, rope_theta, eps, plan->st_out, s);
+  if (st != GQA_OK) return st;
+  if (cudaMemcpyAsync(out_host, plan->st_out, bq, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
+                          const int32_t *positions, const void *q_norm_w, const void *k_norm_w, float rope_theta,
+                          float eps, void *stream) {
+  gqa_status_t st = check_step_args(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
+                                    rope_theta, eps, q_new);
+  if (st != GQA_OK) return st;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_prologue(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w,
+                      k_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_cache, const void *v_cache,
+                                   const int32_t *page_table, const int32_t *seq_lens, void *stream) {
+  if (!plan || !k_cache || !v_cache || !seq_lens) return GQA_ERR_INVALID_ARG;
+  if ((plan->desc.block_size > 0) != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_attention(plan, k_cache, v_cache, page_table, seq_lens, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out, void *stream) {
+  if (!plan || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_combine(plan, seq_lens, out, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host) {
+  if (!plan || !q_rot_host) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  const int B = plan->desc.batch, Hkv = plan->desc.num_kv_heads, G = plan->G, npad = plan->npad;
+  std::vector<uint16_t> img(static_cast<size_t>(B) * Hkv * npad * kHeadDim);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(img.data(), plan->q_rot, img.size() * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  for (int b = 0; b < B; ++b)
+    for (int kv = 0; kv < Hkv; ++kv)
+      for (int g = 0; g < G; ++g)
+        for (int e = 0; e < kHeadDim; ++e) {
+          const int half = e >> 6, chunk = (e & 63) >> 3, within = e & 7;
+          const size_t off = (static_cast<size_t>(b) * Hkv + kv) * npad * kHeadDim +
+                             (half * npad * 128 + swz128(g, chunk)) / 2 + within;
+          q_rot_host[((static_cast<size_t>(b) * Hkv + kv) * G + g) * kHeadDim + e] = img[off];
+        }
+  return GQA_OK;
+}
+
+gqa_status_t gqa_plan_device_errors(const gqa_plan_t *plan, uint32_t *flags, int clear) {
+  if (!plan || !flags) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(flags, plan->err, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (clear && (cudaMemset(plan->err, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}
+
+long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int num_kv_heads, int max_seq_len,
+                                 int num_workers, long long *worker_range) {
+  if (!seq_lens_host || !worker_range || batch < 1 || num_kv_heads < 1 || max_seq_len < 1 || num_workers < 1)
+    return -1;
+  long long T = 0;
+  for (int b = 0; b < batch; ++b) T += static_cast<long long>(num_kv_heads) * tiles_of(seq_lens_host[b], max_seq_len);
+  for (int w = 0; w < num_workers; ++w) {
+    worker_range[2 * w] = worker_begin(T, num_workers, w);
+    worker_range[2 * w + 1] = worker_begin(T, num_workers, w + 1);
+  }
+  return T;
+}
+
+const char *gqa_status_string(gqa_status_t status) {
+  switch (status) {
+    case GQA_OK: return "ok";
+    case GQA_ERR_INVALID_ARG: return "invalid argument";
+    case GQA_ERR_UNSUPPORTED: return "unsupported geometry";
+    case GQA_ERR_CUDA: return "CUDA error";
+    case GQA_ERR_WORKSPACE: return "workspace allocation failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -161,9 +161,10 @@ def make(B: int, Hq: int, Hkv: int, lens: Sequence[int], *, paged: bool, seed: i
             pt[b, :n] = perm[k:k + n]
             k += n
         page_table = pt.to(device)
+    # theta and eps cross the C ABI as binary32; keep exactly the values the library sees
     return Workload(name=name, B=B, Hq=Hq, Hkv=Hkv, d=d, block_size=BLOCK if paged else 0,
-                    max_seq=int(max_seq), num_blocks=num_blocks, rope_theta=float(rope_theta),
-                    eps=float(eps), q_new=q_new, k_new=k_new, v_new=v_new, k_cache=k_cache,
+                    max_seq=int(max_seq), num_blocks=num_blocks, rope_theta=float(np.float32(rope_theta)),
+                    eps=float(np.float32(eps)), q_new=q_new, k_new=k_new, v_new=v_new, k_cache=k_cache,
                     v_cache=v_cache, page_table=page_table, seq_lens=seq_lens.to(device),
                     positions=pos.to(device), q_norm_w=q_norm_w, k_norm_w=k_norm_w)
 

@@ -1,0 +1,92 @@
+"""CPU checks of the C ABI: the library loads and exports every function the header
+declares, host-side validation rejects bad geometry before touching a device, and the
+split-KV partition covers every tile exactly once in contiguous, balanced ranges."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from gqa_decode_attention_fa_gb300 import binding
+
+
+def test_library_exports_every_declared_function():
+    lib = binding.load()
+    names = binding.header_functions()
+    assert "gqa_decode_attn" in names and "gqa_plan_create" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    lib = binding.load()
+    for s in range(5):
+        assert lib.gqa_status_string(s)
+    assert binding.status_string(1) == "invalid argument"
+
+
+def _create(**over):
+    d = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=64, max_seq_len=128,
+             num_cache_blocks=4, num_workers=0, device=0)
+    d.update(over)
+    desc = binding.PlanDesc(*[d[n] for n, _ in binding.PlanDesc._fields_])
+    h = ctypes.c_void_p()
+    return binding.load().gqa_plan_create(ctypes.byref(desc), None, ctypes.byref(h))
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(batch=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(num_q_heads=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(max_seq_len=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(num_workers=-1), binding.GQA_ERR_INVALID_ARG),
+    (dict(block_size=-64), binding.GQA_ERR_INVALID_ARG),
+    (dict(num_cache_blocks=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(head_dim=64), binding.GQA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=10, num_kv_heads=4), binding.GQA_ERR_UNSUPPORTED),   # H_q % H_kv != 0
+    (dict(num_q_heads=34, num_kv_heads=2), binding.GQA_ERR_UNSUPPORTED),   # G = 17
+    (dict(batch=1025), binding.GQA_ERR_UNSUPPORTED),
+    (dict(block_size=32), binding.GQA_ERR_UNSUPPORTED),
+    (dict(block_size=0, batch=1024, max_seq_len=1 << 21), binding.GQA_ERR_UNSUPPORTED),  # rows > 2^31
+])
+def test_plan_create_rejects_bad_geometry(over, status):
+    assert _create(**over) == status
+
+
+def test_null_arguments_are_rejected():
+    lib = binding.load()
+    assert lib.gqa_plan_create(None, None, None) == binding.GQA_ERR_INVALID_ARG
+    args = [None] * 11 + [ctypes.c_float(1e6), ctypes.c_float(1e-6), None, None]
+    assert lib.gqa_decode_attn(*args) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_decode_attn_host(*args) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_prologue(*args[:-1]) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_attention_splitkv(None, None, None, None, None, None) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_combine(None, None, None, None) == binding.GQA_ERR_INVALID_ARG
+    assert lib.gqa_plan_destroy(None) == binding.GQA_OK
+    assert lib.gqa_plan_num_workers(None) == 0
+    f = ctypes.c_uint32()
+    assert lib.gqa_plan_device_errors(None, ctypes.byref(f), 0) == binding.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("lens,hkv,W", [
+    ([256], 8, 32), ([4096], 8, 152), ([131072], 8, 152), ([1, 64, 65, 1000], 2, 7),
+    ([1, 64, 65, 1000], 2, 1000), ([5, 0, 7], 3, 4),
+])
+def test_partition_covers_every_tile_once_in_balanced_contiguous_ranges(lens, hkv, W):
+    max_seq = max(max(lens), 1)
+    T, rng = binding.partition_describe(lens, hkv, max_seq, W)
+    tiles = [(L + 63) // 64 if 1 <= L <= max_seq else 0 for L in lens]
+    assert T == hkv * sum(tiles)
+    assert rng[0, 0] == 0 and rng[-1, 1] == T
+    assert np.all(rng[1:, 0] == rng[:-1, 1])                 # contiguous, no gaps or overlaps
+    sizes = rng[:, 1] - rng[:, 0]
+    assert sizes.min() >= 0 and sizes.max() - sizes.min() <= 1  # balanced to one tile
+
+
+def test_partition_worker_lookup_agrees_with_ranges():
+    """The kernels find a tile's worker arithmetically as floor(((x+1)W - 1)/T); check it
+    against the published ranges for many (T, W)."""
+    for T in (1, 2, 31, 32, 33, 1000, 16384, 17411):
+        for W in (1, 2, 3, 7, 152, 1000):
+            _, rng = binding.partition_describe([64 * T], 1, 64 * T, W)
+            for x in set([0, T - 1, T // 2, T // 3] + list(range(0, T, max(1, T // 50)))):
+                w = ((x + 1) * W - 1) // T
+                assert rng[w, 0] <= x < rng[w, 1]

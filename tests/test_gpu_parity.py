@@ -1,0 +1,240 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs.  Output: max |err| <= 1e-2 and relative L2 <= 2e-3.  Appended cache rows: bit-exact
+(ties within 2^-40 of a bf16 midpoint excepted, expected zero), every other cache row
+untouched; rotated q: equal bf16 bits except at binary32 rounding ties."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_decode_attention_fa_gb300 import binding, workloads as wl
+from gqa_decode_attention_fa_gb300.workloads import bits, ints
+
+from _util import (K_MIDPOINT_WINDOW, Q_MIDPOINT_WINDOW, appended_rows, assert_out_close,
+                   check_rounded_rows, oracle_step, rotated_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(w, plan=None, num_workers=0):
+    plan = plan or binding.Plan.for_workload(w, num_workers=num_workers)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    plan.run(w, out)
+    torch.cuda.synchronize()
+    return plan, out
+
+
+def full_check(w, num_workers=0, what=""):
+    """Run both sides on workload w (on the GPU) and check output, cache and q."""
+    k0, v0 = bits(w.k_cache), bits(w.v_cache)
+    ref = oracle_step(w)
+    assert ref["status"] == 0
+    plan, out = run_gpu(w, num_workers=num_workers)
+    assert plan.device_errors() == 0
+    stats = assert_out_close(out, ref["out"], what)
+    # cache: only the appended rows may change, V bit copies, K bit-exact (midpoint ties aside)
+    kc, vc = bits(w.k_cache), bits(w.v_cache)
+    np.testing.assert_array_equal(vc, ref["v_cache"])
+    rows_g, rows_o = appended_rows(w, kc), appended_rows(w, ref["k_cache"])
+    mask = np.ones(kc.reshape(-1, w.Hkv, w.d).shape[0], bool)
+    pos = ints(w.positions)
+    for b in range(w.B):
+        p = int(pos[b])
+        r = int(ints(w.page_table)[b, p // 64]) * 64 + p % 64 if w.paged else b * w.max_seq + p
+        mask[r] = False
+    np.testing.assert_array_equal(kc.reshape(-1, w.Hkv, w.d)[mask], k0.reshape(-1, w.Hkv, w.d)[mask])
+    zk, _ = rotated_rows(w, "k")
+    ties_k = check_rounded_rows(rows_g, rows_o, zk, K_MIDPOINT_WINDOW * np.abs(zk), f"{what} k rows")
+    assert ties_k == 0
+    zq, sq = rotated_rows(w, "q")
+    ties_q = check_rounded_rows(plan.read_q_rot(), ref["q_rot"], zq, Q_MIDPOINT_WINDOW * sq, f"{what} q rows")
+    assert ties_q <= max(4, zq.size // 1000)
+    del k0, v0
+    return stats, plan, out
+
+
+# ------------------------------------------------------------------ the named workloads
+
+@pytest.mark.parametrize("name", ["qwen3-14b-tiny", "qwen3-14b-4k", "qwen3-14b-ragged", "llama3-70b-128k"])
+def test_named_workload_full_parity(name):
+    w = wl.named(name, device="cuda")
+    full_check(w, what=name)
+
+
+def test_40_layer_sweep_parity():
+    """All 40 layers of the sweep through one plan, as the benchmark runs them: three layers
+    checked in full, every layer checked on all heads of one sampled sequence."""
+    plan = None
+    out = None
+    rng = np.random.default_rng(0)
+    for layer in range(wl.LAYERS_40):
+        w = wl.named("qwen3-14b-40layer", device="cuda", layer=layer)
+        if plan is None:
+            plan = binding.Plan.for_workload(w)
+            out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+        if layer in (0, 17, 39):
+            full_check(w, what=f"layer {layer}")
+            del w
+            torch.cuda.empty_cache()
+            continue
+        b = int(rng.integers(0, w.B))
+        plan.run(w, out)
+        torch.cuda.synchronize()
+        # one sequence, gathered to a contiguous single-sequence problem for the oracle
+        k, v = wl.gather_sequence(w, b)
+        L = int(w.seq_lens[b].item())
+        g = oracle.geom(1, w.Hq, w.Hkv, w.d, 0, k.shape[0], k.shape[0])
+        pos = ints(w.positions)[b:b + 1]
+        # the caches were already updated by the library: the oracle re-runs the prologue
+        # on the same new-token inputs, which rewrites the same slot with its own values
+        ref = oracle.decode_step(g, bits(w.q_new[b:b + 1]), bits(w.k_new[b:b + 1]), bits(w.v_new[b:b + 1]),
+                                 bits(k), bits(v), None, np.array([L], np.int32), pos, bits(w.q_norm_w),
+                                 bits(w.k_norm_w), w.rope_theta, w.eps)
+        assert ref["status"] == 0
+        assert_out_close(out[b:b + 1], ref["out"], f"layer {layer} seq {b}")
+        del w, k, v
+    assert plan.device_errors() == 0
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("lens", [[1], [2], [63], [64], [65], [127, 128, 129], [1, 64, 65, 300, 7]])
+@pytest.mark.parametrize("paged", [False, True])
+def test_ragged_tails_and_tiny_lengths(lens, paged):
+    w = wl.make(len(lens), 10, 2, lens, paged=paged, seed=len(lens) * 7 + 1, device="cuda", extra_blocks=3)
+    full_check(w, what=f"lens={lens} paged={paged}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (8, 2), (10, 2), (16, 2), (24, 2), (32, 2), (64, 8)])
+def test_group_sizes(Hq, Hkv):
+    w = wl.make(3, Hq, Hkv, [70, 200, 5], paged=True, seed=Hq + Hkv, device="cuda")
+    full_check(w, what=f"G={Hq // Hkv}")
+
+
+@pytest.mark.parametrize("qk_norm", [False, True])
+def test_with_and_without_qk_norm(qk_norm):
+    w = wl.make(2, 40, 8, [300, 1000], paged=False, qk_norm=qk_norm, seed=3, device="cuda")
+    full_check(w, what=f"qk_norm={qk_norm}")
+
+
+def test_one_sided_norm_weights():
+    w = wl.make(2, 8, 2, [100, 33], paged=True, seed=4, device="cuda")
+    w.k_norm_w = None
+    full_check(w, what="q norm only")
+    w = wl.make(2, 8, 2, [100, 33], paged=True, seed=5, device="cuda")
+    w.q_norm_w = None
+    full_check(w, what="k norm only")
+
+
+def test_new_token_mid_sequence_and_capacity_not_a_tile_multiple():
+    w = wl.make(3, 10, 2, [100, 150, 37], paged=False, max_seq=150, positions=[10, 149, 0], seed=6,
+                device="cuda")
+    full_check(w, what="positions < L-1, max_seq=150")
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 151, 1000])
+def test_worker_counts(workers):
+    w = wl.make(5, 40, 8, [1, 700, 64, 3000, 129], paged=True, seed=8, device="cuda")
+    full_check(w, num_workers=workers, what=f"W={workers}")
+
+
+def test_large_scores_and_outliers_are_stable():
+    """K outliers x20 (as in the 40-layer sweep) and a long context on a small batch."""
+    w = wl.make(2, 40, 8, [20000, 9000], paged=True, seed=9, k_outlier_frac=0.01, device="cuda")
+    full_check(w, what="outliers")
+
+
+def test_max_batch():
+    lens = (np.arange(1024) % 97 + 1).tolist()
+    w = wl.make(1024, 8, 2, lens, paged=True, seed=10, device="cuda")
+    full_check(w, what="B=1024")
+
+
+# ------------------------------------------------------------------ API behaviour
+
+def test_determinism_bitwise():
+    w = wl.named("qwen3-14b-ragged", device="cuda")
+    plan, out1 = run_gpu(w)
+    out2 = torch.empty_like(out1)
+    plan.run(w, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_steps_equal_fused_call():
+    w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=11, device="cuda")
+    plan, out1 = run_gpu(w)
+    out2 = torch.empty_like(out1)
+    plan.prologue(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                  w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps)
+    plan.attention_splitkv(w.k_cache, w.v_cache, w.page_table, w.seq_lens)
+    plan.combine(w.seq_lens, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_host_buffer_entry_point_matches_device_call():
+    w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=12, device="cuda")
+    plan, out1 = run_gpu(w)
+    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q_new", "k_new", "v_new", "seq_lens", "positions")}
+    out_h = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.decode_attn_host(host["q_new"], host["k_new"], host["v_new"], w.k_cache, w.v_cache, w.page_table,
+                              host["seq_lens"], host["positions"], w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps,
+                              out_h, stream=s)
+    s.synchronize()
+    assert torch.equal(out1.cpu().view(torch.int16), out_h.view(torch.int16))
+
+
+def test_device_index_errors_are_flagged_not_faulted():
+    """Out-of-range positions, lengths and page ids set error bits, zero that sequence's
+    output and leave the others correct; nothing faults (the kernels bound-check)."""
+    w = wl.make(3, 10, 2, [100, 70, 5], paged=True, seed=13, device="cuda", extra_blocks=2)
+    ref = oracle_step(w)
+    plan = binding.Plan.for_workload(w)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    # position == seq_len for sequence 1
+    w.positions[1] = 70
+    plan.run(w, out)
+    assert plan.device_errors() & binding.DEVERR_POSITION
+    # seq_len beyond capacity for sequence 2
+    w.positions[1] = 69
+    w.seq_lens[2] = w.max_seq + 1
+    plan.run(w, out)
+    assert plan.device_errors() & binding.DEVERR_SEQLEN
+    assert torch.count_nonzero(out[2].float()) == 0
+    assert_out_close(out[0:1], ref["out"][0:1], "valid sequence beside a bad one")
+    # page id outside the pool for sequence 0's first page
+    w.seq_lens[2] = 5
+    w.page_table[0, 0] = 10 ** 6
+    plan.run(w, out)
+    assert plan.device_errors() & binding.DEVERR_PAGE
+    assert plan.device_errors() == 0  # cleared by the previous read
+
+
+def test_host_validation_rejects_bad_arguments():
+    w = wl.make(2, 8, 2, [10, 20], paged=True, seed=14, device="cuda")
+    plan = binding.Plan.for_workload(w)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.GqaError) as e:
+        plan.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, None, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    with pytest.raises(binding.GqaError) as e:
+        plan.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, -1.0, w.eps, out)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    with pytest.raises(binding.GqaError) as e:
+        plan.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, w.rope_theta, float("nan"), out)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    with pytest.raises(binding.GqaError) as e:
+        binding.Plan(2, 8, 2, 64, block_size=64, num_cache_blocks=0)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    with pytest.raises(binding.GqaError) as e:
+        binding.Plan(2, 8, 2, 64, head_dim=64)
+    assert e.value.status == binding.GQA_ERR_UNSUPPORTED
+    with pytest.raises(binding.GqaError) as e:
+        binding.Plan(2, 34, 2, 64)
+    assert e.value.status == binding.GQA_ERR_UNSUPPORTED
