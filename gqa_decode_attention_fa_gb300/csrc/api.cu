@@ -22,6 +22,9 @@ struct gqa_plan {
   uint32_t *prefix = nullptr, *err = nullptr;
   uint16_t *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
   int32_t *st_sl = nullptr, *st_pos = nullptr;
+  double2 *rope_tab = nullptr;  // [max_seq_len][64] binary64 (cos, sin) for tab_theta
+  mutable bool tab_valid = false;
+  mutable float tab_theta = 0.f;
   // tensor maps of the last cache pair seen (re-encoded when the pointers change)
   mutable std::mutex tm_mu;
   mutable const void *tm_k_ptr = nullptr, *tm_v_ptr = nullptr;
@@ -119,21 +122,32 @@ gqa_status_t cache_maps(const gqa_plan_t *plan, const void *kc, const void *vc, 
   return GQA_OK;
 }
 
-gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
-                          const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
-                          float theta, float eps, cudaStream_t stream) {
+// (Re)builds the plan's RoPE table for `theta` on `stream` when it holds another theta.
+gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t stream) {
+  if (plan->tab_valid && plan->tab_theta == theta) return GQA_OK;
+  RopeTableParams t;
+  t.rope_tab = plan->rope_tab;
+  t.max_seq = plan->desc.max_seq_len;
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    t.inv_freq[i] = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(kHeadDim));
+  plan->tab_valid = false;
+  if (launch_rope_table(t, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  plan->tab_valid = true;
+  plan->tab_theta = theta;
+  return GQA_OK;
+}
+
+gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const int32_t *sl, const int32_t *pos,
+                          const void *qw, float theta, float eps, cudaStream_t stream) {
+  gqa_status_t st = ensure_rope_table(plan, theta, stream);
+  if (st != GQA_OK) return st;
   PrologueParams p;
   memset(&p, 0, sizeof p);
   p.q_new = static_cast<const uint16_t *>(q);
-  p.k_new = static_cast<const uint16_t *>(k);
-  p.v_new = static_cast<const uint16_t *>(v);
-  p.k_cache = static_cast<uint16_t *>(kc);
-  p.v_cache = static_cast<uint16_t *>(vc);
-  p.page_table = pt;
   p.seq_lens = sl;
   p.positions = pos;
   p.q_norm_w = static_cast<const uint16_t *>(qw);
-  p.k_norm_w = static_cast<const uint16_t *>(kw);
+  p.rope_tab = plan->rope_tab;
   p.q_rot = plan->q_rot;
   p.err = plan->err;
   p.B = plan->desc.batch;
@@ -141,26 +155,30 @@ gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const void *k, 
   p.Hkv = plan->desc.num_kv_heads;
   p.G = plan->G;
   p.npad = plan->npad;
-  p.paged = plan->desc.block_size > 0;
   p.max_seq = plan->desc.max_seq_len;
-  p.max_blocks = plan->max_blocks;
-  p.num_blocks = plan->desc.num_cache_blocks;
-  p.num_rows = plan->num_rows;
   p.eps = static_cast<double>(eps);
-  for (int i = 0; i < kHeadDim / 2; ++i)
-    p.inv_freq[i] = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(kHeadDim));
   return launch_prologue(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
-gqa_status_t run_attention(const gqa_plan_t *plan, const void *kc, const void *vc, const int32_t *pt,
-                           const int32_t *sl, cudaStream_t stream) {
+gqa_status_t run_attention(const gqa_plan_t *plan, const void *k, const void *v, void *kc, void *vc,
+                           const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *kw, float theta,
+                           float eps, cudaStream_t stream) {
+  gqa_status_t st = ensure_rope_table(plan, theta, stream);
+  if (st != GQA_OK) return st;
   CUtensorMap tk, tv;
-  gqa_status_t st = cache_maps(plan, kc, vc, &tk, &tv);
+  st = cache_maps(plan, kc, vc, &tk, &tv);
   if (st != GQA_OK) return st;
   AttnParams p;
   memset(&p, 0, sizeof p);
   p.seq_lens = sl;
   p.page_table = pt;
+  p.positions = pos;
+  p.k_new = static_cast<const uint16_t *>(k);
+  p.v_new = static_cast<const uint16_t *>(v);
+  p.k_cache = static_cast<uint16_t *>(kc);
+  p.v_cache = static_cast<uint16_t *>(vc);
+  p.k_norm_w = static_cast<const uint16_t *>(kw);
+  p.rope_tab = plan->rope_tab;
   p.q_rot = plan->q_rot;
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
@@ -173,6 +191,7 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *kc, const void *v
   p.max_seq = plan->desc.max_seq_len;
   p.max_blocks = plan->max_blocks;
   p.num_blocks = plan->desc.num_cache_blocks;
+  p.eps = static_cast<double>(eps);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
   return launch_attention(tk, tv, p, plan->npad, plan->W, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -197,9 +216,9 @@ gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, c
 gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
                       const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
                       float theta, float eps, void *out, cudaStream_t stream) {
-  gqa_status_t st = run_prologue(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream);
+  gqa_status_t st = run_prologue(plan, q, sl, pos, qw, theta, eps, stream);
   if (st != GQA_OK) return st;
-  st = run_attention(plan, kc, vc, pt, sl, stream);
+  st = run_attention(plan, k, v, kc, vc, pt, sl, pos, kw, theta, eps, stream);
   if (st != GQA_OK) return st;
   return run_combine(plan, sl, out, stream);
 }
@@ -261,7 +280,8 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   const size_t sz_err = 256;
   const size_t sz_sq = align256(B * Hq * kHeadDim * 2), sz_skv = align256(B * Hkv * kHeadDim * 2);
   const size_t sz_si = align256(B * 4);
-  p->ws_bytes = sz_q + sz_o + sz_ml + sz_pre + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si;
+  const size_t sz_tab = align256(static_cast<size_t>(d.max_seq_len) * (kHeadDim / 2) * sizeof(double2));
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_pre + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
   if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -279,7 +299,9 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_v = reinterpret_cast<uint16_t *>(c); c += sz_skv;
   p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
+  p->rope_tab = reinterpret_cast<double2 *>(c); c += sz_tab;
   if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad, d.batch) != cudaSuccess ||
+      configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(p->ws);
@@ -340,26 +362,27 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan, const void *q_new_host
   return GQA_OK;
 }
 
-gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const void *k_new, const void *v_new,
-                          void *k_cache, void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
-                          const int32_t *positions, const void *q_norm_w, const void *k_norm_w, float rope_theta,
-                          float eps, void *stream) {
-  gqa_status_t st = check_step_args(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions,
-                                    rope_theta, eps, q_new);
-  if (st != GQA_OK) return st;
+gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
+                          const int32_t *positions, const void *q_norm_w, float rope_theta, float eps,
+                          void *stream) {
+  if (!plan || !q_new || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
-  return run_prologue(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w,
-                      k_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
+  return run_prologue(plan, q_new, seq_lens, positions, q_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
 }
 
-gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_cache, const void *v_cache,
-                                   const int32_t *page_table, const int32_t *seq_lens, void *stream) {
-  if (!plan || !k_cache || !v_cache || !seq_lens) return GQA_ERR_INVALID_ARG;
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new, const void *v_new, void *k_cache,
+                                   void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
+                                   const int32_t *positions, const void *k_norm_w, float rope_theta, float eps,
+                                   void *stream) {
+  if (!plan || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
   if ((plan->desc.block_size > 0) != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
-  return run_attention(plan, k_cache, v_cache, page_table, seq_lens, static_cast<cudaStream_t>(stream));
+  return run_attention(plan, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, k_norm_w, rope_theta,
+                       eps, static_cast<cudaStream_t>(stream));
 }
 
 gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out, void *stream) {

@@ -23,8 +23,8 @@
 //    take every sixth tile, run the recurrence in registers and release the stage.
 //  * Workers own contiguous, equal ranges of the batch's tiles (see gqa_common.cuh), so
 //    ragged batches stay balanced; CTA 0 publishes the batch prefix for the combine.
-#include "gqa_common.cuh"
 #include "launch.h"
+#include "rowmath.cuh"
 
 namespace gqa {
 
@@ -45,6 +45,34 @@ __device__ __forceinline__ void locate(const uint32_t *pre, const int32_t *Ls, i
   const int within = static_cast<int>(x - static_cast<long long>(pre[lo]));
   kv = within / nt;
   j = within - kv * nt;
+}
+
+// Appends sequence b's new token for KV head kv: k = RoPE_pos(RMSNorm(k_new)) in binary64
+// rounded once to bf16, v = v_new, written to the cache row of position pos (skipped when
+// the page id is out of range; the producer flags that) and returned per lane (dims
+// lane + 32 t) for the shared-memory patch.
+__device__ __forceinline__ void append_new_row(const AttnParams &p, int b, int kv, int pos, int lane,
+                                               uint16_t (&kz)[4], uint16_t (&vz)[4]) {
+  const long long nrow = (static_cast<long long>(b) * p.Hkv + kv) * kHeadDim;
+  const double2 cs0 = p.rope_tab[static_cast<long long>(pos) * 64 + lane];
+  const double2 cs1 = p.rope_tab[static_cast<long long>(pos) * 64 + lane + 32];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) vz[t] = p.v_new[nrow + lane + 32 * t];
+  rotate_row_fp64(p.k_new + nrow, p.k_norm_w, p.eps, cs0, cs1, lane, kz);
+  long long grow = -1;
+  if (p.paged) {
+    const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + pos / kTile];
+    if (pg >= 0 && pg < p.num_blocks) grow = static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
+  } else {
+    grow = static_cast<long long>(b) * p.max_seq + pos;
+  }
+  if (grow >= 0) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      p.k_cache[(grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = kz[t];
+      p.v_cache[(grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = vz[t];
+    }
+  }
 }
 
 template <int NT>
@@ -108,39 +136,74 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     if (lane == 0) pre[0] = 0;
   }
   __syncthreads();
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= p.B; i += blockDim.x) p.prefix[i] = pre[i];
-  }
 
   const long long T = pre[p.B];
   const int W = gridDim.x, w = blockIdx.x;
   const long long xs = worker_begin(T, W, w), xe = worker_begin(T, W, w + 1);
   const long long n = xe - xs;
-  if (n <= 0) return;
+
+  // Where tile xs + i lives: its (b, kv) segment and the cache row of its first token (the
+  // TMA z coordinate).
+  auto describe = [&](long long i, int &row, int &kv, int &seg) {
+    int b, j;
+    locate(pre, Ls, p.B, p.Hkv, xs + i, b, kv, j);
+    seg = b * p.Hkv + kv;
+    if (p.paged) {
+      const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+      if (pg < 0 || pg >= p.num_blocks) {
+        atomicOr(p.err, GQA_DEVERR_PAGE);
+        row = -kTile;  // whole box out of bounds: TMA fills zeros
+      } else {
+        row = pg * kTile;
+      }
+    } else {
+      row = b * p.max_seq + j * kTile;
+    }
+  };
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    bool fail = false;
-    long long issued = 0;
-    for (long long i0 = 0; i0 < n && !fail; i0 += 32) {
-      const long long i = i0 + lane;
-      int row = 0, kv = 0, seg = 0;
-      if (i < n) {
-        int b, j;
-        locate(pre, Ls, p.B, p.Hkv, xs + i, b, kv, j);
-        seg = b * p.Hkv + kv;
-        if (p.paged) {
-          const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
-          if (pg < 0 || pg >= p.num_blocks) {
-            atomicOr(p.err, GQA_DEVERR_PAGE);
-            row = -kTile;  // whole box out of bounds: TMA fills zeros
-          } else {
-            row = pg * kTile;
-          }
-        } else {
-          row = b * p.max_seq + j * kTile;
-        }
+    // The first kStages tiles' K/V loads go out before waiting on the prologue: they read
+    // only the caller's cache (the prologue writes none of it; a tile holding a new
+    // token's row is patched in shared memory by its consumer).  The rotated q follows
+    // once the prologue has finished.
+    if (n <= 0) {
+      griddep_wait();
+      griddep_launch_dependents();
+      return;
+    }
+    const int npre = static_cast<int>(n < kStages ? n : kStages);
+    int row = 0, kv = 0, seg = 0;
+    if (lane < npre) describe(lane, row, kv, seg);
+    for (int k = 0; k < npre; ++k) {
+      const int r_row = __shfl_sync(0xffffffffu, row, k), r_kv = __shfl_sync(0xffffffffu, kv, k);
+      if (lane == 0) {
+        const uint32_t fb = smem_addr(&full_bar[k]);
+        const uint32_t base = smem_addr(smem + k * C::kStageBytes);
+        mbar_arrive_expect_tx(fb, C::kStageBytes);
+        tma_load_3d(base, &tmK, fb, 0, r_kv, r_row);
+        tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, r_kv, r_row);
+        tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, r_kv, r_row);
+        tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, r_kv, r_row);
       }
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    for (int k = 0; k < npre; ++k) {
+      const int r_seg = __shfl_sync(0xffffffffu, seg, k);
+      if (lane == 0) {
+        const uint32_t fb = smem_addr(&full_bar[k]);
+        const uint32_t base = smem_addr(smem + k * C::kStageBytes);
+        bulk_load(base + 4 * kHalfTileBytes, p.q_rot + static_cast<long long>(r_seg) * C::kNpad * kHeadDim,
+                  C::kQBytes, fb);
+      }
+    }
+    bool fail = false;
+    long long issued = npre;
+    for (long long i0 = npre; i0 < n && !fail; i0 += 32) {
+      const long long i = i0 + lane;
+      row = 0, kv = 0, seg = 0;
+      if (i < n) describe(i, row, kv, seg);
       const int cnt = static_cast<int>(n - i0 < 32 ? n - i0 : 32);
       for (int k = 0; k < cnt; ++k) {
         const int r_row = __shfl_sync(0xffffffffu, row, k);
@@ -150,7 +213,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const int s = static_cast<int>(ii % kStages);
         int ok = 1;
         if (lane == 0) {
-          if (ii >= kStages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((ii / kStages) - 1) & 1));
+          ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((ii / kStages) - 1) & 1));
           if (ok) {
             const uint32_t fb = smem_addr(&full_bar[s]);
             const uint32_t base = smem_addr(smem + s * C::kStageBytes);
@@ -179,6 +242,15 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     return;
   }
+
+  // The rotated q, the appended cache rows and the workspace belong to earlier kernels
+  // until this returns.
+  griddep_wait();
+  griddep_launch_dependents();
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= p.B; i += kConsumerWarps * 32) p.prefix[i] = pre[i];
+  }
+  if (n <= 0) return;
 
   // ------------------------------------------------------------------ consumer warps
   const int cw = warp;
@@ -235,11 +307,43 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
   };
 
+  // The new-token k/v rows this warp appends: the first two are computed now, while the
+  // first tiles are still in flight, written to the cache and kept packed in registers for
+  // the shared-memory patch; any further ones are computed when their tile arrives.
+  long long ex0 = -1, ex1 = -1;
+  uint32_t ek0[2] = {0, 0}, ev0[2] = {0, 0}, ek1[2] = {0, 0}, ev1[2] = {0, 0};
+  {
+    int b0, kv0, j0, b1, kv1, j1;
+    locate(pre, Ls, p.B, p.Hkv, xs, b0, kv0, j0);
+    locate(pre, Ls, p.B, p.Hkv, xe - 1, b1, kv1, j1);
+    const int seg_first = b0 * p.Hkv + kv0, seg_last = b1 * p.Hkv + kv1;
+    for (int sg = seg_first; sg <= seg_last && ex1 < 0; ++sg) {
+      const int b = sg / p.Hkv, kv = sg - b * p.Hkv;
+      const int L = Ls[b], pos = p.positions[b];
+      if (L <= 0 || pos < 0 || pos >= L) continue;
+      const int nt = (L + kTile - 1) / kTile;
+      const long long x_new = static_cast<long long>(pre[b]) + static_cast<long long>(kv) * nt + pos / kTile;
+      if (x_new < xs || x_new >= xe || (x_new - xs) % kConsumerWarps != cw) continue;
+      uint16_t kz[4], vz[4];
+      append_new_row(p, b, kv, pos, lane, kz, vz);
+      if (ex0 < 0) {
+        ex0 = x_new;
+        ek0[0] = kz[0] | (uint32_t(kz[1]) << 16), ek0[1] = kz[2] | (uint32_t(kz[3]) << 16);
+        ev0[0] = vz[0] | (uint32_t(vz[1]) << 16), ev0[1] = vz[2] | (uint32_t(vz[3]) << 16);
+      } else {
+        ex1 = x_new;
+        ek1[0] = kz[0] | (uint32_t(kz[1]) << 16), ek1[1] = kz[2] | (uint32_t(kz[3]) << 16);
+        ev1[0] = vz[0] | (uint32_t(vz[1]) << 16), ev1[1] = vz[2] | (uint32_t(vz[3]) << 16);
+      }
+    }
+  }
+
   int cur_seg = -1;
   for (long long i = cw; i < n; i += kConsumerWarps) {
     int b, kv, j;
     locate(pre, Ls, p.B, p.Hkv, xs + i, b, kv, j);
     const int seg = b * p.Hkv + kv;
+    const int pos_b = p.positions[b];
     if (seg != cur_seg) {
       if (cur_seg >= 0) flush(cur_seg);
       cur_seg = seg;
@@ -267,6 +371,29 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       for (int c = lane; c < nchunks; c += 32) {
         v0[valid * 8 + c] = make_uint4(0, 0, 0, 0);
         v1[valid * 8 + c] = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+    // The tile holding sequence b's new token: the TMA filled this stage from the cache
+    // before the row was appended, so patch the appended k and v rows into it.
+    const bool holds_new = pos_b >= 0 && pos_b < Ls[b] && (pos_b >> 6) == j;
+    if (holds_new) {
+      uint16_t kz[4], vz[4];
+      const long long x = xs + i;
+      if (x == ex0 || x == ex1) {
+        const uint32_t *k2 = x == ex0 ? ek0 : ek1, *v2 = x == ex0 ? ev0 : ev1;
+        kz[0] = k2[0] & 0xffff, kz[1] = k2[0] >> 16, kz[2] = k2[1] & 0xffff, kz[3] = k2[1] >> 16;
+        vz[0] = v2[0] & 0xffff, vz[1] = v2[0] >> 16, vz[2] = v2[1] & 0xffff, vz[3] = v2[1] >> 16;
+      } else {
+        append_new_row(p, b, kv, pos_b, lane, kz, vz);
+      }
+      const int r = pos_b & (kTile - 1);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int e = lane + 32 * t;
+        const uint32_t off = (e >> 6) * kHalfTileBytes + swz128(r, (e & 63) >> 3) + (e & 7) * 2;
+        *reinterpret_cast<uint16_t *>(stage + off) = kz[t];
+        *reinterpret_cast<uint16_t *>(stage + 2 * kHalfTileBytes + off) = vz[t];
       }
       __syncwarp();
     }
@@ -377,7 +504,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         }
       }
 
-    if (valid < kTile) fence_proxy_async_smem();  // generic writes above precede the next TMA into this stage
+    if (valid < kTile || holds_new) fence_proxy_async_smem();  // generic writes precede the next TMA here
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
   }
@@ -399,10 +526,8 @@ cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, con
                              int num_workers, cudaStream_t stream) {
   const size_t bytes = attn_smem_bytes(npad, p.B);
   if (npad == 8)
-    attn_splitkv_kernel<1><<<num_workers, kThreadsAttn, bytes, stream>>>(tmK, tmV, p);
-  else
-    attn_splitkv_kernel<2><<<num_workers, kThreadsAttn, bytes, stream>>>(tmK, tmV, p);
-  return cudaGetLastError();
+    return launch_pdl(attn_splitkv_kernel<1>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
+  return launch_pdl(attn_splitkv_kernel<2>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
 }
 
 }  // namespace gqa

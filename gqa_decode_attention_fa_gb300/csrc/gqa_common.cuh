@@ -61,21 +61,28 @@ __host__ __device__ inline bool warp_has_tile(long long i0, long long i1, int c)
 // Kernel parameter blocks -------------------------------------------------------------
 
 struct PrologueParams {
-  const uint16_t *q_new, *k_new, *v_new;   // [B,Hq,d], [B,Hkv,d], [B,Hkv,d]
-  uint16_t *k_cache, *v_cache;
-  const int32_t *page_table, *seq_lens, *positions;
-  const uint16_t *q_norm_w, *k_norm_w;     // [d] or null
+  const uint16_t *q_new;                    // [B,Hq,d]
+  const int32_t *seq_lens, *positions;
+  const uint16_t *q_norm_w;                 // [d] or null
+  const double2 *rope_tab;                  // [max_seq][64] (cos, sin) of pos * theta^(-2i/d)
   uint16_t *q_rot;                          // workspace [B*Hkv][npad rows][128] (swizzled image)
   uint32_t *err;
-  int B, Hq, Hkv, G, npad;
-  int paged, max_seq, max_blocks, num_blocks;
-  long long num_rows;
+  int B, Hq, Hkv, G, npad, max_seq;
   double eps;
+};
+
+struct RopeTableParams {
+  double2 *rope_tab;                        // [max_seq][64]
+  int max_seq;
   double inv_freq[kHeadDim / 2];            // theta^(-2i/d), i < 64
 };
 
 struct AttnParams {
-  const int32_t *seq_lens, *page_table;
+  const int32_t *seq_lens, *page_table, *positions;
+  const uint16_t *k_new, *v_new;            // [B,Hkv,d] new-token rows (appended by this kernel)
+  uint16_t *k_cache, *v_cache;              // the caches (the TMA maps view the same memory)
+  const uint16_t *k_norm_w;                 // [d] or null
+  const double2 *rope_tab;                  // [max_seq][64] (cos, sin)
   const uint16_t *q_rot;                    // [B*Hkv][npad][128] swizzled
   float *part_o;                            // [slots * kConsumerWarps * G][128]
   float *part_ml;                           // [slots * kConsumerWarps * G][2]  (m in log2 units, l)
@@ -83,6 +90,7 @@ struct AttnParams {
   uint32_t *err;
   int B, Hkv, G;
   int paged, max_seq, max_blocks, num_blocks;
+  double eps;
   float scale_log2;                         // log2(e) / sqrt(d)
 };
 
@@ -129,6 +137,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (clock64() - t0 > kSpinLimitCycles) return false;
   }
   return true;
+}
+
+// Programmatic dependent launch: every kernel of the step is launched so that it may
+// start while the previous kernel in the stream drains; each one waits here before it
+// touches memory an earlier kernel writes, and then lets the next kernel launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

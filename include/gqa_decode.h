@@ -26,6 +26,13 @@
  *     legacy default stream) and never synchronise, except the functions documented
  *     as synchronous.  Two calls that share a plan must not run concurrently (they
  *     share the plan's workspace); order them on one stream.
+ *   - Every kernel is launched with programmatic stream serialization: it may start
+ *     while the previous kernel on the stream drains, and waits (griddepcontrol.wait)
+ *     before it reads anything an earlier kernel may write, so stream order holds.
+ *   - The first call with a given rope_theta (and the first after a different one)
+ *     also launches, on the same stream, the build of the plan's binary64 RoPE table:
+ *     cos/sin(p * theta^(-2i/d)) for every p < max_seq_len (max_seq_len x 1 KiB).
+ *     Make that first call before capturing the step in a CUDA graph.
  *   - Argument errors are reported before anything is launched.  Index errors that can
  *     only be seen on the device (a position outside [0, seq_len), a seq_len outside
  *     [1, max_seq_len], a page id outside the pool) do not fault: the kernels skip the
@@ -87,7 +94,9 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * split-KV workers (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
  * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
  * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
- * workspace once, so no call allocates.
+ * workspace once, so no call allocates.  The workspace holds the rotated queries, the
+ * fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats), the RoPE
+ * table (max_seq_len x 1 KiB) and staging buffers for gqa_decode_attn_host.
  *   desc          : geometry (copied).
  *   seq_lens_host : optional host array [B] of expected lengths used only to size the
  *                   worker count; NULL plans for B sequences of max_seq_len tokens.
@@ -157,23 +166,26 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
                                   float rope_theta, float eps, void *out_host, void *stream);
 
 /*
- * The three steps of gqa_decode_attn as separate launches, for callers that schedule
- * them themselves (and for step-level tests).  They communicate through the plan's
- * workspace and must be issued in this order on one stream.
- *   gqa_prologue: QK-norm + RoPE of q into the workspace, k/v rows into the cache.
- *   gqa_attention_splitkv: reads the rotated q and the cache, writes fp32 partials.
+ * The steps of gqa_decode_attn as separate launches, for callers that schedule them
+ * themselves (and for step-level tests and timing).  They communicate through the plan's
+ * workspace and must be issued in this order on one stream; arguments are those of
+ * gqa_decode_attn, and so are the errors.
+ *   gqa_prologue: QK-norm + RoPE of the new queries into the workspace.
+ *   gqa_attention_splitkv: appends the new k (QK-norm + RoPE) and v rows to the cache and
+ *     runs the split-KV attention over the cache, writing fp32 partials.  It starts
+ *     streaming KV tiles before the preceding prologue has finished (the prologue writes
+ *     no cache row); the page holding a sequence's new token must belong to that sequence
+ *     alone.
  *   gqa_combine: merges the partials into `out`.
- * Arguments and errors as for gqa_decode_attn.
  */
-gqa_status_t gqa_prologue(const gqa_plan_t *plan,
-                          const void *q_new, const void *k_new, const void *v_new,
-                          void *k_cache, void *v_cache, const int32_t *page_table,
-                          const int32_t *seq_lens, const int32_t *positions,
-                          const void *q_norm_w, const void *k_norm_w,
-                          float rope_theta, float eps, void *stream);
-gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_cache,
-                                   const void *v_cache, const int32_t *page_table,
-                                   const int32_t *seq_lens, void *stream);
+gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
+                          const int32_t *positions, const void *q_norm_w, float rope_theta,
+                          float eps, void *stream);
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new,
+                                   const void *v_new, void *k_cache, void *v_cache,
+                                   const int32_t *page_table, const int32_t *seq_lens,
+                                   const int32_t *positions, const void *k_norm_w,
+                                   float rope_theta, float eps, void *stream);
 gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out,
                          void *stream);
 

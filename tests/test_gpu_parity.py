@@ -165,10 +165,7 @@ def test_steps_equal_fused_call():
     w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=11, device="cuda")
     plan, out1 = run_gpu(w)
     out2 = torch.empty_like(out1)
-    plan.prologue(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
-                  w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps)
-    plan.attention_splitkv(w.k_cache, w.v_cache, w.page_table, w.seq_lens)
-    plan.combine(w.seq_lens, out2)
+    plan.run_steps(w, out2)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
