@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
 inputs.  Output: max |err| <= 1e-2 and relative L2 <= 2e-3.  Appended cache rows: bit-exact
-(ties within 2^-40 of a bf16 midpoint excepted, expected zero), every other cache row
-untouched; rotated q: equal bf16 bits except at binary32 rounding ties."""
+(the binary64 computation may differ only within 2^-40 (|y_i| + |y_partner|) of a bf16
+rounding boundary; no such element is expected), every other cache row untouched; rotated
+q: the bf16 rounding of a value within the binary32 error bound of the exact value."""
 import numpy as np
 import pytest
 import torch
@@ -10,8 +11,8 @@ import oracle
 from gqa_decode_attention_fa_gb300 import binding, workloads as wl
 from gqa_decode_attention_fa_gb300.workloads import bits, ints
 
-from _util import (K_MIDPOINT_WINDOW, Q_MIDPOINT_WINDOW, appended_rows, assert_out_close,
-                   check_rounded_rows, oracle_step, rotated_rows)
+from _util import (K_WINDOW, Q_WINDOW, appended_rows, assert_out_close, check_rounded_rows, oracle_step,
+                   rotated_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,12 +44,12 @@ def full_check(w, num_workers=0, what=""):
         r = int(ints(w.page_table)[b, p // 64]) * 64 + p % 64 if w.paged else b * w.max_seq + p
         mask[r] = False
     np.testing.assert_array_equal(kc.reshape(-1, w.Hkv, w.d)[mask], k0.reshape(-1, w.Hkv, w.d)[mask])
-    zk, _ = rotated_rows(w, "k")
-    ties_k = check_rounded_rows(rows_g, rows_o, zk, K_MIDPOINT_WINDOW * np.abs(zk), f"{what} k rows")
-    assert ties_k == 0
+    zk, sk = rotated_rows(w, "k")
+    diff_k = check_rounded_rows(rows_g, rows_o, zk, K_WINDOW * sk, f"{what} k rows")
+    assert diff_k == 0   # binary64: bit-exact in practice
     zq, sq = rotated_rows(w, "q")
-    ties_q = check_rounded_rows(plan.read_q_rot(), ref["q_rot"], zq, Q_MIDPOINT_WINDOW * sq, f"{what} q rows")
-    assert ties_q <= max(4, zq.size // 1000)
+    diff_q = check_rounded_rows(plan.read_q_rot(), ref["q_rot"], zq, Q_WINDOW * sq, f"{what} q rows")
+    assert diff_q <= max(4, zq.size // 1000)
     del k0, v0
     return stats, plan, out
 
@@ -144,6 +145,17 @@ def test_large_scores_and_outliers_are_stable():
     full_check(w, what="outliers")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(40, 8), (24, 2)])
+def test_many_short_segments_per_worker(Hq, Hkv):
+    """Short sequences put many (sequence, KV head) segments into one worker's range, so
+    the query-rotation ring wraps (G <= 8 and G > 8 layouts)."""
+    rng = np.random.default_rng(15)
+    lens = rng.integers(1, 200, size=96).tolist()
+    w = wl.make(96, Hq, Hkv, lens, paged=True, seed=16, device="cuda")
+    full_check(w, what=f"short segments G={Hq // Hkv}")
+    full_check(w, num_workers=7, what=f"short segments G={Hq // Hkv} W=7")
+
+
 def test_max_batch():
     lens = (np.arange(1024) % 97 + 1).tolist()
     w = wl.make(1024, 8, 2, lens, paged=True, seed=10, device="cuda")
@@ -157,15 +169,6 @@ def test_determinism_bitwise():
     plan, out1 = run_gpu(w)
     out2 = torch.empty_like(out1)
     plan.run(w, out2)
-    torch.cuda.synchronize()
-    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
-
-
-def test_steps_equal_fused_call():
-    w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=11, device="cuda")
-    plan, out1 = run_gpu(w)
-    out2 = torch.empty_like(out1)
-    plan.run_steps(w, out2)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
