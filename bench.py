@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 HEADLINE = "qwen3-14b-4k"
 METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_splitkv_traffic.json")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -63,15 +63,15 @@ def hbm_peak():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("decode_step.cu", "gqa_common.cuh", "rowmath.cuh"):
+    for name in ("attention.cu", "gqa_common.cuh", "rowmath.cuh"):
         with open(os.path.join(ROOT, "gqa_decode_attention_fa_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
-    the current kernel source and scales to this workload; else None."""
+    """DRAM bytes per attention launch (read + write) from the committed ncu capture of this
+    workload, if it was taken on the current kernel source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -79,8 +79,8 @@ def recorded_traffic(workload: str):
         return None
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
-    per_kv_byte = d.get("dram_bytes_per_kv_byte")
-    return per_kv_byte
+    rec = d.get("workloads", {}).get(workload)
+    return None if rec is None else int(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -188,7 +188,7 @@ def run_ours(args, rank, world, local):
     outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev) for w in sets[0]]
     stream = torch.cuda.current_stream()
     kv_per_step = algorithmic_kv_bytes(sets[0])
-    launches_per_step = len(sets[0])
+    launches_per_step = 3 * len(sets[0])
 
     def step(k):
         """One decode step through the fused entry point (prologue, attention, combine)."""
@@ -196,12 +196,11 @@ def run_ours(args, rank, world, local):
             plan.run(w, outs[li], stream)
 
     def step_timed(k, ev_pairs):
-        """The same step with CUDA events around each layer's launch (the events cost the
-        overlap of consecutive launches, so this pass gives the kernel's own duration)."""
+        """The same step through the three step entry points with CUDA events around the
+        split-KV attention launch (events between launches cost the overlap of consecutive
+        launches, so this pass gives the attention kernel's own duration)."""
         for li, w in enumerate(sets[k % len(sets)]):
-            ev_pairs[li][0].record(stream)
-            plan.run(w, outs[li], stream)
-            ev_pairs[li][1].record(stream)
+            plan.run_steps(w, outs[li], stream, between=lambda i, li=li: ev_pairs[li][i].record(stream))
 
     barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
     K, W = args.steps, args.warmup
@@ -225,7 +224,7 @@ def run_ours(args, rank, world, local):
         e_end.record(stream)
         torch.cuda.synchronize()
         barrier()
-        # second timed pass: the step kernel's own duration per launch
+        # second timed pass: the attention kernel's own duration per launch
         attn_events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                         for _ in sets[0]] for _ in range(K)]
         for k in range(K):
@@ -275,7 +274,7 @@ def run_ours(args, rank, world, local):
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     kv_per_launch = kv_per_step / len(sets[0])
     achieved = kv_per_launch / (attn_avg_ms * 1e-3) / 1e9
-    per_kv = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload)
     result = {
         "metric": METRIC,
         "value": round(us_step, 3),
@@ -297,16 +296,16 @@ def run_ours(args, rank, world, local):
                    "workers": plan.num_workers, "parallelism": f"replicas x{world}"},
         "kv_bytes_per_step": kv_per_step,
         "kv_gbs": round(kv_per_step / (us_step * 1e-6) / 1e9, 1),
-        "roofline": {"bound": "hbm", "kernel": "decode_step_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "attn_splitkv_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of_8TBs": round(achieved / 8000.0, 4), "avg_launch_us": round(attn_avg_ms * 1e3, 3),
                      "algorithmic_bytes_per_launch": int(kv_per_launch),
-                     "traffic": None if per_kv is None else int(per_kv * kv_per_launch)},
+                     "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
-        "gpu_launches_note": "one fused decode-step kernel per layer (the RoPE table kernel runs once per theta, "
-                             "before the timed region)",
+        "gpu_launches_note": "prologue + split-KV attention + combine per layer (the RoPE table kernel runs once "
+                             "per theta, before the timed region)",
         "clocks": clocks,
     }
     return result, sets

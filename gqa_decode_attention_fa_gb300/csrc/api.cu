@@ -1,10 +1,11 @@
 // C ABI of libgqa_decode.so: plan (split planner + workspace), argument validation, tensor
-// maps and the launch of the fused decode step.
+// maps and the launch sequence prologue -> split-KV attention -> combine.
 #include <math.h>
 #include <string.h>
 
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "launch.h"
 
@@ -16,15 +17,12 @@ struct gqa_plan {
   long long num_rows = 0;
   void *ws = nullptr;
   size_t ws_bytes = 0;
-  uint16_t *q_rot = nullptr;                 // [B, Hq, d] rotated queries of the last step
-  float *part_o = nullptr, *part_ml = nullptr;    // warp partials
-  float *cpart_o = nullptr, *cpart_ml = nullptr;  // CTA partials of shared segments
-  uint32_t *seg_count = nullptr;             // [B * Hkv] arrival tickets
-  uint32_t *err = nullptr;
+  uint16_t *q_rot = nullptr;
+  float *part_o = nullptr, *part_ml = nullptr;
+  uint32_t *prefix = nullptr, *err = nullptr;
   uint16_t *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
   int32_t *st_sl = nullptr, *st_pos = nullptr;
   double2 *rope_tab = nullptr;  // [max_seq_len][64] binary64 (cos, sin) for tab_theta
-  size_t seg_count_bytes = 0;
   mutable bool tab_valid = false;
   mutable float tab_theta = 0.f;
   // tensor maps of the last cache pair seen (re-encoded when the pointers change)
@@ -139,37 +137,54 @@ gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t
   return GQA_OK;
 }
 
-gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
-                      const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
-                      float theta, float eps, void *out, cudaStream_t stream) {
+gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const int32_t *sl, const int32_t *pos,
+                          const void *qw, float theta, float eps, cudaStream_t stream) {
+  gqa_status_t st = ensure_rope_table(plan, theta, stream);
+  if (st != GQA_OK) return st;
+  PrologueParams p;
+  memset(&p, 0, sizeof p);
+  p.q_new = static_cast<const uint16_t *>(q);
+  p.seq_lens = sl;
+  p.positions = pos;
+  p.q_norm_w = static_cast<const uint16_t *>(qw);
+  p.rope_tab = plan->rope_tab;
+  p.q_rot = plan->q_rot;
+  p.err = plan->err;
+  p.B = plan->desc.batch;
+  p.Hq = plan->desc.num_q_heads;
+  p.Hkv = plan->desc.num_kv_heads;
+  p.G = plan->G;
+  p.npad = plan->npad;
+  p.max_seq = plan->desc.max_seq_len;
+  p.eps = static_cast<double>(eps);
+  return launch_prologue(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_attention(const gqa_plan_t *plan, const void *k, const void *v, void *kc, void *vc,
+                           const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *kw, float theta,
+                           float eps, cudaStream_t stream) {
   gqa_status_t st = ensure_rope_table(plan, theta, stream);
   if (st != GQA_OK) return st;
   CUtensorMap tk, tv;
   st = cache_maps(plan, kc, vc, &tk, &tv);
   if (st != GQA_OK) return st;
-  StepParams p;
+  AttnParams p;
   memset(&p, 0, sizeof p);
-  p.q_new = static_cast<const uint16_t *>(q);
+  p.seq_lens = sl;
+  p.page_table = pt;
+  p.positions = pos;
   p.k_new = static_cast<const uint16_t *>(k);
   p.v_new = static_cast<const uint16_t *>(v);
   p.k_cache = static_cast<uint16_t *>(kc);
   p.v_cache = static_cast<uint16_t *>(vc);
-  p.page_table = pt;
-  p.seq_lens = sl;
-  p.positions = pos;
-  p.q_norm_w = static_cast<const uint16_t *>(qw);
   p.k_norm_w = static_cast<const uint16_t *>(kw);
   p.rope_tab = plan->rope_tab;
-  p.out = static_cast<uint16_t *>(out);
   p.q_rot = plan->q_rot;
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
-  p.cpart_o = plan->cpart_o;
-  p.cpart_ml = plan->cpart_ml;
-  p.seg_count = plan->seg_count;
+  p.prefix = plan->prefix;
   p.err = plan->err;
   p.B = plan->desc.batch;
-  p.Hq = plan->desc.num_q_heads;
   p.Hkv = plan->desc.num_kv_heads;
   p.G = plan->G;
   p.paged = plan->desc.block_size > 0;
@@ -178,7 +193,34 @@ gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, cons
   p.num_blocks = plan->desc.num_cache_blocks;
   p.eps = static_cast<double>(eps);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
-  return launch_step(tk, tv, p, plan->npad, plan->W, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return launch_attention(tk, tv, p, plan->npad, plan->W, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, cudaStream_t stream) {
+  CombineParams p;
+  memset(&p, 0, sizeof p);
+  p.seq_lens = sl;
+  p.prefix = plan->prefix;
+  p.part_o = plan->part_o;
+  p.part_ml = plan->part_ml;
+  p.out = static_cast<uint16_t *>(out);
+  p.B = plan->desc.batch;
+  p.Hq = plan->desc.num_q_heads;
+  p.Hkv = plan->desc.num_kv_heads;
+  p.G = plan->G;
+  p.W = plan->W;
+  p.max_seq = plan->desc.max_seq_len;
+  return launch_combine(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
+                      const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                      float theta, float eps, void *out, cudaStream_t stream) {
+  gqa_status_t st = run_prologue(plan, q, sl, pos, qw, theta, eps, stream);
+  if (st != GQA_OK) return st;
+  st = run_attention(plan, k, v, kc, vc, pt, sl, pos, kw, theta, eps, stream);
+  if (st != GQA_OK) return st;
+  return run_combine(plan, sl, out, stream);
 }
 
 }  // namespace
@@ -231,17 +273,15 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
 
   const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
   const long long slots = B * Hkv + p->W;
-  const size_t sz_q = align256(B * Hq * kHeadDim * 2);
+  const size_t sz_q = align256(B * Hkv * p->npad * kHeadDim * 2);
   const size_t sz_o = align256(slots * kConsumerWarps * p->G * kHeadDim * 4);
   const size_t sz_ml = align256(slots * kConsumerWarps * p->G * 2 * 4);
-  const size_t sz_co = align256(slots * p->G * kHeadDim * 4);
-  const size_t sz_cml = align256(slots * p->G * 2 * 4);
-  const size_t sz_cnt = align256(B * Hkv * 4);
+  const size_t sz_pre = align256((B + 1) * 4);
   const size_t sz_err = 256;
   const size_t sz_sq = align256(B * Hq * kHeadDim * 2), sz_skv = align256(B * Hkv * kHeadDim * 2);
   const size_t sz_si = align256(B * 4);
   const size_t sz_tab = align256(static_cast<size_t>(d.max_seq_len) * (kHeadDim / 2) * sizeof(double2));
-  p->ws_bytes = sz_q + sz_o + sz_ml + sz_co + sz_cml + sz_cnt + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_pre + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
   if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -251,10 +291,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->q_rot = reinterpret_cast<uint16_t *>(c); c += sz_q;
   p->part_o = reinterpret_cast<float *>(c); c += sz_o;
   p->part_ml = reinterpret_cast<float *>(c); c += sz_ml;
-  p->cpart_o = reinterpret_cast<float *>(c); c += sz_co;
-  p->cpart_ml = reinterpret_cast<float *>(c); c += sz_cml;
-  p->seg_count = reinterpret_cast<uint32_t *>(c); c += sz_cnt;
-  p->seg_count_bytes = sz_cnt;
+  p->prefix = reinterpret_cast<uint32_t *>(c); c += sz_pre;
   p->err = reinterpret_cast<uint32_t *>(c); c += sz_err;
   p->st_q = reinterpret_cast<uint16_t *>(c); c += sz_sq;
   p->st_out = reinterpret_cast<uint16_t *>(c); c += sz_sq;
@@ -263,8 +300,9 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->rope_tab = reinterpret_cast<double2 *>(c); c += sz_tab;
-  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || step_configure(p->npad, d.batch) != cudaSuccess ||
-      rope_table_configure() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad, d.batch) != cudaSuccess ||
+      configure_small_kernels() != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     cudaFree(p->ws);
     delete p;
@@ -324,14 +362,54 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan, const void *q_new_host
   return GQA_OK;
 }
 
+gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
+                          const int32_t *positions, const void *q_norm_w, float rope_theta, float eps,
+                          void *stream) {
+  if (!plan || !q_new || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_prologue(plan, q_new, seq_lens, positions, q_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new, const void *v_new, void *k_cache,
+                                   void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
+                                   const int32_t *positions, const void *k_norm_w, float rope_theta, float eps,
+                                   void *stream) {
+  if (!plan || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
+  if ((plan->desc.block_size > 0) != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_attention(plan, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, k_norm_w, rope_theta,
+                       eps, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out, void *stream) {
+  if (!plan || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->desc.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  return run_combine(plan, seq_lens, out, static_cast<cudaStream_t>(stream));
+}
+
 gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host) {
   if (!plan || !q_rot_host) return GQA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
-  const size_t bytes = static_cast<size_t>(plan->desc.batch) * plan->desc.num_q_heads * kHeadDim * 2;
+  const int B = plan->desc.batch, Hkv = plan->desc.num_kv_heads, G = plan->G, npad = plan->npad;
+  std::vector<uint16_t> img(static_cast<size_t>(B) * Hkv * npad * kHeadDim);
   if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(q_rot_host, plan->q_rot, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+      cudaMemcpy(img.data(), plan->q_rot, img.size() * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
     return GQA_ERR_CUDA;
+  for (int b = 0; b < B; ++b)
+    for (int kv = 0; kv < Hkv; ++kv)
+      for (int g = 0; g < G; ++g)
+        for (int e = 0; e < kHeadDim; ++e) {
+          const int half = e >> 6, chunk = (e & 63) >> 3, within = e & 7;
+          const size_t off = (static_cast<size_t>(b) * Hkv + kv) * npad * kHeadDim +
+                             (half * npad * 128 + swz128(g, chunk)) / 2 + within;
+          q_rot_host[((static_cast<size_t>(b) * Hkv + kv) * G + g) * kHeadDim + e] = img[off];
+        }
   return GQA_OK;
 }
 
@@ -342,10 +420,7 @@ gqa_status_t gqa_plan_device_errors(const gqa_plan_t *plan, uint32_t *flags, int
   if (cudaDeviceSynchronize() != cudaSuccess ||
       cudaMemcpy(flags, plan->err, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return GQA_ERR_CUDA;
-  // Clearing also resets the arrival tickets, which an aborted step may have left behind.
-  if (clear && (cudaMemset(plan->err, 0, sizeof(uint32_t)) != cudaSuccess ||
-                cudaMemset(plan->seg_count, 0, plan->seg_count_bytes) != cudaSuccess ||
-                cudaDeviceSynchronize() != cudaSuccess))
+  if (clear && (cudaMemset(plan->err, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess))
     return GQA_ERR_CUDA;
   return GQA_OK;
 }

@@ -1,6 +1,6 @@
-// Shared definitions of the decode-step kernels: geometry constants, the split-KV work
-// partition (host and device), kernel parameter blocks and thin inline-PTX wrappers for
-// mbarrier, TMA, ldmatrix, movmatrix and mma.sync.
+// Shared definitions of the decode-attention kernels: geometry constants, the split-KV
+// work partition (host and device), kernel parameter blocks and thin inline-PTX wrappers
+// for mbarrier, TMA / bulk copies, ldmatrix, movmatrix and mma.sync.
 #pragma once
 
 #include <cuda.h>
@@ -34,10 +34,10 @@ constexpr long long kSpinLimitCycles = 4000000000LL;      // ~2 s at 2 GHz
 // Worker w of W owns the contiguous range [T*w/W, T*(w+1)/W) of the T tiles (the
 // contiguous-block placement of ADR-0060 section 2.1 applied to the whole batch), and
 // consumer warp c of that worker takes local tiles i = c, c + kConsumerWarps, ...  The
-// piece of segment seg that worker w processed lives in slot seg + w (its warps' partials
-// in rows (seg + w) * kConsumerWarps + c): as one walks the tiles in order, seg + w
-// strictly increases from one (segment, worker) piece to the next, so slots never
-// collide and B*H_kv + W - 1 slots suffice.
+// partial of (segment seg, worker w, warp c) lives in slot seg + w, row group
+// (seg + w) * kConsumerWarps + c: as one walks the tiles in order, seg + w strictly
+// increases from one (segment, worker) piece to the next, so slots never collide and
+// B*H_kv + W - 1 slots suffice.
 
 __host__ __device__ inline int tiles_of(int L, int max_seq) {
   return (L >= 1 && L <= max_seq) ? (L + kTile - 1) / kTile : 0;
@@ -48,16 +48,6 @@ __host__ __device__ inline long long worker_begin(long long T, int W, int w) {
 // The worker whose range holds tile x (0 <= x < T).
 __host__ __device__ inline int worker_of(long long T, int W, long long x) {
   return (int)(((x + 1) * (long long)W - 1) / T);
-}
-// Does worker w hold any tile?  With W <= T every worker holds at least floor(T/W) >= 1
-// tiles; with W > T each holds zero or one.
-__host__ __device__ inline bool worker_nonempty(long long T, int W, int w) {
-  return W <= T || worker_begin(T, W, w + 1) > worker_begin(T, W, w);
-}
-// Workers holding tiles of the segment [beg, end) (end > beg): all of w0..w1 when W <= T,
-// one per tile otherwise.
-__host__ __device__ inline int workers_of_segment(long long T, int W, long long beg, long long end) {
-  return W <= T ? worker_of(T, W, end - 1) - worker_of(T, W, beg) + 1 : static_cast<int>(end - beg);
 }
 // Does consumer warp c take any local tile index in [i0, i1)?
 __host__ __device__ inline bool warp_has_tile(long long i0, long long i1, int c) {
@@ -70,28 +60,46 @@ __host__ __device__ inline bool warp_has_tile(long long i0, long long i1, int c)
 
 // Kernel parameter blocks -------------------------------------------------------------
 
-struct StepParams {
-  const uint16_t *q_new, *k_new, *v_new;    // [B,Hq,d], [B,Hkv,d], [B,Hkv,d]
-  uint16_t *k_cache, *v_cache;              // the caches (the TMA maps view the same memory)
-  const int32_t *page_table, *seq_lens, *positions;
-  const uint16_t *q_norm_w, *k_norm_w;      // [d] or null
+struct PrologueParams {
+  const uint16_t *q_new;                    // [B,Hq,d]
+  const int32_t *seq_lens, *positions;
+  const uint16_t *q_norm_w;                 // [d] or null
   const double2 *rope_tab;                  // [max_seq][64] (cos, sin) of pos * theta^(-2i/d)
-  uint16_t *out;                            // [B,Hq,d]
-  uint16_t *q_rot;                          // [B,Hq,d] the rotated bf16 queries (diagnostic copy)
-  float *part_o, *part_ml;                  // warp partials [slots * kConsumerWarps * G][128] / [..][2]
-  float *cpart_o, *cpart_ml;                // CTA partials  [slots * G][128] / [..][2]
-  uint32_t *seg_count;                      // [B*Hkv] arrival tickets, zero between calls
+  uint16_t *q_rot;                          // workspace [B*Hkv][npad rows][128] (swizzled image)
   uint32_t *err;
-  int B, Hq, Hkv, G;
-  int paged, max_seq, max_blocks, num_blocks;
+  int B, Hq, Hkv, G, npad, max_seq;
   double eps;
-  float scale_log2;                         // log2(e) / sqrt(d)
 };
 
 struct RopeTableParams {
   double2 *rope_tab;                        // [max_seq][64]
   int max_seq;
   double inv_freq[kHeadDim / 2];            // theta^(-2i/d), i < 64
+};
+
+struct AttnParams {
+  const int32_t *seq_lens, *page_table, *positions;
+  const uint16_t *k_new, *v_new;            // [B,Hkv,d] new-token rows (appended by this kernel)
+  uint16_t *k_cache, *v_cache;              // the caches (the TMA maps view the same memory)
+  const uint16_t *k_norm_w;                 // [d] or null
+  const double2 *rope_tab;                  // [max_seq][64] (cos, sin)
+  const uint16_t *q_rot;                    // [B*Hkv][npad][128] swizzled
+  float *part_o;                            // [slots * kConsumerWarps * G][128]
+  float *part_ml;                           // [slots * kConsumerWarps * G][2]  (m in log2 units, l)
+  uint32_t *prefix;                         // [B+1] written by CTA 0 for the combine
+  uint32_t *err;
+  int B, Hkv, G;
+  int paged, max_seq, max_blocks, num_blocks;
+  double eps;
+  float scale_log2;                         // log2(e) / sqrt(d)
+};
+
+struct CombineParams {
+  const int32_t *seq_lens;
+  const uint32_t *prefix;
+  const float *part_o, *part_ml;
+  uint16_t *out;                            // [B,Hq,d]
+  int B, Hq, Hkv, G, W, max_seq;
 };
 
 // Inline PTX -----------------------------------------------------------------------------

@@ -7,6 +7,9 @@
 
 namespace gqa {
 
+cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
+cudaError_t launch_rope_table(const RopeTableParams &p, cudaStream_t stream);
+
 // Launches `kernel` with programmatic stream serialization (it may begin while the
 // previous kernel in the stream finishes; the kernels order themselves with
 // griddepcontrol.wait).
@@ -26,14 +29,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// The fused decode step (decode_step.cu).
-size_t step_smem_bytes(int npad, int batch);
-cudaError_t step_configure(int npad, int batch);  // dynamic shared-memory limit on the current device
-cudaError_t launch_step(const CUtensorMap &tmK, const CUtensorMap &tmV, const StepParams &p, int npad,
-                        int num_workers, cudaStream_t stream);
+// Dynamic shared memory the split-KV kernel needs for a group padded to npad rows.
+size_t attn_smem_bytes(int npad, int batch);
+// Raises the kernel's dynamic shared-memory limit on the current device.
+cudaError_t attn_configure(int npad, int batch);
+cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
+                             int num_workers, cudaStream_t stream);
 
-// The binary64 RoPE table (rope_table.cu).
-cudaError_t launch_rope_table(const RopeTableParams &p, cudaStream_t stream);
-cudaError_t rope_table_configure();
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+// Gives the prologue, combine and table kernels the attention kernel's shared-memory
+// carveout, so that consecutive kernels of a step never make an SM switch configuration.
+cudaError_t configure_small_kernels();
 
 }  // namespace gqa

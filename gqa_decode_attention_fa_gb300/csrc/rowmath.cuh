@@ -85,12 +85,11 @@ __device__ __forceinline__ void rotate_row_fp64(const uint16_t *x, const uint16_
 
 // The same in binary32 (for query rows, which are not stored): x*w is exact, one rounding
 // for the norm scalar, one fused multiply-add per rotated element, one rounding to bf16.
-// xr holds this lane's four elements of the row (dims lane + 32 t), already loaded.
-__device__ __forceinline__ void rotate_row_fp32_regs(const uint16_t (&xr)[4], const uint16_t *w, float eps,
-                                                     float2 cs0, float2 cs1, int lane, uint16_t (&out)[4]) {
+__device__ __forceinline__ void rotate_row_fp32(const uint16_t *x, const uint16_t *w, float eps, float2 cs0,
+                                                float2 cs1, int lane, uint16_t (&out)[4]) {
   float y[4];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) y[t] = bf16_bits_to_float(xr[t]);
+  for (int t = 0; t < 4; ++t) y[t] = bf16_bits_to_float(x[lane + 32 * t]);
   float r = 1.0f;
   if (w) {
     float ss = 0.f;

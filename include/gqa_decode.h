@@ -1,20 +1,20 @@
 /*
  * gqa_decode.h -- C ABI of the GB300 fused GQA decode-attention library (libgqa_decode.so).
  *
- * One decode step for one new token per sequence, in one kernel launch:
+ * One decode step for one new token per sequence:
  *   1. prologue: per-head QK RMSNorm, then RoPE at the token's position, on q and k;
  *      k (post-RoPE) and v (raw) are appended to the bf16 KV cache at that position
  *      ("Qwen3-14B Optimization", section 2.1 Shape 4 and "Then: buy it" / #796, where
  *      QK-norm and RoPE are folded into the attention kernel; section 3.3 for the folded
  *      norm reciprocal and the lo/hi RoPE halves; "ADR-0060: AHBM GQA Fused Attention
  *      Kernel (Llama3-70B)", section 0.5.1 preconditions P2-P4: K cached post-RoPE,
- *      V raw, the new row in place before attention reads it).
+ *      V raw, the new row written before attention reads the cache).
  *   2. split-KV attention: the G = H_q / H_kv query heads that share a KV head are
  *      stacked into one tile (ADR-0060 section 5.2, M-fold), the KV cache is streamed in
- *      64-token tiles with an online softmax (ADR-0060 section 3), and each split keeps
+ *      64-token tiles with an online softmax (ADR-0060 section 3), and each split writes
  *      an unnormalised (m, l, O) partial (ADR-0060 sections 0.5.4 and 4).
  *   3. combine: the log-sum-exp merge of the partials, normalised once (ADR-0060
- *      section 4, merge()), done by the CTA that finishes a sequence's KV head last.
+ *      section 4, merge()).
  *
  * Conventions shared by every entry point
  *   - bf16 tensors are passed as pointers to 16-bit storage (IEEE bfloat16 bits).
@@ -26,11 +26,9 @@
  *     legacy default stream) and never synchronise, except the functions documented
  *     as synchronous.  Two calls that share a plan must not run concurrently (they
  *     share the plan's workspace); order them on one stream.
- *   - The step kernel is launched with programmatic stream serialization: it may start
+ *   - Every kernel is launched with programmatic stream serialization: it may start
  *     while the previous kernel on the stream drains, and waits (griddepcontrol.wait)
- *     before it reads any input or the workspace, so stream order holds.
- *   - The page holding a sequence's new token must belong to that sequence alone (no
- *     other sequence of the batch may map it).
+ *     before it reads anything an earlier kernel may write, so stream order holds.
  *   - The first call with a given rope_theta (and the first after a different one)
  *     also launches, on the same stream, the build of the plan's binary64 RoPE table:
  *     cos/sin(p * theta^(-2i/d)) for every p < max_seq_len (max_seq_len x 1 KiB).
@@ -97,9 +95,8 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
  * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
  * workspace once, so no call allocates.  The workspace holds the rotated queries, the
- * fp32 (m, l, O) partials ((B*H_kv + workers) * 7 * G rows of 130 floats), the arrival
- * tickets, the RoPE table (max_seq_len x 1 KiB) and staging buffers for
- * gqa_decode_attn_host.
+ * fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats), the RoPE
+ * table (max_seq_len x 1 KiB) and staging buffers for gqa_decode_attn_host.
  *   desc          : geometry (copied).
  *   seq_lens_host : optional host array [B] of expected lengths used only to size the
  *                   worker count; NULL plans for B sequences of max_seq_len tokens.
@@ -169,18 +166,40 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
                                   float rope_theta, float eps, void *out_host, void *stream);
 
 /*
- * gqa_plan_read_q_rot -- copies the rotated, bf16-rounded queries of the last step out of
- * the workspace into host memory as [B, H_q, d] bf16.  Synchronous (waits for the
- * device).  For tests and debugging.
+ * The steps of gqa_decode_attn as separate launches, for callers that schedule them
+ * themselves (and for step-level tests and timing).  They communicate through the plan's
+ * workspace and must be issued in this order on one stream; arguments are those of
+ * gqa_decode_attn, and so are the errors.
+ *   gqa_prologue: QK-norm + RoPE of the new queries into the workspace.
+ *   gqa_attention_splitkv: appends the new k (QK-norm + RoPE) and v rows to the cache and
+ *     runs the split-KV attention over the cache, writing fp32 partials.  It starts
+ *     streaming KV tiles before the preceding prologue has finished (the prologue writes
+ *     no cache row); the page holding a sequence's new token must belong to that sequence
+ *     alone.
+ *   gqa_combine: merges the partials into `out`.
+ */
+gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
+                          const int32_t *positions, const void *q_norm_w, float rope_theta,
+                          float eps, void *stream);
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new,
+                                   const void *v_new, void *k_cache, void *v_cache,
+                                   const int32_t *page_table, const int32_t *seq_lens,
+                                   const int32_t *positions, const void *k_norm_w,
+                                   float rope_theta, float eps, void *stream);
+gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out,
+                         void *stream);
+
+/*
+ * gqa_plan_read_q_rot -- copies the rotated, bf16-rounded queries of the last prologue
+ * out of the workspace into host memory as [B, H_q, d] bf16.  Synchronous (waits for
+ * the device).  For tests and debugging.
  */
 gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host);
 
 /*
  * gqa_plan_device_errors -- reads the plan's device error word (GQA_DEVERR_* bits set by
- * any call since the last clear) into *flags, and clears it when `clear` is non-zero;
- * clearing also resets the per-(sequence, KV head) arrival tickets of the combine, which
- * a step that gave up (GQA_DEVERR_TIMEOUT) can leave behind.  Synchronous: waits for all
- * work on the plan's device.
+ * any call since the last clear) into *flags, and clears it when `clear` is non-zero.
+ * Synchronous: waits for all work on the plan's device.
  */
 gqa_status_t gqa_plan_device_errors(const gqa_plan_t *plan, uint32_t *flags, int clear);
 

@@ -173,6 +173,16 @@ def test_determinism_bitwise():
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
+def test_steps_equal_fused_call():
+    """The three step entry points in order give the fused call's output bit for bit."""
+    w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=11, device="cuda")
+    plan, out1 = run_gpu(w)
+    out2 = torch.empty_like(out1)
+    plan.run_steps(w, out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
 def test_host_buffer_entry_point_matches_device_call():
     w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=12, device="cuda")
     plan, out1 = run_gpu(w)
