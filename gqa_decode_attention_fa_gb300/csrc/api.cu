@@ -300,7 +300,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->rope_tab = reinterpret_cast<double2 *>(c); c += sz_tab;
-  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad, d.batch) != cudaSuccess ||
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad) != cudaSuccess ||
       configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();

@@ -516,8 +516,8 @@ size_t attn_smem_bytes(int npad, int batch) {
   return 1024 + static_cast<size_t>(kStages) * stage + 16 * kStages + 4 * (batch + 1) + 4 * batch;
 }
 
-cudaError_t attn_configure(int npad, int batch) {
-  const int bytes = static_cast<int>(attn_smem_bytes(npad, batch));
+cudaError_t attn_configure(int npad) {
+  const int bytes = static_cast<int>(attn_smem_bytes(npad, GQA_MAX_BATCH));
   if (npad == 8) return cudaFuncSetAttribute(attn_splitkv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return cudaFuncSetAttribute(attn_splitkv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }

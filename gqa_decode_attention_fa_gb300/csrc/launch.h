@@ -31,8 +31,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Dynamic shared memory the split-KV kernel needs for a group padded to npad rows.
 size_t attn_smem_bytes(int npad, int batch);
-// Raises the kernel's dynamic shared-memory limit on the current device.
-cudaError_t attn_configure(int npad, int batch);
+// Raises the kernel's dynamic shared-memory limit on the current device to what a launch
+// of the largest supported batch needs.  The limit is per function, not per plan, so it
+// never depends on one plan's batch: a plan made later for a smaller batch must not lower
+// it under an earlier plan's launches.
+cudaError_t attn_configure(int npad);
 cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
                              int num_workers, cudaStream_t stream);
 

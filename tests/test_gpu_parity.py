@@ -164,6 +164,22 @@ def test_max_batch():
 
 # ------------------------------------------------------------------ API behaviour
 
+def test_plans_of_different_batches_coexist():
+    """A plan made after another one, for a smaller batch, leaves the first one usable (the
+    attention kernel's shared-memory limit is set for the largest batch, not per plan)."""
+    big = wl.make(256, 8, 2, (np.arange(256) % 97 + 1).tolist(), paged=True, seed=13, device="cuda")
+    small = wl.make(1, 8, 2, [100], paged=False, seed=14, device="cuda")
+    ref = oracle_step(big)
+    plan_big = binding.Plan.for_workload(big)
+    plan_small = binding.Plan.for_workload(small)
+    out = torch.empty((big.B, big.Hq, big.d), dtype=torch.bfloat16, device="cuda")
+    plan_big.run(big, out)
+    torch.cuda.synchronize()
+    assert plan_big.device_errors() == 0
+    assert_out_close(out, ref["out"], "B=256 after a B=1 plan")
+    run_gpu(small, plan=plan_small)
+
+
 def test_determinism_bitwise():
     w = wl.named("qwen3-14b-ragged", device="cuda")
     plan, out1 = run_gpu(w)
