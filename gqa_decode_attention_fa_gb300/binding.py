@@ -17,7 +17,9 @@ import numpy as np
 
 from . import build as _build
 
-GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE = range(5)
+(GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE,
+ GQA_ERR_SCRATCH_LIMIT) = range(6)
+STATIC_SCRATCH_BYTES = 32 << 20
 DEVERR_POSITION, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 HEADER = os.path.join(_build.ROOT, "include", "gqa_decode.h")
 
@@ -72,11 +74,12 @@ def load(build: bool = True):
         lib.gqa_plan_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
         lib.gqa_partition_describe.argtypes = [P, I, I, I, I, P]
         lib.gqa_partition_describe.restype = ctypes.c_longlong
+        lib.gqa_decode_attn_static.argtypes = [ctypes.POINTER(PlanDesc)] + step[1:] + [P, P, P]
         lib.gqa_status_string.argtypes = [I]
         lib.gqa_status_string.restype = ctypes.c_char_p
         for name in ("gqa_plan_create", "gqa_plan_destroy", "gqa_decode_attn", "gqa_decode_attn_host",
                      "gqa_prologue", "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
-                     "gqa_plan_device_errors"):
+                     "gqa_plan_device_errors", "gqa_decode_attn_static"):
             getattr(lib, name).restype = I
         _lib = lib
     return _lib
@@ -134,6 +137,29 @@ def partition_describe(seq_lens, num_kv_heads: int, max_seq_len: int, num_worker
     if T < 0:
         raise ValueError("bad partition arguments")
     return int(T), rng
+
+
+def decode_attn_static(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, q_new, k_new, v_new,
+                       k_cache, v_cache, page_table, seq_lens, positions, q_norm_w, k_norm_w, rope_theta: float,
+                       eps: float, out, *, block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128,
+                       num_workers: int = 0, device: int = 0, device_errors=None, stream=None):
+    """One decode step through gqa_decode_attn_static: no plan, no device allocation; the
+    workspace is the library's fixed static scratch of the device.  `device_errors` is an
+    optional int32/uint32 device tensor of one element the kernels OR error bits into."""
+    desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                    int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device))
+    _check(load().gqa_decode_attn_static(
+        ctypes.byref(desc), _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache),
+        _dptr(page_table), _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta),
+        float(eps), _dptr(out), _dptr(device_errors), _stream(stream)), "gqa_decode_attn_static")
+
+
+def decode_attn_static_workload(w, out, *, num_workers: int = 0, device: int = 0, device_errors=None, stream=None):
+    """gqa_decode_attn_static on a workload's tensors (see workloads.Workload)."""
+    decode_attn_static(w.B, w.Hq, w.Hkv, w.max_seq, w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table,
+                       w.seq_lens, w.positions, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out,
+                       block_size=w.block_size, num_cache_blocks=w.num_blocks, num_workers=num_workers,
+                       device=device, device_errors=device_errors, stream=stream)
 
 
 class Plan:

@@ -33,24 +33,6 @@ struct gqa_plan {
 
 namespace {
 
-// Runs the calling thread on `dev` for the guard's lifetime.
-struct DeviceGuard {
-  int prev = -1;
-  bool ok = true;
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev) != cudaSuccess) {
-      ok = false;
-      prev = -1;
-      return;
-    }
-    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
-  }
-  ~DeviceGuard() {
-    int cur = -1;
-    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-  }
-};
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -224,6 +206,69 @@ gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, cons
 }
 
 }  // namespace
+
+namespace gqa {
+
+gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay) {
+  if (d.batch < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.max_seq_len < 1 || d.num_workers < 0 ||
+      d.block_size < 0)
+    return GQA_ERR_INVALID_ARG;
+  if (d.head_dim != GQA_HEAD_DIM || d.num_q_heads % d.num_kv_heads != 0 ||
+      d.num_q_heads / d.num_kv_heads > GQA_MAX_GROUP || d.batch > GQA_MAX_BATCH ||
+      (d.block_size != 0 && d.block_size != GQA_BLOCK_SIZE))
+    return GQA_ERR_UNSUPPORTED;
+  const bool paged = d.block_size > 0;
+  if (paged && d.num_cache_blocks < 1) return GQA_ERR_INVALID_ARG;
+  const long long B = d.batch, Hkv = d.num_kv_heads;
+  const long long max_blocks = (d.max_seq_len + kTile - 1) / kTile;
+  const long long num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile : B * d.max_seq_len;
+  if (num_rows > 0x7fffffffLL - kTile) return GQA_ERR_UNSUPPORTED;
+  if (B * Hkv * max_blocks > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  StepLayout l;
+  l.G = d.num_q_heads / d.num_kv_heads;
+  l.npad = l.G <= 8 ? 8 : 16;
+  l.max_blocks = static_cast<int>(max_blocks);
+  l.num_rows = num_rows;
+  l.W = d.num_workers > 0 ? d.num_workers : plan_workers(num_sms, B * Hkv * max_blocks);
+  const long long slots = B * Hkv + l.W;
+  l.tab_bytes = align256(static_cast<size_t>(d.max_seq_len) * (kHeadDim / 2) * sizeof(double2));
+  l.off_q = l.tab_bytes;
+  l.off_o = l.off_q + align256(B * Hkv * l.npad * kHeadDim * 2);
+  l.off_ml = l.off_o + align256(slots * kConsumerWarps * l.G * kHeadDim * 4);
+  l.off_pre = l.off_ml + align256(slots * kConsumerWarps * l.G * 2 * 4);
+  l.off_err = l.off_pre + align256((B + 1) * 4);
+  l.total = l.off_err + 256;
+  *lay = l;
+  return GQA_OK;
+}
+
+gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *base, uint32_t *err,
+                         bool table_ready, const void *q, const void *k, const void *v, void *kc, void *vc,
+                         const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                         float theta, float eps, void *out, cudaStream_t stream) {
+  if (!base || !err) return GQA_ERR_INVALID_ARG;
+  gqa_plan_t plan;
+  plan.desc = d;
+  plan.G = lay.G;
+  plan.npad = lay.npad;
+  plan.W = lay.W;
+  plan.max_blocks = lay.max_blocks;
+  plan.num_rows = lay.num_rows;
+  char *c = static_cast<char *>(base);
+  plan.rope_tab = reinterpret_cast<double2 *>(c);
+  plan.q_rot = reinterpret_cast<uint16_t *>(c + lay.off_q);
+  plan.part_o = reinterpret_cast<float *>(c + lay.off_o);
+  plan.part_ml = reinterpret_cast<float *>(c + lay.off_ml);
+  plan.prefix = reinterpret_cast<uint32_t *>(c + lay.off_pre);
+  plan.err = err;
+  plan.tab_valid = table_ready;
+  plan.tab_theta = theta;
+  gqa_status_t st = check_step_args(&plan, q, k, v, kc, vc, pt, sl, pos, theta, eps, out);
+  if (st != GQA_OK) return st;
+  return run_step(&plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, out, stream);
+}
+
+}  // namespace gqa
 
 extern "C" {
 
@@ -445,6 +490,7 @@ const char *gqa_status_string(gqa_status_t status) {
     case GQA_ERR_UNSUPPORTED: return "unsupported geometry";
     case GQA_ERR_CUDA: return "CUDA error";
     case GQA_ERR_WORKSPACE: return "workspace allocation failed";
+    case GQA_ERR_SCRATCH_LIMIT: return "geometry needs more than the fixed static scratch";
   }
   return "unknown status";
 }

@@ -41,6 +41,46 @@ cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, con
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
+// Runs the calling thread on `dev` for the guard's lifetime.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      prev = -1;
+      return;
+    }
+    if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// Workspace of one decode step run without a plan: byte offsets of its regions from a
+// 256-byte-aligned base.  The RoPE table comes first, so that its place does not depend on
+// the batch geometry and a table built by one call stays usable by the next.
+struct StepLayout {
+  int G = 0, npad = 0, W = 0, max_blocks = 0;
+  long long num_rows = 0;
+  size_t tab_bytes = 0, off_q = 0, off_o = 0, off_ml = 0, off_pre = 0, off_err = 0, total = 0;
+};
+
+// Checks `d` as gqa_plan_create does (except the device index) and lays out its workspace;
+// the worker count is d.num_workers, else one per SM up to B * H_kv * ceil(max_seq/64).
+gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay);
+
+// One decode step (prologue -> split-KV attention -> combine) on the workspace at `base`,
+// laid out by `lay`, on the current device.  `err` is the device error word the kernels
+// OR into; `table_ready` says the table at `base` already holds cos/sin for rope_theta
+// at every position below d.max_seq_len (else the call rebuilds it first).
+gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *base, uint32_t *err,
+                         bool table_ready, const void *q, const void *k, const void *v, void *kc, void *vc,
+                         const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                         float theta, float eps, void *out, cudaStream_t stream);
+
 // Gives the prologue, combine and table kernels the attention kernel's shared-memory
 // carveout, so that consecutive kernels of a step never make an SM switch configuration.
 cudaError_t configure_small_kernels();

@@ -62,7 +62,9 @@ typedef enum gqa_status {
     GQA_ERR_INVALID_ARG = 1,   /* a NULL pointer, a bad size, or an inconsistent argument */
     GQA_ERR_UNSUPPORTED = 2,   /* a geometry outside the supported set above */
     GQA_ERR_CUDA = 3,          /* a CUDA runtime call or a kernel launch failed */
-    GQA_ERR_WORKSPACE = 4      /* the plan's workspace could not be allocated */
+    GQA_ERR_WORKSPACE = 4,     /* the plan's workspace could not be allocated */
+    GQA_ERR_SCRATCH_LIMIT = 5  /* gqa_decode_attn_static: the geometry needs more workspace
+                                  than the library's fixed scratch (GQA_STATIC_SCRATCH_BYTES) */
 } gqa_status_t;
 
 /* Bits of the device error word (gqa_plan_device_errors). */
@@ -212,6 +214,59 @@ gqa_status_t gqa_plan_device_errors(const gqa_plan_t *plan, uint32_t *flags, int
  */
 long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int num_kv_heads,
                                  int max_seq_len, int num_workers, long long *worker_range);
+
+/*
+ * gqa_decode_attn_static -- the decode step of gqa_decode_attn without a plan and without
+ * allocating anything.  The source pages define no such call: it exists for callers that
+ * may not allocate device memory at the point of the step -- a serving loop that has
+ * handed all free HBM to its own KV pool, a runtime that forbids a library from owning
+ * device memory, or a step that must not take the allocator's implicit synchronisation.
+ *
+ * The workspace (RoPE table, rotated queries, fp32 partials, batch prefix) lives in one
+ * array of GQA_STATIC_SCRATCH_BYTES (32 MiB) of static device memory inside the library,
+ * one copy per device, which exists for as long as the library is loaded.  Its layout is
+ * that of a plan's workspace without the host staging buffers:
+ *   max_seq_len * 1 KiB                         RoPE table (first, at a fixed place)
+ * + B * H_kv * npad * 256 B                     rotated queries (npad = 8 if G <= 8, else 16)
+ * + (B * H_kv + W) * 6 * G * 520 B              fp32 (m, l, O) partials
+ * + 4 * (B + 1) B                               batch tile prefix
+ * each rounded up to 256 bytes, plus 256; W = desc->num_workers, or when 0 the SM count
+ * capped at B * H_kv * ceil(max_seq_len / 64).  A geometry that needs more is rejected
+ * with GQA_ERR_SCRATCH_LIMIT before anything is launched; use a plan for it.  (For example
+ * B = 32, H_q = 40, H_kv = 8, max_seq_len = 8192 needs about 15 MiB; max_seq_len = 131072
+ * does not fit whatever the batch.)
+ *
+ *   desc       the geometry, as for gqa_plan_create (desc->device is the device the call
+ *              runs on); it is read during the call only.
+ *   q_new ... out, stream    as for gqa_decode_attn.
+ *   device_errors            optional device pointer to a uint32 the kernels OR the
+ *              GQA_DEVERR_* bits into; the caller owns it and clears it.  NULL sends them
+ *              to a word in the scratch that nothing reads.
+ *
+ * Set-up: the first call on a device (per process) looks up the scratch array's device
+ * address (cudaGetSymbolAddress, with that device current), which may load the library's
+ * device code, and raises the kernels' shared-memory limits.  Make that first call before
+ * any stream capture, e.g. once at start-up.  Each call with a rope_theta other than the
+ * last call's on the device, or a max_seq_len above it, first rebuilds the RoPE table in
+ * the scratch on `stream` (max_seq_len x 1 KiB of writes).
+ *
+ * Sharing: every call on a device uses the same scratch.  Nothing in it has to start at
+ * zero (each region is written by the call before it is read), but calls that overlap on
+ * the device -- on different streams, or from threads that do not order their streams --
+ * race on it and give wrong results.  Order all calls of a device on one stream (or
+ * through events).  Host-side bookkeeping is guarded by a mutex.
+ *
+ * Errors: those of gqa_plan_create (GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED) and of
+ * gqa_decode_attn, GQA_ERR_SCRATCH_LIMIT, and GQA_ERR_CUDA when the set-up fails.
+ */
+#define GQA_STATIC_SCRATCH_BYTES (32u << 20)
+gqa_status_t gqa_decode_attn_static(const gqa_plan_desc_t *desc,
+                                    const void *q_new, const void *k_new, const void *v_new,
+                                    void *k_cache, void *v_cache, const int32_t *page_table,
+                                    const int32_t *seq_lens, const int32_t *positions,
+                                    const void *q_norm_w, const void *k_norm_w,
+                                    float rope_theta, float eps, void *out,
+                                    uint32_t *device_errors, void *stream);
 
 /* Static description of a status code. */
 const char *gqa_status_string(gqa_status_t status);
