@@ -67,8 +67,7 @@ def load(build: bool = True):
         step = [P, P, P, P, P, P, P, P, P, P, P, F, F]
         lib.gqa_decode_attn.argtypes = step + [P, P]
         lib.gqa_decode_attn_host.argtypes = step + [P, P]
-        lib.gqa_prologue.argtypes = [P, P, P, P, P, F, F, P]
-        lib.gqa_attention_splitkv.argtypes = [P, P, P, P, P, P, P, P, P, F, F, P]
+        lib.gqa_attention_splitkv.argtypes = [P, P, P, P, P, P, P, P, P, P, P, F, F, P]
         lib.gqa_combine.argtypes = [P, P, P, P]
         lib.gqa_plan_read_q_rot.argtypes = [P, P]
         lib.gqa_plan_device_errors.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), I]
@@ -78,7 +77,7 @@ def load(build: bool = True):
         lib.gqa_status_string.argtypes = [I]
         lib.gqa_status_string.restype = ctypes.c_char_p
         for name in ("gqa_plan_create", "gqa_plan_destroy", "gqa_decode_attn", "gqa_decode_attn_host",
-                     "gqa_prologue", "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
+                     "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
                      "gqa_plan_device_errors", "gqa_decode_attn_static"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -223,16 +222,12 @@ class Plan:
             _hptr(seq_lens), _hptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
             _hptr(out), _stream(stream)), "gqa_decode_attn_host")
 
-    def prologue(self, q_new, seq_lens, positions, q_norm_w, rope_theta: float, eps: float, stream=None):
-        _check(self._lib.gqa_prologue(self._h, _dptr(q_new), _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w),
-                                      float(rope_theta), float(eps), _stream(stream)), "gqa_prologue")
-
-    def attention_splitkv(self, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, k_norm_w,
-                          rope_theta: float, eps: float, stream=None):
+    def attention_splitkv(self, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w,
+                          k_norm_w, rope_theta: float, eps: float, stream=None):
         _check(self._lib.gqa_attention_splitkv(
-            self._h, _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
-            _dptr(seq_lens), _dptr(positions), _dptr(k_norm_w), float(rope_theta), float(eps), _stream(stream)),
-            "gqa_attention_splitkv")
+            self._h, _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache), _dptr(page_table),
+            _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
+            _stream(stream)), "gqa_attention_splitkv")
 
     def combine(self, seq_lens, out, stream=None):
         _check(self._lib.gqa_combine(self._h, _dptr(seq_lens), _dptr(out), _stream(stream)), "gqa_combine")
@@ -255,13 +250,12 @@ class Plan:
                          w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out, stream)
 
     def run_steps(self, w, out, stream=None, between=None):
-        """The same step as three separate launches; between(i) is called after launch i
-        (0: prologue, 1: attention) -- e.g. to record CUDA events around the attention."""
-        self.prologue(w.q_new, w.seq_lens, w.positions, w.q_norm_w, w.rope_theta, w.eps, stream)
+        """The same step as its two launches; between(i) is called before (i = 0) and
+        after (i = 1) the attention launch -- e.g. to record CUDA events around it."""
         if between:
             between(0)
-        self.attention_splitkv(w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
-                               w.k_norm_w, w.rope_theta, w.eps, stream)
+        self.attention_splitkv(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens,
+                               w.positions, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, stream)
         if between:
             between(1)
         self.combine(w.seq_lens, out, stream)

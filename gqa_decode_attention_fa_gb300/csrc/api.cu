@@ -1,11 +1,10 @@
 // C ABI of libgqa_decode.so: plan (split planner + workspace), argument validation, tensor
-// maps and the launch sequence prologue -> split-KV attention -> combine.
+// maps and the launch sequence split-KV attention (with the prologue folded in) -> combine.
 #include <math.h>
 #include <string.h>
 
 #include <mutex>
 #include <new>
-#include <vector>
 
 #include "launch.h"
 
@@ -13,16 +12,18 @@ using namespace gqa;
 
 struct gqa_plan {
   gqa_plan_desc_t desc;
-  int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0;
+  int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0, combine_split = 1;
   long long num_rows = 0;
   void *ws = nullptr;
   size_t ws_bytes = 0;
   uint16_t *q_rot = nullptr;
   float *part_o = nullptr, *part_ml = nullptr;
-  uint32_t *prefix = nullptr, *err = nullptr;
+  uint32_t *err = nullptr;
   uint16_t *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
   int32_t *st_sl = nullptr, *st_pos = nullptr;
-  double2 *rope_tab = nullptr;  // [max_seq_len][64] binary64 (cos, sin) for tab_theta
+  // [max_seq_len][64] double-word (cos_hi, sin_hi, cos_lo, sin_lo) for tab_theta, followed
+  // by the same rounded to binary32 ([max_seq_len][64] float2)
+  float4 *rope_tab = nullptr;
   mutable bool tab_valid = false;
   mutable float tab_theta = 0.f;
   // tensor maps of the last cache pair seen (re-encoded when the pointers change)
@@ -67,6 +68,14 @@ bool make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Bytes of the two RoPE tables of a max_seq-token capacity.
+size_t rope_tables_bytes(int max_seq) {
+  return align256(static_cast<size_t>(max_seq) * (kHeadDim / 2) * (sizeof(float4) + sizeof(float2)));
+}
+const float2 *rope_tab32_of(const gqa_plan_t *plan) {
+  return reinterpret_cast<const float2 *>(plan->rope_tab + static_cast<size_t>(plan->desc.max_seq_len) * 64);
+}
+
 // The split planner: one worker CTA per SM (the kernel holds ~210 KiB of shared memory,
 // so one CTA fits an SM), never more workers than tiles.  Workers take equal contiguous
 // tile ranges, so the count needs no per-length tuning beyond this clamp.
@@ -77,6 +86,15 @@ int plan_workers(int num_sms, long long total_tiles) {
 }
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.f; }
+
+// The kernels read and write whole 16-byte chunks of the bf16 tensors (and bulk-prefetch
+// them), and 4-byte words of the int32 ones; NULL passes (optional tensors).
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool device_args_aligned(const void *q, const void *k, const void *v, const void *kc, const void *vc,
+                         const void *qw, const void *kw, const int32_t *pt, const int32_t *sl, const int32_t *pos) {
+  return aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(kc, 16) && aligned(vc, 16) &&
+         aligned(qw, 16) && aligned(kw, 16) && aligned(pt, 4) && aligned(sl, 4) && aligned(pos, 4);
+}
 
 gqa_status_t check_step_args(const gqa_plan_t *plan, const void *q, const void *k, const void *v, const void *kc,
                              const void *vc, const int32_t *pt, const int32_t *sl, const int32_t *pos,
@@ -104,11 +122,14 @@ gqa_status_t cache_maps(const gqa_plan_t *plan, const void *kc, const void *vc, 
   return GQA_OK;
 }
 
-// (Re)builds the plan's RoPE table for `theta` on `stream` when it holds another theta.
-gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t stream) {
+// (Re)builds the plan's RoPE table for `theta` on `stream` when it holds another theta;
+// *rebuilt says whether it launched the build.
+gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t stream, bool *rebuilt) {
+  *rebuilt = false;
   if (plan->tab_valid && plan->tab_theta == theta) return GQA_OK;
   RopeTableParams t;
-  t.rope_tab = plan->rope_tab;
+  t.rope_dw = plan->rope_tab;
+  t.rope_tab32 = const_cast<float2 *>(rope_tab32_of(plan));
   t.max_seq = plan->desc.max_seq_len;
   for (int i = 0; i < kHeadDim / 2; ++i)
     t.inv_freq[i] = pow(static_cast<double>(theta), -2.0 * i / static_cast<double>(kHeadDim));
@@ -116,36 +137,16 @@ gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t
   if (launch_rope_table(t, stream) != cudaSuccess) return GQA_ERR_CUDA;
   plan->tab_valid = true;
   plan->tab_theta = theta;
+  *rebuilt = true;
   return GQA_OK;
 }
 
-gqa_status_t run_prologue(const gqa_plan_t *plan, const void *q, const int32_t *sl, const int32_t *pos,
-                          const void *qw, float theta, float eps, cudaStream_t stream) {
-  gqa_status_t st = ensure_rope_table(plan, theta, stream);
-  if (st != GQA_OK) return st;
-  PrologueParams p;
-  memset(&p, 0, sizeof p);
-  p.q_new = static_cast<const uint16_t *>(q);
-  p.seq_lens = sl;
-  p.positions = pos;
-  p.q_norm_w = static_cast<const uint16_t *>(qw);
-  p.rope_tab = plan->rope_tab;
-  p.q_rot = plan->q_rot;
-  p.err = plan->err;
-  p.B = plan->desc.batch;
-  p.Hq = plan->desc.num_q_heads;
-  p.Hkv = plan->desc.num_kv_heads;
-  p.G = plan->G;
-  p.npad = plan->npad;
-  p.max_seq = plan->desc.max_seq_len;
-  p.eps = static_cast<double>(eps);
-  return launch_prologue(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
-}
-
-gqa_status_t run_attention(const gqa_plan_t *plan, const void *k, const void *v, void *kc, void *vc,
-                           const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *kw, float theta,
-                           float eps, cudaStream_t stream) {
-  gqa_status_t st = ensure_rope_table(plan, theta, stream);
+gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
+                           const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
+                           float theta, float eps, cudaStream_t stream) {
+  if (!device_args_aligned(q, k, v, kc, vc, qw, kw, pt, sl, pos)) return GQA_ERR_INVALID_ARG;
+  bool rebuilt = false;
+  gqa_status_t st = ensure_rope_table(plan, theta, stream, &rebuilt);
   if (st != GQA_OK) return st;
   CUtensorMap tk, tv;
   st = cache_maps(plan, kc, vc, &tk, &tv);
@@ -155,18 +156,21 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *k, const void *v,
   p.seq_lens = sl;
   p.page_table = pt;
   p.positions = pos;
+  p.q_new = static_cast<const uint16_t *>(q);
   p.k_new = static_cast<const uint16_t *>(k);
   p.v_new = static_cast<const uint16_t *>(v);
   p.k_cache = static_cast<uint16_t *>(kc);
   p.v_cache = static_cast<uint16_t *>(vc);
+  p.q_norm_w = static_cast<const uint16_t *>(qw);
   p.k_norm_w = static_cast<const uint16_t *>(kw);
-  p.rope_tab = plan->rope_tab;
+  p.rope_dw = plan->rope_tab;
+  p.rope_tab32 = rope_tab32_of(plan);
   p.q_rot = plan->q_rot;
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
-  p.prefix = plan->prefix;
   p.err = plan->err;
   p.B = plan->desc.batch;
+  p.Hq = plan->desc.num_q_heads;
   p.Hkv = plan->desc.num_kv_heads;
   p.G = plan->G;
   p.paged = plan->desc.block_size > 0;
@@ -175,14 +179,14 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *k, const void *v,
   p.num_blocks = plan->desc.num_cache_blocks;
   p.eps = static_cast<double>(eps);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
-  return launch_attention(tk, tv, p, plan->npad, plan->W, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return launch_attention(tk, tv, p, plan->npad, plan->W, !rebuilt, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, cudaStream_t stream) {
+  if (!aligned(out, 16) || !aligned(sl, 4)) return GQA_ERR_INVALID_ARG;
   CombineParams p;
   memset(&p, 0, sizeof p);
   p.seq_lens = sl;
-  p.prefix = plan->prefix;
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
   p.out = static_cast<uint16_t *>(out);
@@ -192,15 +196,14 @@ gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, c
   p.G = plan->G;
   p.W = plan->W;
   p.max_seq = plan->desc.max_seq_len;
-  return launch_combine(p, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  return launch_combine(p, plan->combine_split, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
                       const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
                       float theta, float eps, void *out, cudaStream_t stream) {
-  gqa_status_t st = run_prologue(plan, q, sl, pos, qw, theta, eps, stream);
-  if (st != GQA_OK) return st;
-  st = run_attention(plan, k, v, kc, vc, pt, sl, pos, kw, theta, eps, stream);
+  if (!aligned(out, 16)) return GQA_ERR_INVALID_ARG;  // checked before anything is launched
+  gqa_status_t st = run_attention(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream);
   if (st != GQA_OK) return st;
   return run_combine(plan, sl, out, stream);
 }
@@ -230,13 +233,13 @@ gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay)
   l.max_blocks = static_cast<int>(max_blocks);
   l.num_rows = num_rows;
   l.W = d.num_workers > 0 ? d.num_workers : plan_workers(num_sms, B * Hkv * max_blocks);
+  l.combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, l.W, num_sms);
   const long long slots = B * Hkv + l.W;
-  l.tab_bytes = align256(static_cast<size_t>(d.max_seq_len) * (kHeadDim / 2) * sizeof(double2));
+  l.tab_bytes = rope_tables_bytes(d.max_seq_len);
   l.off_q = l.tab_bytes;
-  l.off_o = l.off_q + align256(B * Hkv * l.npad * kHeadDim * 2);
+  l.off_o = l.off_q + align256(B * d.num_q_heads * kHeadDim * 2);
   l.off_ml = l.off_o + align256(slots * kConsumerWarps * l.G * kHeadDim * 4);
-  l.off_pre = l.off_ml + align256(slots * kConsumerWarps * l.G * 2 * 4);
-  l.off_err = l.off_pre + align256((B + 1) * 4);
+  l.off_err = l.off_ml + align256(slots * kConsumerWarps * l.G * 2 * 4);
   l.total = l.off_err + 256;
   *lay = l;
   return GQA_OK;
@@ -253,13 +256,13 @@ gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *
   plan.npad = lay.npad;
   plan.W = lay.W;
   plan.max_blocks = lay.max_blocks;
+  plan.combine_split = lay.combine_split;
   plan.num_rows = lay.num_rows;
   char *c = static_cast<char *>(base);
-  plan.rope_tab = reinterpret_cast<double2 *>(c);
+  plan.rope_tab = reinterpret_cast<float4 *>(c);
   plan.q_rot = reinterpret_cast<uint16_t *>(c + lay.off_q);
   plan.part_o = reinterpret_cast<float *>(c + lay.off_o);
   plan.part_ml = reinterpret_cast<float *>(c + lay.off_ml);
-  plan.prefix = reinterpret_cast<uint32_t *>(c + lay.off_pre);
   plan.err = err;
   plan.tab_valid = table_ready;
   plan.tab_theta = theta;
@@ -315,18 +318,18 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
     total_tiles += d.num_kv_heads * ((L + kTile - 1) / kTile);
   }
   p->W = d.num_workers > 0 ? d.num_workers : plan_workers(sms, total_tiles);
+  p->combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, p->W, sms);
 
   const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
   const long long slots = B * Hkv + p->W;
-  const size_t sz_q = align256(B * Hkv * p->npad * kHeadDim * 2);
+  const size_t sz_q = align256(B * Hq * kHeadDim * 2);
   const size_t sz_o = align256(slots * kConsumerWarps * p->G * kHeadDim * 4);
   const size_t sz_ml = align256(slots * kConsumerWarps * p->G * 2 * 4);
-  const size_t sz_pre = align256((B + 1) * 4);
   const size_t sz_err = 256;
   const size_t sz_sq = align256(B * Hq * kHeadDim * 2), sz_skv = align256(B * Hkv * kHeadDim * 2);
   const size_t sz_si = align256(B * 4);
-  const size_t sz_tab = align256(static_cast<size_t>(d.max_seq_len) * (kHeadDim / 2) * sizeof(double2));
-  p->ws_bytes = sz_q + sz_o + sz_ml + sz_pre + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
+  const size_t sz_tab = rope_tables_bytes(d.max_seq_len);
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
   if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -336,7 +339,6 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->q_rot = reinterpret_cast<uint16_t *>(c); c += sz_q;
   p->part_o = reinterpret_cast<float *>(c); c += sz_o;
   p->part_ml = reinterpret_cast<float *>(c); c += sz_ml;
-  p->prefix = reinterpret_cast<uint32_t *>(c); c += sz_pre;
   p->err = reinterpret_cast<uint32_t *>(c); c += sz_err;
   p->st_q = reinterpret_cast<uint16_t *>(c); c += sz_sq;
   p->st_out = reinterpret_cast<uint16_t *>(c); c += sz_sq;
@@ -344,7 +346,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_v = reinterpret_cast<uint16_t *>(c); c += sz_skv;
   p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
-  p->rope_tab = reinterpret_cast<double2 *>(c); c += sz_tab;
+  p->rope_tab = reinterpret_cast<float4 *>(c); c += sz_tab;
   if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad) != cudaSuccess ||
       configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
@@ -407,27 +409,18 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan, const void *q_new_host
   return GQA_OK;
 }
 
-gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
-                          const int32_t *positions, const void *q_norm_w, float rope_theta, float eps,
-                          void *stream) {
-  if (!plan || !q_new || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
-  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
-  DeviceGuard guard(plan->desc.device);
-  if (!guard.ok) return GQA_ERR_CUDA;
-  return run_prologue(plan, q_new, seq_lens, positions, q_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
-}
-
-gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new, const void *v_new, void *k_cache,
-                                   void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
-                                   const int32_t *positions, const void *k_norm_w, float rope_theta, float eps,
-                                   void *stream) {
-  if (!plan || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !positions) return GQA_ERR_INVALID_ARG;
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *q_new, const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *page_table, const int32_t *seq_lens,
+                                   const int32_t *positions, const void *q_norm_w, const void *k_norm_w,
+                                   float rope_theta, float eps, void *stream) {
+  if (!plan || !q_new || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !positions)
+    return GQA_ERR_INVALID_ARG;
   if ((plan->desc.block_size > 0) != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
   if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
-  return run_attention(plan, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, k_norm_w, rope_theta,
-                       eps, static_cast<cudaStream_t>(stream));
+  return run_attention(plan, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens, positions, q_norm_w,
+                       k_norm_w, rope_theta, eps, static_cast<cudaStream_t>(stream));
 }
 
 gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out, void *stream) {
@@ -441,20 +434,10 @@ gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host) {
   if (!plan || !q_rot_host) return GQA_ERR_INVALID_ARG;
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
-  const int B = plan->desc.batch, Hkv = plan->desc.num_kv_heads, G = plan->G, npad = plan->npad;
-  std::vector<uint16_t> img(static_cast<size_t>(B) * Hkv * npad * kHeadDim);
+  const size_t bytes = static_cast<size_t>(plan->desc.batch) * plan->desc.num_q_heads * kHeadDim * 2;
   if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpy(img.data(), plan->q_rot, img.size() * 2, cudaMemcpyDeviceToHost) != cudaSuccess)
+      cudaMemcpy(q_rot_host, plan->q_rot, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
     return GQA_ERR_CUDA;
-  for (int b = 0; b < B; ++b)
-    for (int kv = 0; kv < Hkv; ++kv)
-      for (int g = 0; g < G; ++g)
-        for (int e = 0; e < kHeadDim; ++e) {
-          const int half = e >> 6, chunk = (e & 63) >> 3, within = e & 7;
-          const size_t off = (static_cast<size_t>(b) * Hkv + kv) * npad * kHeadDim +
-                             (half * npad * 128 + swz128(g, chunk)) / 2 + within;
-          q_rot_host[((static_cast<size_t>(b) * Hkv + kv) * G + g) * kHeadDim + e] = img[off];
-        }
   return GQA_OK;
 }
 

@@ -17,12 +17,20 @@
 //    (bf16 in, fp32 accumulate).  G <= 8 pads to 8 columns (G = 5 wastes 3), not 16 rows.
 //  * P enters the P.V product as bf16 hi + bf16 lo (two mma), so rounding P costs no
 //    accuracy (the bf16 output rounding is then the only sizeable error).
-//  * One CTA per SM: a producer warp streams 64-token K/V tiles (2 x 8 KiB each) with
-//    3-D TMA loads (128-byte swizzle, no multicast) into a 6-stage mbarrier ring, plus
-//    the group's rotated q (2-4 KiB bulk copy); six consumer warps each own one stage,
-//    take every sixth tile, run the recurrence in registers and release the stage.
+//  * One CTA per SM: a producer warp streams 64-token K/V tiles (2 x 16 KiB) with 3-D
+//    TMA loads (128-byte swizzle, no multicast) into a 6-stage mbarrier ring; six
+//    consumer warps each own one stage, take every sixth tile, run the recurrence in
+//    registers and release the stage.
+//  * The decode prologue is folded in ("Qwen3-14B Optimization", section 2.1 Shape 4 and
+//    "Then: buy it" (#796): QK-norm and RoPE inside the attention kernel).  Each consumer
+//    warp builds the rotated queries of the segment it works on straight into its mma B
+//    fragments (binary32, one bf16 rounding), and the warp owning the tile that holds a
+//    sequence's new token computes the rotated key (double-word arithmetic, rounded as the
+//    exact value rounds), appends k and v to the cache and patches them into its tile.  Their inputs are loaded before
+//    the KV stream starts, and both happen before the kernel waits on the preceding
+//    kernel, overlapping the first KV loads.
 //  * Workers own contiguous, equal ranges of the batch's tiles (see gqa_common.cuh), so
-//    ragged batches stay balanced; CTA 0 publishes the batch prefix for the combine.
+//    ragged batches stay balanced.
 #include "launch.h"
 #include "rowmath.cuh"
 
@@ -47,39 +55,140 @@ __device__ __forceinline__ void locate(const uint32_t *pre, const int32_t *Ls, i
   j = within - kv * nt;
 }
 
-// Appends sequence b's new token for KV head kv: k = RoPE_pos(RMSNorm(k_new)) in binary64
-// rounded once to bf16, v = v_new, written to the cache row of position pos (skipped when
-// the page id is out of range; the producer flags that) and returned per lane (dims
-// lane + 32 t) for the shared-memory patch.
-__device__ __forceinline__ void append_new_row(const AttnParams &p, int b, int kv, int pos, int lane,
-                                               uint16_t (&kz)[4], uint16_t (&vz)[4]) {
+// Inputs of one new-token k/v row, loaded ahead of their use (lane l holds dims l + 32 t).
+struct KvRowIn {
+  uint16_t x[4], v[4], w[4];  // bf16 bits of k_new, v_new and k_norm_w (w unused without a norm)
+  float4 cs0, cs1;            // double-word (cos, sin) of pairs l and l + 32
+  long long grow;             // cache row of the new token; -1 when its page is out of range
+};
+
+__device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, int pos, int lane, KvRowIn &in) {
   const long long nrow = (static_cast<long long>(b) * p.Hkv + kv) * kHeadDim;
-  const double2 cs0 = p.rope_tab[static_cast<long long>(pos) * 64 + lane];
-  const double2 cs1 = p.rope_tab[static_cast<long long>(pos) * 64 + lane + 32];
 #pragma unroll
-  for (int t = 0; t < 4; ++t) vz[t] = p.v_new[nrow + lane + 32 * t];
-  rotate_row_fp64(p.k_new + nrow, p.k_norm_w, p.eps, cs0, cs1, lane, kz);
-  long long grow = -1;
+  for (int t = 0; t < 4; ++t) {
+    in.x[t] = p.k_new[nrow + lane + 32 * t];
+    in.v[t] = p.v_new[nrow + lane + 32 * t];
+    in.w[t] = p.k_norm_w ? p.k_norm_w[lane + 32 * t] : uint16_t(0);
+  }
+  in.cs0 = p.rope_dw[static_cast<long long>(pos) * 64 + lane];
+  in.cs1 = p.rope_dw[static_cast<long long>(pos) * 64 + lane + 32];
+  in.grow = -1;
   if (p.paged) {
     const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + pos / kTile];
-    if (pg >= 0 && pg < p.num_blocks) grow = static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
+    if (pg >= 0 && pg < p.num_blocks) in.grow = static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
   } else {
-    grow = static_cast<long long>(b) * p.max_seq + pos;
+    in.grow = static_cast<long long>(b) * p.max_seq + pos;
   }
-  if (grow >= 0) {
+}
+
+// Appends one new token for KV head kv: k = RoPE_pos(RMSNorm(k_new)) rounded once to bf16
+// as its exact value rounds (rotate_row_k), v = v_new, written to the token's cache row
+// (skipped when its page id is out of range; the producer flags that) and returned per
+// lane for the shared-memory patch.
+__device__ __forceinline__ void append_kv_row(const AttnParams &p, int kv, int lane, const KvRowIn &in,
+                                              uint16_t (&kz)[4], uint16_t (&vz)[4]) {
+  rotate_row_k(in.x, in.w, p.k_norm_w != nullptr, static_cast<float>(p.eps), in.cs0, in.cs1, kz);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) vz[t] = in.v[t];
+  if (in.grow >= 0) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      p.k_cache[(grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = kz[t];
-      p.v_cache[(grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = vz[t];
+      p.k_cache[(in.grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = kz[t];
+      p.v_cache[(in.grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = vz[t];
     }
+  }
+}
+
+// The rotated queries of segment (b, kv) -- RoPE_pos(RMSNorm(q_new)) for the G heads
+// kv*G .. kv*G+G-1, in binary32, rounded once to bf16 -- go straight into the B operand of
+// S^T = K_j q^T: lane l holds head 8 nt + l/4 (zero past G) at dims
+// 16 ks + 8 hf + 2 (l mod 4) + {0, 1} in qf[ks][nt][hf].  The RoPE partner of dim i is
+// i + 64, i.e. ks + 4 in the same lane; the norm's sum of squares is completed over the
+// four lanes that share a head.  QIn holds the inputs, loaded ahead of their use.
+template <int NT>
+struct QIn {
+  uint32_t x[NT][8][2];  // q_new bf16 pairs
+  uint32_t w[8][2];      // q_norm_w bf16 pairs at the same dims
+  float4 cs[4][2];       // (cos, sin) of pairs i and i + 1, i = 16 ks + 8 hf + 2 (l mod 4), ks < 4
+};
+
+template <int NT>
+__device__ __forceinline__ void load_q_inputs(const AttnParams &p, int b, int kv, int pos, int lane, QIn<NT> &in) {
+  const int c2 = 2 * (lane & 3);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = 8 * nt + (lane >> 2);
+    const long long row = (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        in.x[nt][ks][hf] = g < p.G ? *reinterpret_cast<const uint32_t *>(p.q_new + row + 16 * ks + 8 * hf + c2) : 0u;
+  }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+      in.w[ks][hf] = p.q_norm_w ? *reinterpret_cast<const uint32_t *>(p.q_norm_w + 16 * ks + 8 * hf + c2) : 0u;
+  const float2 *cs = p.rope_tab32 + static_cast<long long>(pos) * 64;
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) in.cs[ks][hf] = *reinterpret_cast<const float4 *>(cs + 16 * ks + 8 * hf + c2);
+}
+
+// `publish`: also store the rows, as plain [B, H_q, d] rows, to the workspace copy of the
+// rotated queries.
+template <int NT>
+__device__ __forceinline__ void rotate_q(const AttnParams &p, int b, int kv, int lane, bool publish,
+                                         const QIn<NT> &in, uint32_t (&qf)[8][NT][2]) {
+  const int c2 = 2 * (lane & 3);
+  const float eps = static_cast<float>(p.eps);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = 8 * nt + (lane >> 2);
+    const bool real = g < p.G;
+    const long long row = (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim;
+    float ss = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const float a = bf16_lo_to_float(in.x[nt][ks][hf]), c = bf16_hi_to_float(in.x[nt][ks][hf]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(c, c, ss);
+      }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float r = p.q_norm_w ? 1.0f / sqrtf(ss * (1.0f / 128.0f) + eps) : 1.0f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int i = 16 * ks + 8 * hf + c2;  // pairs i, i + 1 (< 64)
+        float y0 = bf16_lo_to_float(in.x[nt][ks][hf]), y1 = bf16_hi_to_float(in.x[nt][ks][hf]);
+        float p0 = bf16_lo_to_float(in.x[nt][ks + 4][hf]), p1 = bf16_hi_to_float(in.x[nt][ks + 4][hf]);
+        if (p.q_norm_w) {
+          y0 *= bf16_lo_to_float(in.w[ks][hf]), y1 *= bf16_hi_to_float(in.w[ks][hf]);
+          p0 *= bf16_lo_to_float(in.w[ks + 4][hf]), p1 *= bf16_hi_to_float(in.w[ks + 4][hf]);
+        }
+        const float4 cs = in.cs[ks][hf];  // (cos_i, sin_i, cos_i+1, sin_i+1)
+        uint32_t lo = pack_bf16(r * fmaf(y0, cs.x, -p0 * cs.y), r * fmaf(y1, cs.z, -p1 * cs.w));
+        uint32_t hi = pack_bf16(r * fmaf(p0, cs.x, y0 * cs.y), r * fmaf(p1, cs.z, y1 * cs.w));
+        if (!real) lo = hi = 0u;
+        qf[ks][nt][hf] = lo;
+        qf[ks + 4][nt][hf] = hi;
+        if (publish && real) {
+          *reinterpret_cast<uint32_t *>(p.q_rot + row + i) = lo;
+          *reinterpret_cast<uint32_t *>(p.q_rot + row + i + 64) = hi;
+        }
+      }
   }
 }
 
 template <int NT>
 struct Cfg {
-  static constexpr int kNpad = 8 * NT;
-  static constexpr int kQBytes = kNpad * 256;
-  static constexpr int kStageBytes = 4 * kHalfTileBytes + kQBytes;
+  static constexpr int kStageBytes = 4 * kHalfTileBytes;
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
 };
 
@@ -96,6 +205,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   uint64_t *empty_bar = full_bar + kStages;
   uint32_t *pre = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [B + 1]
   int32_t *Ls = reinterpret_cast<int32_t *>(pre + p.B + 1);           // [B], 0 if invalid
+  int32_t *Ps = Ls + p.B;                                              // [B], -1 if invalid
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -106,23 +216,40 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+  if (warp == kConsumerWarps && lane < 3) {
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    // Every CTA pulls its share of the new-token rows into L2 while the batch prefix (which
+    // says whose rows it needs) is still being worked out.
+    const uint16_t *src = lane == 0 ? p.q_new : lane == 1 ? p.k_new : p.v_new;
+    const long long bytes = static_cast<long long>(p.B) * (lane == 0 ? p.Hq : p.Hkv) * kHeadDim * 2;
+    const long long chunk = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~15LL;
+    const long long off = chunk * blockIdx.x;
+    if (off < bytes) {
+      const long long len = bytes - off < chunk ? bytes - off : chunk;
+      prefetch_l2(reinterpret_cast<const char *>(src) + off, static_cast<uint32_t>(len));
+    }
   }
-  if (warp == 0) {  // tile prefix over the batch
+  if (warp == 0) {  // tile prefix over the batch; lengths and positions checked once
     uint32_t run = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int b = b0 + lane;
       uint32_t v = 0;
       if (b < p.B) {
-        int L = p.seq_lens[b];
+        int L = p.seq_lens[b], pos = p.positions[b];
         const int nt = tiles_of(L, p.max_seq);
         if (nt == 0) {
           if (blockIdx.x == 0) atomicOr(p.err, GQA_DEVERR_SEQLEN);
           L = 0;
+          pos = -1;
+        } else if (pos < 0 || pos >= L) {
+          if (blockIdx.x == 0) atomicOr(p.err, GQA_DEVERR_POSITION);
+          pos = -1;
         }
         Ls[b] = L;
+        Ps[b] = pos;
         v = static_cast<uint32_t>(nt) * static_cast<uint32_t>(p.Hkv);
       }
 #pragma unroll
@@ -141,6 +268,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const int W = gridDim.x, w = blockIdx.x;
   const long long xs = worker_begin(T, W, w), xe = worker_begin(T, W, w + 1);
   const long long n = xe - xs;
+  const bool producer = warp == kConsumerWarps;
+  const int cw = warp;
 
   // Where tile xs + i lives: its (b, kv) segment and the cache row of its first token (the
   // TMA z coordinate).
@@ -161,20 +290,53 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
   };
 
-  if (warp == kConsumerWarps) {
-    // ---------------------------------------------------------------- producer warp
-    // The first kStages tiles' K/V loads go out before waiting on the prologue: they read
-    // only the caller's cache (the prologue writes none of it; a tile holding a new
-    // token's row is patched in shared memory by its consumer).  The rotated q follows
-    // once the prologue has finished.
-    if (n <= 0) {
-      griddep_wait();
-      griddep_launch_dependents();
-      return;
-    }
-    const int npre = static_cast<int>(n < kStages ? n : kStages);
-    int row = 0, kv = 0, seg = 0;
+  // ---------------------------------------------------------------- early loads
+  // The producer resolves its first tiles' cache rows; each consumer warp loads what the
+  // rotated queries of its first segment and the first new-token row it appends need.
+  // These small reads go out before the KV stream starts; the new-token rows among them
+  // were prefetched into L2 above, so they do not wait behind the stream.
+  const int npre = static_cast<int>(n < kStages ? n : kStages);
+  int row = 0, kv = 0, seg = 0;                 // producer: lane k < npre describes tile k
+  QIn<NT> qin;
+  KvRowIn kin;
+  int q_b = -1, q_kv = 0, q_j = 0;              // consumer: first tile's segment
+  long long ex0 = -1, ex1 = -1;                 // consumer: tiles holding new tokens it appends
+  int ex0_b = 0, ex0_kv = 0, ex1_b = 0, ex1_kv = 0;
+  if (producer) {
     if (lane < npre) describe(lane, row, kv, seg);
+  } else if (n > 0) {
+    if (cw < n) {
+      locate(pre, Ls, p.B, p.Hkv, xs + cw, q_b, q_kv, q_j);
+      if (Ps[q_b] >= 0) load_q_inputs<NT>(p, q_b, q_kv, Ps[q_b], lane, qin);
+    }
+    int b0, kv0, j0, b1, kv1, j1;
+    locate(pre, Ls, p.B, p.Hkv, xs, b0, kv0, j0);
+    locate(pre, Ls, p.B, p.Hkv, xe - 1, b1, kv1, j1);
+    const int seg_first = b0 * p.Hkv + kv0, seg_last = b1 * p.Hkv + kv1;
+    for (int sg = seg_first; sg <= seg_last && ex1 < 0; ++sg) {
+      const int b = sg / p.Hkv, k = sg - b * p.Hkv;
+      const int pos = Ps[b];
+      if (pos < 0) continue;
+      const int nt = (Ls[b] + kTile - 1) / kTile;
+      const long long x_new = static_cast<long long>(pre[b]) + static_cast<long long>(k) * nt + pos / kTile;
+      if (x_new < xs || x_new >= xe || (x_new - xs) % kConsumerWarps != cw) continue;
+      if (ex0 < 0) {
+        ex0 = x_new, ex0_b = b, ex0_kv = k;
+      } else {
+        ex1 = x_new, ex1_b = b, ex1_kv = k;
+      }
+    }
+    if (ex0 >= 0) load_kv_row(p, ex0_b, ex0_kv, Ps[ex0_b], lane, kin);
+  }
+  __syncthreads();
+
+  if (producer) {
+    // ---------------------------------------------------------------- producer warp
+    // The producer reads only the caller's cache and page table, which no kernel of the
+    // step writes before it is read (a tile holding a new token's row is patched in
+    // shared memory by its consumer), so it streams from the start and never waits on the
+    // preceding kernel.
+    if (n <= 0) return;
     for (int k = 0; k < npre; ++k) {
       const int r_row = __shfl_sync(0xffffffffu, row, k), r_kv = __shfl_sync(0xffffffffu, kv, k);
       if (lane == 0) {
@@ -187,17 +349,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, r_kv, r_row);
       }
     }
-    griddep_wait();
-    griddep_launch_dependents();
-    for (int k = 0; k < npre; ++k) {
-      const int r_seg = __shfl_sync(0xffffffffu, seg, k);
-      if (lane == 0) {
-        const uint32_t fb = smem_addr(&full_bar[k]);
-        const uint32_t base = smem_addr(smem + k * C::kStageBytes);
-        bulk_load(base + 4 * kHalfTileBytes, p.q_rot + static_cast<long long>(r_seg) * C::kNpad * kHeadDim,
-                  C::kQBytes, fb);
-      }
-    }
     bool fail = false;
     long long issued = npre;
     for (long long i0 = npre; i0 < n && !fail; i0 += 32) {
@@ -208,7 +359,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       for (int k = 0; k < cnt; ++k) {
         const int r_row = __shfl_sync(0xffffffffu, row, k);
         const int r_kv = __shfl_sync(0xffffffffu, kv, k);
-        const int r_seg = __shfl_sync(0xffffffffu, seg, k);
         const long long ii = i0 + k;
         const int s = static_cast<int>(ii % kStages);
         int ok = 1;
@@ -222,8 +372,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
             tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, r_kv, r_row);
             tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, r_kv, r_row);
             tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, r_kv, r_row);
-            bulk_load(base + 4 * kHalfTileBytes, p.q_rot + static_cast<long long>(r_seg) * C::kNpad * kHeadDim,
-                      C::kQBytes, fb);
             issued = ii + 1;
           }
         }
@@ -243,17 +391,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     return;
   }
 
-  // The rotated q, the appended cache rows and the workspace belong to earlier kernels
-  // until this returns.
-  griddep_wait();
-  griddep_launch_dependents();
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= p.B; i += kConsumerWarps * 32) p.prefix[i] = pre[i];
-  }
-  if (n <= 0) return;
-
   // ------------------------------------------------------------------ consumer warps
-  const int cw = warp;
+  // Until griddep_wait() returns, the preceding kernel in the stream (the previous step's
+  // combine) may still be reading the partials, so those are written only after it; everything before it reads only the caller's inputs and the RoPE table
+  // and writes only the new cache rows, which that kernel does not touch.
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -270,7 +411,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       l_run[nt][jj] = 0.f;
     }
 
-  auto flush = [&](int seg) {
+  auto flush = [&](int sg) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -281,7 +422,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         l_run[nt][jj] = l;
       }
-    const long long base_row = (static_cast<long long>(seg + w) * kConsumerWarps + cw) * p.G;
+    const long long base_row = (static_cast<long long>(sg + w) * kConsumerWarps + cw) * p.G;
 #pragma unroll
     for (int md = 0; md < 8; ++md)
 #pragma unroll
@@ -307,46 +448,58 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
   };
 
+  // The rotated queries of the segment in hand, as mma B fragments (rebuilt whenever the
+  // warp moves to another segment; the warp holding a segment's first tile also publishes
+  // them to the workspace).  A sequence whose position is out of range gets zeros.
+  uint32_t qf[8][NT][2];
+  auto zero_q = [&]() {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) qf[ks][nt][0] = qf[ks][nt][1] = 0u;
+  };
+  int cur_seg = -1;
+  if (q_b >= 0) {
+    if (Ps[q_b] >= 0) rotate_q<NT>(p, q_b, q_kv, lane, q_j == 0, qin, qf);
+    else zero_q();
+    cur_seg = q_b * p.Hkv + q_kv;
+  }
+
   // The new-token k/v rows this warp appends: the first two are computed now, while the
   // first tiles are still in flight, written to the cache and kept packed in registers for
   // the shared-memory patch; any further ones are computed when their tile arrives.
-  long long ex0 = -1, ex1 = -1;
   uint32_t ek0[2] = {0, 0}, ev0[2] = {0, 0}, ek1[2] = {0, 0}, ev1[2] = {0, 0};
-  {
-    int b0, kv0, j0, b1, kv1, j1;
-    locate(pre, Ls, p.B, p.Hkv, xs, b0, kv0, j0);
-    locate(pre, Ls, p.B, p.Hkv, xe - 1, b1, kv1, j1);
-    const int seg_first = b0 * p.Hkv + kv0, seg_last = b1 * p.Hkv + kv1;
-    for (int sg = seg_first; sg <= seg_last && ex1 < 0; ++sg) {
-      const int b = sg / p.Hkv, kv = sg - b * p.Hkv;
-      const int L = Ls[b], pos = p.positions[b];
-      if (L <= 0 || pos < 0 || pos >= L) continue;
-      const int nt = (L + kTile - 1) / kTile;
-      const long long x_new = static_cast<long long>(pre[b]) + static_cast<long long>(kv) * nt + pos / kTile;
-      if (x_new < xs || x_new >= xe || (x_new - xs) % kConsumerWarps != cw) continue;
-      uint16_t kz[4], vz[4];
-      append_new_row(p, b, kv, pos, lane, kz, vz);
-      if (ex0 < 0) {
-        ex0 = x_new;
-        ek0[0] = kz[0] | (uint32_t(kz[1]) << 16), ek0[1] = kz[2] | (uint32_t(kz[3]) << 16);
-        ev0[0] = vz[0] | (uint32_t(vz[1]) << 16), ev0[1] = vz[2] | (uint32_t(vz[3]) << 16);
-      } else {
-        ex1 = x_new;
-        ek1[0] = kz[0] | (uint32_t(kz[1]) << 16), ek1[1] = kz[2] | (uint32_t(kz[3]) << 16);
-        ev1[0] = vz[0] | (uint32_t(vz[1]) << 16), ev1[1] = vz[2] | (uint32_t(vz[3]) << 16);
-      }
-    }
+  if (ex0 >= 0) {
+    uint16_t kz[4], vz[4];
+    append_kv_row(p, ex0_kv, lane, kin, kz, vz);
+    ek0[0] = kz[0] | (uint32_t(kz[1]) << 16), ek0[1] = kz[2] | (uint32_t(kz[3]) << 16);
+    ev0[0] = vz[0] | (uint32_t(vz[1]) << 16), ev0[1] = vz[2] | (uint32_t(vz[3]) << 16);
+  }
+  if (ex1 >= 0) {
+    uint16_t kz[4], vz[4];
+    load_kv_row(p, ex1_b, ex1_kv, Ps[ex1_b], lane, kin);
+    append_kv_row(p, ex1_kv, lane, kin, kz, vz);
+    ek1[0] = kz[0] | (uint32_t(kz[1]) << 16), ek1[1] = kz[2] | (uint32_t(kz[3]) << 16);
+    ev1[0] = vz[0] | (uint32_t(vz[1]) << 16), ev1[1] = vz[2] | (uint32_t(vz[3]) << 16);
   }
 
-  int cur_seg = -1;
+  griddep_wait();
+  griddep_launch_dependents();
+
   for (long long i = cw; i < n; i += kConsumerWarps) {
     int b, kv, j;
     locate(pre, Ls, p.B, p.Hkv, xs + i, b, kv, j);
-    const int seg = b * p.Hkv + kv;
-    const int pos_b = p.positions[b];
-    if (seg != cur_seg) {
-      if (cur_seg >= 0) flush(cur_seg);
-      cur_seg = seg;
+    const int sg = b * p.Hkv + kv;
+    const int pos_b = Ps[b];
+    if (sg != cur_seg) {
+      flush(cur_seg);
+      cur_seg = sg;
+      if (pos_b >= 0) {
+        load_q_inputs<NT>(p, b, kv, pos_b, lane, qin);
+        rotate_q<NT>(p, b, kv, lane, j == 0, qin, qf);
+      } else {
+        zero_q();
+      }
     }
     const int s = static_cast<int>(i % kStages);
     const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
@@ -359,7 +512,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     uint8_t *stage = smem + s * C::kStageBytes;
     const uint32_t kLo = smem_addr(stage), kHi = kLo + kHalfTileBytes;
     const uint32_t vLo = kLo + 2 * kHalfTileBytes, vHi = kLo + 3 * kHalfTileBytes;
-    const uint32_t qS = kLo + 4 * kHalfTileBytes;
 
     if (valid < kTile) {
       // Rows past L_b hold whatever the cache holds there; zero the V rows so that
@@ -376,7 +528,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     // The tile holding sequence b's new token: the TMA filled this stage from the cache
     // before the row was appended, so patch the appended k and v rows into it.
-    const bool holds_new = pos_b >= 0 && pos_b < Ls[b] && (pos_b >> 6) == j;
+    const bool holds_new = pos_b >= 0 && (pos_b >> 6) == j;
     if (holds_new) {
       uint16_t kz[4], vz[4];
       const long long x = xs + i;
@@ -385,7 +537,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         kz[0] = k2[0] & 0xffff, kz[1] = k2[0] >> 16, kz[2] = k2[1] & 0xffff, kz[3] = k2[1] >> 16;
         vz[0] = v2[0] & 0xffff, vz[1] = v2[0] >> 16, vz[2] = v2[1] & 0xffff, vz[3] = v2[1] >> 16;
       } else {
-        append_new_row(p, b, kv, pos_b, lane, kz, vz);
+        load_kv_row(p, b, kv, pos_b, lane, kin);
+        append_kv_row(p, kv, lane, kin, kz, vz);
       }
       const int r = pos_b & (kTile - 1);
 #pragma unroll
@@ -397,18 +550,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       }
       __syncwarp();
     }
-
-    // q^T as the B operand: 8 k-steps (16 dims) x NT column tiles of 8 heads.
-    uint32_t qf[8][NT][2];
-#pragma unroll
-    for (int ks2 = 0; ks2 < 4; ++ks2)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int chunk = 4 * ks2 + (lane >> 3);
-        const int g = 8 * nt + (lane & 7);
-        const uint32_t addr = qS + (chunk >> 3) * (C::kNpad * 128) + swz128(g, chunk & 7);
-        ldsm_x4(addr, qf[2 * ks2][nt][0], qf[2 * ks2][nt][1], qf[2 * ks2 + 1][nt][0], qf[2 * ks2 + 1][nt][1]);
-      }
 
     // S^T = K_j q^T : 4 token blocks of 16 x NT head blocks of 8.
     float sacc[4][NT][4];
@@ -512,8 +653,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 }
 
 size_t attn_smem_bytes(int npad, int batch) {
-  const int stage = 4 * kHalfTileBytes + npad * 256;
-  return 1024 + static_cast<size_t>(kStages) * stage + 16 * kStages + 4 * (batch + 1) + 4 * batch;
+  (void)npad;  // the rotated queries live in registers: the stage size does not depend on G
+  const int stage = 4 * kHalfTileBytes;
+  return 1024 + static_cast<size_t>(kStages) * stage + 16 * kStages + 4 * (batch + 1) + 8 * batch;
 }
 
 cudaError_t attn_configure(int npad) {
@@ -523,11 +665,11 @@ cudaError_t attn_configure(int npad) {
 }
 
 cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
-                             int num_workers, cudaStream_t stream) {
+                             int num_workers, bool pdl, cudaStream_t stream) {
   const size_t bytes = attn_smem_bytes(npad, p.B);
   if (npad == 8)
-    return launch_pdl(attn_splitkv_kernel<1>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
-  return launch_pdl(attn_splitkv_kernel<2>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
+    return launch_ex(pdl, attn_splitkv_kernel<1>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
+  return launch_ex(pdl, attn_splitkv_kernel<2>, dim3(num_workers), dim3(kThreadsAttn), bytes, stream, tmK, tmV, p);
 }
 
 }  // namespace gqa

@@ -1,6 +1,6 @@
 // Shared definitions of the decode-attention kernels: geometry constants, the split-KV
 // work partition (host and device), kernel parameter blocks and thin inline-PTX wrappers
-// for mbarrier, TMA / bulk copies, ldmatrix, movmatrix and mma.sync.
+// for mbarrier, TMA copies, ldmatrix, movmatrix and mma.sync.
 #pragma once
 
 #include <cuda.h>
@@ -60,35 +60,26 @@ __host__ __device__ inline bool warp_has_tile(long long i0, long long i1, int c)
 
 // Kernel parameter blocks -------------------------------------------------------------
 
-struct PrologueParams {
-  const uint16_t *q_new;                    // [B,Hq,d]
-  const int32_t *seq_lens, *positions;
-  const uint16_t *q_norm_w;                 // [d] or null
-  const double2 *rope_tab;                  // [max_seq][64] (cos, sin) of pos * theta^(-2i/d)
-  uint16_t *q_rot;                          // workspace [B*Hkv][npad rows][128] (swizzled image)
-  uint32_t *err;
-  int B, Hq, Hkv, G, npad, max_seq;
-  double eps;
-};
-
 struct RopeTableParams {
-  double2 *rope_tab;                        // [max_seq][64]
+  float4 *rope_dw;                          // [max_seq][64] (cos_hi, sin_hi, cos_lo, sin_lo)
+  float2 *rope_tab32;                       // [max_seq][64] (cos, sin) rounded to binary32
   int max_seq;
   double inv_freq[kHeadDim / 2];            // theta^(-2i/d), i < 64
 };
 
 struct AttnParams {
   const int32_t *seq_lens, *page_table, *positions;
+  const uint16_t *q_new;                    // [B,Hq,d] new-token queries (rotated by this kernel)
   const uint16_t *k_new, *v_new;            // [B,Hkv,d] new-token rows (appended by this kernel)
   uint16_t *k_cache, *v_cache;              // the caches (the TMA maps view the same memory)
-  const uint16_t *k_norm_w;                 // [d] or null
-  const double2 *rope_tab;                  // [max_seq][64] (cos, sin)
-  const uint16_t *q_rot;                    // [B*Hkv][npad][128] swizzled
+  const uint16_t *q_norm_w, *k_norm_w;      // [d] or null
+  const float4 *rope_dw;                    // [max_seq][64] (cos, sin) as double-word hi, lo
+  const float2 *rope_tab32;                 // [max_seq][64] (cos, sin) rounded to binary32
+  uint16_t *q_rot;                          // [B,Hq,d] copy of the rotated bf16 queries
   float *part_o;                            // [slots * kConsumerWarps * G][128]
   float *part_ml;                           // [slots * kConsumerWarps * G][2]  (m in log2 units, l)
-  uint32_t *prefix;                         // [B+1] written by CTA 0 for the combine
   uint32_t *err;
-  int B, Hkv, G;
+  int B, Hq, Hkv, G;
   int paged, max_seq, max_blocks, num_blocks;
   double eps;
   float scale_log2;                         // log2(e) / sqrt(d)
@@ -96,7 +87,6 @@ struct AttnParams {
 
 struct CombineParams {
   const int32_t *seq_lens;
-  const uint32_t *prefix;
   const float *part_o, *part_ml;
   uint16_t *out;                            // [B,Hq,d]
   int B, Hq, Hkv, G, W, max_seq;
@@ -163,12 +153,10 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-// Plain (untiled) bulk copy global -> shared; 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

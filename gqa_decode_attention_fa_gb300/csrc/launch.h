@@ -7,15 +7,14 @@
 
 namespace gqa {
 
-cudaError_t launch_prologue(const PrologueParams &p, cudaStream_t stream);
 cudaError_t launch_rope_table(const RopeTableParams &p, cudaStream_t stream);
 
-// Launches `kernel` with programmatic stream serialization (it may begin while the
-// previous kernel in the stream finishes; the kernels order themselves with
-// griddepcontrol.wait).
+// Launches `kernel`, with programmatic stream serialization when `pdl` is set (it may
+// begin while the previous kernel in the stream finishes; the kernels order themselves
+// with griddepcontrol.wait), else in plain stream order.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args &&...args) {
+cudaError_t launch_ex(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -25,8 +24,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  return launch_ex(true, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
 }
 
 // Dynamic shared memory the split-KV kernel needs for a group padded to npad rows.
@@ -36,10 +40,16 @@ size_t attn_smem_bytes(int npad, int batch);
 // never depends on one plan's batch: a plan made later for a smaller batch must not lower
 // it under an earlier plan's launches.
 cudaError_t attn_configure(int npad);
+// The split-KV attention kernel.  It reads the caller's inputs and the RoPE table before
+// waiting on the preceding kernel, so it is launched in plain stream order (`pdl` false)
+// when the preceding kernel may write any of them (a RoPE table rebuild).
 cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
-                             int num_workers, cudaStream_t stream);
+                             int num_workers, bool pdl, cudaStream_t stream);
 
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+// The combine: split 0 runs one CTA per (sequence, KV head) segment, split 4, 2 or 1 that
+// many CTAs per query head; combine_split picks it from the geometry and worker count.
+int combine_split(int batch, int num_q_heads, int num_kv_heads, int num_workers, int num_sms);
+cudaError_t launch_combine(const CombineParams &p, int split, cudaStream_t stream);
 
 // Runs the calling thread on `dev` for the guard's lifetime.
 struct DeviceGuard {
@@ -63,25 +73,26 @@ struct DeviceGuard {
 // 256-byte-aligned base.  The RoPE table comes first, so that its place does not depend on
 // the batch geometry and a table built by one call stays usable by the next.
 struct StepLayout {
-  int G = 0, npad = 0, W = 0, max_blocks = 0;
+  int G = 0, npad = 0, W = 0, max_blocks = 0, combine_split = 1;
   long long num_rows = 0;
-  size_t tab_bytes = 0, off_q = 0, off_o = 0, off_ml = 0, off_pre = 0, off_err = 0, total = 0;
+  size_t tab_bytes = 0, off_q = 0, off_o = 0, off_ml = 0, off_err = 0, total = 0;
 };
 
 // Checks `d` as gqa_plan_create does (except the device index) and lays out its workspace;
 // the worker count is d.num_workers, else one per SM up to B * H_kv * ceil(max_seq/64).
 gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay);
 
-// One decode step (prologue -> split-KV attention -> combine) on the workspace at `base`,
-// laid out by `lay`, on the current device.  `err` is the device error word the kernels
-// OR into; `table_ready` says the table at `base` already holds cos/sin for rope_theta
-// at every position below d.max_seq_len (else the call rebuilds it first).
+// One decode step (split-KV attention with the prologue folded in -> combine) on the
+// workspace at `base`, laid out by `lay`, on the current device.  `err` is the device
+// error word the kernels OR into; `table_ready` says the table at `base` already holds
+// cos/sin for rope_theta at every position below d.max_seq_len (else the call rebuilds it
+// first).
 gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *base, uint32_t *err,
                          bool table_ready, const void *q, const void *k, const void *v, void *kc, void *vc,
                          const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
                          float theta, float eps, void *out, cudaStream_t stream);
 
-// Gives the prologue, combine and table kernels the attention kernel's shared-memory
+// Gives the combine and table kernels the attention kernel's shared-memory
 // carveout, so that consecutive kernels of a step never make an SM switch configuration.
 cudaError_t configure_small_kernels();
 

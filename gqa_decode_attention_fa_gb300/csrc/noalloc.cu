@@ -5,13 +5,13 @@
 // memory when they run the step: a serving loop that has given every free byte of HBM to
 // its own KV pool (a cudaMalloc there would fail), a host runtime that does not let a
 // library own device memory, or a step that must not pay the allocator's implicit
-// synchronisation.  It runs the same three kernels as gqa_decode_attn; only the place of
+// synchronisation.  It runs the same kernels as gqa_decode_attn; only the place of
 // the workspace differs.
 //
 // The array is one per device (the runtime gives every device its own copy of a
 // __device__ variable) and lives while the library is loaded.  Each call lays out its
-// workspace in it from offset 0 (RoPE table first, then rotated queries, partials, batch
-// prefix), so all calls on a device share it: they must not overlap on the device.  No
+// workspace in it from offset 0 (RoPE tables first, then rotated queries and partials),
+// so all calls on a device share it: they must not overlap on the device.  No
 // region has to start at zero -- every one is written by the call before it is read --
 // and the device error word is the caller's (or a scratch word nobody reads), so the
 // array is never cleared.
@@ -26,7 +26,7 @@ namespace {
 static_assert(GQA_STATIC_SCRATCH_BYTES % 256 == 0, "scratch size must keep 256-byte regions");
 
 // Per-device bookkeeping of the scratch: its device address once looked up, and which
-// RoPE table (theta, rows) its first bytes hold.
+// RoPE tables (theta, capacity in positions) its first bytes hold.
 struct ScratchState {
   bool ready = false;
   void *base = nullptr;
@@ -93,12 +93,13 @@ extern "C" gqa_status_t gqa_decode_attn_static(const gqa_plan_desc_t *desc, cons
   st = set_up(s);
   if (st != GQA_OK) return st;
   uint32_t *err = device_errors ? device_errors : reinterpret_cast<uint32_t *>(static_cast<char *>(s.base) + lay.off_err);
-  const bool table_ready = s.tab_valid && s.tab_theta == rope_theta && s.tab_rows >= d.max_seq_len;
+  // The binary32 table follows the binary64 one, so its place depends on max_seq_len:
+  // reuse the tables only for the same theta and the same capacity.
+  const bool table_ready = s.tab_valid && s.tab_theta == rope_theta && s.tab_rows == d.max_seq_len;
   st = run_step_at(d, lay, s.base, err, table_ready, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens,
                    positions, q_norm_w, k_norm_w, rope_theta, eps, out, static_cast<cudaStream_t>(stream));
   if (st == GQA_OK) {
-    // the table now holds this theta for rows < max_seq_len; the regions after it may
-    // have overwritten any rows beyond
+    // the tables now hold this theta for a max_seq_len capacity
     s.tab_valid = true;
     s.tab_theta = rope_theta;
     s.tab_rows = d.max_seq_len;

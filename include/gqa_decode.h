@@ -8,36 +8,47 @@
  *      QK-norm and RoPE are folded into the attention kernel; section 3.3 for the folded
  *      norm reciprocal and the lo/hi RoPE halves; "ADR-0060: AHBM GQA Fused Attention
  *      Kernel (Llama3-70B)", section 0.5.1 preconditions P2-P4: K cached post-RoPE,
- *      V raw, the new row written before attention reads the cache).
+ *      V raw, the new row seen by attention).
  *   2. split-KV attention: the G = H_q / H_kv query heads that share a KV head are
  *      stacked into one tile (ADR-0060 section 5.2, M-fold), the KV cache is streamed in
  *      64-token tiles with an online softmax (ADR-0060 section 3), and each split writes
  *      an unnormalised (m, l, O) partial (ADR-0060 sections 0.5.4 and 4).
  *   3. combine: the log-sum-exp merge of the partials, normalised once (ADR-0060
  *      section 4, merge()).
+ * Steps 1 and 2 run in one kernel (the prologue folded into the attention kernel, as
+ * the pages do); step 3 is a second kernel.
  *
  * Conventions shared by every entry point
  *   - bf16 tensors are passed as pointers to 16-bit storage (IEEE bfloat16 bits).
  *   - Device pointers must be device-accessible on the plan's device; all device
- *     tensors are dense, row-major, with the shapes stated, and 16-byte aligned.
+ *     tensors are dense, row-major, with the shapes stated; bf16 tensors 16-byte aligned,
+ *     int32 ones 4-byte aligned (else GQA_ERR_INVALID_ARG, before anything is launched).
  *   - The caller owns every tensor.  The library writes only `out` (or the host
  *     output buffer), the B new cache rows, and its own plan workspace.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
  *     legacy default stream) and never synchronise, except the functions documented
  *     as synchronous.  Two calls that share a plan must not run concurrently (they
  *     share the plan's workspace); order them on one stream.
- *   - Every kernel is launched with programmatic stream serialization: it may start
- *     while the previous kernel on the stream drains, and waits (griddepcontrol.wait)
- *     before it reads anything an earlier kernel may write, so stream order holds.
+ *   - Kernels are launched with programmatic stream serialization: a kernel may start
+ *     while the previous kernel on the stream drains.  The attention kernel reads its
+ *     inputs (q/k/v_new, seq_lens, positions, page table, norm weights, the cache)
+ *     before it waits (griddepcontrol.wait) on that kernel, and writes the workspace
+ *     only after; the combine waits before it reads anything.  So the kernel launched
+ *     immediately before a step must not write the step's inputs if it triggers
+ *     programmatic completion early (kernels launched without programmatic dependent
+ *     launch, the usual case, never do).  After a RoPE table rebuild the attention kernel
+ *     is launched in plain stream order.
  *   - The first call with a given rope_theta (and the first after a different one)
- *     also launches, on the same stream, the build of the plan's binary64 RoPE table:
- *     cos/sin(p * theta^(-2i/d)) for every p < max_seq_len (max_seq_len x 1 KiB).
+ *     also launches, on the same stream, the build of the plan's RoPE tables:
+ *     cos/sin(p * theta^(-2i/d)) for every p < max_seq_len in binary64 and rounded to
+ *     binary32 (max_seq_len x 1.5 KiB).
  *     Make that first call before capturing the step in a CUDA graph.
  *   - Argument errors are reported before anything is launched.  Index errors that can
- *     only be seen on the device (a position outside [0, seq_len), a seq_len outside
- *     [1, max_seq_len], a page id outside the pool) do not fault: the kernels skip the
- *     offending sequence, write zeros for its output, and set a bit in the plan's
- *     device error word (gqa_plan_device_errors).
+ *     only be seen on the device do not fault; the kernels set a bit in the plan's
+ *     device error word (gqa_plan_device_errors) and contain the damage to the offending
+ *     sequence: a seq_len outside [1, max_seq_len] gives zeros for its output; a position
+ *     outside [0, seq_len) appends nothing and attends with a zero query; a page id
+ *     outside the pool reads that page as zeros and appends nothing there.
  *
  * Supported geometry: head_dim == 128, H_q % H_kv == 0, 1 <= G <= 16, batch <= 1024,
  * paged cache with 64-token blocks or a contiguous per-sequence cache.
@@ -96,9 +107,9 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * split-KV workers (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
  * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
  * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
- * workspace once, so no call allocates.  The workspace holds the rotated queries, the
- * fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats), the RoPE
- * table (max_seq_len x 1 KiB) and staging buffers for gqa_decode_attn_host.
+ * workspace once, so no call allocates.  The workspace holds a copy of the rotated
+ * queries, the fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats),
+ * the RoPE tables (max_seq_len x 1.5 KiB) and staging buffers for gqa_decode_attn_host.
  *   desc          : geometry (copied).
  *   seq_lens_host : optional host array [B] of expected lengths used only to size the
  *                   worker count; NULL plans for B sequences of max_seq_len tokens.
@@ -168,33 +179,35 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
                                   float rope_theta, float eps, void *out_host, void *stream);
 
 /*
- * The steps of gqa_decode_attn as separate launches, for callers that schedule them
+ * The two launches of gqa_decode_attn, separately, for callers that schedule them
  * themselves (and for step-level tests and timing).  They communicate through the plan's
  * workspace and must be issued in this order on one stream; arguments are those of
  * gqa_decode_attn, and so are the errors.
- *   gqa_prologue: QK-norm + RoPE of the new queries into the workspace.
- *   gqa_attention_splitkv: appends the new k (QK-norm + RoPE) and v rows to the cache and
- *     runs the split-KV attention over the cache, writing fp32 partials.  It starts
- *     streaming KV tiles before the preceding prologue has finished (the prologue writes
- *     no cache row); the page holding a sequence's new token must belong to that sequence
- *     alone.
+ *   gqa_attention_splitkv: the prologue and the split-KV attention in one kernel.  Its
+ *     consumer warps apply QK-norm + RoPE to the new queries (into registers, with a copy
+ *     to the workspace), append the new k (QK-norm + RoPE) and v rows to the cache, and
+ *     run the split-KV attention over the cache, writing fp32 partials.  It reads its
+ *     inputs and streams KV tiles before the preceding kernel in the stream has finished
+ *     (it waits for that kernel only before writing the workspace's partials), so the
+ *     inputs must not be written by an immediately preceding kernel that triggers
+ *     programmatic completion early; the page holding a sequence's new token must belong
+ *     to that sequence alone.
  *   gqa_combine: merges the partials into `out`.
  */
-gqa_status_t gqa_prologue(const gqa_plan_t *plan, const void *q_new, const int32_t *seq_lens,
-                          const int32_t *positions, const void *q_norm_w, float rope_theta,
-                          float eps, void *stream);
-gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *k_new,
-                                   const void *v_new, void *k_cache, void *v_cache,
-                                   const int32_t *page_table, const int32_t *seq_lens,
-                                   const int32_t *positions, const void *k_norm_w,
+gqa_status_t gqa_attention_splitkv(const gqa_plan_t *plan, const void *q_new,
+                                   const void *k_new, const void *v_new,
+                                   void *k_cache, void *v_cache, const int32_t *page_table,
+                                   const int32_t *seq_lens, const int32_t *positions,
+                                   const void *q_norm_w, const void *k_norm_w,
                                    float rope_theta, float eps, void *stream);
 gqa_status_t gqa_combine(const gqa_plan_t *plan, const int32_t *seq_lens, void *out,
                          void *stream);
 
 /*
- * gqa_plan_read_q_rot -- copies the rotated, bf16-rounded queries of the last prologue
- * out of the workspace into host memory as [B, H_q, d] bf16.  Synchronous (waits for
- * the device).  For tests and debugging.
+ * gqa_plan_read_q_rot -- copies the rotated, bf16-rounded queries of the last step out of
+ * the workspace into host memory as [B, H_q, d] bf16 (rows of sequences with an invalid
+ * length or position are left as they were).  Synchronous (waits for the device).  For
+ * tests and debugging.
  */
 gqa_status_t gqa_plan_read_q_rot(const gqa_plan_t *plan, uint16_t *q_rot_host);
 
@@ -222,18 +235,17 @@ long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int nu
  * handed all free HBM to its own KV pool, a runtime that forbids a library from owning
  * device memory, or a step that must not take the allocator's implicit synchronisation.
  *
- * The workspace (RoPE table, rotated queries, fp32 partials, batch prefix) lives in one
+ * The workspace (RoPE tables, rotated queries, fp32 partials) lives in one
  * array of GQA_STATIC_SCRATCH_BYTES (32 MiB) of static device memory inside the library,
  * one copy per device, which exists for as long as the library is loaded.  Its layout is
  * that of a plan's workspace without the host staging buffers:
- *   max_seq_len * 1 KiB                         RoPE table (first, at a fixed place)
- * + B * H_kv * npad * 256 B                     rotated queries (npad = 8 if G <= 8, else 16)
+ *   max_seq_len * 1.5 KiB                       RoPE tables (binary64 and binary32, first)
+ * + B * H_q * 256 B                             rotated queries
  * + (B * H_kv + W) * 6 * G * 520 B              fp32 (m, l, O) partials
- * + 4 * (B + 1) B                               batch tile prefix
  * each rounded up to 256 bytes, plus 256; W = desc->num_workers, or when 0 the SM count
  * capped at B * H_kv * ceil(max_seq_len / 64).  A geometry that needs more is rejected
  * with GQA_ERR_SCRATCH_LIMIT before anything is launched; use a plan for it.  (For example
- * B = 32, H_q = 40, H_kv = 8, max_seq_len = 8192 needs about 15 MiB; max_seq_len = 131072
+ * B = 32, H_q = 40, H_kv = 8, max_seq_len = 8192 needs about 18 MiB; max_seq_len = 131072
  * does not fit whatever the batch.)
  *
  *   desc       the geometry, as for gqa_plan_create (desc->device is the device the call
@@ -246,9 +258,9 @@ long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int nu
  * Set-up: the first call on a device (per process) looks up the scratch array's device
  * address (cudaGetSymbolAddress, with that device current), which may load the library's
  * device code, and raises the kernels' shared-memory limits.  Make that first call before
- * any stream capture, e.g. once at start-up.  Each call with a rope_theta other than the
- * last call's on the device, or a max_seq_len above it, first rebuilds the RoPE table in
- * the scratch on `stream` (max_seq_len x 1 KiB of writes).
+ * any stream capture, e.g. once at start-up.  Each call with a rope_theta or a max_seq_len
+ * other than the last call's on the device first rebuilds the RoPE tables in the scratch
+ * on `stream` (max_seq_len x 1.5 KiB of writes).
  *
  * Sharing: every call on a device uses the same scratch.  Nothing in it has to start at
  * zero (each region is written by the call before it is read), but calls that overlap on

@@ -58,8 +58,7 @@ def test_null_arguments_are_rejected():
     assert lib.gqa_decode_attn(*args) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_decode_attn_host(*args) == binding.GQA_ERR_INVALID_ARG
     f1, f2 = ctypes.c_float(1e6), ctypes.c_float(1e-6)
-    assert lib.gqa_prologue(None, None, None, None, None, f1, f2, None) == binding.GQA_ERR_INVALID_ARG
-    assert lib.gqa_attention_splitkv(None, None, None, None, None, None, None, None, None, f1, f2,
+    assert lib.gqa_attention_splitkv(None, None, None, None, None, None, None, None, None, None, None, f1, f2,
                                      None) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_combine(None, None, None, None) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_plan_destroy(None) == binding.GQA_OK

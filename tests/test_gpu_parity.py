@@ -255,6 +255,19 @@ def test_host_validation_rejects_bad_arguments():
         plan.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
                          w.q_norm_w, w.k_norm_w, w.rope_theta, float("nan"), out)
     assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    # misaligned device tensors are rejected before anything is launched
+    q_shift = torch.empty(w.q_new.numel() + 1, dtype=torch.bfloat16, device="cuda")[1:].view_as(w.q_new)
+    q_shift.copy_(w.q_new)
+    with pytest.raises(binding.GqaError) as e:
+        plan.decode_attn(q_shift, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    out_shift = torch.empty(out.numel() + 4, dtype=torch.bfloat16, device="cuda")[4:].view_as(out)
+    with pytest.raises(binding.GqaError) as e:
+        plan.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,
+                         w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out_shift)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
     with pytest.raises(binding.GqaError) as e:
         binding.Plan(2, 8, 2, 64, block_size=64, num_cache_blocks=0)
     assert e.value.status == binding.GQA_ERR_INVALID_ARG
