@@ -19,6 +19,7 @@ struct gqa_plan {
   uint16_t *q_rot = nullptr;
   float *part_o = nullptr, *part_ml = nullptr;
   uint32_t *err = nullptr;
+  int2 *spec = nullptr;  // [W][kStages] first tiles of each worker at the previous launch
   uint16_t *st_q = nullptr, *st_k = nullptr, *st_v = nullptr, *st_out = nullptr;
   int32_t *st_sl = nullptr, *st_pos = nullptr;
   // [max_seq_len][64] double-word (cos_hi, sin_hi, cos_lo, sin_lo) for tab_theta, followed
@@ -169,6 +170,7 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k,
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
   p.err = plan->err;
+  p.spec = plan->desc.block_size > 0 ? nullptr : plan->spec;
   p.B = plan->desc.batch;
   p.Hq = plan->desc.num_q_heads;
   p.Hkv = plan->desc.num_kv_heads;
@@ -329,7 +331,8 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   const size_t sz_sq = align256(B * Hq * kHeadDim * 2), sz_skv = align256(B * Hkv * kHeadDim * 2);
   const size_t sz_si = align256(B * 4);
   const size_t sz_tab = rope_tables_bytes(d.max_seq_len);
-  p->ws_bytes = sz_q + sz_o + sz_ml + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab;
+  const size_t sz_spec = align256(static_cast<size_t>(p->W) * kStages * sizeof(int2));
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab + sz_spec;
   if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -347,7 +350,9 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_sl = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->rope_tab = reinterpret_cast<float4 *>(c); c += sz_tab;
-  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || attn_configure(p->npad) != cudaSuccess ||
+  p->spec = reinterpret_cast<int2 *>(c); c += sz_spec;
+  if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || cudaMemset(p->spec, 0xff, sz_spec) != cudaSuccess ||
+      attn_configure(p->npad) != cudaSuccess ||
       configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();

@@ -232,6 +232,22 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       prefetch_l2(reinterpret_cast<const char *>(src) + off, static_cast<uint32_t>(len));
     }
   }
+  if (warp == kConsumerWarps && p.spec && lane < kStages) {
+    // The first tiles this worker streamed at the previous launch: unless the lengths
+    // changed the tile partition (in decode, once every 64 steps of a sequence), they are
+    // its first tiles again, so they are pulled into L2 now, a DRAM round trip before the
+    // partition is known.  A wrong guess costs only the prefetched bytes.  (The host
+    // passes spec for contiguous caches only: with a page table the producer needs one
+    // more small dependent read before its first load, and measured, a stream of
+    // prefetches ahead of it cost more than it saved.)
+    const int2 t = p.spec[blockIdx.x * kStages + lane];
+    if (t.x >= 0) {
+      tma_prefetch_3d(&tmK, 0, t.y, t.x);
+      tma_prefetch_3d(&tmK, 64, t.y, t.x);
+      tma_prefetch_3d(&tmV, 0, t.y, t.x);
+      tma_prefetch_3d(&tmV, 64, t.y, t.x);
+    }
+  }
   if (warp == 0) {  // tile prefix over the batch; lengths and positions checked once
     uint32_t run = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -304,6 +320,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   int ex0_b = 0, ex0_kv = 0, ex1_b = 0, ex1_kv = 0;
   if (producer) {
     if (lane < npre) describe(lane, row, kv, seg);
+    if (p.spec && lane < kStages)
+      p.spec[blockIdx.x * kStages + lane] = lane < npre ? make_int2(row, kv) : make_int2(-1, 0);
   } else if (n > 0) {
     if (cw < n) {
       locate(pre, Ls, p.B, p.Hkv, xs + cw, q_b, q_kv, q_j);

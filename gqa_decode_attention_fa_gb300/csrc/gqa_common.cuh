@@ -76,6 +76,9 @@ struct AttnParams {
   const float4 *rope_dw;                    // [max_seq][64] (cos, sin) as double-word hi, lo
   const float2 *rope_tab32;                 // [max_seq][64] (cos, sin) rounded to binary32
   uint16_t *q_rot;                          // [B,Hq,d] copy of the rotated bf16 queries
+  int2 *spec;                               // [W][kStages] (cache row, KV head) of each worker's
+                                            // first tiles at the previous launch (row < 0: none),
+                                            // or null
   float *part_o;                            // [slots * kConsumerWarps * G][128]
   float *part_ml;                           // [slots * kConsumerWarps * G][2]  (m in log2 units, l)
   uint32_t *err;
@@ -152,6 +155,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+// TMA prefetch of a 3-D tile into L2 (no shared memory, no barrier); out-of-range
+// coordinates are allowed, as for loads.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {

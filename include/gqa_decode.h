@@ -109,7 +109,9 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
  * workspace once, so no call allocates.  The workspace holds a copy of the rotated
  * queries, the fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats),
- * the RoPE tables (max_seq_len x 1.5 KiB) and staging buffers for gqa_decode_attn_host.
+ * the RoPE tables (max_seq_len x 1.5 KiB), the first tiles each worker streamed at the
+ * last call (contiguous caches: prefetched into L2 at the start of the next call) and
+ * staging buffers for gqa_decode_attn_host.
  *   desc          : geometry (copied).
  *   seq_lens_host : optional host array [B] of expected lengths used only to size the
  *                   worker count; NULL plans for B sequences of max_seq_len tokens.

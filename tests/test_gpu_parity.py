@@ -180,6 +180,22 @@ def test_plans_of_different_batches_coexist():
     run_gpu(small, plan=plan_small)
 
 
+def test_plan_reused_across_changed_lengths():
+    """One plan, calls whose lengths (and so the tile partition) change: the first tiles
+    each worker prefetches from the previous call's partition are then wrong guesses, which
+    must cost nothing but time."""
+    w1 = wl.make(2, 40, 8, [3000, 1000], paged=False, max_seq=4096, seed=31, device="cuda")
+    w2 = wl.make(2, 40, 8, [1500, 4000], paged=False, max_seq=4096, seed=32, device="cuda")
+    plan = binding.Plan(2, 40, 8, 4096)
+    for w in (w1, w2, w1):
+        ref = oracle_step(w)
+        out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
+        plan.run(w, out)
+        torch.cuda.synchronize()
+        assert plan.device_errors() == 0
+        assert_out_close(out, ref["out"], f"lengths {ints(w.seq_lens).tolist()}")
+
+
 def test_determinism_bitwise():
     w = wl.named("qwen3-14b-ragged", device="cuda")
     plan, out1 = run_gpu(w)
