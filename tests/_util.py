@@ -16,7 +16,7 @@ REL_L2 = 2e-3
 
 # Rounding acceptance for the appended k rows and the rotated q rows.  A row element is
 # RoPE(RMSNorm(x))_i = r (y_i cos - y_partner sin); its computed value differs from the exact
-# one by at most WINDOW * (|y_i| + |y_partner|) (binary64 k rows: ~2^-50, taken as 2^-40;
+# one by at most WINDOW * (|y_i| + |y_partner|) (double-word k rows: ~2^-44, taken as 2^-40;
 # binary32 q rows: norm scalar, cos/sin rounding and one fma, ~2^-20, taken as 2^-18).  An
 # element is accepted iff its bf16 value is the round-to-nearest-even of some real within
 # that bound of the exact value -- identical bits unless the exact value sits near a rounding

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
 inputs.  Output: max |err| <= 1e-2 and relative L2 <= 2e-3.  Appended cache rows: bit-exact
-(the binary64 computation may differ only within 2^-40 (|y_i| + |y_partner|) of a bf16
+(the double-word computation may differ only within 2^-40 (|y_i| + |y_partner|) of a bf16
 rounding boundary; no such element is expected), every other cache row untouched; rotated
 q: the bf16 rounding of a value within the binary32 error bound of the exact value."""
 import numpy as np
@@ -46,7 +46,7 @@ def full_check(w, num_workers=0, what=""):
     np.testing.assert_array_equal(kc.reshape(-1, w.Hkv, w.d)[mask], k0.reshape(-1, w.Hkv, w.d)[mask])
     zk, sk = rotated_rows(w, "k")
     diff_k = check_rounded_rows(rows_g, rows_o, zk, K_WINDOW * sk, f"{what} k rows")
-    assert diff_k == 0   # binary64: bit-exact in practice
+    assert diff_k == 0   # double-word arithmetic: bit-exact in practice
     zq, sq = rotated_rows(w, "q")
     diff_q = check_rounded_rows(plan.read_q_rot(), ref["q_rot"], zq, Q_WINDOW * sq, f"{what} q rows")
     assert diff_q <= max(4, zq.size // 1000)
