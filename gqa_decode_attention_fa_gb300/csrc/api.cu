@@ -88,6 +88,20 @@ int plan_workers(int num_sms, long long total_tiles) {
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.f; }
 
+// Is host pointer h page-locked memory mapped into the device's address space, 16-byte
+// aligned?  Then *d is its device address.  (Asked on every call: a cached answer could
+// outlive the allocation it describes.)
+bool mapped_host(const void *h, void **d) {
+  cudaPointerAttributes a;
+  *d = nullptr;
+  if (cudaPointerGetAttributes(&a, h) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer &&
+      (reinterpret_cast<uintptr_t>(a.devicePointer) & 15) == 0)
+    *d = a.devicePointer;
+  else
+    cudaGetLastError();
+  return *d != nullptr;
+}
+
 // The kernels read and write whole 16-byte chunks of the bf16 tensors (and bulk-prefetch
 // them), and 4-byte words of the int32 ones; NULL passes (optional tensors).
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -144,7 +158,7 @@ gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t
 
 gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
                            const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
-                           float theta, float eps, cudaStream_t stream) {
+                           float theta, float eps, cudaStream_t stream, bool host_inputs = false) {
   if (!device_args_aligned(q, k, v, kc, vc, qw, kw, pt, sl, pos)) return GQA_ERR_INVALID_ARG;
   bool rebuilt = false;
   gqa_status_t st = ensure_rope_table(plan, theta, stream, &rebuilt);
@@ -170,6 +184,7 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k,
   p.part_o = plan->part_o;
   p.part_ml = plan->part_ml;
   p.err = plan->err;
+  p.inputs_in_host_memory = host_inputs ? 1 : 0;
   p.spec = plan->desc.block_size > 0 ? nullptr : plan->spec;
   p.B = plan->desc.batch;
   p.Hq = plan->desc.num_q_heads;
@@ -203,9 +218,9 @@ gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, c
 
 gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
                       const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
-                      float theta, float eps, void *out, cudaStream_t stream) {
+                      float theta, float eps, void *out, cudaStream_t stream, bool host_inputs = false) {
   if (!aligned(out, 16)) return GQA_ERR_INVALID_ARG;  // checked before anything is launched
-  gqa_status_t st = run_attention(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream);
+  gqa_status_t st = run_attention(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream, host_inputs);
   if (st != GQA_OK) return st;
   return run_combine(plan, sl, out, stream);
 }
@@ -399,6 +414,17 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan, const void *q_new_host
   DeviceGuard guard(plan->desc.device);
   if (!guard.ok) return GQA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Page-locked host buffers are mapped into the device's address space: the kernels then
+  // read the inputs and write the output through the host link directly (NVLink-C2C on a
+  // Grace-Blackwell node), with no staging copies.  Other host memory is copied through
+  // the plan's staging buffers.
+  const void *hp[6] = {q_new_host, k_new_host, v_new_host, seq_lens_host, positions_host, out_host};
+  void *dp[6];
+  bool mapped = true;
+  for (int i = 0; i < 6 && mapped; ++i) mapped = mapped_host(hp[i], &dp[i]);
+  if (mapped)
+    return run_step(plan, dp[0], dp[1], dp[2], k_cache, v_cache, page_table, static_cast<const int32_t *>(dp[3]),
+                    static_cast<const int32_t *>(dp[4]), q_norm_w, k_norm_w, rope_theta, eps, dp[5], s, true);
   const size_t B = plan->desc.batch, Hq = plan->desc.num_q_heads, Hkv = plan->desc.num_kv_heads;
   const size_t bq = B * Hq * kHeadDim * 2, bkv = B * Hkv * kHeadDim * 2, bi = B * 4;
   if (cudaMemcpyAsync(plan->st_q, q_new_host, bq, cudaMemcpyHostToDevice, s) != cudaSuccess ||

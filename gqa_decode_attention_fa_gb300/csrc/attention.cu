@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
+  }
+  if (warp == kConsumerWarps && lane < 3 && !p.inputs_in_host_memory) {
     // Every CTA pulls its share of the new-token rows into L2 while the batch prefix (which
     // says whose rows it needs) is still being worked out.
     const uint16_t *src = lane == 0 ? p.q_new : lane == 1 ? p.k_new : p.v_new;

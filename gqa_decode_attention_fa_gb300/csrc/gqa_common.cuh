@@ -76,6 +76,7 @@ struct AttnParams {
   const float4 *rope_dw;                    // [max_seq][64] (cos, sin) as double-word hi, lo
   const float2 *rope_tab32;                 // [max_seq][64] (cos, sin) rounded to binary32
   uint16_t *q_rot;                          // [B,Hq,d] copy of the rotated bf16 queries
+  int inputs_in_host_memory;                // q/k/v_new, seq_lens, positions are mapped host memory
   int2 *spec;                               // [W][kStages] (cache row, KV head) of each worker's
                                             // first tiles at the previous launch (row < 0: none),
                                             // or null

@@ -166,11 +166,14 @@ gqa_status_t gqa_decode_attn(const gqa_plan_t *plan,
 /*
  * gqa_decode_attn_host -- the same step with the per-step inputs and the output in host
  * memory: q_new, k_new, v_new, seq_lens, positions are read from host buffers and `out`
- * is written to a host buffer, each through one cudaMemcpyAsync on `stream` into or out
+ * is written to a host buffer.  When all six are page-locked (cudaHostAlloc /
+ * cudaHostRegister; mapped into the device's address space) and 16-byte aligned, the
+ * kernels read and write them in place over the host link (NVLink-C2C on Grace-Blackwell)
+ * with no copies; otherwise each goes through one cudaMemcpyAsync on `stream` into or out
  * of the plan's staging area.  The KV caches, the page table and the norm weights stay
- * device-resident (model state).  Shapes as for gqa_decode_attn.  The host output is
- * valid once `stream` has been synchronised; pinned host buffers make the copies
- * asynchronous.  Errors as for gqa_decode_attn.
+ * device-resident (model state).  Shapes as for gqa_decode_attn.  The host buffers must
+ * stay unchanged, and the output is valid, only once `stream` has been synchronised.
+ * Errors as for gqa_decode_attn.
  */
 gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
                                   const void *q_new_host, const void *k_new_host,

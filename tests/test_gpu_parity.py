@@ -215,11 +215,15 @@ def test_steps_equal_fused_call():
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-def test_host_buffer_entry_point_matches_device_call():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_point_matches_device_call(pinned):
+    """Page-locked host buffers are read and written in place by the kernels; pageable ones
+    go through the staging copies.  Both give the device entry point's output bit for bit."""
     w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=12, device="cuda")
     plan, out1 = run_gpu(w)
-    host = {k: getattr(w, k).cpu().pin_memory() for k in ("q_new", "k_new", "v_new", "seq_lens", "positions")}
-    out_h = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory()
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    host = {k: pin(getattr(w, k).cpu()) for k in ("q_new", "k_new", "v_new", "seq_lens", "positions")}
+    out_h = pin(torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16))
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         plan.decode_attn_host(host["q_new"], host["k_new"], host["v_new"], w.k_cache, w.v_cache, w.page_table,
