@@ -77,7 +77,7 @@ const float2 *rope_tab32_of(const gqa_plan_t *plan) {
   return reinterpret_cast<const float2 *>(plan->rope_tab + static_cast<size_t>(plan->desc.max_seq_len) * 64);
 }
 
-// The split planner: one worker CTA per SM (the kernel holds ~210 KiB of shared memory,
+// The split planner: one worker CTA per SM (the kernel holds ~200 KiB of shared memory,
 // so one CTA fits an SM), never more workers than tiles.  Workers take equal contiguous
 // tile ranges, so the count needs no per-length tuning beyond this clamp.
 int plan_workers(int num_sms, long long total_tiles) {

@@ -216,11 +216,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane < 3) {
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
   }
   if (warp == kConsumerWarps && lane < 3 && !p.inputs_in_host_memory) {
     // Every CTA pulls its share of the new-token rows into L2 while the batch prefix (which
@@ -352,10 +350,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   if (producer) {
     // ---------------------------------------------------------------- producer warp
-    // The producer reads only the caller's cache and page table, which no kernel of the
-    // step writes before it is read (a tile holding a new token's row is patched in
-    // shared memory by its consumer), so it streams from the start and never waits on the
-    // preceding kernel.
+    // The producer reads only the cache and the page table.  The preceding step has
+    // finished by the time this kernel starts (the combine between the two launches it
+    // only after waiting for that step's attention kernel), and this step's new rows are
+    // patched into the shared-memory tiles by their consumers, so it streams from the
+    // start and never waits on the preceding kernel.
     if (n <= 0) return;
     for (int k = 0; k < npre; ++k) {
       const int r_row = __shfl_sync(0xffffffffu, row, k), r_kv = __shfl_sync(0xffffffffu, kv, k);
@@ -413,8 +412,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   // ------------------------------------------------------------------ consumer warps
   // Until griddep_wait() returns, the preceding kernel in the stream (the previous step's
-  // combine) may still be reading the partials, so those are written only after it; everything before it reads only the caller's inputs and the RoPE table
-  // and writes only the new cache rows, which that kernel does not touch.
+  // combine) may still be reading the partials, so those are written only after it;
+  // everything before it reads only the caller's inputs and the RoPE table and writes only
+  // the new cache rows, which that kernel does not touch.
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
