@@ -146,6 +146,11 @@ def build_layers(name: str, device: str, l2_bytes: int):
 
     if name == "qwen3-14b-40layer":
         return [[wl.named(name, device=device, layer=l) for l in range(wl.LAYERS_40)]], "inputs > L2 (1 GiB KV per layer)"
+    if name == "qwen3-14b-4k-decode":
+        steps = wl.decode_sweep(device=device)
+        kvb = sum(w.kv_bytes() for w in steps[-1])
+        return steps, (f"inputs > L2 ({kvb / 2**20:.0f} MiB KV over {len(steps[-1])} layers); the {len(steps)} "
+                       f"autoregressive steps repeat (each rewrites the rows it appended)")
     w = wl.named(name, device=device)
     kvb = w.kv_bytes()
     if kvb >= 2 * l2_bytes:
@@ -187,7 +192,7 @@ def run_ours(args, rank, world, local):
                         seq_lens_host=first.seq_lens.cpu().numpy())
     outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev) for w in sets[0]]
     stream = torch.cuda.current_stream()
-    kv_per_step = algorithmic_kv_bytes(sets[0])
+    kv_per_step = sum(algorithmic_kv_bytes(s) for s in sets) // len(sets)  # mean over the step list
     launches_per_step = 2 * len(sets[0])
 
     def step(k):
@@ -291,7 +296,9 @@ def run_ours(args, rank, world, local):
         "config": {"workload": args.workload, "batch": first.B, "q_heads": first.Hq, "kv_heads": first.Hkv,
                    "head_dim": first.d, "layers": len(sets[0]),
                    "seq_lens": "ragged U[512,8192]" if first.B > 1 and args.workload == "qwen3-14b-ragged"
-                   else int(first.seq_lens[0].item()),
+                   else (f"{int(sets[0][0].seq_lens[0])}..{int(sets[-1][0].seq_lens[0])} (one token per step)"
+                         if len(sets) > 1 and args.workload == "qwen3-14b-4k-decode"
+                         else int(first.seq_lens[0].item())),
                    "cache": "paged-64" if first.paged else "contiguous", "l2": l2_note,
                    "workers": plan.num_workers, "parallelism": f"replicas x{world}"},
         "kv_bytes_per_step": kv_per_step,
@@ -391,7 +398,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--warmup-seconds", type=float, default=0.3,
                     help="keep warming up for at least this long (so the clock record sees the loaded GPU)")
-    ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer",
+    ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer,"
+                                           "qwen3-14b-4k-decode",
                     help="other workloads to time (GPU only) into the line's by_config; '' for none")
     args = ap.parse_args()
     rank, world, local = dist_env()

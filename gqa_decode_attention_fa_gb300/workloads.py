@@ -18,6 +18,9 @@ Named workloads (the five decode geometries the step is measured on):
 * ``llama3-70b-128k``   B=1, 64/8 (G=8), L=131072, contiguous, no QK-norm, theta 5e5.
 * ``qwen3-14b-40layer`` 40 layers x (B=8, 40/8, L=32768, paged, per-layer page tables,
   1 % of K-cache elements scaled x20 before rounding), QK-norm, theta 1e6.
+
+And one sweep over steps (``decode_sweep``): ``qwen3-14b-4k-decode``, 64 autoregressive
+steps through 40 layers of the 4k geometry, the length growing from 4033 to 4096.
 """
 from __future__ import annotations
 
@@ -197,6 +200,36 @@ def named(name: str, *, device="cpu", seed: int = 0, layer: int = 0) -> Workload
         return make(8, 40, 8, [32768] * 8, paged=True, seed=seed * 1000 + layer, rope_theta=1e6,
                     k_outlier_frac=0.01, k_outlier_scale=20.0, device=device, name=f"{name}/layer{layer}")
     raise KeyError(name)
+
+
+DECODE_STEPS = 64
+
+
+def decode_sweep(steps: int = DECODE_STEPS, layers: int = LAYERS_40, L_end: int = 4096, *, device="cpu",
+                 seed: int = 0) -> list:
+    """Autoregressive decode through a stack of `layers` layers of the 4k geometry (B=1,
+    40/8 heads, contiguous, QK-norm, theta 1e6, capacity L_end): step t appends the token
+    at position L_end - steps + t with fresh q/k/v and attends to the L_end - steps + t + 1
+    tokens up to it.  Returns [steps][layers] workloads; the steps of a layer share its
+    caches, norm weights and table (layer l's cache draws from seed * 1000 + l, its step
+    t inputs from (seed * 1000 + l) * 4096 + t)."""
+    base = [make(1, 40, 8, [L_end], paged=False, seed=seed * 1000 + l, rope_theta=1e6, device=device,
+                 name=f"qwen3-14b-4k-decode/layer{l}") for l in range(layers)]
+    out = []
+    for t in range(steps):
+        L = L_end - steps + t + 1
+        row = []
+        for l, w in enumerate(base):
+            gen = torch.Generator(device=device)
+            gen.manual_seed((seed * 1000 + l) * 4096 + t)
+            row.append(dataclasses.replace(
+                w, name=f"{w.name}/step{t}",
+                q_new=_normal_bf16(gen, (1, w.Hq, w.d), device), k_new=_normal_bf16(gen, (1, w.Hkv, w.d), device),
+                v_new=_normal_bf16(gen, (1, w.Hkv, w.d), device),
+                seq_lens=torch.tensor([L], dtype=torch.int32, device=device),
+                positions=torch.tensor([L - 1], dtype=torch.int32, device=device)))
+        out.append(row)
+    return out
 
 
 def kv_bytes_named(name: str, seed: int = 0) -> int:

@@ -196,6 +196,28 @@ def test_plan_reused_across_changed_lengths():
         assert_out_close(out, ref["out"], f"lengths {ints(w.seq_lens).tolist()}")
 
 
+def test_step_replays_from_a_cuda_graph():
+    """After a first eager call (which builds the RoPE tables) the step can be captured into
+    a CUDA graph; replays give the eager output bit for bit."""
+    w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=15, device="cuda")
+    plan, out_eager = run_gpu(w)
+    out = torch.empty_like(out_eager)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.run(w, out, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(w, out, s)
+    for _ in range(2):
+        out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out_eager.view(torch.int16))
+    assert plan.device_errors() == 0
+
+
 def test_determinism_bitwise():
     w = wl.named("qwen3-14b-ragged", device="cuda")
     plan, out1 = run_gpu(w)
