@@ -27,10 +27,16 @@ struct gqa_plan {
   float4 *rope_tab = nullptr;
   mutable bool tab_valid = false;
   mutable float tab_theta = 0.f;
-  // tensor maps of the last cache pair seen (re-encoded when the pointers change)
+  // tensor maps of the cache pairs seen, most recent kMapCache of them (a model's layers
+  // each bring their own pair; encoding one is a driver call on every step otherwise)
+  static constexpr int kMapCache = 128;
+  struct CacheMaps {
+    const void *k = nullptr, *v = nullptr;
+    CUtensorMap tk, tv;
+  };
   mutable std::mutex tm_mu;
-  mutable const void *tm_k_ptr = nullptr, *tm_v_ptr = nullptr;
-  mutable CUtensorMap tmK, tmV;
+  mutable CacheMaps tm[kMapCache];
+  mutable int tm_next = 0, tm_last = 0;
 };
 
 namespace {
@@ -121,19 +127,33 @@ gqa_status_t check_step_args(const gqa_plan_t *plan, const void *q, const void *
   return GQA_OK;
 }
 
+// The tensor maps of a cache pair: looked up among the pairs seen recently (searching
+// from the last hit, as successive layers come in order), else encoded into the oldest
+// slot.  A map describes only an address and the plan's geometry, so a cached one stays
+// right for that address.
 gqa_status_t cache_maps(const gqa_plan_t *plan, const void *kc, const void *vc, CUtensorMap *tk, CUtensorMap *tv) {
   std::lock_guard<std::mutex> lk(plan->tm_mu);
-  if (plan->tm_k_ptr != kc || plan->tm_v_ptr != vc) {
-    if (!make_cache_map(&plan->tmK, kc, plan->desc.num_kv_heads, plan->num_rows) ||
-        !make_cache_map(&plan->tmV, vc, plan->desc.num_kv_heads, plan->num_rows)) {
-      plan->tm_k_ptr = plan->tm_v_ptr = nullptr;
-      return GQA_ERR_CUDA;
+  constexpr int N = gqa_plan::kMapCache;
+  for (int i = 0; i < N; ++i) {
+    const gqa_plan::CacheMaps &e = plan->tm[(plan->tm_last + i) % N];
+    if (e.k == kc && e.v == vc && kc) {
+      plan->tm_last = (plan->tm_last + i) % N;
+      *tk = e.tk;
+      *tv = e.tv;
+      return GQA_OK;
     }
-    plan->tm_k_ptr = kc;
-    plan->tm_v_ptr = vc;
   }
-  *tk = plan->tmK;
-  *tv = plan->tmV;
+  gqa_plan::CacheMaps &e = plan->tm[plan->tm_next];
+  e.k = e.v = nullptr;
+  if (!make_cache_map(&e.tk, kc, plan->desc.num_kv_heads, plan->num_rows) ||
+      !make_cache_map(&e.tv, vc, plan->desc.num_kv_heads, plan->num_rows))
+    return GQA_ERR_CUDA;
+  e.k = kc;
+  e.v = vc;
+  plan->tm_last = plan->tm_next;
+  plan->tm_next = (plan->tm_next + 1) % N;
+  *tk = e.tk;
+  *tv = e.tv;
   return GQA_OK;
 }
 
