@@ -48,6 +48,15 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum over all ranks of the initialised process group (the slowest
+    replica sets a time-like metric)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -271,9 +280,7 @@ def run_ours(args, rank, world, local):
     us_step = region_ms * 1e3 / K
     e2e_us = e2e_s * 1e6 / K
     if world > 1:
-        t = torch.tensor([us_step, e2e_us], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us_step, e2e_us = float(t[0]), float(t[1])
+        us_step, e2e_us = max_over_ranks([us_step, e2e_us], dev)
 
     peak, peak_src = hbm_peak()
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
