@@ -63,6 +63,14 @@ def _load():
             lib.oracle_attention_streaming.argtypes = [
                 ctypes.POINTER(Geom), P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 P, ctypes.c_int, P]
+            lib.oracle_prefill_prologue.argtypes = [ctypes.POINTER(Geom), ctypes.c_int] + [P] * 9 + [
+                ctypes.c_double, ctypes.c_double, P]
+            lib.oracle_prefill_prologue.restype = ctypes.c_int
+            lib.oracle_prefill_attention.argtypes = [ctypes.POINTER(Geom), ctypes.c_int, P, P, P, P, P, P,
+                                                     ctypes.c_int, P]
+            lib.oracle_prefill_attention.restype = ctypes.c_int
+            lib.oracle_prefill_blocked.argtypes = [ctypes.POINTER(Geom), ctypes.c_int, P, P, P, P, P,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -170,6 +178,67 @@ def decode_step(g: Geom, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_
     q_rot, kc, vc, st = prologue(g, q_new, k_new, v_new, k_cache, v_cache, page_table, seq_lens,
                                  positions, q_norm_w, k_norm_w, rope_theta, eps)
     out, used = attention(g, q_rot, kc, vc, page_table, seq_lens, pairs=pairs, threads=threads)
+    return dict(out=out, q_rot=q_rot, k_cache=kc, v_cache=vc, status=st, threads=used)
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+def prefill_prologue(g: Geom, T: int, q_new, k_new, v_new, k_cache, v_cache, page_table, q_start,
+                     q_norm_w, k_norm_w, rope_theta: float, eps: float):
+    """The per-token prologue of a chunk of T tokens per sequence.  q_new [B,T,Hq,d],
+    k_new/v_new [B,T,Hkv,d] bits; q_start [B].  Returns (q_rot bits [B,T,Hq,d], k_cache',
+    v_cache', status); the input caches are not modified."""
+    q_new, k_new, v_new = (_c(a, np.uint16) for a in (q_new, k_new, v_new))
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    pt, qs = _c(page_table, np.int32), _c(q_start, np.int32)
+    qw, kw = _c(q_norm_w, np.uint16), _c(k_norm_w, np.uint16)
+    q_rot = np.zeros((g.B, int(T), g.Hq, g.d), dtype=np.uint16)
+    st = _load().oracle_prefill_prologue(ctypes.byref(g), int(T), _ptr(q_new), _ptr(k_new), _ptr(v_new),
+                                         _ptr(kc), _ptr(vc), _ptr(pt), _ptr(qs), _ptr(qw), _ptr(kw),
+                                         float(rope_theta), float(eps), _ptr(q_rot))
+    return q_rot, kc, vc, st
+
+
+def prefill_attention(g: Geom, T: int, q_rot, k_cache, v_cache, page_table, q_start, triples=None,
+                      threads: int | None = None):
+    """Causal attention of the chunk, brute force, fp64.  Returns (out, threads_used); out is
+    [B,T,Hq,d], or [len(triples), d] for a list of (b, i, h) triples."""
+    lib = _load()
+    if threads:
+        lib.oracle_set_threads(int(threads))
+    q_rot, kc, vc = (_c(a, np.uint16) for a in (q_rot, k_cache, v_cache))
+    pt, qs = _c(page_table, np.int32), _c(q_start, np.int32)
+    if triples is not None:
+        tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
+        out = np.zeros((tr.shape[0], g.d), dtype=np.float64)
+        used = lib.oracle_prefill_attention(ctypes.byref(g), int(T), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt),
+                                            _ptr(qs), _ptr(tr), tr.shape[0], _ptr(out))
+    else:
+        out = np.zeros((g.B, int(T), g.Hq, g.d), dtype=np.float64)
+        used = lib.oracle_prefill_attention(ctypes.byref(g), int(T), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt),
+                                            _ptr(qs), None, 0, _ptr(out))
+    return out, used
+
+
+def prefill_blocked(g: Geom, T: int, q_rot, k_cache, v_cache, page_table, q_start, b: int, h: int,
+                    q_block: int, kv_tile: int) -> np.ndarray:
+    """The past / partial / future tile-class form for one (b, h); returns [T, d]."""
+    q_rot, kc, vc = (_c(a, np.uint16) for a in (q_rot, k_cache, v_cache))
+    pt, qs = _c(page_table, np.int32), _c(q_start, np.int32)
+    out = np.zeros((int(T), g.d), dtype=np.float64)
+    _load().oracle_prefill_blocked(ctypes.byref(g), int(T), _ptr(q_rot), _ptr(kc), _ptr(vc), _ptr(pt), _ptr(qs),
+                                   int(b), int(h), int(q_block), int(kv_tile), _ptr(out))
+    return out
+
+
+def prefill_step(g: Geom, T: int, q_new, k_new, v_new, k_cache, v_cache, page_table, q_start,
+                 q_norm_w, k_norm_w, rope_theta: float, eps: float, triples=None, threads: int | None = None):
+    """The whole chunk: prologue (T cache rows per sequence) then causal attention.
+    Returns dict(out, q_rot, k_cache, v_cache, status, threads)."""
+    q_rot, kc, vc, st = prefill_prologue(g, T, q_new, k_new, v_new, k_cache, v_cache, page_table, q_start,
+                                         q_norm_w, k_norm_w, rope_theta, eps)
+    out, used = prefill_attention(g, T, q_rot, kc, vc, page_table, q_start, triples=triples, threads=threads)
     return dict(out=out, q_rot=q_rot, k_cache=kc, v_cache=vc, status=st, threads=used)
 
 

@@ -24,8 +24,12 @@
  *     per-tile recurrence of ADR-0060 section 3 and the log-sum-exp merge of section 4,
  *     so that the two can be checked against each other.
  *
+ *   - Chunked causal prefill: the same per-token prologue for a block of T new tokens,
+ *     then causal attention of each of them over the cache (ADR-0060 section 5.4); a
+ *     blocked form follows that section's past / partial / future tile classes.
+ *
  * Parity pins (the tests that tie this file to the pages and to mathematics, not to
- * itself) live in tests/test_oracle_pins.py.
+ * itself) live in tests/test_oracle_pins.py and tests/test_oracle_prefill_pins.py.
  */
 #include <math.h>
 #include <stdint.h>
@@ -300,6 +304,206 @@ void oracle_attention_streaming(const oracle_geom_t *g, const uint16_t *q_rot,
     }
     for (int i = 0; i < d; ++i) out[i] = Oacc[i] / l_acc;
     free(O); free(Oacc); free(s);
+}
+
+/* ------------------------------------------------------------------ chunked prefill */
+
+/* Chunked causal prefill ("ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)",
+ * section 5.4 PREFILL, no SP: the prompt is resident in the cache and the query is a
+ * block of T tokens).  Sequence b receives T new tokens at positions s_b .. s_b + T - 1,
+ * s_b = q_start[b]; its cache already holds positions [0, s_b).  Token i of the chunk
+ * (position p = s_b + i) goes through the same per-token prologue as a decode step:
+ *   q_rot[b, i, h]      = bf16(RoPE_p(RMSNorm(q_new[b, i, h])))
+ *   k_cache[slot(b, p)] = bf16(RoPE_p(RMSNorm(k_new[b, i, kv])))
+ *   v_cache[slot(b, p)] = v_new[b, i, kv]                          (bit copy)
+ * Tensors: q_new, q_rot [B, T, H_q, d]; k_new, v_new [B, T, H_kv, d].
+ * Returns 0, or a positive code (nothing written for that sequence): 1 = q_start < 0,
+ * 2 = s_b + T > max_seq, 3 = a page id outside the pool.                               */
+int oracle_prefill_prologue(const oracle_geom_t *g, int T,
+                            const uint16_t *q_new, const uint16_t *k_new, const uint16_t *v_new,
+                            uint16_t *k_cache, uint16_t *v_cache, const int32_t *page_table,
+                            const int32_t *q_start, const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                            double rope_theta, double eps, uint16_t *q_rot) {
+    const int d = g->d;
+    int status = 0;
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    double *x = malloc(sizeof(double) * d), *y = malloc(sizeof(double) * d);
+    double *z = malloc(sizeof(double) * d);
+    double *qw = malloc(sizeof(double) * d), *kw = malloc(sizeof(double) * d);
+    for (int i = 0; i < d; ++i) {
+        qw[i] = q_norm_w ? oracle_bf16_to_double(q_norm_w[i]) : 1.0;
+        kw[i] = k_norm_w ? oracle_bf16_to_double(k_norm_w[i]) : 1.0;
+    }
+    for (int b = 0; b < g->B; ++b) {
+        int s = q_start[b];
+        if (s < 0) { status = 1; continue; }
+        if ((long long)s + T > g->max_seq) { status = 2; continue; }
+        int bad_page = 0;
+        for (int i = 0; i < T && !bad_page; ++i) {
+            long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, s + i);
+            if (row < 0 || row >= g->num_rows) bad_page = 1;
+        }
+        if (bad_page) { status = 3; continue; }
+        for (int i = 0; i < T; ++i) {
+            const int p = s + i;
+            const long long tok = (long long)b * T + i;
+            for (int h = 0; h < g->Hq; ++h) {
+                const uint16_t *src = q_new + (tok * g->Hq + h) * d;
+                for (int e = 0; e < d; ++e) x[e] = oracle_bf16_to_double(src[e]);
+                oracle_rmsnorm(x, q_norm_w ? qw : NULL, d, eps, y);
+                oracle_rope(y, d, p, rope_theta, z);
+                uint16_t *dst = q_rot + (tok * g->Hq + h) * d;
+                for (int e = 0; e < d; ++e) dst[e] = oracle_round_bf16(z[e]);
+            }
+            long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, p);
+            for (int kv = 0; kv < g->Hkv; ++kv) {
+                const uint16_t *src = k_new + (tok * g->Hkv + kv) * d;
+                for (int e = 0; e < d; ++e) x[e] = oracle_bf16_to_double(src[e]);
+                oracle_rmsnorm(x, k_norm_w ? kw : NULL, d, eps, y);
+                oracle_rope(y, d, p, rope_theta, z);
+                uint16_t *kdst = k_cache + (row * g->Hkv + kv) * d;
+                uint16_t *vdst = v_cache + (row * g->Hkv + kv) * d;
+                const uint16_t *vsrc = v_new + (tok * g->Hkv + kv) * d;
+                for (int e = 0; e < d; ++e) {
+                    kdst[e] = oracle_round_bf16(z[e]);
+                    vdst[e] = vsrc[e];
+                }
+            }
+        }
+    }
+    free(x); free(y); free(z); free(qw); free(kw);
+    return status;
+}
+
+/* Causal attention of the chunk, brute force: for chunk token i of sequence b (position
+ * p = q_start[b] + i) and query head h (KV head floor(h / G)),
+ *     out[b, i, h] = sum_{t <= p} softmax_t(q_rot[b, i, h] . K_t / sqrt(d)) V_t
+ * over the cache after the prologue -- every earlier token and the token itself, none
+ * after it.  out is [B, T, H_q, d]; or, when triples != NULL, one d-vector per listed
+ * (b, i, h) in list order.  Returns the thread count used.                              */
+int oracle_prefill_attention(const oracle_geom_t *g, int T, const uint16_t *q_rot,
+                             const uint16_t *k_cache, const uint16_t *v_cache,
+                             const int32_t *page_table, const int32_t *q_start,
+                             const int32_t *triples, int n_triples, double *out) {
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    long long n = triples ? n_triples : (long long)g->B * T * g->Hq;
+    int threads = 1;
+#pragma omp parallel
+    {
+#ifdef _OPENMP
+#pragma omp single
+        threads = omp_get_num_threads();
+#endif
+        double *scores = malloc(sizeof(double) * (size_t)(g->max_seq > 0 ? g->max_seq : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long long k = 0; k < n; ++k) {
+            int b, i, h;
+            if (triples) {
+                b = triples[3 * k]; i = triples[3 * k + 1]; h = triples[3 * k + 2];
+            } else {
+                b = (int)(k / ((long long)T * g->Hq));
+                i = (int)((k / g->Hq) % T);
+                h = (int)(k % g->Hq);
+            }
+            const int L = q_start[b] + i + 1;
+            const int G = g->Hq / g->Hkv, kv = h / G;
+            const double scale = 1.0 / sqrt((double)g->d);
+            const uint16_t *q = q_rot + (((long long)b * T + i) * g->Hq + h) * g->d;
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                const uint16_t *kr = k_cache + (row * g->Hkv + kv) * g->d;
+                double acc = 0.0;
+                for (int e = 0; e < g->d; ++e) acc += oracle_bf16_to_double(q[e]) * oracle_bf16_to_double(kr[e]);
+                scores[t] = acc * scale;
+                if (scores[t] > m) m = scores[t];
+            }
+            double l = 0.0;
+            double *o = out + k * g->d;
+            for (int e = 0; e < g->d; ++e) o[e] = 0.0;
+            for (int t = 0; t < L; ++t) {
+                double w = exp(scores[t] - m);
+                l += w;
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                const uint16_t *vr = v_cache + (row * g->Hkv + kv) * g->d;
+                for (int e = 0; e < g->d; ++e) o[e] += w * oracle_bf16_to_double(vr[e]);
+            }
+            for (int e = 0; e < g->d; ++e) o[e] /= l;
+        }
+        free(scores);
+    }
+    return threads;
+}
+
+/* Blocked form for one (b, h), used only to check the brute-force form: the chunk's
+ * queries are cut into blocks of qb tokens and the keys into tiles of kt tokens, and
+ * each (query block [qs, qe), key tile [ks, ke)) pair, in absolute positions, is one of
+ * the three classes of ADR-0060 section 5.4:
+ *     ke <= qs  -> all past:   no mask;
+ *     ks >= qe  -> all future: skipped;
+ *     otherwise -> partial:    the triangular additive mask (0 where key <= query,
+ *                              -inf after it) is added to the tile's scores.
+ * Each query row runs the online-softmax recurrence of section 3 over the tiles it does
+ * not skip (seeded m = -inf, l = 0, O = 0; a row whose tile is all masked leaves its
+ * state unchanged), normalised once at the end.  out is [T, d].                         */
+void oracle_prefill_blocked(const oracle_geom_t *g, int T, const uint16_t *q_rot,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *page_table, const int32_t *q_start, int b, int h,
+                            int qb, int kt, double *out) {
+    const int d = g->d, G = g->Hq / g->Hkv, kv = h / G;
+    const double scale = 1.0 / sqrt((double)d);
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    const int s0 = q_start[b];
+    double *S = malloc(sizeof(double) * (size_t)qb * kt);
+    double *m = malloc(sizeof(double) * qb), *l = malloc(sizeof(double) * qb);
+    for (int i0 = 0; i0 < T; i0 += qb) {
+        const int nq = T - i0 < qb ? T - i0 : qb;
+        const int qs = s0 + i0, qe = qs + nq;
+        for (int r = 0; r < nq; ++r) {
+            m[r] = -INFINITY; l[r] = 0.0;
+            for (int e = 0; e < d; ++e) out[(long long)(i0 + r) * d + e] = 0.0;
+        }
+        for (int ks = 0; ks < qe; ks += kt) {      /* tiles with ks >= qe: all future, skipped */
+            const int ke = ks + kt;
+            const int partial = !(ke <= qs);
+            for (int r = 0; r < nq; ++r) {
+                const uint16_t *q = q_rot + (((long long)b * T + i0 + r) * g->Hq + h) * d;
+                for (int c = 0; c < kt; ++c) {
+                    const int t = ks + c;
+                    double mask = 0.0;
+                    if (partial && t > qs + r) mask = -INFINITY;
+                    if (mask == -INFINITY) { S[r * kt + c] = -INFINITY; continue; }
+                    long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                    const uint16_t *kr = k_cache + (row * g->Hkv + kv) * d;
+                    double acc = 0.0;
+                    for (int e = 0; e < d; ++e) acc += oracle_bf16_to_double(q[e]) * oracle_bf16_to_double(kr[e]);
+                    S[r * kt + c] = acc * scale + mask;
+                }
+            }
+            for (int r = 0; r < nq; ++r) {
+                double mt = -INFINITY;
+                for (int c = 0; c < kt; ++c) if (S[r * kt + c] > mt) mt = S[r * kt + c];
+                if (mt == -INFINITY) continue;          /* every key of this tile masked */
+                const double m_new = m[r] > mt ? m[r] : mt;
+                const double corr = exp(m[r] - m_new);  /* 0 on the row's first tile */
+                double *o = out + (long long)(i0 + r) * d;
+                l[r] *= corr;
+                for (int e = 0; e < d; ++e) o[e] *= corr;
+                for (int c = 0; c < kt; ++c) {
+                    if (S[r * kt + c] == -INFINITY) continue;
+                    const double P = exp(S[r * kt + c] - m_new);
+                    l[r] += P;
+                    long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, ks + c);
+                    const uint16_t *vr = v_cache + (row * g->Hkv + kv) * d;
+                    for (int e = 0; e < d; ++e) o[e] += P * oracle_bf16_to_double(vr[e]);
+                }
+                m[r] = m_new;
+            }
+        }
+        for (int r = 0; r < nq; ++r)
+            for (int e = 0; e < d; ++e) out[(long long)(i0 + r) * d + e] /= l[r];
+    }
+    free(S); free(m); free(l);
 }
 
 /* ------------------------------------------------------------------ threads */
