@@ -1,4 +1,4 @@
-"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h).
+"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h, include/gqa_prefill.h).
 
 Argument marshalling only: every step of the decode path runs in the library's CUDA
 kernels.  Device tensors are torch tensors (device memory and streams come from torch);
@@ -22,6 +22,7 @@ from . import build as _build
 STATIC_SCRATCH_BYTES = 32 << 20
 DEVERR_POSITION, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 HEADER = os.path.join(_build.ROOT, "include", "gqa_decode.h")
+HEADERS = _build.HEADERS
 
 _lock = threading.Lock()
 _lib = None
@@ -39,11 +40,19 @@ class PlanDesc(ctypes.Structure):
         "num_cache_blocks", "num_workers", "device")]
 
 
+class PrefillDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "batch", "num_q_heads", "num_kv_heads", "head_dim", "chunk_len", "block_size", "max_seq_len",
+        "num_cache_blocks", "device")]
+
+
 def header_functions() -> list:
-    """Names of the functions include/gqa_decode.h declares."""
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text)))
+    """Names of the functions the headers under include/ declare."""
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names.update(re.findall(r"\b(gqa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def load(build: bool = True):
@@ -74,11 +83,12 @@ def load(build: bool = True):
         lib.gqa_partition_describe.argtypes = [P, I, I, I, I, P]
         lib.gqa_partition_describe.restype = ctypes.c_longlong
         lib.gqa_decode_attn_static.argtypes = [ctypes.POINTER(PlanDesc)] + step[1:] + [P, P, P]
+        lib.gqa_prefill_attn.argtypes = [ctypes.POINTER(PrefillDesc)] + [P] * 9 + [F, F, P, P, P]
         lib.gqa_status_string.argtypes = [I]
         lib.gqa_status_string.restype = ctypes.c_char_p
         for name in ("gqa_plan_create", "gqa_plan_destroy", "gqa_decode_attn", "gqa_decode_attn_host",
                      "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
-                     "gqa_plan_device_errors", "gqa_decode_attn_static"):
+                     "gqa_plan_device_errors", "gqa_decode_attn_static", "gqa_prefill_attn"):
             getattr(lib, name).restype = I
         _lib = lib
     return _lib
@@ -159,6 +169,26 @@ def decode_attn_static_workload(w, out, *, num_workers: int = 0, device: int = 0
                        w.seq_lens, w.positions, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out,
                        block_size=w.block_size, num_cache_blocks=w.num_blocks, num_workers=num_workers,
                        device=device, device_errors=device_errors, stream=stream)
+
+
+def prefill_attn(batch: int, num_q_heads: int, num_kv_heads: int, chunk_len: int, max_seq_len: int, q_new, k_new,
+                 v_new, k_cache, v_cache, page_table, q_start, q_norm_w, k_norm_w, rope_theta: float, eps: float, out,
+                 *, block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128, device: int = 0,
+                 device_errors=None, stream=None):
+    """One chunk of causal prefill through gqa_prefill_attn (include/gqa_prefill.h)."""
+    desc = PrefillDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(chunk_len),
+                       int(block_size), int(max_seq_len), int(num_cache_blocks), int(device))
+    _check(load().gqa_prefill_attn(
+        ctypes.byref(desc), _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache),
+        _dptr(page_table), _dptr(q_start), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta), float(eps),
+        _dptr(out), _dptr(device_errors), _stream(stream)), "gqa_prefill_attn")
+
+
+def prefill_attn_workload(w, out, *, device: int = 0, device_errors=None, stream=None):
+    """gqa_prefill_attn on a prefill workload's tensors (see workloads.PrefillWorkload)."""
+    prefill_attn(w.B, w.Hq, w.Hkv, w.T, w.max_seq, w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table,
+                 w.q_start, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out, block_size=w.block_size,
+                 num_cache_blocks=w.num_blocks, device=device, device_errors=device_errors, stream=stream)
 
 
 class Plan:

@@ -58,20 +58,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// K or V cache viewed as [rows][H_kv][128] bf16; box = 64 dims (128 B, 128-byte swizzle)
-// x 1 head x 64 tokens.
-bool make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows) {
+}  // namespace
+
+bool gqa::encode_bf16_map(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims,
+                          const cuuint64_t *strides, const cuuint32_t *box) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
+  if (!enc || rank < 1 || rank > 5) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void *>(base), dims,
+             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The box is 64 dims (128 B, the 128-byte swizzle span) x 1 head x 64 tokens.
+bool gqa::make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
                               static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(Hkv) * kHeadDim * 2};
   const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_bf16_map(m, 3, base, dims, strides, box);
 }
+
+namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 

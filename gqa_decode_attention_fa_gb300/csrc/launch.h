@@ -4,6 +4,7 @@
 #include <utility>
 
 #include "gqa_common.cuh"
+#include "../../include/gqa_prefill.h"
 
 namespace gqa {
 
@@ -50,6 +51,13 @@ cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, con
 // many CTAs per query head; combine_split picks it from the geometry and worker count.
 int combine_split(int batch, int num_q_heads, int num_kv_heads, int num_workers, int num_sms);
 cudaError_t launch_combine(const CombineParams &p, int split, cudaStream_t stream);
+
+// Tiled bf16 tensor map with 128-byte swizzling over `rank` dimensions (innermost first;
+// `strides` in bytes for dimensions 1..rank-1), no interleave, zero fill out of bounds.
+bool encode_bf16_map(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+                     const cuuint32_t *box);
+// K or V cache viewed as [rows][H_kv][128] bf16; box = 64 dims x 1 head x 64 tokens.
+bool make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows);
 
 // Runs the calling thread on `dev` for the guard's lifetime.
 struct DeviceGuard {

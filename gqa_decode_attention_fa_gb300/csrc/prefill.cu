@@ -1,0 +1,617 @@
+// Chunked causal prefill attention on the 5th-generation tensor core (sm_103a).
+//
+// What it computes ("ADR-0060: AHBM GQA Fused Attention Kernel (Llama3-70B)", section 5.4,
+// PREFILL with no sequence parallelism): sequence b receives a chunk of T new tokens at
+// positions s_b .. s_b + T - 1 (s_b = q_start[b]) on top of a cache that holds positions
+// [0, s_b).  Each chunk token gets the decode prologue -- QK RMSNorm, RoPE at its position,
+// k and v appended to the cache ("Qwen3-14B Optimization", section 2.1 Shape 4 and
+// section 3.3) -- and then attends causally: query token p sees keys 0 .. p.  The G query
+// heads of a KV head share one operand (section 5.4: "GQA batches the group's query heads
+// along the same axis as decode").
+//
+// Two kernels:
+//  * prefill_rope_kernel: one CTA per chunk token.  cos/sin of the token's position in
+//    binary64, the rotated queries (binary32, rounded once to bf16) written to `out`, which
+//    holds them until the attention kernel has read them, and the appended k row
+//    (double-word arithmetic, rounded to bf16 as the exact value rounds) and v row.
+//  * prefill_attn_kernel: one CTA per (sequence, KV head, block of Tt = 128 / G chunk
+//    tokens); its 128-row M tile stacks those tokens' G heads.  A TMA warp streams 64-token
+//    K/V tiles into a 3-stage ring; an MMA warp issues S = Q K^T (M = 128, N = 64, K = 128)
+//    into tensor memory (two S buffers) and O += P V (N = 128, K = 64) into a tensor-memory
+//    accumulator; four softmax warps own one row each per thread (tensor-memory lane = row),
+//    apply the causal mask of the tile classes -- KV tiles wholly after the block's last
+//    query are never loaded, the others are masked per row (key <= query position) -- run
+//    the online softmax and write P to shared memory as bf16 hi + lo, both multiplied into
+//    O, so that rounding P costs no accuracy.  The running maximum is raised lazily: O in
+//    tensor memory is rescaled only when a row's maximum grows by more than 2^8, so P stays
+//    below 256 and most tiles need no rescale.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "launch.h"
+#include "rowmath.cuh"
+#include "tc05.cuh"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kPfStages = 3;                    // K/V ring depth
+constexpr int kPfSoftmaxWarps = 4;              // one row per thread, 128 rows
+constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 2);  // + TMA warp + MMA warp
+constexpr int kPfProducerWarp = kPfSoftmaxWarps;
+constexpr int kPfMmaWarp = kPfSoftmaxWarps + 1;
+constexpr int kPfRows = 128;                    // M of every MMA
+constexpr uint32_t kPfTmemCols = 256;           // S buffers at columns 0 and 64, O at 128
+constexpr float kRescaleLog2 = 8.f;             // lazy rescale threshold (P <= 2^8)
+
+constexpr int kQBytes = 2 * kPfRows * kHalfRowBytes;     // 32 KiB: two 64-dim panels
+constexpr int kStageBytes = 4 * kHalfTileBytes;           // 32 KiB: K lo, K hi, V lo, V hi
+constexpr int kPBytes = kPfRows * kHalfRowBytes;          // 16 KiB: one P panel (64 tokens)
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + kPfStages * kStageBytes;   // 2 buffers x (hi, lo)
+constexpr int kOffBar = kOffP + 4 * kPBytes;
+// barriers: q_full, kv_full[3], kv_empty[3], s_full[2], s_free[2], p_full[2], o_done, drain
+constexpr int kNumBars = 1 + 2 * kPfStages + 2 + 2 + 2 + 1 + 1;
+constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
+static_assert(kSmemBytes <= 227 * 1024, "prefill attention shared memory");
+
+}  // namespace
+
+struct PrefillParams {
+  const uint16_t *q_new;       // [B, T, Hq, d]
+  const uint16_t *k_new;       // [B, T, Hkv, d]
+  const uint16_t *v_new;       // [B, T, Hkv, d]
+  uint16_t *k_cache, *v_cache;
+  const int32_t *page_table;   // [B, max_blocks] or null
+  const int32_t *q_start;      // [B]
+  const uint16_t *q_norm_w, *k_norm_w;
+  uint16_t *out;               // [B, T, Hq, d]: rotated queries, then the attention output
+  uint32_t *err;
+  int B, T, Hq, Hkv, G, Tt, nqb;
+  int paged, max_seq, max_blocks, num_blocks;
+  float eps, scale_log2;
+  double inv_freq[kHeadDim / 2];
+};
+
+namespace {
+
+__device__ __forceinline__ bool chunk_ok(const PrefillParams &p, int s) {
+  return s >= 0 && static_cast<long long>(s) + p.T <= p.max_seq;
+}
+
+// Cache row of token position pos of sequence b, or -1 when its page id is out of range.
+__device__ __forceinline__ long long cache_row_of(const PrefillParams &p, int b, int pos) {
+  if (!p.paged) return static_cast<long long>(b) * p.max_seq + pos;
+  const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + pos / kTile];
+  if (pg < 0 || pg >= p.num_blocks) return -1;
+  return static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------ prologue
+// One CTA per chunk token (blockIdx.x = b * T + i); warp w rotates rows w, w + 8, ... of
+// the token's H_q query heads followed by its H_kv key heads (lane l holds dims l + 32 t).
+__global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p) {
+  __shared__ float4 cs[kHeadDim / 2];  // (cos_hi, sin_hi, cos_lo, sin_lo) of pair i
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x / p.T, i = blockIdx.x - b * p.T;
+  const int s = p.q_start[b];
+  if (!chunk_ok(p, s)) {
+    if (i == 0 && threadIdx.x == 0) atomicOr(p.err, s < 0 ? GQA_DEVERR_POSITION : GQA_DEVERR_SEQLEN);
+    return;
+  }
+  const int pos = s + i;
+  if (threadIdx.x < kHeadDim / 2) {
+    double sv, cv;
+    sincos(static_cast<double>(pos) * p.inv_freq[threadIdx.x], &sv, &cv);
+    const float ch = static_cast<float>(cv), sh = static_cast<float>(sv);
+    cs[threadIdx.x] = make_float4(ch, sh, static_cast<float>(cv - ch), static_cast<float>(sv - sh));
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long tok = static_cast<long long>(b) * p.T + i;
+  const long long crow = cache_row_of(p, b, pos);
+  if (crow < 0 && threadIdx.x == 0) atomicOr(p.err, GQA_DEVERR_PAGE);
+  const float4 c0 = cs[lane], c1 = cs[lane + 32];
+  for (int r = warp; r < p.Hq + p.Hkv; r += 8) {
+    if (r < p.Hq) {
+      // query row: binary32, one bf16 rounding (it is not stored in the cache)
+      const uint16_t *src = p.q_new + (tok * p.Hq + r) * kHeadDim;
+      float y[4], ss = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float x = bf16_bits_to_float(src[lane + 32 * t]);
+        ss = fmaf(x, x, ss);
+        y[t] = p.q_norm_w ? x * bf16_bits_to_float(p.q_norm_w[lane + 32 * t]) : x;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rn = p.q_norm_w ? 1.0f / sqrtf(ss * (1.0f / 128.0f) + p.eps) : 1.0f;
+      uint16_t *dst = p.out + (tok * p.Hq + r) * kHeadDim;
+      const float z0 = rn * fmaf(y[0], c0.x, -y[2] * c0.y), z2 = rn * fmaf(y[2], c0.x, y[0] * c0.y);
+      const float z1 = rn * fmaf(y[1], c1.x, -y[3] * c1.y), z3 = rn * fmaf(y[3], c1.x, y[1] * c1.y);
+      const float z[4] = {z0, z1, z2, z3};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(z[t]);
+        dst[lane + 32 * t] = *reinterpret_cast<const uint16_t *>(&h);
+      }
+    } else if (crow >= 0) {
+      const int kv = r - p.Hq;
+      const uint16_t *ksrc = p.k_new + (tok * p.Hkv + kv) * kHeadDim;
+      const uint16_t *vsrc = p.v_new + (tok * p.Hkv + kv) * kHeadDim;
+      uint16_t x[4], w[4], kz[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        x[t] = ksrc[lane + 32 * t];
+        w[t] = p.k_norm_w ? p.k_norm_w[lane + 32 * t] : uint16_t(0);
+      }
+      rotate_row_k(x, w, p.k_norm_w != nullptr, p.eps, c0, c1, kz);
+      uint16_t *kd = p.k_cache + (crow * p.Hkv + kv) * kHeadDim;
+      uint16_t *vd = p.v_cache + (crow * p.Hkv + kv) * kHeadDim;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        kd[lane + 32 * t] = kz[t];
+        vd[lane + 32 * t] = vsrc[lane + 32 * t];
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- attention
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint64_t *q_full = bars;
+  uint64_t *kv_full = bars + 1;
+  uint64_t *kv_empty = kv_full + kPfStages;
+  uint64_t *s_full = kv_empty + kPfStages;
+  uint64_t *s_free = s_full + 2;
+  uint64_t *p_full = s_free + 2;
+  uint64_t *o_done = p_full + 2;
+  uint64_t *drain = o_done + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Work item: query blocks in decreasing order of their key count first, so that the
+  // longest CTAs start in the first wave.
+  const int bk = p.B * p.Hkv;
+  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x) / bk;
+  const int rem = static_cast<int>(blockIdx.x) % bk;
+  const int b = rem / p.Hkv, kv = rem - b * p.Hkv;
+  const int t0 = qb * p.Tt;                       // first chunk token of the block
+  const int t_end = min(t0 + p.Tt, p.T);          // one past its last
+
+  if (tid == 0) {
+    mbar_init(smem_addr(q_full), 1);
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(smem_addr(&kv_full[s]), 1);
+      mbar_init(smem_addr(&kv_empty[s]), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_addr(&s_full[k]), 1);
+      mbar_init(smem_addr(&s_free[k]), kPfSoftmaxWarps);
+      mbar_init(smem_addr(&p_full[k]), kPfSoftmaxWarps);
+    }
+    mbar_init(smem_addr(o_done), 1);
+    mbar_init(smem_addr(drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == kPfProducerWarp && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == kPfMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kPfTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // Everything below reads what the prologue kernel wrote (the rotated queries in `out`,
+  // the appended cache rows).
+  griddep_wait();
+  const int s0 = p.q_start[b];
+  const bool seq_ok = chunk_ok(p, s0);
+  // KV tiles the block needs: up to the one holding its last query's position; the
+  // tiles after it are wholly in the future of every query and are never loaded.
+  const int kmax = s0 + t_end - 1;
+  const int n = seq_ok ? kmax / kTile + 1 : 0;
+  uint8_t *const qs = smem + kOffQ;
+  auto stage_ptr = [&](int s) { return smem + kOffKV + s * kStageBytes; };
+  auto p_hi = [&](int k) { return smem + kOffP + k * 2 * kPBytes; };
+  auto p_lo = [&](int k) { return smem + kOffP + k * 2 * kPBytes + kPBytes; };
+
+  if (warp == kPfProducerWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      const uint32_t qb_bytes = 2u * 64u * 2u * static_cast<uint32_t>(p.G * p.Tt);
+      mbar_arrive_expect_tx(smem_addr(q_full), qb_bytes);
+      tma_load_4d(smem_addr(qs), &tmQ, smem_addr(q_full), 0, kv * p.G, t0, b);
+      tma_load_4d(smem_addr(qs + kPfRows * kHalfRowBytes), &tmQ, smem_addr(q_full), 64, kv * p.G, t0, b);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % kPfStages;
+        if (j >= kPfStages) {
+          ok = mbar_wait(smem_addr(&kv_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1));
+          if (!ok) break;
+        }
+        int row;
+        if (p.paged) {
+          const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+          if (pg < 0 || pg >= p.num_blocks) {
+            atomicOr(p.err, GQA_DEVERR_PAGE);
+            row = -kTile;  // the whole box out of bounds: TMA fills zeros
+          } else {
+            row = pg * kTile;
+          }
+        } else {
+          row = b * p.max_seq + j * kTile;
+        }
+        const uint32_t fb = smem_addr(&kv_full[s]);
+        const uint32_t base = smem_addr(stage_ptr(s));
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        tma_load_3d(base, &tmK, fb, 0, kv, row);
+        tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, row);
+        tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, row);
+        tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, row);
+        issued = j + 1;
+      }
+      if (!ok) {
+        atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+        // Do not leave while copies into this CTA's shared memory may still be in flight.
+        (void)mbar_wait(smem_addr(q_full), 0);
+        for (int j = (issued > kPfStages ? issued - kPfStages : 0); j < issued; ++j)
+          (void)mbar_wait(smem_addr(&kv_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
+      }
+    }
+  } else if (warp == kPfMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kPfRows, kTile, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kPfRows, kHeadDim, false, true);
+      const uint32_t qa = smem_addr(qs);
+      bool ok = mbar_wait(smem_addr(q_full), 0);
+      // O += P_t V_t for tile t (hi then lo part of P), then release the tile's stage and
+      // mark O current.
+      auto issue_pv = [&](int t) -> bool {
+        const int pb = t & 1;
+        if (!mbar_wait(smem_addr(&p_full[pb]), static_cast<uint32_t>((t >> 1) & 1))) return false;
+        tc_fence_after();
+        const uint32_t va = smem_addr(stage_ptr(t % kPfStages)) + 2 * kHalfTileBytes;
+        const uint32_t ph = smem_addr(p_hi(pb)), pl = smem_addr(p_lo(pb));
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16(tmem + 128, sdesc_sw128(ph + 32 * k, 16, 1024), sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024),
+                    kIdO, (t > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16(tmem + 128, sdesc_sw128(pl + 32 * k, 16, 1024), sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024),
+                    kIdO, 1u);
+        umma_commit(smem_addr(&kv_empty[t % kPfStages]));
+        umma_commit(smem_addr(o_done));
+        return true;
+      };
+      for (int j = 0; j < n && ok; ++j) {
+        const int s = j % kPfStages, sb = j & 1;
+        ok = mbar_wait(smem_addr(&kv_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
+        if (ok && j >= 2) ok = mbar_wait(smem_addr(&s_free[sb]), static_cast<uint32_t>(((j >> 1) - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ka = smem_addr(stage_ptr(s));
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 16; ++k)
+          umma_bf16(tmem + 64 * sb, sdesc_sw128(qa + (k >> 2) * (kPfRows * kHalfRowBytes) + 32 * (k & 3), 16, 1024),
+                    sdesc_sw128(ka + (k >> 2) * kHalfTileBytes + 32 * (k & 3), 16, 1024), kIdS, k > 0 ? 1u : 0u);
+        umma_commit(smem_addr(&s_full[sb]));
+        if (j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(n - 1);
+      if (!ok) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+      umma_commit(smem_addr(drain));  // lets the teardown wait for every MMA issued
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warps
+    const int row = warp * 32 + lane;
+    const int tl = row / p.G, g = row - tl * p.G;
+    const int t = t0 + tl;
+    const bool in_block = tl < p.Tt && t < t_end;
+    const bool valid = in_block && seq_ok;
+    const int qpos = valid ? s0 + t : -1;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_run = valid ? -INFINITY : 0.f;  // invalid rows: every score masked, P = 0
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(smem_addr(&s_full[sb]), static_cast<uint32_t>((j >> 1) & 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64];
+      {
+        float a[32], c[32];
+        tmem_ld32(tmem + lane_base + 64 * sb, a);
+        tmem_ld32(tmem + lane_base + 64 * sb + 32, c);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = a[e];
+          sv[32 + e] = c[e];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&s_free[sb]));
+
+      // scale (log2 domain) and the causal mask: key j*64 + c is visible iff <= qpos
+      const int klim = qpos - j * kTile;  // last visible column (may be >= 64 or < 0)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        sv[c] = c <= klim ? sv[c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[c]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      float corr = 1.f;
+      bool resc = false;
+      if (m_new > m_run + kRescaleLog2) {
+        corr = fast_exp2(m_run - m_new);  // m_run = -inf on the first tile: 0
+        m_run = m_new;
+        l_run *= corr;
+        resc = j > 0;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold P_0..P_{j-1} V before it is scaled: wait for the last P V.
+        ok = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((j - 1) & 1));
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + 128 + 32 * c4, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= corr;
+          tmem_st32(tmem + lane_base + 128 + 32 * c4, o);
+        }
+        tmem_wait_st();
+      }
+
+      // P = 2^(s - m) as bf16 hi + lo into the K-major P panels (128-byte swizzle)
+      const int pb = j & 1;
+      uint8_t *ph = p_hi(pb), *pl = p_lo(pb);
+      float rs = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          v[e] = fast_exp2(sv[8 * c8 + e] - m_run);
+          rs += v[e];
+        }
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+          l[e] = pack_bf16(v[2 * e] - bf16_lo_to_float(h[e]), v[2 * e + 1] - bf16_hi_to_float(h[e]));
+        }
+        const uint32_t off = swz128(row, c8);
+        *reinterpret_cast<uint4 *>(ph + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(pl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+      }
+      l_run += rs;
+
+      // The last tile may hold cache rows past the block's last query, which nothing
+      // has written: zero those V rows so that P = 0 never meets a non-finite value.
+      if (j == n - 1) {
+        const int vz = kmax - j * kTile + 1;  // first row to clear
+        if (vz < kTile) {
+          const int s = j % kPfStages;
+          (void)mbar_wait(smem_addr(&kv_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
+          uint4 *v0 = reinterpret_cast<uint4 *>(stage_ptr(s) + 2 * kHalfTileBytes);
+          uint4 *v1 = reinterpret_cast<uint4 *>(stage_ptr(s) + 3 * kHalfTileBytes);
+          for (int c = vz * 8 + row; c < kTile * 8; c += kPfRows) {
+            v0[c] = make_uint4(0, 0, 0, 0);
+            v1[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&p_full[pb]));
+    }
+    if (!ok && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+
+    // epilogue: O / l as bf16 into this row's output (zeros for a sequence whose chunk is
+    // out of range)
+    griddep_launch_dependents();
+    bool have_o = false;
+    if (ok && n > 0) {
+      const bool done = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((n - 1) & 1));
+      have_o = __all_sync(0xffffffffu, done);
+      if (!have_o && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+    }
+    if (have_o) tc_fence_after();
+    uint16_t *dst = p.out + ((static_cast<long long>(b) * p.T + t) * p.Hq + kv * p.G + g) * kHeadDim;
+    const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      float o[32];
+      if (have_o) {
+        tmem_ld32(tmem + lane_base + 128 + 32 * c4, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      }
+      if (in_block) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c4);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv), pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                             pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv), pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();  // the producer and MMA warps ran their loops on lane 0 alone
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kPfMmaWarp) {
+    tc_fence_after();
+    if (n > 0) (void)mbar_wait(smem_addr(drain), 0);
+    __syncwarp();
+    tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+
+namespace {
+
+std::mutex g_pf_mu;
+bool g_pf_configured[64];
+
+gqa_status_t check_desc(const gqa_prefill_desc_t &d) {
+  if (d.head_dim != kHeadDim) return GQA_ERR_UNSUPPORTED;
+  if (d.batch < 1 || d.batch > GQA_MAX_BATCH || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.chunk_len < 1 ||
+      d.max_seq_len < 1 || d.chunk_len > d.max_seq_len)
+    return GQA_ERR_INVALID_ARG;
+  if (d.num_q_heads % d.num_kv_heads != 0) return GQA_ERR_UNSUPPORTED;
+  if (d.num_q_heads / d.num_kv_heads > GQA_MAX_GROUP) return GQA_ERR_UNSUPPORTED;
+  if (d.block_size != 0 && d.block_size != GQA_BLOCK_SIZE) return GQA_ERR_UNSUPPORTED;
+  if (d.block_size > 0 && d.num_cache_blocks < 1) return GQA_ERR_INVALID_ARG;
+  const long long rows = d.block_size > 0 ? static_cast<long long>(d.num_cache_blocks) * kTile
+                                          : static_cast<long long>(d.batch) * d.max_seq_len;
+  if (rows > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  return GQA_OK;
+}
+
+bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+// A per-call error word when the caller passes none (nothing reads it).
+static __device__ uint32_t g_prefill_err_sink;
+
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const void *q_new, const void *k_new,
+                                         const void *v_new, void *k_cache, void *v_cache, const int32_t *page_table,
+                                         const int32_t *q_start, const void *q_norm_w, const void *k_norm_w,
+                                         float rope_theta, float eps, void *out, uint32_t *device_errors,
+                                         void *stream) {
+  if (!desc) return GQA_ERR_INVALID_ARG;
+  const gqa_prefill_desc_t d = *desc;
+  gqa_status_t st = check_desc(d);
+  if (st != GQA_OK) return st;
+  if (!q_new || !k_new || !v_new || !k_cache || !v_cache || !q_start || !out) return GQA_ERR_INVALID_ARG;
+  const bool paged = d.block_size > 0;
+  if (paged != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
+  if (!(isfinite(rope_theta) && rope_theta > 0.f) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
+  if (!aligned_to(q_new, 16) || !aligned_to(k_new, 16) || !aligned_to(v_new, 16) || !aligned_to(k_cache, 16) ||
+      !aligned_to(v_cache, 16) || !aligned_to(out, 16) || !aligned_to(q_norm_w, 16) || !aligned_to(k_norm_w, 16) ||
+      !aligned_to(page_table, 4) || !aligned_to(q_start, 4))
+    return GQA_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) return GQA_ERR_CUDA;
+  if (d.device < 0 || d.device >= ndev) return GQA_ERR_INVALID_ARG;
+  if (d.device >= 64) return GQA_ERR_UNSUPPORTED;
+  DeviceGuard guard(d.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_pf_mu);
+    if (!g_pf_configured[d.device]) {
+      if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+      }
+      g_pf_configured[d.device] = true;
+    }
+  }
+  uint32_t *err = device_errors;
+  if (!err) {
+    void *sink = nullptr;
+    if (cudaGetSymbolAddress(&sink, g_prefill_err_sink) != cudaSuccess) {
+      cudaGetLastError();
+      return GQA_ERR_CUDA;
+    }
+    err = static_cast<uint32_t *>(sink);
+  }
+
+  PrefillParams p;
+  memset(&p, 0, sizeof p);
+  p.q_new = static_cast<const uint16_t *>(q_new);
+  p.k_new = static_cast<const uint16_t *>(k_new);
+  p.v_new = static_cast<const uint16_t *>(v_new);
+  p.k_cache = static_cast<uint16_t *>(k_cache);
+  p.v_cache = static_cast<uint16_t *>(v_cache);
+  p.page_table = page_table;
+  p.q_start = q_start;
+  p.q_norm_w = static_cast<const uint16_t *>(q_norm_w);
+  p.k_norm_w = static_cast<const uint16_t *>(k_norm_w);
+  p.out = static_cast<uint16_t *>(out);
+  p.err = err;
+  p.B = d.batch;
+  p.T = d.chunk_len;
+  p.Hq = d.num_q_heads;
+  p.Hkv = d.num_kv_heads;
+  p.G = d.num_q_heads / d.num_kv_heads;
+  p.Tt = kPfRows / p.G;
+  p.nqb = (p.T + p.Tt - 1) / p.Tt;
+  p.paged = paged ? 1 : 0;
+  p.max_seq = d.max_seq_len;
+  p.max_blocks = (d.max_seq_len + kTile - 1) / kTile;
+  p.num_blocks = paged ? d.num_cache_blocks : 0;
+  p.eps = eps;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
+  for (int i = 0; i < kHeadDim / 2; ++i)
+    p.inv_freq[i] = pow(static_cast<double>(rope_theta), -2.0 * i / static_cast<double>(kHeadDim));
+
+  const long long rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile
+                               : static_cast<long long>(d.batch) * d.max_seq_len;
+  CUtensorMap tq, tk, tv;
+  // queries (in `out`) viewed as [B][T][H_q][128]; box = 64 dims x G heads x Tt tokens x 1
+  const cuuint64_t qdims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(p.Hq),
+                               static_cast<cuuint64_t>(p.T), static_cast<cuuint64_t>(p.B)};
+  const cuuint64_t qstrides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(p.Hq) * kHeadDim * 2,
+                                  static_cast<cuuint64_t>(p.T) * p.Hq * kHeadDim * 2};
+  const cuuint32_t qbox[4] = {64, static_cast<cuuint32_t>(p.G), static_cast<cuuint32_t>(p.Tt), 1};
+  if (!encode_bf16_map(&tq, 4, out, qdims, qstrides, qbox) || !make_cache_map(&tk, k_cache, p.Hkv, rows) ||
+      !make_cache_map(&tv, v_cache, p.Hkv, rows))
+    return GQA_ERR_CUDA;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_pdl(prefill_rope_kernel, dim3(static_cast<unsigned>(p.B * p.T)), dim3(256), 0, s, p) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(p.nqb * p.B * p.Hkv);
+  if (launch_pdl(prefill_attn_kernel, dim3(grid), dim3(kPfThreads), static_cast<size_t>(kSmemBytes), s, tq, tk, tv,
+                 p) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return GQA_OK;
+}

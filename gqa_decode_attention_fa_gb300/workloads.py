@@ -269,3 +269,106 @@ def gather_sequence(w: Workload, b: int):
         k = w.k_cache[b]
         v = w.v_cache[b]
     return k, v
+
+
+# ----------------------------------------------------------------------------- chunked prefill
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    """One chunk of causal prefill: T new tokens per sequence at positions
+    q_start[b] .. q_start[b] + T - 1 on a cache holding the tokens before them."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    T: int
+    block_size: int
+    max_seq: int
+    num_blocks: int
+    rope_theta: float
+    eps: float
+    q_new: torch.Tensor      # [B, T, Hq, d] bf16
+    k_new: torch.Tensor      # [B, T, Hkv, d] bf16
+    v_new: torch.Tensor      # [B, T, Hkv, d] bf16
+    k_cache: torch.Tensor    # paged [nb, 64, Hkv, d] or contiguous [B, max_seq, Hkv, d] bf16
+    v_cache: torch.Tensor
+    page_table: Optional[torch.Tensor]  # [B, ceil(max_seq/64)] int32
+    q_start: torch.Tensor    # [B] int32
+    q_norm_w: Optional[torch.Tensor]
+    k_norm_w: Optional[torch.Tensor]
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def paged(self) -> bool:
+        return self.block_size > 0
+
+    @property
+    def num_rows(self) -> int:
+        return self.num_blocks * BLOCK if self.paged else self.B * self.max_seq
+
+    def flops(self) -> int:
+        """Algorithmic flops of the attention: 4 d per (query head, visible key) pair --
+        2 d for q.k and 2 d for p v -- over every chunk token, which sees q_start + i + 1 keys."""
+        starts = [int(x) for x in self.q_start.cpu()]
+        keys = sum(self.T * s + self.T * (self.T + 1) // 2 for s in starts)
+        return 4 * self.d * self.Hq * keys
+
+
+def make_prefill(B: int, Hq: int, Hkv: int, T: int, q_start: Sequence[int], *, paged: bool, seed: int = 0,
+                 qk_norm: bool = True, rope_theta: float = 1e6, eps: float = 1e-6, max_seq: Optional[int] = None,
+                 device="cpu", name: str = "custom-prefill") -> PrefillWorkload:
+    """Build one prefill chunk's inputs.  Draw order: q/k/v of the chunk, QK-norm weights,
+    K cache, V cache, page-table permutation (the same distributions as a decode step).
+    Every cache row is drawn, including the chunk's own rows (which the call overwrites)
+    and rows past it (which it must never read).  Paged pools hold ceil(max_seq / 64)
+    blocks per sequence, mapped in order onto a random permutation of the pool."""
+    d = HEAD_DIM
+    starts = [int(x) for x in q_start]
+    assert len(starts) == B
+    if max_seq is None:
+        max_seq = max(starts) + T
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    q_new = _normal_bf16(gen, (B, T, Hq, d), device)
+    k_new = _normal_bf16(gen, (B, T, Hkv, d), device)
+    v_new = _normal_bf16(gen, (B, T, Hkv, d), device)
+    if qk_norm:
+        q_norm_w = _normal_bf16(gen, (d,), device, scale=0.1, mean=1.0)
+        k_norm_w = _normal_bf16(gen, (d,), device, scale=0.1, mean=1.0)
+    else:
+        q_norm_w = k_norm_w = None
+    mb = -(-max_seq // BLOCK)
+    if paged:
+        num_blocks = B * mb
+        shape = (num_blocks, BLOCK, Hkv, d)
+    else:
+        num_blocks = 0
+        shape = (B, max_seq, Hkv, d)
+    k_cache = _normal_bf16(gen, shape, device)
+    v_cache = _normal_bf16(gen, shape, device)
+    page_table = None
+    if paged:
+        perm = torch.randperm(num_blocks, generator=gen, device=device).to(torch.int32)
+        page_table = perm.reshape(B, mb).contiguous()
+    return PrefillWorkload(name=name, B=B, Hq=Hq, Hkv=Hkv, d=d, T=int(T), block_size=BLOCK if paged else 0,
+                           max_seq=int(max_seq), num_blocks=num_blocks, rope_theta=float(np.float32(rope_theta)),
+                           eps=float(np.float32(eps)), q_new=q_new, k_new=k_new, v_new=v_new, k_cache=k_cache,
+                           v_cache=v_cache, page_table=page_table,
+                           q_start=torch.tensor(starts, dtype=torch.int32, device=device),
+                           q_norm_w=q_norm_w, k_norm_w=k_norm_w)
+
+
+PREFILL_WORKLOADS = ("qwen3-14b-prefill-4k",)
+
+
+def named_prefill(name: str, *, device="cpu", seed: int = 0) -> PrefillWorkload:
+    """``qwen3-14b-prefill-4k``: the last 1024-token chunk of a 4096-token prompt (B=1,
+    40/8 heads, contiguous cache of 4096 tokens, QK-norm, theta 1e6): 1024 new tokens at
+    positions 3072..4095 over the 3072 cached ones."""
+    if name == "qwen3-14b-prefill-4k":
+        return make_prefill(1, 40, 8, 1024, [3072], paged=False, seed=seed, max_seq=4096, device=device, name=name)
+    raise KeyError(name)
