@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 HEADLINE = "qwen3-14b-4k"
 METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_splitkv_traffic.json")
 
 
@@ -68,6 +69,20 @@ def hbm_peak():
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: the prefill call is timed alone):
+    MEASURED_PEAKS.json when present, else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        v = d.get("bf16_tflops")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -325,6 +340,54 @@ def run_ours(args, rank, world, local):
     return result, sets
 
 
+# ----------------------------------------------------------------------------- prefill
+
+PREFILL = "qwen3-14b-prefill-4k"
+
+
+def run_prefill(name: str, steps: int, warmup: int, local: int):
+    """One chunk of causal prefill (gqa_prefill_attn: the prologue kernel and the tcgen05
+    attention kernel) timed call by call with CUDA events; L2 is flushed between calls by
+    writing a buffer twice its size outside the events.  The roofline is the tensor pipe:
+    algorithmic flops (4 d per query head and visible key) over the call's duration."""
+    import torch
+
+    from gqa_decode_attention_fa_gb300 import binding, workloads as wl
+
+    dev = f"cuda:{local}"
+    w = wl.named_prefill(name, device=dev)
+    out = torch.empty((w.B, w.T, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        binding.prefill_attn_workload(w, out, device_errors=err, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(local) as clk:
+        for a, b in ev:
+            flush.fill_(1)
+            a.record(stream)
+            binding.prefill_attn_workload(w, out, device_errors=err, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit("bench: device error flags set during the prefill calls")
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    flops = w.flops()
+    peak, src = bf16_peak()
+    achieved = flops / (us * 1e-6) / 1e12
+    return {"us_per_call": round(us, 3), "tokens": w.B * w.T, "q_start": int(w.q_start[0]),
+            "tflops": round(achieved, 1),
+            "roofline": {"bound": "tensor", "kernel": "prefill_rope_kernel + prefill_attn_kernel (whole call)",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_source": src, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "algorithmic_flops_per_call": int(flops)},
+            "l2": "flushed between calls (2x L2 write outside the events)", "steps": steps,
+            "clocks_sm_mhz": clk.result["sm_mhz"]}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0):
     """The fp64 oracle, as it stands, on the host cores: whole decode steps of the workload
     (for the 40-layer sweep: whole layers, scaled by 40) until ~budget_s of CPU time."""
@@ -406,7 +469,7 @@ def main():
     ap.add_argument("--warmup-seconds", type=float, default=0.3,
                     help="keep warming up for at least this long (so the clock record sees the loaded GPU)")
     ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer,"
-                                           "qwen3-14b-4k-decode",
+                                           "qwen3-14b-4k-decode," + PREFILL,
                     help="other workloads to time (GPU only) into the line's by_config; '' for none")
     args = ap.parse_args()
     rank, world, local = dist_env()
@@ -431,6 +494,10 @@ def main():
         result["cpu_baseline"] = cpu_baseline(args.workload)
     by = {}
     for name in [n for n in args.by_config.split(",") if n and n != args.workload]:
+        if name == PREFILL:
+            by[name] = run_prefill(name, min(args.steps, 20), args.warmup, local)
+            torch.cuda.empty_cache()
+            continue
         sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50)})
         r, s = run_ours(sub, rank, world, local)
         del s

@@ -16,13 +16,16 @@
 //    (double-word arithmetic, rounded to bf16 as the exact value rounds) and v row.
 //  * prefill_attn_kernel: one CTA per (sequence, KV head, block of Tt = 128 / G chunk
 //    tokens); its 128-row M tile stacks those tokens' G heads.  A TMA warp streams 64-token
-//    K/V tiles into a 3-stage ring; an MMA warp issues S = Q K^T (M = 128, N = 64, K = 128)
-//    into tensor memory (two S buffers) and O += P V (N = 128, K = 64) into a tensor-memory
-//    accumulator; four softmax warps own one row each per thread (tensor-memory lane = row),
+//    K/V tiles into a 2-stage ring (K and V released separately); an MMA warp issues
+//    S = Q K^T (M = 128, N = 64, K = 128) into tensor memory (two S buffers) and
+//    O += P V (N = 128, K = 64) into a tensor-memory accumulator, P read from tensor
+//    memory; four softmax warps own one row each per thread (tensor-memory lane = row),
 //    apply the causal mask of the tile classes -- KV tiles wholly after the block's last
 //    query are never loaded, the others are masked per row (key <= query position) -- run
-//    the online softmax and write P to shared memory as bf16 hi + lo, both multiplied into
-//    O, so that rounding P costs no accuracy.  The running maximum is raised lazily: O in
+//    the online softmax and store P over S as bf16 hi + lo, both multiplied into O, so
+//    that rounding P costs no accuracy.  Two CTAs share an SM (about 97 KB of shared
+//    memory and 256 tensor-memory columns each), so one CTA's softmax overlaps the
+//    other's tensor work.  The running maximum is raised lazily: O in
 //    tensor memory is rescaled only when a row's maximum grows by more than 2^8, so P stays
 //    below 256 and most tiles need no rescale.
 #include <math.h>
@@ -38,26 +41,31 @@ namespace gqa {
 
 namespace {
 
-constexpr int kPfStages = 3;                    // K/V ring depth
+constexpr int kPfStages = 2;                    // K/V ring depth (K and V released separately)
 constexpr int kPfSoftmaxWarps = 4;              // one row per thread, 128 rows
 constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 2);  // + TMA warp + MMA warp
 constexpr int kPfProducerWarp = kPfSoftmaxWarps;
 constexpr int kPfMmaWarp = kPfSoftmaxWarps + 1;
+constexpr int kPfCtasPerSm = 2;                 // two CTAs share an SM: their softmax warps interleave
 constexpr int kPfRows = 128;                    // M of every MMA
-constexpr uint32_t kPfTmemCols = 256;           // S buffers at columns 0 and 64, O at 128
+// Tensor memory per CTA: two S buffers (64 fp32 columns each; after the softmax has read
+// S it stores P there as bf16 pairs, hi in the first 32 columns, lo in the next 32) and
+// the O accumulator (128 columns).  Two CTAs fill the SM's 512 columns.
+constexpr uint32_t kPfTmemCols = 256;
+constexpr uint32_t kTmemO = 128;
 constexpr float kRescaleLog2 = 8.f;             // lazy rescale threshold (P <= 2^8)
 
 constexpr int kQBytes = 2 * kPfRows * kHalfRowBytes;     // 32 KiB: two 64-dim panels
 constexpr int kStageBytes = 4 * kHalfTileBytes;           // 32 KiB: K lo, K hi, V lo, V hi
-constexpr int kPBytes = kPfRows * kHalfRowBytes;          // 16 KiB: one P panel (64 tokens)
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kPfStages * kStageBytes;   // 2 buffers x (hi, lo)
-constexpr int kOffBar = kOffP + 4 * kPBytes;
-// barriers: q_full, kv_full[3], kv_empty[3], s_full[2], s_free[2], p_full[2], o_done, drain
-constexpr int kNumBars = 1 + 2 * kPfStages + 2 + 2 + 2 + 1 + 1;
+constexpr int kOffBar = kOffKV + kPfStages * kStageBytes;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
+// o_done, drain
+constexpr int kNumBars = 1 + 4 * kPfStages + 2 + 2 + 1 + 1;
 constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
-static_assert(kSmemBytes <= 227 * 1024, "prefill attention shared memory");
+static_assert(kPfCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two prefill CTAs must share an SM");
+static_assert(kPfCtasPerSm * kPfTmemCols <= 512, "tensor memory of the co-resident CTAs");
 
 }  // namespace
 
@@ -165,18 +173,19 @@ __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p
 }
 
 // ----------------------------------------------------------------------------- attention
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bars;
-  uint64_t *kv_full = bars + 1;
-  uint64_t *kv_empty = kv_full + kPfStages;
-  uint64_t *s_full = kv_empty + kPfStages;
-  uint64_t *s_free = s_full + 2;
-  uint64_t *p_full = s_free + 2;
+  uint64_t *k_full = bars + 1;
+  uint64_t *k_empty = k_full + kPfStages;
+  uint64_t *v_full = k_empty + kPfStages;
+  uint64_t *v_empty = v_full + kPfStages;
+  uint64_t *s_full = v_empty + kPfStages;
+  uint64_t *p_full = s_full + 2;
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
@@ -193,18 +202,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int t_end = min(t0 + p.Tt, p.T);          // one past its last
 
   if (tid == 0) {
-    mbar_init(smem_addr(q_full), 1);
-    for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(smem_addr(&kv_full[s]), 1);
-      mbar_init(smem_addr(&kv_empty[s]), 1);
-    }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_addr(&s_full[k]), 1);
-      mbar_init(smem_addr(&s_free[k]), kPfSoftmaxWarps);
-      mbar_init(smem_addr(&p_full[k]), kPfSoftmaxWarps);
-    }
-    mbar_init(smem_addr(o_done), 1);
-    mbar_init(smem_addr(drain), 1);
+    for (int i = 0; i < kNumBars; ++i)  // p_full collects one arrival per softmax warp
+      mbar_init(smem_addr(&bars[i]), (&bars[i] == &p_full[0] || &bars[i] == &p_full[1]) ? kPfSoftmaxWarps : 1);
     fence_barrier_init();
   }
   if (warp == kPfProducerWarp && lane == 0) {
@@ -232,84 +231,98 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int n = seq_ok ? kmax / kTile + 1 : 0;
   uint8_t *const qs = smem + kOffQ;
   auto stage_ptr = [&](int s) { return smem + kOffKV + s * kStageBytes; };
-  auto p_hi = [&](int k) { return smem + kOffP + k * 2 * kPBytes; };
-  auto p_lo = [&](int k) { return smem + kOffP + k * 2 * kPBytes + kPBytes; };
 
   if (warp == kPfProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
+    // Order: K_0, K_1, V_0, K_2, V_1, ... -- a K tile is released once S has used it, a V
+    // tile only after P V, so K runs one tile ahead.
     if (lane == 0 && n > 0) {
       const uint32_t qb_bytes = 2u * 64u * 2u * static_cast<uint32_t>(p.G * p.Tt);
       mbar_arrive_expect_tx(smem_addr(q_full), qb_bytes);
       tma_load_4d(smem_addr(qs), &tmQ, smem_addr(q_full), 0, kv * p.G, t0, b);
       tma_load_4d(smem_addr(qs + kPfRows * kHalfRowBytes), &tmQ, smem_addr(q_full), 64, kv * p.G, t0, b);
-      int issued = 0;
+      auto row_of = [&](int j) {
+        if (!p.paged) return b * p.max_seq + j * kTile;
+        const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+        if (pg < 0 || pg >= p.num_blocks) {
+          atomicOr(p.err, GQA_DEVERR_PAGE);
+          return -kTile;  // the whole box out of bounds: TMA fills zeros
+        }
+        return pg * kTile;
+      };
+      int kissued = 0, vissued = 0;
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
+      auto load_k = [&](int j) -> bool {
         const int s = j % kPfStages;
-        if (j >= kPfStages) {
-          ok = mbar_wait(smem_addr(&kv_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1));
-          if (!ok) break;
-        }
-        int row;
-        if (p.paged) {
-          const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
-          if (pg < 0 || pg >= p.num_blocks) {
-            atomicOr(p.err, GQA_DEVERR_PAGE);
-            row = -kTile;  // the whole box out of bounds: TMA fills zeros
-          } else {
-            row = pg * kTile;
-          }
-        } else {
-          row = b * p.max_seq + j * kTile;
-        }
-        const uint32_t fb = smem_addr(&kv_full[s]);
-        const uint32_t base = smem_addr(stage_ptr(s));
-        mbar_arrive_expect_tx(fb, kStageBytes);
+        if (j >= kPfStages && !mbar_wait(smem_addr(&k_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1)))
+          return false;
+        const int row = row_of(j);
+        const uint32_t fb = smem_addr(&k_full[s]), base = smem_addr(stage_ptr(s));
+        mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
         tma_load_3d(base, &tmK, fb, 0, kv, row);
         tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, row);
-        tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, row);
-        tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, row);
-        issued = j + 1;
+        kissued = j + 1;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = j % kPfStages;
+        if (j >= kPfStages && !mbar_wait(smem_addr(&v_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1)))
+          return false;
+        const int row = row_of(j);
+        const uint32_t fb = smem_addr(&v_full[s]), base = smem_addr(stage_ptr(s)) + 2 * kHalfTileBytes;
+        mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
+        tma_load_3d(base, &tmV, fb, 0, kv, row);
+        tma_load_3d(base + kHalfTileBytes, &tmV, fb, 64, kv, row);
+        vissued = j + 1;
+        return true;
+      };
+      for (int j = 0; j < n && ok; ++j) {
+        ok = load_k(j);
+        if (ok && j >= 1) ok = load_v(j - 1);
       }
+      if (ok) ok = load_v(n - 1);
       if (!ok) {
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
         // Do not leave while copies into this CTA's shared memory may still be in flight.
         (void)mbar_wait(smem_addr(q_full), 0);
-        for (int j = (issued > kPfStages ? issued - kPfStages : 0); j < issued; ++j)
-          (void)mbar_wait(smem_addr(&kv_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
+        for (int j = (kissued > kPfStages ? kissued - kPfStages : 0); j < kissued; ++j)
+          (void)mbar_wait(smem_addr(&k_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
+        for (int j = (vissued > kPfStages ? vissued - kPfStages : 0); j < vissued; ++j)
+          (void)mbar_wait(smem_addr(&v_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
       }
     }
   } else if (warp == kPfMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
+    // Issue order: S_0, S_1, PV_0, S_2, PV_1, ...  S_j overwrites the buffer that held
+    // P_{j-2}; P_{j-2} V was issued before it and the tensor pipe runs them in order.
     if (lane == 0 && n > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kPfRows, kTile, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kPfRows, kHeadDim, false, true);
       const uint32_t qa = smem_addr(qs);
       bool ok = mbar_wait(smem_addr(q_full), 0);
-      // O += P_t V_t for tile t (hi then lo part of P), then release the tile's stage and
-      // mark O current.
+      // O += P_t V_t (hi then lo part of P, read from tensor memory), then release V_t
+      // and mark O current.
       auto issue_pv = [&](int t) -> bool {
-        const int pb = t & 1;
+        const int pb = t & 1, s = t % kPfStages;
+        if (!mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((t / kPfStages) & 1))) return false;
         if (!mbar_wait(smem_addr(&p_full[pb]), static_cast<uint32_t>((t >> 1) & 1))) return false;
         tc_fence_after();
-        const uint32_t va = smem_addr(stage_ptr(t % kPfStages)) + 2 * kHalfTileBytes;
-        const uint32_t ph = smem_addr(p_hi(pb)), pl = smem_addr(p_lo(pb));
+        const uint32_t va = smem_addr(stage_ptr(s)) + 2 * kHalfTileBytes;
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16(tmem + 128, sdesc_sw128(ph + 32 * k, 16, 1024), sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024),
-                    kIdO, (t > 0 || k > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kTmemO, tmem + 64 * pb + 8 * k, sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024), kIdO,
+                       (t > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16(tmem + 128, sdesc_sw128(pl + 32 * k, 16, 1024), sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024),
-                    kIdO, 1u);
-        umma_commit(smem_addr(&kv_empty[t % kPfStages]));
+          umma_bf16_ts(tmem + kTmemO, tmem + 64 * pb + 32 + 8 * k, sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024),
+                       kIdO, 1u);
+        umma_commit(smem_addr(&v_empty[s]));
         umma_commit(smem_addr(o_done));
         return true;
       };
       for (int j = 0; j < n && ok; ++j) {
         const int s = j % kPfStages, sb = j & 1;
-        ok = mbar_wait(smem_addr(&kv_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
-        if (ok && j >= 2) ok = mbar_wait(smem_addr(&s_free[sb]), static_cast<uint32_t>(((j >> 1) - 1) & 1));
+        ok = mbar_wait(smem_addr(&k_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
         if (!ok) break;
         tc_fence_after();
         const uint32_t ka = smem_addr(stage_ptr(s));
@@ -317,6 +330,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int k = 0; k < kHeadDim / 16; ++k)
           umma_bf16(tmem + 64 * sb, sdesc_sw128(qa + (k >> 2) * (kPfRows * kHalfRowBytes) + 32 * (k & 3), 16, 1024),
                     sdesc_sw128(ka + (k >> 2) * kHalfTileBytes + 32 * (k & 3), 16, 1024), kIdS, k > 0 ? 1u : 0u);
+        umma_commit(smem_addr(&k_empty[s]));
         umma_commit(smem_addr(&s_full[sb]));
         if (j >= 1) ok = issue_pv(j - 1);
       }
@@ -356,19 +370,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           sv[32 + e] = c[e];
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&s_free[sb]));
 
-      // scale (log2 domain) and the causal mask: key j*64 + c is visible iff <= qpos
+      // The causal mask -- key j*64 + c is visible iff <= qpos -- only on tiles that some
+      // row of the warp does not see whole (the partial tiles of the page's tile classes).
       const int klim = qpos - j * kTile;  // last visible column (may be >= 64 or < 0)
-      float mx = -INFINITY;
+      if (!__all_sync(0xffffffffu, klim >= kTile - 1)) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        sv[c] = c <= klim ? sv[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+        for (int c = 0; c < 64; ++c) sv[c] = c <= klim ? sv[c] : -INFINITY;
       }
-      const float m_new = fmaxf(m_run, mx);
+      float m8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m8[e] = fmaxf(sv[e], sv[e + 8]);
+#pragma unroll
+      for (int c = 16; c < 64; c += 8)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], sv[c + e]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // scores in log2 units: s * scale_log2 (a positive scale keeps the maximum's place)
+      const float m_new = fmaxf(m_run, mx * p.scale_log2);
       float corr = 1.f;
       bool resc = false;
       if (m_new > m_run + kRescaleLog2) {
@@ -378,7 +397,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         resc = j > 0;
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // O must hold P_0..P_{j-1} V before it is scaled: wait for the last P V.
+        // O must hold P_0..P_{j-1} V before it is scaled: wait for the last P V.  (S_j was
+        // issued after P_{j-2} V, so o_done has completed that phase: the parity wait
+        // below is never more than one phase ahead of the barrier.)
         ok = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((j - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -388,38 +409,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float o[32];
-          tmem_ld32(tmem + lane_base + 128 + 32 * c4, o);
+          tmem_ld32(tmem + lane_base + kTmemO + 32 * c4, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= corr;
-          tmem_st32(tmem + lane_base + 128 + 32 * c4, o);
+          tmem_st32(tmem + lane_base + kTmemO + 32 * c4, o);
         }
-        tmem_wait_st();
       }
 
-      // P = 2^(s - m) as bf16 hi + lo into the K-major P panels (128-byte swizzle)
-      const int pb = j & 1;
-      uint8_t *ph = p_hi(pb), *pl = p_lo(pb);
-      float rs = 0.f;
+      // P = 2^(s - m) as bf16 hi + lo pairs into the S buffer's columns
+      uint32_t ph[32], pl[32];
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float neg_m = -m_run;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          v[e] = fast_exp2(sv[8 * c8 + e] - m_run);
-          rs += v[e];
-        }
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          h[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
-          l[e] = pack_bf16(v[2 * e] - bf16_lo_to_float(h[e]), v[2 * e + 1] - bf16_hi_to_float(h[e]));
-        }
-        const uint32_t off = swz128(row, c8);
-        *reinterpret_cast<uint4 *>(ph + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4 *>(pl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float v0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
+        const float v1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, neg_m));
+        rs8[c & 7] += v0 + v1;
+        ph[c] = pack_bf16(v0, v1);
+        pl[c] = pack_bf16(v0 - bf16_lo_to_float(ph[c]), v1 - bf16_hi_to_float(ph[c]));
       }
-      l_run += rs;
+      tmem_st32(tmem + lane_base + 64 * sb, ph);
+      tmem_st32(tmem + lane_base + 64 * sb + 32, pl);
+      l_run += ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
 
       // The last tile may hold cache rows past the block's last query, which nothing
       // has written: zero those V rows so that P = 0 never meets a non-finite value.
@@ -427,28 +439,33 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int vz = kmax - j * kTile + 1;  // first row to clear
         if (vz < kTile) {
           const int s = j % kPfStages;
-          (void)mbar_wait(smem_addr(&kv_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
+          (void)mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
           uint4 *v0 = reinterpret_cast<uint4 *>(stage_ptr(s) + 2 * kHalfTileBytes);
           uint4 *v1 = reinterpret_cast<uint4 *>(stage_ptr(s) + 3 * kHalfTileBytes);
           for (int c = vz * 8 + row; c < kTile * 8; c += kPfRows) {
             v0[c] = make_uint4(0, 0, 0, 0);
             v1[c] = make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&p_full[pb]));
+      if (lane == 0) mbar_arrive(smem_addr(&p_full[sb]));
     }
     if (!ok && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
 
     // epilogue: O / l as bf16 into this row's output (zeros for a sequence whose chunk is
     // out of range)
     griddep_launch_dependents();
+    // The final O is complete when the MMA thread's last commit (`drain`, one phase) fires.
+    // (o_done cannot say it: when the last S has been read, the P V before the last one may
+    // still be running, so o_done can be two phases behind, where a parity wait is
+    // ambiguous.)
     bool have_o = false;
     if (ok && n > 0) {
-      const bool done = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((n - 1) & 1));
+      const bool done = mbar_wait(smem_addr(drain), 0);
       have_o = __all_sync(0xffffffffu, done);
       if (!have_o && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
     }
@@ -459,7 +476,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int c4 = 0; c4 < 4; ++c4) {
       float o[32];
       if (have_o) {
-        tmem_ld32(tmem + lane_base + 128 + 32 * c4, o);
+        tmem_ld32(tmem + lane_base + kTmemO + 32 * c4, o);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -547,7 +564,9 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
     std::lock_guard<std::mutex> lk(g_pf_mu);
     if (!g_pf_configured[d.device]) {
       if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-          cudaSuccess) {
+              cudaSuccess ||
+          cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
         cudaGetLastError();
         return GQA_ERR_CUDA;
       }

@@ -124,6 +124,32 @@ def test_prompt_fed_in_chunks_matches_one_call():
     np.testing.assert_array_equal(bits(w.v_cache), ref["v_cache"])
 
 
+def test_repeated_calls_are_bitwise_identical():
+    """The kernels are deterministic: a race between the pipeline roles (a read of the
+    accumulator before its last product landed, a tile overwritten early) would show as
+    run-to-run differences.  Twelve calls of a 512-token chunk, then twelve of a chunked
+    prompt whose query blocks see one to five KV tiles."""
+    w = wl.make_prefill(1, 40, 8, 512, [1536], paged=False, seed=16, max_seq=2048, device="cuda")
+    first = run_gpu(w)
+    for _ in range(11):
+        assert torch.equal(run_gpu(w).view(torch.int16), first.view(torch.int16))
+    w = wl.make_prefill(1, 40, 8, 300, [0], paged=True, seed=12, max_seq=320, device="cuda")
+    k0, v0 = w.k_cache.clone(), w.v_cache.clone()
+    runs = []
+    for _ in range(12):
+        w.k_cache.copy_(k0)
+        w.v_cache.copy_(v0)
+        outs = []
+        for a, e in ((0, 128), (128, 256), (256, 300)):
+            part = wl.PrefillWorkload(**{**w.__dict__, "T": e - a, "q_new": w.q_new[:, a:e].contiguous(),
+                                         "k_new": w.k_new[:, a:e].contiguous(), "v_new": w.v_new[:, a:e].contiguous(),
+                                         "q_start": torch.tensor([a], dtype=torch.int32, device="cuda")})
+            outs.append(run_gpu(part))
+        runs.append(torch.cat(outs, dim=1).view(torch.int16))
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0])
+
+
 def test_out_of_range_chunks_give_zeros_and_flags():
     """Sequence 1's chunk runs past max_seq_len and sequence 2's starts before 0: both are
     flagged, write no cache row and output zeros; sequence 0 is unaffected."""
