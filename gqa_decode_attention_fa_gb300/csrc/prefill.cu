@@ -31,6 +31,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "launch.h"
@@ -64,6 +65,11 @@ constexpr int kOffBar = kOffKV + kPfStages * kStageBytes;
 // o_done, drain
 constexpr int kNumBars = 1 + 4 * kPfStages + 2 + 2 + 1 + 1;
 constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
+constexpr int kPfMaxSlots = 320;                // split-tile partials the static scratch holds
+constexpr int kPfMaxSplit = 4;                  // KV parts of one split query tile
+// A partial is column-major, [130][128 rows] floats: O columns, then m, then l, so that the
+// softmax warps (thread = row) write and read it in coalesced 128-byte lines.
+constexpr int kPartFloats = (kHeadDim + 2) * kPfRows;
 static_assert(kPfCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two prefill CTAs must share an SM");
 static_assert(kPfCtasPerSm * kPfTmemCols <= 512, "tensor memory of the co-resident CTAs");
 
@@ -83,6 +89,12 @@ struct PrefillParams {
   int paged, max_seq, max_blocks, num_blocks;
   float eps, scale_log2;
   double inv_freq[kHeadDim / 2];
+  // Work items (CTAs): ndp whole query tiles, then ntail tiles cut into ksplit KV parts
+  // each; a cut tile's parts leave fp32 partials in part[ntail * ksplit][kPartFloats] and
+  // the last to finish (ticket[tail index]) merges them.
+  int ndp, ntail, ksplit;
+  float *part;
+  unsigned int *ticket;
 };
 
 namespace {
@@ -109,9 +121,15 @@ __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x / p.T, i = blockIdx.x - b * p.T;
+  if (blockIdx.x == 0)  // the merge tickets start at zero (a merge also returns its ticket to zero)
+    for (int r = threadIdx.x; r < p.ntail; r += blockDim.x) p.ticket[r] = 0;
   const int s = p.q_start[b];
   if (!chunk_ok(p, s)) {
+    // a chunk outside [0, max_seq_len): flagged, nothing appended, zeros for its output
+    // (the attention kernel gives it no work)
     if (i == 0 && threadIdx.x == 0) atomicOr(p.err, s < 0 ? GQA_DEVERR_POSITION : GQA_DEVERR_SEQLEN);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<long long>(b) * p.T + i) * p.Hq * kHeadDim);
+    for (int c = threadIdx.x; c < p.Hq * kHeadDim / 8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
     return;
   }
   const int pos = s + i;
@@ -189,14 +207,24 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+  int *merge_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Work item: query blocks in decreasing order of their key count first, so that the
-  // longest CTAs start in the first wave.
+  // Work item: query tiles in decreasing order of their key count (query blocks from the
+  // last to the first), so that the longest start first.  The first ndp items are whole
+  // tiles; the rest are the KV parts of the last ntail tiles -- the final partial round of
+  // CTA slots -- which fill the slots that free up first.
+  const int x = static_cast<int>(blockIdx.x);
+  int tile = x, part = 0;
+  if (x >= p.ndp) {
+    tile = p.ndp + (x - p.ndp) / p.ksplit;
+    part = (x - p.ndp) % p.ksplit;
+  }
+  const bool split = x >= p.ndp;
   const int bk = p.B * p.Hkv;
-  const int qb = p.nqb - 1 - static_cast<int>(blockIdx.x) / bk;
-  const int rem = static_cast<int>(blockIdx.x) % bk;
+  const int qb = p.nqb - 1 - tile / bk;
+  const int rem = tile % bk;
   const int b = rem / p.Hkv, kv = rem - b * p.Hkv;
   const int t0 = qb * p.Tt;                       // first chunk token of the block
   const int t_end = min(t0 + p.Tt, p.T);          // one past its last
@@ -228,7 +256,10 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   // KV tiles the block needs: up to the one holding its last query's position; the
   // tiles after it are wholly in the future of every query and are never loaded.
   const int kmax = s0 + t_end - 1;
-  const int n = seq_ok ? kmax / kTile + 1 : 0;
+  const int n = seq_ok ? kmax / kTile + 1 : 0;  // 0: the prologue kernel wrote its zeros
+  // this item's KV tiles [j0, j1) of the n (a part of a cut tile may be empty)
+  const int j0 = split ? n * part / p.ksplit : 0, j1 = split ? n * (part + 1) / p.ksplit : n;
+  const int nt = j1 - j0;
   uint8_t *const qs = smem + kOffQ;
   auto stage_ptr = [&](int s) { return smem + kOffKV + s * kStageBytes; };
 
@@ -236,7 +267,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     // ------------------------------------------------------------------ TMA producer
     // Order: K_0, K_1, V_0, K_2, V_1, ... -- a K tile is released once S has used it, a V
     // tile only after P V, so K runs one tile ahead.
-    if (lane == 0 && n > 0) {
+    if (lane == 0 && nt > 0) {
       const uint32_t qb_bytes = 2u * 64u * 2u * static_cast<uint32_t>(p.G * p.Tt);
       mbar_arrive_expect_tx(smem_addr(q_full), qb_bytes);
       tma_load_4d(smem_addr(qs), &tmQ, smem_addr(q_full), 0, kv * p.G, t0, b);
@@ -252,35 +283,36 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       };
       int kissued = 0, vissued = 0;
       bool ok = true;
-      auto load_k = [&](int j) -> bool {
-        const int s = j % kPfStages;
-        if (j >= kPfStages && !mbar_wait(smem_addr(&k_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1)))
+      // i counts the item's KV tiles (stages and phases), j = j0 + i is the tile
+      auto load_k = [&](int i) -> bool {
+        const int s = i % kPfStages;
+        if (i >= kPfStages && !mbar_wait(smem_addr(&k_empty[s]), static_cast<uint32_t>((i / kPfStages - 1) & 1)))
           return false;
-        const int row = row_of(j);
+        const int row = row_of(j0 + i);
         const uint32_t fb = smem_addr(&k_full[s]), base = smem_addr(stage_ptr(s));
         mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
         tma_load_3d(base, &tmK, fb, 0, kv, row);
         tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, row);
-        kissued = j + 1;
+        kissued = i + 1;
         return true;
       };
-      auto load_v = [&](int j) -> bool {
-        const int s = j % kPfStages;
-        if (j >= kPfStages && !mbar_wait(smem_addr(&v_empty[s]), static_cast<uint32_t>((j / kPfStages - 1) & 1)))
+      auto load_v = [&](int i) -> bool {
+        const int s = i % kPfStages;
+        if (i >= kPfStages && !mbar_wait(smem_addr(&v_empty[s]), static_cast<uint32_t>((i / kPfStages - 1) & 1)))
           return false;
-        const int row = row_of(j);
+        const int row = row_of(j0 + i);
         const uint32_t fb = smem_addr(&v_full[s]), base = smem_addr(stage_ptr(s)) + 2 * kHalfTileBytes;
         mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
         tma_load_3d(base, &tmV, fb, 0, kv, row);
         tma_load_3d(base + kHalfTileBytes, &tmV, fb, 64, kv, row);
-        vissued = j + 1;
+        vissued = i + 1;
         return true;
       };
-      for (int j = 0; j < n && ok; ++j) {
-        ok = load_k(j);
-        if (ok && j >= 1) ok = load_v(j - 1);
+      for (int i = 0; i < nt && ok; ++i) {
+        ok = load_k(i);
+        if (ok && i >= 1) ok = load_v(i - 1);
       }
-      if (ok) ok = load_v(n - 1);
+      if (ok) ok = load_v(nt - 1);
       if (!ok) {
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
         // Do not leave while copies into this CTA's shared memory may still be in flight.
@@ -295,7 +327,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     // ------------------------------------------------------------------ MMA issuer
     // Issue order: S_0, S_1, PV_0, S_2, PV_1, ...  S_j overwrites the buffer that held
     // P_{j-2}; P_{j-2} V was issued before it and the tensor pipe runs them in order.
-    if (lane == 0 && n > 0) {
+    if (lane == 0 && nt > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kPfRows, kTile, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(kPfRows, kHeadDim, false, true);
       const uint32_t qa = smem_addr(qs);
@@ -320,7 +352,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         umma_commit(smem_addr(o_done));
         return true;
       };
-      for (int j = 0; j < n && ok; ++j) {
+      for (int j = 0; j < nt && ok; ++j) {  // j counts the item's KV tiles
         const int s = j % kPfStages, sb = j & 1;
         ok = mbar_wait(smem_addr(&k_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
         if (!ok) break;
@@ -334,7 +366,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         umma_commit(smem_addr(&s_full[sb]));
         if (j >= 1) ok = issue_pv(j - 1);
       }
-      if (ok) ok = issue_pv(n - 1);
+      if (ok) ok = issue_pv(nt - 1);
       if (!ok) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
       umma_commit(smem_addr(drain));  // lets the teardown wait for every MMA issued
     }
@@ -350,9 +382,9 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     float m_run = valid ? -INFINITY : 0.f;  // invalid rows: every score masked, P = 0
     float l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(smem_addr(&s_full[sb]), static_cast<uint32_t>((j >> 1) & 1));
+    for (int i = 0; i < nt; ++i) {  // i counts the item's KV tiles, j is the tile
+      const int j = j0 + i, sb = i & 1;
+      ok = mbar_wait(smem_addr(&s_full[sb]), static_cast<uint32_t>((i >> 1) & 1));
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -391,16 +423,16 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       float corr = 1.f;
       bool resc = false;
       if (m_new > m_run + kRescaleLog2) {
-        corr = fast_exp2(m_run - m_new);  // m_run = -inf on the first tile: 0
+        corr = fast_exp2(m_run - m_new);  // m_run = -inf before the row's first visible key: 0
         m_run = m_new;
         l_run *= corr;
-        resc = j > 0;
+        resc = i > 0;
       }
       if (__any_sync(0xffffffffu, resc)) {
         // O must hold P_0..P_{j-1} V before it is scaled: wait for the last P V.  (S_j was
         // issued after P_{j-2} V, so o_done has completed that phase: the parity wait
         // below is never more than one phase ahead of the barrier.)
-        ok = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((j - 1) & 1));
+        ok = mbar_wait(smem_addr(o_done), static_cast<uint32_t>((i - 1) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -420,7 +452,9 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       // P = 2^(s - m) as bf16 hi + lo pairs into the S buffer's columns
       uint32_t ph[32], pl[32];
       float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      const float neg_m = -m_run;
+      // (a row that has seen no visible key yet -- in a part that starts past its position --
+      // keeps m = -inf and gets P = 0)
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float v0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, neg_m));
@@ -438,8 +472,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       if (j == n - 1) {
         const int vz = kmax - j * kTile + 1;  // first row to clear
         if (vz < kTile) {
-          const int s = j % kPfStages;
-          (void)mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
+          const int s = i % kPfStages;
+          (void)mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((i / kPfStages) & 1));
           uint4 *v0 = reinterpret_cast<uint4 *>(stage_ptr(s) + 2 * kHalfTileBytes);
           uint4 *v1 = reinterpret_cast<uint4 *>(stage_ptr(s) + 3 * kHalfTileBytes);
           for (int c = vz * 8 + row; c < kTile * 8; c += kPfRows) {
@@ -456,38 +490,123 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     }
     if (!ok && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
 
-    // epilogue: O / l as bf16 into this row's output (zeros for a sequence whose chunk is
-    // out of range)
+    // epilogue: O / l as bf16 into this row's output, or, for a part of a cut tile, its
+    // partial and the merge
     griddep_launch_dependents();
     // The final O is complete when the MMA thread's last commit (`drain`, one phase) fires.
     // (o_done cannot say it: when the last S has been read, the P V before the last one may
     // still be running, so o_done can be two phases behind, where a parity wait is
     // ambiguous.)
     bool have_o = false;
-    if (ok && n > 0) {
+    if (ok && nt > 0) {
       const bool done = mbar_wait(smem_addr(drain), 0);
       have_o = __all_sync(0xffffffffu, done);
       if (!have_o && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
     }
     if (have_o) tc_fence_after();
     uint16_t *dst = p.out + ((static_cast<long long>(b) * p.T + t) * p.Hq + kv * p.G + g) * kHeadDim;
-    const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
+    if (nt > 0 && !split) {
+      const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      float o[32];
-      if (have_o) {
-        tmem_ld32(tmem + lane_base + kTmemO + 32 * c4, o);
-        tmem_wait_ld();
-      } else {
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + kTmemO + 32 * c4, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0.f;
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+        if (in_block) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c4);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv),
+                               pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                               pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                               pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+        }
       }
-      if (in_block) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c4);
+    } else if (nt > 0) {
+      // A part of a cut tile: leave (O, m, l) in its slot, take the tile's ticket; the last
+      // of its non-empty parts merges them: M = max m_k,
+      // out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k.
+      const int r = tile - p.ndp;
+      auto slot = [&](int pt) { return p.part + (static_cast<long long>(r) * p.ksplit + pt) * kPartFloats; };
+      auto part_has_tiles = [&](int pt) { return n * pt / p.ksplit < n * (pt + 1) / p.ksplit; };
+      float *mine = slot(part);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack_bf16(o[8 * q] * inv, o[8 * q + 1] * inv), pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                             pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv), pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float o[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + kTmemO + 32 * c4, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mine[(32 * c4 + e) * kPfRows + row] = o[e];
+      }
+      mine[kHeadDim * kPfRows + row] = m_run;
+      mine[(kHeadDim + 1) * kPfRows + row] = have_o ? l_run : 0.f;
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kPfRows) : "memory");  // the four softmax warps
+      if (row == 0) {
+        int np = 0;
+        for (int pt = 0; pt < p.ksplit; ++pt) np += part_has_tiles(pt) ? 1 : 0;
+        const unsigned prev = atomicAdd(&p.ticket[r], 1u);
+        const bool last = prev == static_cast<unsigned>(np - 1);
+        if (last) {
+          __threadfence();
+          p.ticket[r] = 0;  // ready for the next call
+        }
+        *merge_flag = last ? 1 : 0;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kPfRows) : "memory");
+      if (*merge_flag) {
+        // weight of part pt for this row: 2^(m_pt - M) / L (0 for an empty part or a row
+        // the part did not see)
+        float wgt[kPfMaxSplit];
+        float M = -INFINITY, L = 0.f;
+#pragma unroll
+        for (int pt = 0; pt < kPfMaxSplit; ++pt) {
+          wgt[pt] = 0.f;
+          if (pt < p.ksplit && part_has_tiles(pt)) {
+            const float lv = __ldcg(slot(pt) + (kHeadDim + 1) * kPfRows + row);
+            const float mv = __ldcg(slot(pt) + kHeadDim * kPfRows + row);
+            wgt[pt] = lv > 0.f ? mv : -INFINITY;  // m for now
+            if (lv > 0.f) M = fmaxf(M, mv);
+          } else {
+            wgt[pt] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int pt = 0; pt < kPfMaxSplit; ++pt) {
+          if (wgt[pt] != -INFINITY) {
+            const float f = fast_exp2(wgt[pt] - M);
+            L += f * __ldcg(slot(pt) + (kHeadDim + 1) * kPfRows + row);
+            wgt[pt] = f;
+          } else {
+            wgt[pt] = 0.f;
+          }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int pt = 0; pt < kPfMaxSplit; ++pt) wgt[pt] *= inv;
+        for (int c8 = 0; c8 < kHeadDim / 8; ++c8) {
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int pt = 0; pt < kPfMaxSplit; ++pt) {
+            if (wgt[pt] == 0.f) continue;
+            const float *pp = slot(pt) + (8 * c8) * kPfRows + row;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt[pt], __ldcg(pp + e * kPfRows), acc[e]);
+          }
+          if (in_block)
+            reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                                                            pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+        }
       }
     }
   }
@@ -498,7 +617,7 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   __syncthreads();
   if (warp == kPfMmaWarp) {
     tc_fence_after();
-    if (n > 0) (void)mbar_wait(smem_addr(drain), 0);
+    if (nt > 0) (void)mbar_wait(smem_addr(drain), 0);
     __syncwarp();
     tmem_dealloc(tmem, kPfTmemCols);
   }
@@ -509,7 +628,13 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
 namespace {
 
 std::mutex g_pf_mu;
-bool g_pf_configured[64];
+struct PfDevice {
+  bool configured = false;
+  int sms = 0;
+  float *part = nullptr;
+  unsigned int *ticket = nullptr;
+};
+PfDevice g_pf_dev[64];
 
 gqa_status_t check_desc(const gqa_prefill_desc_t &d) {
   if (d.head_dim != kHeadDim) return GQA_ERR_UNSUPPORTED;
@@ -532,6 +657,9 @@ bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 
 // A per-call error word when the caller passes none (nothing reads it).
 static __device__ uint32_t g_prefill_err_sink;
+// Partials of the query tiles cut into KV parts, and their merge tickets.
+static __device__ __align__(16) float g_pf_part[kPfMaxSlots * kPartFloats];
+static __device__ unsigned int g_pf_ticket[kPfMaxSlots];
 
 }  // namespace gqa
 
@@ -560,18 +688,28 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   if (d.device >= 64) return GQA_ERR_UNSUPPORTED;
   DeviceGuard guard(d.device);
   if (!guard.ok) return GQA_ERR_CUDA;
+  PfDevice dev;
   {
+    // first call on the device: shared-memory limits, SM count, the split-tile scratch
     std::lock_guard<std::mutex> lk(g_pf_mu);
-    if (!g_pf_configured[d.device]) {
+    PfDevice &pd = g_pf_dev[d.device];
+    if (!pd.configured) {
+      void *part = nullptr, *ticket = nullptr;
       if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
               cudaSuccess ||
           cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+                               cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+          cudaDeviceGetAttribute(&pd.sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
+          cudaGetSymbolAddress(&part, g_pf_part) != cudaSuccess ||
+          cudaGetSymbolAddress(&ticket, g_pf_ticket) != cudaSuccess) {
         cudaGetLastError();
         return GQA_ERR_CUDA;
       }
-      g_pf_configured[d.device] = true;
+      pd.part = static_cast<float *>(part);
+      pd.ticket = static_cast<unsigned int *>(ticket);
+      pd.configured = true;
     }
+    dev = pd;
   }
   uint32_t *err = device_errors;
   if (!err) {
@@ -596,6 +734,8 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   p.k_norm_w = static_cast<const uint16_t *>(k_norm_w);
   p.out = static_cast<uint16_t *>(out);
   p.err = err;
+  p.part = dev.part;
+  p.ticket = dev.ticket;
   p.B = d.batch;
   p.T = d.chunk_len;
   p.Hq = d.num_q_heads;
@@ -603,6 +743,25 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   p.G = d.num_q_heads / d.num_kv_heads;
   p.Tt = kPfRows / p.G;
   p.nqb = (p.T + p.Tt - 1) / p.Tt;
+  // Work items: whole query tiles fill complete rounds of the CTA slots (two per SM); the
+  // tiles of the last, partial round are cut into up to kPfMaxSplit KV parts each, so that
+  // their parts fill the slots the whole tiles leave free (the cut tiles' partials must fit
+  // the static scratch: ntail * ksplit <= kPfMaxSlots).
+  {
+    const long long tiles = static_cast<long long>(p.nqb) * p.B * p.Hkv;
+    const long long slots = std::min<long long>(static_cast<long long>(dev.sms) * kPfCtasPerSm, kPfMaxSlots);
+    const long long tail = tiles % slots;
+    const long long k = tail > 0 ? std::min<long long>(kPfMaxSplit, slots / tail) : 1;
+    if (k > 1) {
+      p.ndp = static_cast<int>(tiles - tail);
+      p.ntail = static_cast<int>(tail);
+      p.ksplit = static_cast<int>(k);
+    } else {
+      p.ndp = static_cast<int>(tiles);
+      p.ntail = 0;
+      p.ksplit = 1;
+    }
+  }
   p.paged = paged ? 1 : 0;
   p.max_seq = d.max_seq_len;
   p.max_blocks = (d.max_seq_len + kTile - 1) / kTile;
@@ -628,7 +787,7 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_pdl(prefill_rope_kernel, dim3(static_cast<unsigned>(p.B * p.T)), dim3(256), 0, s, p) != cudaSuccess)
     return GQA_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>(p.nqb * p.B * p.Hkv);
+  const unsigned grid = static_cast<unsigned>(p.ndp + p.ntail * p.ksplit);
   if (launch_pdl(prefill_attn_kernel, dim3(grid), dim3(kPfThreads), static_cast<size_t>(kSmemBytes), s, tq, tk, tv,
                  p) != cudaSuccess)
     return GQA_ERR_CUDA;
