@@ -91,3 +91,51 @@ def test_partition_worker_lookup_agrees_with_ranges():
             for x in set([0, T - 1, T // 2, T // 3] + list(range(0, T, max(1, T // 50)))):
                 w = ((x + 1) * W - 1) // T
                 assert rng[w, 0] <= x < rng[w, 1]
+
+
+# ----------------------------------------------------------------------------- prefill entry
+
+def _prefill(**over):
+    """gqa_prefill_attn with non-null dummy tensors: rejected on its arguments before any
+    device work (the pointers are never dereferenced)."""
+    d = dict(batch=1, num_q_heads=40, num_kv_heads=8, head_dim=128, chunk_len=16, block_size=0,
+             max_seq_len=64, num_cache_blocks=0, device=0)
+    d.update(over)
+    desc = binding.PrefillDesc(*[d[n] for n, _ in binding.PrefillDesc._fields_])
+    dummy = ctypes.c_void_p(4096)
+    pt = dummy if d["block_size"] else None
+    return binding.load().gqa_prefill_attn(ctypes.byref(desc), dummy, dummy, dummy, dummy, dummy, pt, dummy, None,
+                                           None, ctypes.c_float(1e6), ctypes.c_float(1e-6), dummy, None, None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(batch=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(chunk_len=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(chunk_len=65), binding.GQA_ERR_INVALID_ARG),          # longer than the capacity
+    (dict(head_dim=64), binding.GQA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=34, num_kv_heads=2), binding.GQA_ERR_UNSUPPORTED),   # G = 17
+    (dict(num_q_heads=10, num_kv_heads=4), binding.GQA_ERR_UNSUPPORTED),   # H_q % H_kv != 0
+    (dict(block_size=32), binding.GQA_ERR_UNSUPPORTED),
+    (dict(block_size=64, num_cache_blocks=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(batch=1025), binding.GQA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_geometry(over, status):
+    assert _prefill(**over) == status
+
+
+def test_prefill_rejects_null_and_inconsistent_arguments():
+    lib = binding.load()
+    args = [None] * 10 + [ctypes.c_float(1e6), ctypes.c_float(1e-6), None, None, None]
+    assert lib.gqa_prefill_attn(*args) == binding.GQA_ERR_INVALID_ARG      # NULL desc
+    desc = binding.PrefillDesc(1, 40, 8, 128, 16, 0, 64, 0, 0)
+    dummy = ctypes.c_void_p(4096)
+    # a page table for a contiguous cache
+    assert lib.gqa_prefill_attn(ctypes.byref(desc), dummy, dummy, dummy, dummy, dummy, dummy, dummy, None, None,
+                                ctypes.c_float(1e6), ctypes.c_float(1e-6), dummy, None, None) == binding.GQA_ERR_INVALID_ARG
+    # theta <= 0
+    assert lib.gqa_prefill_attn(ctypes.byref(desc), dummy, dummy, dummy, dummy, dummy, None, dummy, None, None,
+                                ctypes.c_float(0.0), ctypes.c_float(1e-6), dummy, None, None) == binding.GQA_ERR_INVALID_ARG
+    # a misaligned bf16 tensor
+    odd = ctypes.c_void_p(4096 + 2)
+    assert lib.gqa_prefill_attn(ctypes.byref(desc), odd, dummy, dummy, dummy, dummy, None, dummy, None, None,
+                                ctypes.c_float(1e6), ctypes.c_float(1e-6), dummy, None, None) == binding.GQA_ERR_INVALID_ARG
