@@ -71,6 +71,15 @@ def _load():
             lib.oracle_prefill_attention.restype = ctypes.c_int
             lib.oracle_prefill_blocked.argtypes = [ctypes.POINTER(Geom), ctypes.c_int, P, P, P, P, P,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+            lib.oracle_lloyd_max.argtypes = [ctypes.c_int, P, P]
+            lib.oracle_lloyd_max.restype = ctypes.c_int
+            lib.oracle_rotate.argtypes = [P, P, ctypes.c_int, P]
+            lib.oracle_unrotate.argtypes = [P, P, ctypes.c_int, P]
+            lib.oracle_q4_quantize.argtypes = [P, P, P, ctypes.c_int, P, P]
+            lib.oracle_q4_dequantize.argtypes = [P, ctypes.c_double, P, P, ctypes.c_int, P]
+            lib.oracle_q4_decode_step.argtypes = [ctypes.POINTER(Geom)] + [P] * 12 + [
+                ctypes.c_double, ctypes.c_double, P, P, P, ctypes.c_int, P, P]
+            lib.oracle_q4_decode_step.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -240,6 +249,77 @@ def prefill_step(g: Geom, T: int, q_new, k_new, v_new, k_cache, v_cache, page_ta
                                          q_norm_w, k_norm_w, rope_theta, eps)
     out, used = prefill_attention(g, T, q_rot, kc, vc, page_table, q_start, triples=triples, threads=threads)
     return dict(out=out, q_rot=q_rot, k_cache=kc, v_cache=vc, status=st, threads=used)
+
+
+# ----------------------------------------------------------------------------- 4-bit KV cache
+
+def lloyd_max(levels: int = 16):
+    """(levels ascending, thresholds, iterations) of the Lloyd-Max quantizer of N(0,1)."""
+    lv = np.zeros(levels)
+    thr = np.zeros(levels - 1)
+    it = _load().oracle_lloyd_max(int(levels), _ptr(lv), _ptr(thr))
+    return lv, thr, it
+
+
+def rotate(x, signs) -> np.ndarray:
+    x = _c(x, np.float64)
+    sg = _c(signs, np.int8)
+    y = np.empty_like(x)
+    _load().oracle_rotate(_ptr(x), _ptr(sg), x.shape[0], _ptr(y))
+    return y
+
+
+def unrotate(y, signs) -> np.ndarray:
+    y = _c(y, np.float64)
+    sg = _c(signs, np.int8)
+    x = np.empty_like(y)
+    _load().oracle_unrotate(_ptr(y), _ptr(sg), y.shape[0], _ptr(x))
+    return x
+
+
+def q4_quantize(x, signs, codebook_bits):
+    """(packed uint8[d/2], sigma) of one row."""
+    x = _c(x, np.float64)
+    sg, cb = _c(signs, np.int8), _c(codebook_bits, np.uint16)
+    packed = np.zeros(x.shape[0] // 2, dtype=np.uint8)
+    sigma = ctypes.c_double()
+    _load().oracle_q4_quantize(_ptr(x), _ptr(sg), _ptr(cb), x.shape[0], _ptr(packed), ctypes.byref(sigma))
+    return packed, sigma.value
+
+
+def q4_dequantize(packed, sigma: float, signs, codebook_bits) -> np.ndarray:
+    pk = _c(packed, np.uint8)
+    sg, cb = _c(signs, np.int8), _c(codebook_bits, np.uint16)
+    x = np.zeros(pk.shape[0] * 2)
+    _load().oracle_q4_dequantize(_ptr(pk), float(sigma), _ptr(sg), _ptr(cb), x.shape[0], _ptr(x))
+    return x
+
+
+def q4_decode_step(g: Geom, q_new, k_new, v_new, k_idx, v_idx, k_scale, v_scale, page_table, seq_lens, positions,
+                   q_norm_w, k_norm_w, rope_theta: float, eps: float, signs, codebook_bits, pairs=None):
+    """The decode step over a 4-bit cache.  Returns dict(out, q_rot, k_idx, v_idx, k_scale,
+    v_scale, status); the input caches are not modified."""
+    q_new, k_new, v_new = (_c(a, np.uint16) for a in (q_new, k_new, v_new))
+    ki = np.array(k_idx, dtype=np.uint8, copy=True, order="C")
+    vi = np.array(v_idx, dtype=np.uint8, copy=True, order="C")
+    ks = np.array(k_scale, dtype=np.float32, copy=True, order="C")
+    vs = np.array(v_scale, dtype=np.float32, copy=True, order="C")
+    pt, sl, pos = _c(page_table, np.int32), _c(seq_lens, np.int32), _c(positions, np.int32)
+    qw, kw = _c(q_norm_w, np.uint16), _c(k_norm_w, np.uint16)
+    sg, cb = _c(signs, np.int8), _c(codebook_bits, np.uint16)
+    q_rot = np.zeros((g.B, g.Hq, g.d), dtype=np.uint16)
+    if pairs is not None:
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((pr.shape[0], g.d))
+        npairs = pr.shape[0]
+    else:
+        pr, npairs = None, 0
+        out = np.zeros((g.B, g.Hq, g.d))
+    st = _load().oracle_q4_decode_step(ctypes.byref(g), _ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(ki), _ptr(vi),
+                                       _ptr(ks), _ptr(vs), _ptr(pt), _ptr(sl), _ptr(pos), _ptr(qw), _ptr(kw),
+                                       float(rope_theta), float(eps), _ptr(sg), _ptr(cb), _ptr(pr), npairs,
+                                       _ptr(q_rot), _ptr(out))
+    return dict(out=out, q_rot=q_rot, k_idx=ki, v_idx=vi, k_scale=ks, v_scale=vs, status=st)
 
 
 def max_threads() -> int:

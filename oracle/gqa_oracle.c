@@ -24,13 +24,17 @@
  *     per-tile recurrence of ADR-0060 section 3 and the log-sum-exp merge of section 4,
  *     so that the two can be checked against each other.
  *
+ *   - The 4-bit KV cache ("Qwen3-14B Optimization", section 2.3): Lloyd-Max codebook
+ *     indices packed two per byte, dequantized by gather, renormalize, scale, unrotate.
  *   - Chunked causal prefill: the same per-token prologue for a block of T new tokens,
  *     then causal attention of each of them over the cache (ADR-0060 section 5.4); a
  *     blocked form follows that section's past / partial / future tile classes.
  *
  * Parity pins (the tests that tie this file to the pages and to mathematics, not to
- * itself) live in tests/test_oracle_pins.py and tests/test_oracle_prefill_pins.py.
+ * itself) live in tests/test_oracle_pins.py, tests/test_oracle_prefill_pins.py and
+ * tests/test_oracle_q4_pins.py.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -504,6 +508,195 @@ void oracle_prefill_blocked(const oracle_geom_t *g, int T, const uint16_t *q_rot
             for (int e = 0; e < d; ++e) out[(long long)(i0 + r) * d + e] /= l[r];
     }
     free(S); free(m); free(l);
+}
+
+/* ------------------------------------------------------------------ 4-bit KV cache */
+
+/* The quantized KV cache of "Qwen3-14B Optimization", section 2.3 (TurboQuant): each
+ * cache row (one token, one KV head, d = 128) is stored as 4-bit Lloyd-Max codebook
+ * indices, two per byte -- byte c holds idx[c + 64] * 16 + idx[c] -- and dequantized by
+ * gather -> renormalize -> scale -> unrotate.  The pages give neither the codebook, the
+ * rotation nor the scale format; the readings here (and in the library):
+ *   codebook  the 16 reconstruction levels of the Lloyd-Max quantizer of a standard
+ *             normal variable (Lloyd's algorithm; Max 1960), as bf16 values (an input);
+ *   rotation  R = H D / sqrt(d): the Sylvester-ordered Walsh-Hadamard matrix times a
+ *             diagonal of +-1 signs (an input), orthogonal;
+ *   quantize  s = ||x||, t = sqrt(d) R x / s, idx_i = the nearest level to t_i (the lower
+ *             index on a tie);
+ *   scale     one per row: sigma = s / ||c[idx]||, so that the dequantized row is
+ *             x^ = sigma R^T c[idx]  (gather c[idx], renormalize to unit length, scale by
+ *             s, unrotate).  A zero row has s = 0 and dequantizes to zero.            */
+
+/* Lloyd's algorithm for the `levels`-level quantizer of N(0,1): thresholds at the
+ * midpoints of adjacent levels, each level the conditional mean of its cell,
+ *   E[X | a < X < b] = (phi(a) - phi(b)) / (Phi(b) - Phi(a)),
+ * iterated from uniformly spaced levels until nothing moves.  Writes levels[levels]
+ * (ascending) and thresholds[levels - 1]; returns the iterations used.                 */
+static double std_pdf(double x) { return exp(-0.5 * x * x) / sqrt(2.0 * M_PI); }
+static double std_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
+int oracle_lloyd_max(int levels, double *lv, double *thr) {
+    for (int j = 0; j < levels; ++j) lv[j] = -3.0 + 6.0 * (j + 0.5) / levels;
+    int it;
+    for (it = 0; it < 100000; ++it) {
+        for (int j = 0; j + 1 < levels; ++j) thr[j] = 0.5 * (lv[j] + lv[j + 1]);
+        double moved = 0.0;
+        for (int j = 0; j < levels; ++j) {
+            double a = j == 0 ? -INFINITY : thr[j - 1], b = j + 1 == levels ? INFINITY : thr[j];
+            double pa = isinf(a) ? 0.0 : std_pdf(a), pb = isinf(b) ? 0.0 : std_pdf(b);
+            double mass = (isinf(b) ? 1.0 : std_cdf(b)) - (isinf(a) ? 0.0 : std_cdf(a));
+            double c = (pa - pb) / mass;
+            moved = fmax(moved, fabs(c - lv[j]));
+            lv[j] = c;
+        }
+        if (moved < 1e-15) break;
+    }
+    for (int j = 0; j + 1 < levels; ++j) thr[j] = 0.5 * (lv[j] + lv[j + 1]);
+    return it;
+}
+
+/* y = R x = H (D x) / sqrt(d) and x = R^T y = D H y / sqrt(d), H the Sylvester Hadamard
+ * matrix (H[i][j] = (-1)^popcount(i & j)), written out as the plain matrix product.  */
+static int popcount_i(int v) { int c = 0; while (v) { c += v & 1; v >>= 1; } return c; }
+
+void oracle_rotate(const double *x, const int8_t *signs, int d, double *y) {
+    for (int i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += ((popcount_i(i & j) & 1) ? -1.0 : 1.0) * signs[j] * x[j];
+        y[i] = acc / sqrt((double)d);
+    }
+}
+
+void oracle_unrotate(const double *y, const int8_t *signs, int d, double *x) {
+    for (int j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += ((popcount_i(i & j) & 1) ? -1.0 : 1.0) * y[i];
+        x[j] = signs[j] * acc / sqrt((double)d);
+    }
+}
+
+/* Quantize one row x[d] (d = 128): packed[d / 2] bytes and *sigma.                      */
+void oracle_q4_quantize(const double *x, const int8_t *signs, const uint16_t *codebook_bf16, int d,
+                        uint8_t *packed, double *sigma) {
+    double c[16], y[256];
+    int idx[256];
+    for (int j = 0; j < 16; ++j) c[j] = oracle_bf16_to_double(codebook_bf16[j]);
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) s += x[i] * x[i];
+    s = sqrt(s);
+    oracle_rotate(x, signs, d, y);
+    double cn = 0.0;
+    for (int i = 0; i < d; ++i) {
+        double t = s > 0.0 ? sqrt((double)d) * y[i] / s : 0.0;
+        int best = 0;
+        for (int j = 1; j < 16; ++j)
+            if (fabs(t - c[j]) < fabs(t - c[best])) best = j;
+        idx[i] = best;
+        cn += c[best] * c[best];
+    }
+    for (int b = 0; b < d / 2; ++b) packed[b] = (uint8_t)(idx[b + d / 2] * 16 + idx[b]);
+    *sigma = s > 0.0 ? s / sqrt(cn) : 0.0;
+}
+
+/* The dequantized row x^ = sigma R^T c[idx] of a packed row.                            */
+void oracle_q4_dequantize(const uint8_t *packed, double sigma, const int8_t *signs,
+                          const uint16_t *codebook_bf16, int d, double *x) {
+    double y[256];
+    for (int i = 0; i < d; ++i) {
+        int idx = i < d / 2 ? packed[i] % 16 : packed[i - d / 2] / 16;
+        y[i] = sigma * oracle_bf16_to_double(codebook_bf16[idx]);
+    }
+    oracle_unrotate(y, signs, d, x);
+}
+
+/* One decode step over a 4-bit cache.  As oracle_prologue + oracle_attention, except that
+ * the new token's k row (the exact RoPE(RMSNorm(k_new)) value) and v row (v_new) are
+ * quantized into k_idx/v_idx [rows, H_kv, d/2] and k_scale/v_scale [rows, H_kv] (fp32),
+ * and attention reads the dequantized rows x^ of the cache.  Brute force per (b, h); out
+ * [B, H_q, d] (or the listed (b, h) pairs).  Returns the status of the prologue.        */
+int oracle_q4_decode_step(const oracle_geom_t *g,
+                          const uint16_t *q_new, const uint16_t *k_new, const uint16_t *v_new,
+                          uint8_t *k_idx, uint8_t *v_idx, float *k_scale, float *v_scale,
+                          const int32_t *page_table, const int32_t *seq_lens, const int32_t *positions,
+                          const uint16_t *q_norm_w, const uint16_t *k_norm_w, double rope_theta, double eps,
+                          const int8_t *signs, const uint16_t *codebook,
+                          const int32_t *pairs, int n_pairs, uint16_t *q_rot, double *out) {
+    const int d = g->d, half = d / 2;
+    int status = 0;
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    double *x = malloc(sizeof(double) * d), *y = malloc(sizeof(double) * d), *z = malloc(sizeof(double) * d);
+    double *qw = malloc(sizeof(double) * d), *kw = malloc(sizeof(double) * d);
+    for (int i = 0; i < d; ++i) {
+        qw[i] = q_norm_w ? oracle_bf16_to_double(q_norm_w[i]) : 1.0;
+        kw[i] = k_norm_w ? oracle_bf16_to_double(k_norm_w[i]) : 1.0;
+    }
+    int *ok = calloc((size_t)g->B, sizeof(int));
+    for (int b = 0; b < g->B; ++b) {
+        int L = seq_lens[b], p = positions[b];
+        if (L < 1 || L > g->max_seq) { status = 2; continue; }
+        if (p < 0 || p >= L) { status = 1; continue; }
+        long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, p);
+        if (row < 0 || row >= g->num_rows) { status = 3; continue; }
+        ok[b] = 1;
+        for (int h = 0; h < g->Hq; ++h) {
+            const uint16_t *src = q_new + ((long long)b * g->Hq + h) * d;
+            for (int i = 0; i < d; ++i) x[i] = oracle_bf16_to_double(src[i]);
+            oracle_rmsnorm(x, q_norm_w ? qw : NULL, d, eps, y);
+            oracle_rope(y, d, p, rope_theta, z);
+            for (int i = 0; i < d; ++i) q_rot[((long long)b * g->Hq + h) * d + i] = oracle_round_bf16(z[i]);
+        }
+        for (int kv = 0; kv < g->Hkv; ++kv) {
+            const uint16_t *src = k_new + ((long long)b * g->Hkv + kv) * d;
+            for (int i = 0; i < d; ++i) x[i] = oracle_bf16_to_double(src[i]);
+            oracle_rmsnorm(x, k_norm_w ? kw : NULL, d, eps, y);
+            oracle_rope(y, d, p, rope_theta, z);
+            double sg;
+            oracle_q4_quantize(z, signs, codebook, d, k_idx + (row * g->Hkv + kv) * half, &sg);
+            k_scale[row * g->Hkv + kv] = (float)sg;
+            const uint16_t *vs = v_new + ((long long)b * g->Hkv + kv) * d;
+            for (int i = 0; i < d; ++i) x[i] = oracle_bf16_to_double(vs[i]);
+            oracle_q4_quantize(x, signs, codebook, d, v_idx + (row * g->Hkv + kv) * half, &sg);
+            v_scale[row * g->Hkv + kv] = (float)sg;
+        }
+    }
+    long long n = pairs ? n_pairs : (long long)g->B * g->Hq;
+#pragma omp parallel
+    {
+        double *kr = malloc(sizeof(double) * d), *vr = malloc(sizeof(double) * d);
+        double *sc = malloc(sizeof(double) * (size_t)(g->max_seq > 0 ? g->max_seq : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long long k = 0; k < n; ++k) {
+            int b = pairs ? pairs[2 * k] : (int)(k / g->Hq), h = pairs ? pairs[2 * k + 1] : (int)(k % g->Hq);
+            double *o = out + k * d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (!ok[b]) continue;
+            const int G = g->Hq / g->Hkv, kv = h / G, L = seq_lens[b];
+            const uint16_t *q = q_rot + ((long long)b * g->Hq + h) * d;
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                oracle_q4_dequantize(k_idx + (row * g->Hkv + kv) * half, (double)k_scale[row * g->Hkv + kv], signs,
+                                     codebook, d, kr);
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += oracle_bf16_to_double(q[i]) * kr[i];
+                sc[t] = acc / sqrt((double)d);
+                if (sc[t] > m) m = sc[t];
+            }
+            double l = 0.0;
+            for (int t = 0; t < L; ++t) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                oracle_q4_dequantize(v_idx + (row * g->Hkv + kv) * half, (double)v_scale[row * g->Hkv + kv], signs,
+                                     codebook, d, vr);
+                double w = exp(sc[t] - m);
+                l += w;
+                for (int i = 0; i < d; ++i) o[i] += w * vr[i];
+            }
+            for (int i = 0; i < d; ++i) o[i] /= l;
+        }
+        free(kr); free(vr); free(sc);
+    }
+    free(x); free(y); free(z); free(qw); free(kw); free(ok);
+    return status;
 }
 
 /* ------------------------------------------------------------------ threads */
