@@ -1,4 +1,4 @@
-"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h, include/gqa_prefill.h).
+"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h, gqa_prefill.h, gqa_q4.h).
 
 Argument marshalling only: every step of the decode path runs in the library's CUDA
 kernels.  Device tensors are torch tensors (device memory and streams come from torch);
@@ -84,11 +84,14 @@ def load(build: bool = True):
         lib.gqa_partition_describe.restype = ctypes.c_longlong
         lib.gqa_decode_attn_static.argtypes = [ctypes.POINTER(PlanDesc)] + step[1:] + [P, P, P]
         lib.gqa_prefill_attn.argtypes = [ctypes.POINTER(PrefillDesc)] + [P] * 9 + [F, F, P, P, P]
+        lib.gqa_q4_codebook.argtypes = [P]
+        lib.gqa_decode_attn_q4.argtypes = [P] * 15 + [F, F, P, P]
         lib.gqa_status_string.argtypes = [I]
         lib.gqa_status_string.restype = ctypes.c_char_p
         for name in ("gqa_plan_create", "gqa_plan_destroy", "gqa_decode_attn", "gqa_decode_attn_host",
                      "gqa_attention_splitkv", "gqa_combine", "gqa_plan_read_q_rot",
-                     "gqa_plan_device_errors", "gqa_decode_attn_static", "gqa_prefill_attn"):
+                     "gqa_plan_device_errors", "gqa_decode_attn_static", "gqa_prefill_attn", "gqa_q4_codebook",
+                     "gqa_decode_attn_q4"):
             getattr(lib, name).restype = I
         _lib = lib
     return _lib
@@ -191,6 +194,13 @@ def prefill_attn_workload(w, out, *, device: int = 0, device_errors=None, stream
                  num_cache_blocks=w.num_blocks, device=device, device_errors=device_errors, stream=stream)
 
 
+def q4_codebook() -> np.ndarray:
+    """The 16 Lloyd-Max levels of N(0,1) as bf16 bit patterns (gqa_q4_codebook)."""
+    out = np.zeros(16, dtype=np.uint16)
+    _check(load().gqa_q4_codebook(out.ctypes.data), "gqa_q4_codebook")
+    return out
+
+
 class Plan:
     """A gqa_plan_t: geometry, split-worker count and the workspace (allocated once)."""
 
@@ -274,6 +284,22 @@ class Plan:
         return int(f.value)
 
     # ------------------------------------------------------------------ convenience
+    def decode_attn_q4(self, q_new, k_new, v_new, k_idx, v_idx, k_scale, v_scale, page_table, seq_lens,
+                       positions, q_norm_w, k_norm_w, rot_signs, codebook, rope_theta: float, eps: float, out,
+                       stream=None):
+        """The decode step over a 4-bit cache (gqa_decode_attn_q4, include/gqa_q4.h)."""
+        _check(load().gqa_decode_attn_q4(
+            self._h, _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_idx), _dptr(v_idx), _dptr(k_scale),
+            _dptr(v_scale), _dptr(page_table), _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w),
+            _dptr(rot_signs), _dptr(codebook), float(rope_theta), float(eps), _dptr(out), _stream(stream)),
+            "gqa_decode_attn_q4")
+
+    def run_q4(self, w, out, stream=None):
+        """gqa_decode_attn_q4 on a 4-bit-cache workload (workloads.Q4Workload)."""
+        self.decode_attn_q4(w.q_new, w.k_new, w.v_new, w.k_idx, w.v_idx, w.k_scale, w.v_scale, w.page_table,
+                            w.seq_lens, w.positions, w.q_norm_w, w.k_norm_w, w.rot_signs, w.codebook, w.rope_theta,
+                            w.eps, out, stream)
+
     def run(self, w, out, stream=None):
         """One decode step of a workloads.Workload already on this device."""
         self.decode_attn(w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.positions,

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgqa_decode.so")
-HEADERS = [os.path.join(ROOT, "include", "gqa_decode.h"), os.path.join(ROOT, "include", "gqa_prefill.h")]
+HEADERS = [os.path.join(ROOT, "include", "gqa_decode.h"), os.path.join(ROOT, "include", "gqa_prefill.h"),
+           os.path.join(ROOT, "include", "gqa_q4.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <new>
 
@@ -17,6 +19,7 @@ struct gqa_plan {
   void *ws = nullptr;
   size_t ws_bytes = 0;
   uint16_t *q_rot = nullptr;
+  uint16_t *q4_hi = nullptr, *q4_lo = nullptr;  // rotated queries of the 4-bit-cache step
   float *part_o = nullptr, *part_ml = nullptr;
   uint32_t *err = nullptr;
   int2 *spec = nullptr;  // [W][kStages] first tiles of each worker at the previous launch
@@ -68,6 +71,16 @@ bool gqa::encode_bf16_map(CUtensorMap *m, int rank, const void *base, const cuui
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void *>(base), dims,
              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gqa::encode_u8_map(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims,
+                        const cuuint64_t *strides, const cuuint32_t *box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rank < 1 || rank > 5) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<void *>(base), dims, strides,
+             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The box is 64 dims (128 B, the 128-byte swizzle span) x 1 head x 64 tokens.
@@ -375,7 +388,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   const size_t sz_si = align256(B * 4);
   const size_t sz_tab = rope_tables_bytes(d.max_seq_len);
   const size_t sz_spec = align256(static_cast<size_t>(p->W) * kStages * sizeof(int2));
-  p->ws_bytes = sz_q + sz_o + sz_ml + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab + sz_spec;
+  p->ws_bytes = sz_q + sz_o + sz_ml + sz_err + 2 * sz_sq + 2 * sz_skv + 2 * sz_si + sz_tab + sz_spec + 2 * sz_q;
   if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -394,8 +407,10 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->st_pos = reinterpret_cast<int32_t *>(c); c += sz_si;
   p->rope_tab = reinterpret_cast<float4 *>(c); c += sz_tab;
   p->spec = reinterpret_cast<int2 *>(c); c += sz_spec;
+  p->q4_hi = reinterpret_cast<uint16_t *>(c); c += sz_q;
+  p->q4_lo = reinterpret_cast<uint16_t *>(c); c += sz_q;
   if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || cudaMemset(p->spec, 0xff, sz_spec) != cudaSuccess ||
-      attn_configure(p->npad) != cudaSuccess ||
+      attn_configure(p->npad) != cudaSuccess || q4_configure() != cudaSuccess ||
       configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
@@ -538,3 +553,139 @@ const char *gqa_status_string(gqa_status_t status) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------ 4-bit KV cache
+
+extern "C" gqa_status_t gqa_q4_codebook(uint16_t *levels_bf16) {
+  if (!levels_bf16) return GQA_ERR_INVALID_ARG;
+  // Lloyd's algorithm for the 16-level quantizer of N(0,1): cell boundaries at the midpoints
+  // of adjacent levels, each level moved to the mean of N(0,1) over its cell,
+  //   E[X | a < X < b] = (pdf(a) - pdf(b)) / (cdf(b) - cdf(a)),
+  // until no level moves.
+  constexpr int kLv = 16;
+  const double inv_sqrt2pi = 0.3989422804014327;
+  auto pdf = [&](double x) { return std::isinf(x) ? 0.0 : inv_sqrt2pi * exp(-0.5 * x * x); };
+  auto cdf = [](double x) { return 0.5 * erfc(-x * 0.7071067811865476); };
+  double lv[kLv];
+  for (int j = 0; j < kLv; ++j) lv[j] = 3.0 * (2.0 * j + 1.0 - kLv) / kLv;
+  for (int it = 0; it < 200000; ++it) {
+    double edge[kLv + 1];
+    edge[0] = -INFINITY;
+    edge[kLv] = INFINITY;
+    for (int j = 1; j < kLv; ++j) edge[j] = 0.5 * (lv[j - 1] + lv[j]);
+    double step = 0.0;
+    for (int j = 0; j < kLv; ++j) {
+      const double mass = cdf(edge[j + 1]) - cdf(edge[j]);
+      const double mean = (pdf(edge[j]) - pdf(edge[j + 1])) / mass;
+      step = std::max(step, fabs(mean - lv[j]));
+      lv[j] = mean;
+    }
+    if (step < 1e-15) break;
+  }
+  for (int j = 0; j < kLv; ++j) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(static_cast<float>(lv[j]));
+    memcpy(&levels_bf16[j], &b, sizeof(uint16_t));
+  }
+  return GQA_OK;
+}
+
+extern "C" gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan, const void *q_new, const void *k_new,
+                                           const void *v_new, uint8_t *k_idx, uint8_t *v_idx, float *k_scale,
+                                           float *v_scale, const int32_t *page_table, const int32_t *seq_lens,
+                                           const int32_t *positions, const void *q_norm_w, const void *k_norm_w,
+                                           const int8_t *rot_signs, const void *codebook, float rope_theta, float eps,
+                                           void *out, void *stream) {
+  if (!plan || !q_new || !k_new || !v_new || !k_idx || !v_idx || !k_scale || !v_scale || !seq_lens || !positions ||
+      !rot_signs || !codebook || !out)
+    return GQA_ERR_INVALID_ARG;
+  const bool paged = plan->desc.block_size > 0;
+  if (paged != (page_table != nullptr)) return GQA_ERR_INVALID_ARG;
+  if (!finite_pos(rope_theta) || !isfinite(eps) || eps < 0.f) return GQA_ERR_INVALID_ARG;
+  if (!aligned(q_new, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_idx, 16) ||
+      !aligned(v_idx, 16) || !aligned(q_norm_w, 16) || !aligned(k_norm_w, 16) || !aligned(out, 16) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(rot_signs, 4) || !aligned(codebook, 2) ||
+      !aligned(page_table, 4) || !aligned(seq_lens, 4) || !aligned(positions, 4))
+    return GQA_ERR_INVALID_ARG;
+  const gqa_plan_desc_t &d = plan->desc;
+  DeviceGuard guard(d.device);
+  if (!guard.ok) return GQA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool rebuilt = false;
+  gqa_status_t st = ensure_rope_table(plan, rope_theta, s, &rebuilt);
+  if (st != GQA_OK) return st;
+  // index tiles: [rows][H_kv][64 bytes], box = 64 bytes x 1 head x 64 tokens
+  CUtensorMap tk, tv;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(d.num_kv_heads), static_cast<cuuint64_t>(plan->num_rows)};
+  const cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(d.num_kv_heads) * 64};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+  if (!encode_u8_map(&tk, 3, k_idx, dims, strides, box) || !encode_u8_map(&tv, 3, v_idx, dims, strides, box))
+    return GQA_ERR_CUDA;
+
+  Q4PrologueParams pp;
+  memset(&pp, 0, sizeof pp);
+  pp.seq_lens = seq_lens;
+  pp.positions = positions;
+  pp.page_table = page_table;
+  pp.q_new = static_cast<const uint16_t *>(q_new);
+  pp.k_new = static_cast<const uint16_t *>(k_new);
+  pp.v_new = static_cast<const uint16_t *>(v_new);
+  pp.q_norm_w = static_cast<const uint16_t *>(q_norm_w);
+  pp.k_norm_w = static_cast<const uint16_t *>(k_norm_w);
+  pp.rope_tab32 = rope_tab32_of(plan);
+  pp.signs = rot_signs;
+  pp.codebook = static_cast<const uint16_t *>(codebook);
+  pp.q_hi = plan->q4_hi;
+  pp.q_lo = plan->q4_lo;
+  pp.k_idx = k_idx;
+  pp.v_idx = v_idx;
+  pp.k_scale = k_scale;
+  pp.v_scale = v_scale;
+  pp.err = plan->err;
+  pp.B = d.batch;
+  pp.Hq = d.num_q_heads;
+  pp.Hkv = d.num_kv_heads;
+  pp.paged = paged ? 1 : 0;
+  pp.max_seq = d.max_seq_len;
+  pp.max_blocks = plan->max_blocks;
+  pp.num_blocks = paged ? d.num_cache_blocks : 0;
+  pp.eps = eps;
+  if (launch_q4_prologue(pp, s) != cudaSuccess) return GQA_ERR_CUDA;
+
+  Q4AttnParams ap;
+  memset(&ap, 0, sizeof ap);
+  ap.seq_lens = seq_lens;
+  ap.page_table = page_table;
+  ap.q_hi = plan->q4_hi;
+  ap.q_lo = plan->q4_lo;
+  ap.k_scale = k_scale;
+  ap.v_scale = v_scale;
+  ap.codebook = static_cast<const uint16_t *>(codebook);
+  ap.part_o = plan->part_o;
+  ap.part_ml = plan->part_ml;
+  ap.err = plan->err;
+  ap.B = d.batch;
+  ap.Hq = d.num_q_heads;
+  ap.Hkv = d.num_kv_heads;
+  ap.G = plan->G;
+  ap.paged = pp.paged;
+  ap.max_seq = d.max_seq_len;
+  ap.max_blocks = plan->max_blocks;
+  ap.num_blocks = pp.num_blocks;
+  ap.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
+  if (launch_q4_attention(tk, tv, ap, plan->npad, plan->W, s) != cudaSuccess) return GQA_ERR_CUDA;
+
+  CombineParams cp;
+  memset(&cp, 0, sizeof cp);
+  cp.seq_lens = seq_lens;
+  cp.part_o = plan->part_o;
+  cp.part_ml = plan->part_ml;
+  cp.out = static_cast<uint16_t *>(out);
+  cp.B = d.batch;
+  cp.Hq = d.num_q_heads;
+  cp.Hkv = d.num_kv_heads;
+  cp.G = plan->G;
+  cp.W = plan->W;
+  cp.max_seq = d.max_seq_len;
+  if (launch_q4_combine(cp, rot_signs, s) != cudaSuccess) return GQA_ERR_CUDA;
+  return GQA_OK;
+}

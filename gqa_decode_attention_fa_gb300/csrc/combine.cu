@@ -265,11 +265,97 @@ __global__ void __launch_bounds__(32 * kMaxWarps, 2) combine_seg_kernel(const Co
   *reinterpret_cast<uint2 *>(out) = v;
 }
 
+// The combine of the 4-bit-cache step: the same log-sum-exp merge over the same pieces (one
+// CTA per query head, all 128 dims, four groups of 32 lanes), then the merged row -- still
+// in the rotated domain of the cache's codewords -- is rotated back before the bf16
+// rounding: out = R^T o = D H o / sqrt(d), H the Sylvester Hadamard matrix applied as a
+// fast Walsh-Hadamard transform across the 128 threads (thread = dim).
+__global__ void __launch_bounds__(kHeadThreads, 8) q4_combine_kernel(const CombineParams p, const int8_t *signs) {
+  constexpr int kWarps = kHeadThreads / 32;
+  constexpr int kGroups = kHeadThreads / 32;
+  __shared__ int s_piece[kMaxPieces];
+  __shared__ int s_wcount[kWarps];
+  __shared__ long long s_red[kWarps][2];
+  __shared__ __align__(16) float s_o[kGroups][kHeadDim];
+  __shared__ float s_m[kGroups], s_l[kGroups];
+  __shared__ float s_x[kHeadDim];
+
+  const int tid = threadIdx.x;
+  const int bh = blockIdx.x, b = bh / p.Hq, h = bh - b * p.Hq;
+  const int kv = h / p.G, g = h - kv * p.G;
+  const int grp = tid / 32, sub = tid - grp * 32;
+  uint16_t *out = p.out + static_cast<long long>(bh) * kHeadDim;
+
+  const SegSpan s = seg_span(p, b, kv, s_red, kWarps);
+  const long long npairs = static_cast<long long>(s.w1 - s.w0 + 1) * kConsumerWarps;
+  float m_run = -INFINITY, l_run = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool waited = false;
+  for (long long base = 0; base < npairs; base += kMaxPieces) {
+    const int count = plan_pieces(p, s, b * p.Hkv + kv, base, s_piece, s_wcount, kWarps);
+    if (!waited) {
+      griddep_wait();  // the partials come from the attention kernel
+      griddep_launch_dependents();
+      waited = true;
+    }
+    merge_pieces<kUnroll>(p, s_piece, count, grp, kGroups, g, 4 * sub, m_run, l_run, acc);
+    __syncthreads();  // the list is rebuilt by the next pass
+  }
+  if (!waited) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
+  if (s.nt == 0) {  // invalid length: the attention kernel skipped it and flagged the error
+    out[tid] = 0;
+    return;
+  }
+  *reinterpret_cast<float4 *>(&s_o[grp][4 * sub]) = acc;
+  if (sub == 0) {
+    s_m[grp] = m_run;
+    s_l[grp] = l_run;
+  }
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kGroups; ++i) M = fmaxf(M, s_m[i]);
+  float num = 0.f, den = 0.f;
+#pragma unroll
+  for (int i = 0; i < kGroups; ++i) {
+    if (s_l[i] == 0.f) continue;  // a group that merged no piece
+    const float f = exp2f(s_m[i] - M);
+    num = fmaf(f, s_o[i][tid], num);
+    den = fmaf(f, s_l[i], den);
+  }
+  float v = num / den;
+  // H v: butterflies over dim bits 0..4 within the warp, bits 5 and 6 through shared memory
+#pragma unroll
+  for (int hb = 1; hb < 32; hb <<= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, hb);
+    v = (tid & hb) ? u - v : v + u;
+  }
+#pragma unroll
+  for (int hb = 32; hb < kHeadDim; hb <<= 1) {
+    s_x[tid] = v;
+    __syncthreads();
+    const float u = s_x[tid ^ hb];
+    __syncthreads();
+    v = (tid & hb) ? u - v : v + u;
+  }
+  const __nv_bfloat16 r = __float2bfloat16_rn(static_cast<float>(signs[tid]) * v * 0.08838834764831845f);
+  out[tid] = *reinterpret_cast<const uint16_t *>(&r);
+}
+
+cudaError_t launch_q4_combine(const CombineParams &p, const int8_t *signs, cudaStream_t stream) {
+  return launch_pdl(q4_combine_kernel, dim3(static_cast<unsigned>(p.B * p.Hq)), dim3(kHeadThreads), 0, stream, p,
+                    signs);
+}
+
 cudaError_t configure_combine() {
-  const void *fns[4] = {reinterpret_cast<const void *>(combine_head_kernel<1>),
+  const void *fns[5] = {reinterpret_cast<const void *>(combine_head_kernel<1>),
                         reinterpret_cast<const void *>(combine_head_kernel<2>),
                         reinterpret_cast<const void *>(combine_head_kernel<4>),
-                        reinterpret_cast<const void *>(combine_seg_kernel)};
+                        reinterpret_cast<const void *>(combine_seg_kernel),
+                        reinterpret_cast<const void *>(q4_combine_kernel)};
   for (const void *f : fns) {
     const cudaError_t e =
         cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

@@ -5,6 +5,7 @@
 
 #include "gqa_common.cuh"
 #include "../../include/gqa_prefill.h"
+#include "../../include/gqa_q4.h"
 
 namespace gqa {
 
@@ -58,6 +59,40 @@ bool encode_bf16_map(CUtensorMap *m, int rank, const void *base, const cuuint64_
                      const cuuint32_t *box);
 // K or V cache viewed as [rows][H_kv][128] bf16; box = 64 dims x 1 head x 64 tokens.
 bool make_cache_map(CUtensorMap *m, const void *base, int Hkv, long long rows);
+
+// The decode step over a 4-bit KV cache (attention_q4.cu; include/gqa_q4.h).
+struct Q4PrologueParams {
+  const int32_t *seq_lens, *positions, *page_table;
+  const uint16_t *q_new, *k_new, *v_new;    // [B,Hq,d], [B,Hkv,d], [B,Hkv,d]
+  const uint16_t *q_norm_w, *k_norm_w;      // [d] or null
+  const float2 *rope_tab32;                 // [max_seq][64] (cos, sin), binary32
+  const int8_t *signs;                      // [d] +-1
+  const uint16_t *codebook;                 // [16] bf16 levels, ascending
+  uint16_t *q_hi, *q_lo;                    // [B,Hq,d] rotated queries, bf16 hi + lo
+  uint8_t *k_idx, *v_idx;                   // [rows,Hkv,d/2] packed indices
+  float *k_scale, *v_scale;                 // [rows,Hkv]
+  uint32_t *err;
+  int B, Hq, Hkv, paged, max_seq, max_blocks, num_blocks;
+  float eps;
+};
+struct Q4AttnParams {
+  const int32_t *seq_lens, *page_table;
+  const uint16_t *q_hi, *q_lo;
+  const float *k_scale, *v_scale;
+  const uint16_t *codebook;
+  float *part_o, *part_ml;
+  uint32_t *err;
+  int B, Hq, Hkv, G, paged, max_seq, max_blocks, num_blocks;
+  float scale_log2;
+};
+cudaError_t q4_configure();
+cudaError_t launch_q4_prologue(const Q4PrologueParams &p, cudaStream_t stream);
+cudaError_t launch_q4_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4AttnParams &p, int npad,
+                                int num_workers, cudaStream_t stream);
+cudaError_t launch_q4_combine(const CombineParams &p, const int8_t *signs, cudaStream_t stream);
+// Tiled uint8 tensor map over `rank` dimensions, no swizzle (see encode_bf16_map).
+bool encode_u8_map(CUtensorMap *m, int rank, const void *base, const cuuint64_t *dims, const cuuint64_t *strides,
+                   const cuuint32_t *box);
 
 // Runs the calling thread on `dev` for the guard's lifetime.
 struct DeviceGuard {

@@ -372,3 +372,123 @@ def named_prefill(name: str, *, device="cpu", seed: int = 0) -> PrefillWorkload:
     if name == "qwen3-14b-prefill-4k":
         return make_prefill(1, 40, 8, 1024, [3072], paged=False, seed=seed, max_seq=4096, device=device, name=name)
     raise KeyError(name)
+
+
+# ----------------------------------------------------------------------------- 4-bit KV cache
+
+@dataclasses.dataclass
+class Q4Workload:
+    """One decode step over a 4-bit cache (include/gqa_q4.h): the decode step's inputs with
+    the cache as packed Lloyd-Max indices [rows, H_kv, 64] (uint8) and one fp32 scale per
+    row, the rotation's signs [128] (int8, +-1) and the codebook [16] (bf16)."""
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    block_size: int
+    max_seq: int
+    num_blocks: int
+    rope_theta: float
+    eps: float
+    q_new: torch.Tensor
+    k_new: torch.Tensor
+    v_new: torch.Tensor
+    k_idx: torch.Tensor      # uint8 [rows, Hkv, 64]
+    v_idx: torch.Tensor
+    k_scale: torch.Tensor    # float32 [rows, Hkv]
+    v_scale: torch.Tensor
+    page_table: Optional[torch.Tensor]
+    seq_lens: torch.Tensor
+    positions: torch.Tensor
+    q_norm_w: Optional[torch.Tensor]
+    k_norm_w: Optional[torch.Tensor]
+    rot_signs: torch.Tensor  # int8 [128]
+    codebook: torch.Tensor   # bf16 [16]
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def paged(self) -> bool:
+        return self.block_size > 0
+
+    @property
+    def num_rows(self) -> int:
+        return self.num_blocks * BLOCK if self.paged else self.B * self.max_seq
+
+    def kv_bytes(self) -> int:
+        """Bytes of the cache the step reads: per token and KV head, 2 x (64 index bytes +
+        a 4-byte scale)."""
+        return int(self.seq_lens.long().sum().item()) * self.Hkv * 2 * (64 + 4)
+
+
+def make_q4(B: int, Hq: int, Hkv: int, lens: Sequence[int], *, paged: bool, seed: int = 0, qk_norm: bool = True,
+            rope_theta: float = 1e6, eps: float = 1e-6, max_seq: Optional[int] = None, device="cpu",
+            name: str = "custom-q4", codebook_bits: Optional[np.ndarray] = None) -> Q4Workload:
+    """The decode step's draws (lengths, q/k/v of the new token, norm weights, page table),
+    with the cache drawn directly in its stored form: uniformly random index bytes and
+    scales uniform in [0.5, 1.2] (the scale a row of N(0, 1) entries gets), plus random
+    rotation signs.  The codebook is the caller's levels (default: the library's
+    Lloyd-Max levels, gqa_q4_codebook)."""
+    d = HEAD_DIM
+    lens = [int(x) for x in lens]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    if max_seq is None:
+        max_seq = max(lens)
+    q_new = _normal_bf16(gen, (B, Hq, d), device)
+    k_new = _normal_bf16(gen, (B, Hkv, d), device)
+    v_new = _normal_bf16(gen, (B, Hkv, d), device)
+    if qk_norm:
+        q_norm_w = _normal_bf16(gen, (d,), device, scale=0.1, mean=1.0)
+        k_norm_w = _normal_bf16(gen, (d,), device, scale=0.1, mean=1.0)
+    else:
+        q_norm_w = k_norm_w = None
+    if paged:
+        nblk_b = [-(-L // BLOCK) for L in lens]
+        num_blocks = sum(nblk_b)
+        rows = num_blocks * BLOCK
+    else:
+        num_blocks = 0
+        rows = B * max_seq
+    k_idx = torch.randint(0, 256, (rows, Hkv, d // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    v_idx = torch.randint(0, 256, (rows, Hkv, d // 2), generator=gen, device=device, dtype=torch.int32).to(torch.uint8)
+    k_scale = torch.rand((rows, Hkv), generator=gen, device=device) * 0.7 + 0.5
+    v_scale = torch.rand((rows, Hkv), generator=gen, device=device) * 0.7 + 0.5
+    signs = (torch.randint(0, 2, (d,), generator=gen, device=device, dtype=torch.int32) * 2 - 1).to(torch.int8)
+    page_table = None
+    if paged:
+        perm = torch.randperm(num_blocks, generator=gen, device=device).to(torch.int32).cpu()
+        mb = -(-max_seq // BLOCK)
+        pt = torch.full((B, mb), -1, dtype=torch.int32)
+        k = 0
+        for b in range(B):
+            n = nblk_b[b]
+            pt[b, :n] = perm[k:k + n]
+            k += n
+        page_table = pt.to(device)
+    if codebook_bits is None:
+        from .binding import q4_codebook
+        codebook_bits = q4_codebook()
+    codebook = torch.from_numpy(np.asarray(codebook_bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return Q4Workload(name=name, B=B, Hq=Hq, Hkv=Hkv, d=d, block_size=BLOCK if paged else 0, max_seq=int(max_seq),
+                      num_blocks=num_blocks, rope_theta=float(np.float32(rope_theta)), eps=float(np.float32(eps)),
+                      q_new=q_new, k_new=k_new, v_new=v_new, k_idx=k_idx, v_idx=v_idx, k_scale=k_scale,
+                      v_scale=v_scale, page_table=page_table,
+                      seq_lens=torch.tensor(lens, dtype=torch.int32, device=device),
+                      positions=torch.tensor([L - 1 for L in lens], dtype=torch.int32, device=device),
+                      q_norm_w=q_norm_w, k_norm_w=k_norm_w, rot_signs=signs, codebook=codebook.to(device))
+
+
+Q4_WORKLOADS = ("qwen3-14b-4k-q4", "qwen3-14b-ragged-q4")
+
+
+def named_q4(name: str, *, device="cpu", seed: int = 0) -> Q4Workload:
+    """The 4k and ragged decode geometries with a 4-bit cache."""
+    if name == "qwen3-14b-4k-q4":
+        return make_q4(1, 40, 8, [4096], paged=False, seed=seed, device=device, name=name)
+    if name == "qwen3-14b-ragged-q4":
+        return make_q4(32, 40, 8, ragged_lengths(32, 512, 8192, seed), paged=True, seed=seed, device=device, name=name)
+    raise KeyError(name)

@@ -80,6 +80,7 @@ def _load():
             lib.oracle_q4_decode_step.argtypes = [ctypes.POINTER(Geom)] + [P] * 12 + [
                 ctypes.c_double, ctypes.c_double, P, P, P, ctypes.c_int, P, P]
             lib.oracle_q4_decode_step.restype = ctypes.c_int
+            lib.oracle_q4_attention.argtypes = [ctypes.POINTER(Geom)] + [P] * 10 + [P, ctypes.c_int, P]
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -320,6 +321,26 @@ def q4_decode_step(g: Geom, q_new, k_new, v_new, k_idx, v_idx, k_scale, v_scale,
                                        float(rope_theta), float(eps), _ptr(sg), _ptr(cb), _ptr(pr), npairs,
                                        _ptr(q_rot), _ptr(out))
     return dict(out=out, q_rot=q_rot, k_idx=ki, v_idx=vi, k_scale=ks, v_scale=vs, status=st)
+
+
+def q4_attention(g: Geom, q_rot, k_idx, v_idx, k_scale, v_scale, page_table, seq_lens, signs, codebook_bits,
+                 pairs=None) -> np.ndarray:
+    """Attention over a given 4-bit cache (no prologue): [B,Hq,d], or [len(pairs), d]."""
+    q_rot = _c(q_rot, np.uint16)
+    ki, vi = _c(k_idx, np.uint8), _c(v_idx, np.uint8)
+    ks, vs = _c(k_scale, np.float32), _c(v_scale, np.float32)
+    pt, sl = _c(page_table, np.int32), _c(seq_lens, np.int32)
+    sg, cb = _c(signs, np.int8), _c(codebook_bits, np.uint16)
+    if pairs is not None:
+        pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((pr.shape[0], g.d))
+        npairs = pr.shape[0]
+    else:
+        pr, npairs = None, 0
+        out = np.zeros((g.B, g.Hq, g.d))
+    _load().oracle_q4_attention(ctypes.byref(g), _ptr(q_rot), _ptr(ki), _ptr(vi), _ptr(ks), _ptr(vs), _ptr(pt),
+                                _ptr(sl), None, _ptr(sg), _ptr(cb), _ptr(pr), npairs, _ptr(out))
+    return out
 
 
 def max_threads() -> int:

@@ -609,6 +609,54 @@ void oracle_q4_dequantize(const uint8_t *packed, double sigma, const int8_t *sig
     oracle_unrotate(y, signs, d, x);
 }
 
+/* Attention over a 4-bit cache, brute force per (b, h): scores q_rot[b, h] . x^_t / sqrt(d)
+ * over the dequantized rows x^_t = sigma_t R^T c[idx_t], t < seq_lens[b], then the softmax
+ * weights applied to the dequantized value rows.  Sequences with ok[b] == 0 (or ok NULL
+ * meaning all valid) give zeros.  out [B, H_q, d], or the listed (b, h) pairs in order. */
+void oracle_q4_attention(const oracle_geom_t *g, const uint16_t *q_rot, const uint8_t *k_idx, const uint8_t *v_idx,
+                         const float *k_scale, const float *v_scale, const int32_t *page_table,
+                         const int32_t *seq_lens, const int *ok, const int8_t *signs, const uint16_t *codebook,
+                         const int32_t *pairs, int n_pairs, double *out) {
+    const int d = g->d, half = d / 2;
+    int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
+    long long n = pairs ? n_pairs : (long long)g->B * g->Hq;
+#pragma omp parallel
+    {
+        double *kr = malloc(sizeof(double) * d), *vr = malloc(sizeof(double) * d);
+        double *sc = malloc(sizeof(double) * (size_t)(g->max_seq > 0 ? g->max_seq : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long long k = 0; k < n; ++k) {
+            int b = pairs ? pairs[2 * k] : (int)(k / g->Hq), h = pairs ? pairs[2 * k + 1] : (int)(k % g->Hq);
+            double *o = out + k * d;
+            for (int i = 0; i < d; ++i) o[i] = 0.0;
+            if (ok && !ok[b]) continue;
+            const int G = g->Hq / g->Hkv, kv = h / G, L = seq_lens[b];
+            const uint16_t *q = q_rot + ((long long)b * g->Hq + h) * d;
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                oracle_q4_dequantize(k_idx + (row * g->Hkv + kv) * half, (double)k_scale[row * g->Hkv + kv], signs,
+                                     codebook, d, kr);
+                double acc = 0.0;
+                for (int i = 0; i < d; ++i) acc += oracle_bf16_to_double(q[i]) * kr[i];
+                sc[t] = acc / sqrt((double)d);
+                if (sc[t] > m) m = sc[t];
+            }
+            double l = 0.0;
+            for (int t = 0; t < L; ++t) {
+                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
+                oracle_q4_dequantize(v_idx + (row * g->Hkv + kv) * half, (double)v_scale[row * g->Hkv + kv], signs,
+                                     codebook, d, vr);
+                double w = exp(sc[t] - m);
+                l += w;
+                for (int i = 0; i < d; ++i) o[i] += w * vr[i];
+            }
+            for (int i = 0; i < d; ++i) o[i] /= l;
+        }
+        free(kr); free(vr); free(sc);
+    }
+}
+
 /* One decode step over a 4-bit cache.  As oracle_prologue + oracle_attention, except that
  * the new token's k row (the exact RoPE(RMSNorm(k_new)) value) and v row (v_new) are
  * quantized into k_idx/v_idx [rows, H_kv, d/2] and k_scale/v_scale [rows, H_kv] (fp32),
@@ -659,42 +707,8 @@ int oracle_q4_decode_step(const oracle_geom_t *g,
             v_scale[row * g->Hkv + kv] = (float)sg;
         }
     }
-    long long n = pairs ? n_pairs : (long long)g->B * g->Hq;
-#pragma omp parallel
-    {
-        double *kr = malloc(sizeof(double) * d), *vr = malloc(sizeof(double) * d);
-        double *sc = malloc(sizeof(double) * (size_t)(g->max_seq > 0 ? g->max_seq : 1));
-#pragma omp for schedule(dynamic, 1)
-        for (long long k = 0; k < n; ++k) {
-            int b = pairs ? pairs[2 * k] : (int)(k / g->Hq), h = pairs ? pairs[2 * k + 1] : (int)(k % g->Hq);
-            double *o = out + k * d;
-            for (int i = 0; i < d; ++i) o[i] = 0.0;
-            if (!ok[b]) continue;
-            const int G = g->Hq / g->Hkv, kv = h / G, L = seq_lens[b];
-            const uint16_t *q = q_rot + ((long long)b * g->Hq + h) * d;
-            double m = -INFINITY;
-            for (int t = 0; t < L; ++t) {
-                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
-                oracle_q4_dequantize(k_idx + (row * g->Hkv + kv) * half, (double)k_scale[row * g->Hkv + kv], signs,
-                                     codebook, d, kr);
-                double acc = 0.0;
-                for (int i = 0; i < d; ++i) acc += oracle_bf16_to_double(q[i]) * kr[i];
-                sc[t] = acc / sqrt((double)d);
-                if (sc[t] > m) m = sc[t];
-            }
-            double l = 0.0;
-            for (int t = 0; t < L; ++t) {
-                long long row = cache_row(page_table, max_blocks, g->block_size, g->max_seq, b, t);
-                oracle_q4_dequantize(v_idx + (row * g->Hkv + kv) * half, (double)v_scale[row * g->Hkv + kv], signs,
-                                     codebook, d, vr);
-                double w = exp(sc[t] - m);
-                l += w;
-                for (int i = 0; i < d; ++i) o[i] += w * vr[i];
-            }
-            for (int i = 0; i < d; ++i) o[i] /= l;
-        }
-        free(kr); free(vr); free(sc);
-    }
+    oracle_q4_attention(g, q_rot, k_idx, v_idx, k_scale, v_scale, page_table, seq_lens, ok, signs, codebook,
+                        pairs, n_pairs, out);
     free(x); free(y); free(z); free(qw); free(kw); free(ok);
     return status;
 }

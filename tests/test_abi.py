@@ -139,3 +139,19 @@ def test_prefill_rejects_null_and_inconsistent_arguments():
     odd = ctypes.c_void_p(4096 + 2)
     assert lib.gqa_prefill_attn(ctypes.byref(desc), odd, dummy, dummy, dummy, dummy, None, dummy, None, None,
                                 ctypes.c_float(1e6), ctypes.c_float(1e-6), dummy, None, None) == binding.GQA_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------- 4-bit cache entry
+
+def test_q4_codebook_is_the_lloyd_max_quantizer():
+    """The library's levels (its own Lloyd iteration) round to the oracle's, level by level."""
+    import oracle
+    import torch
+    want = torch.tensor(oracle.lloyd_max(16)[0], dtype=torch.float32).to(torch.bfloat16)
+    np.testing.assert_array_equal(binding.q4_codebook(), want.view(torch.int16).numpy().view(np.uint16))
+    assert binding.load().gqa_q4_codebook(None) == binding.GQA_ERR_INVALID_ARG
+
+
+def test_q4_rejects_null_arguments():
+    args = [None] * 15 + [ctypes.c_float(1e6), ctypes.c_float(1e-6), None, None]
+    assert binding.load().gqa_decode_attn_q4(*args) == binding.GQA_ERR_INVALID_ARG

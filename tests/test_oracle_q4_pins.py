@@ -234,3 +234,11 @@ def test_q4_step_is_softmax_attention_over_the_dequantized_cache():
             s = K @ q / math.sqrt(D)
             w = np.exp(s - s.max())
             np.testing.assert_allclose(r["out"][b, h], w @ V / w.sum(), atol=1e-11)
+
+
+def test_q4_attention_over_the_updated_cache_is_the_step():
+    cs = make_q4_case(2, 8, 2, [5, 9], 16, seed=12)
+    r = oracle.q4_decode_step(**cs)
+    out = oracle.q4_attention(cs["g"], r["q_rot"], r["k_idx"], r["v_idx"], r["k_scale"], r["v_scale"], None,
+                              cs["seq_lens"], cs["signs"], CODEBOOK)
+    np.testing.assert_array_equal(out, r["out"])
