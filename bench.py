@@ -388,6 +388,62 @@ def run_prefill(name: str, steps: int, warmup: int, local: int):
             "clocks_sm_mhz": clk.result["sm_mhz"]}
 
 
+# ----------------------------------------------------------------------------- 4-bit KV cache
+
+Q4 = ("qwen3-14b-4k-q4", "qwen3-14b-ragged-q4")
+
+
+def run_q4(name: str, steps: int, warmup: int, local: int):
+    """The decode step over a 4-bit cache (gqa_decode_attn_q4: prologue, attention on the
+    index tiles, combine), K steps back to back between CUDA events after warm-up.  Caches
+    smaller than twice L2 are replicated (> 3x L2 of copies, rotated across steps) so that
+    every step reads from HBM.  Roofline: the cache bytes a step reads (64 index bytes + a
+    4-byte scale per token, KV head and tensor) over the step's time."""
+    import torch
+
+    from gqa_decode_attention_fa_gb300 import binding, workloads as wl
+
+    dev = f"cuda:{local}"
+    w = wl.named_q4(name, device=dev)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
+    kvb = w.kv_bytes()
+    sets = [w]
+    if kvb < 2 * l2:
+        for _ in range(int(math.ceil(3 * l2 / kvb)) - 1):
+            c = wl.Q4Workload(**{**w.__dict__})
+            c.k_idx, c.v_idx = w.k_idx.clone(), w.v_idx.clone()
+            c.k_scale, c.v_scale = w.k_scale.clone(), w.v_scale.clone()
+            sets.append(c)
+    l2_note = (f"rotating {len(sets)} cache copies ({len(sets) * kvb / 2**20:.0f} MiB > 3x L2)" if len(sets) > 1
+               else f"inputs > L2 ({kvb / 2**20:.0f} MiB per step)")
+    plan = binding.Plan(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
+                        device=local, seq_lens_host=w.seq_lens.cpu().numpy())
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    for k in range(max(3, warmup)):
+        plan.run_q4(sets[k % len(sets)], out, stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        a.record(stream)
+        for k in range(steps):
+            plan.run_q4(sets[k % len(sets)], out, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+    if plan.device_errors() != 0:
+        raise SystemExit("bench: device error flags set during the 4-bit-cache steps")
+    us = a.elapsed_time(b) * 1e3 / steps
+    peak, src = hbm_peak()
+    gbs = kvb / (us * 1e-6) / 1e9
+    return {"us_per_step": round(us, 3), "kv_bytes_per_step": kvb, "kv_gbs": round(gbs, 1),
+            "bf16_cache_bytes_per_step": int(w.seq_lens.long().sum().item()) * w.Hkv * w.d * 2 * 2,
+            "roofline": {"bound": "hbm", "kernel": "q4 prologue + attention + combine (whole step)",
+                         "achieved": round(gbs, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4)},
+            "l2": l2_note, "steps": steps, "workers": plan.num_workers, "clocks_sm_mhz": clk.result["sm_mhz"]}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0):
     """The fp64 oracle, as it stands, on the host cores: whole decode steps of the workload
     (for the 40-layer sweep: whole layers, scaled by 40) until ~budget_s of CPU time."""
@@ -469,7 +525,7 @@ def main():
     ap.add_argument("--warmup-seconds", type=float, default=0.3,
                     help="keep warming up for at least this long (so the clock record sees the loaded GPU)")
     ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer,"
-                                           "qwen3-14b-4k-decode," + PREFILL,
+                                           "qwen3-14b-4k-decode," + PREFILL + "," + ",".join(Q4),
                     help="other workloads to time (GPU only) into the line's by_config; '' for none")
     args = ap.parse_args()
     rank, world, local = dist_env()
@@ -496,6 +552,10 @@ def main():
     for name in [n for n in args.by_config.split(",") if n and n != args.workload]:
         if name == PREFILL:
             by[name] = run_prefill(name, min(args.steps, 20), args.warmup, local)
+            torch.cuda.empty_cache()
+            continue
+        if name in Q4:
+            by[name] = run_q4(name, min(args.steps, 50), args.warmup, local)
             torch.cuda.empty_cache()
             continue
         sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50)})

@@ -7,6 +7,7 @@ needs only the driver at run time.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import subprocess
@@ -49,10 +50,23 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile (if stale) and return the path of libgqa_decode.so."""
+    """Compile (if stale) and return the path of libgqa_decode.so.  Concurrent builds (test
+    processes that import the package at once) are serialised by a file lock, so none links
+    objects another is still writing."""
     if not force and not stale():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
+    with open(os.path.join(OUT_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and not stale():  # another process built it meanwhile
+                return LIB
+            return _build_locked(verbose, ptxas_info)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, ptxas_info: bool) -> str:
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 

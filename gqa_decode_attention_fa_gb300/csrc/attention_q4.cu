@@ -12,7 +12,7 @@
 //   q . x^_t = sigma_t (q~ . c[idx_t])   and   sum_t p_t x^_t = R^T sum_t p_t sigma_t c[idx_t],
 // i.e. the scores and the value sum run on the raw codewords in the rotated domain, and
 // the merged output row is rotated back once, by the combine.  Three kernels:
-//  * q4_prologue_kernel (one CTA per sequence): q~ = R RoPE(RMSNorm(q_new)) in binary32,
+//  * q4_prologue_kernel (one warp per row): q~ = R RoPE(RMSNorm(q_new)) in binary32,
 //    kept as bf16 hi + lo (so that rounding q~ costs no accuracy); the new token's k row
 //    RoPE(RMSNorm(k_new)) and v row quantized and appended (R by a fast Walsh-Hadamard
 //    transform across the warp, the nearest level by the midpoint thresholds).
@@ -68,17 +68,19 @@ __device__ __forceinline__ void unpack4(uint2 w, float (&f)[4]) {
 }  // namespace
 
 // ----------------------------------------------------------------------------- prologue
-// One CTA (8 warps) per sequence; warp w handles rows w, w + 8, ... of the H_q query rows,
-// then the H_kv key rows, then the H_kv value rows.  Lane l holds dims 4 l .. 4 l + 3; the
+// One warp per row: CTA (b, y) of 8 warps handles rows 8 y .. 8 y + 7 of sequence b's H_q
+// query rows, then its H_kv key rows, then its H_kv value rows.  Lane l holds dims 4 l .. 4 l + 3; the
 // RoPE partner of dim e (e +- 64) is in lane l ^ 16.
 __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams p) {
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.y * 8 + warp;  // this warp's row
+  if (r >= p.Hq + 2 * p.Hkv) return;
   const int L = p.seq_lens[b], pos = p.positions[b];
   const bool len_ok = L >= 1 && L <= p.max_seq;
   const bool pos_ok = len_ok && pos >= 0 && pos < L;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && blockIdx.y == 0) {
     if (!len_ok) atomicOr(p.err, GQA_DEVERR_SEQLEN);
     else if (!pos_ok) atomicOr(p.err, GQA_DEVERR_POSITION);
   }
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams
     if (p.paged) {
       const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + pos / kTile];
       if (pg >= 0 && pg < p.num_blocks) crow = static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
-      else if (threadIdx.x == 0) atomicOr(p.err, GQA_DEVERR_PAGE);
+      else if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(p.err, GQA_DEVERR_PAGE);
     } else {
       crow = static_cast<long long>(b) * p.max_seq + pos;
     }
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams
     packed = mine | (hi << 4);
   };
 
-  for (int r = warp; r < p.Hq + 2 * p.Hkv; r += 8) {
+  {
     if (r < p.Hq) {
       const long long row = static_cast<long long>(b) * p.Hq + r;
       float z[4] = {0.f, 0.f, 0.f, 0.f};
@@ -240,8 +242,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4OffBar);
   uint64_t *empty_bar = full_bar + kStages;
-  uint16_t *cbs = reinterpret_cast<uint16_t *>(empty_bar + kStages);  // [16] codebook
-  uint32_t *pre = reinterpret_cast<uint32_t *>(cbs + 16);              // [B + 1]
+  // pair table: entry (a | b << 4) = bf16 c[a] | bf16 c[b] << 16, the codewords of two
+  // adjacent dims from their two nibbles
+  uint32_t *cpair = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [256]
+  uint32_t *pre = cpair + 256;                                           // [B + 1]
   int32_t *Ls = reinterpret_cast<int32_t *>(pre + p.B + 1);            // [B]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -256,7 +260,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
-  if (warp == 1 && lane < 16) cbs[lane] = p.codebook[lane];
+  for (int e = tid; e < 256; e += blockDim.x)
+    cpair[e] = static_cast<uint32_t>(p.codebook[e & 15]) | (static_cast<uint32_t>(p.codebook[e >> 4]) << 16);
   griddep_wait();  // the prologue kernel appended the new rows and wrote q~
   if (warp == 0) {  // tile prefix over the batch
     uint32_t run = 0;
@@ -386,12 +391,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const int byte = (it * 32 + lane) * 4;
       const int t = byte >> 6, c = byte & 63;
       const uint32_t w4 = *reinterpret_cast<const uint32_t *>(idx + byte);
+      // bytes c + 2u, c + 2u + 1: low nibbles = dims (c + 2u, +1), high nibbles = dims + 64
       uint32_t lo[2], hi[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint32_t b0 = (w4 >> (16 * u)) & 0xffu, b1 = (w4 >> (16 * u + 8)) & 0xffu;
-        lo[u] = static_cast<uint32_t>(cbs[b0 & 15]) | (static_cast<uint32_t>(cbs[b1 & 15]) << 16);
-        hi[u] = static_cast<uint32_t>(cbs[b0 >> 4]) | (static_cast<uint32_t>(cbs[b1 >> 4]) << 16);
+        const uint32_t h2 = w4 >> (16 * u);
+        lo[u] = cpair[(h2 & 0x0fu) | ((h2 >> 4) & 0xf0u)];
+        hi[u] = cpair[((h2 >> 4) & 0x0fu) | ((h2 >> 8) & 0xf0u)];
       }
       const uint32_t off = swz128(t, c >> 3) + (c & 7) * 2;
       *reinterpret_cast<uint2 *>(buf + off) = make_uint2(lo[0], lo[1]);
@@ -427,16 +433,28 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     // per-token scales of this lane's 8 tokens (16 mt + lane / 4 + 8 h); 0 past the length
     const int row0 = tile_row(b, j, false);
     float sk[4][2], sv[4][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    {
+      // lane l loads tokens l and l + 32, then each lane takes its eight by shuffles
+      float k2[2], v2[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int tok = 16 * mt + (lane >> 2) + 8 * hh;
+        const int tok = lane + 32 * hh;
         const bool in = tok < valid && row0 >= 0;
         const long long r = (static_cast<long long>(row0) + tok) * p.Hkv + kv;
-        sk[mt][hh] = in ? p.k_scale[r] * p.scale_log2 : 0.f;
-        sv[mt][hh] = in ? p.v_scale[r] : 0.f;
+        k2[hh] = in ? p.k_scale[r] * p.scale_log2 : 0.f;
+        v2[hh] = in ? p.v_scale[r] : 0.f;
       }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tok = 16 * mt + (lane >> 2) + 8 * hh;  // held by lane tok & 31, slot tok >> 5
+          const float ka = __shfl_sync(0xffffffffu, k2[0], tok & 31), kb = __shfl_sync(0xffffffffu, k2[1], tok & 31);
+          const float va = __shfl_sync(0xffffffffu, v2[0], tok & 31), vb = __shfl_sync(0xffffffffu, v2[1], tok & 31);
+          sk[mt][hh] = tok < 32 ? ka : kb;
+          sv[mt][hh] = tok < 32 ? va : vb;
+        }
+    }
     const int s = static_cast<int>(i % kStages);
     const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
     __syncwarp();
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 }
 
 size_t q4_attn_smem_bytes(int batch) {
-  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kStages + 32 + 4 * (batch + 1) + 4 * batch;
+  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kStages + 4 * 256 + 4 * (batch + 1) + 4 * batch;
 }
 
 cudaError_t q4_configure() {
@@ -564,7 +582,8 @@ cudaError_t q4_configure() {
 }
 
 cudaError_t launch_q4_prologue(const Q4PrologueParams &p, cudaStream_t stream) {
-  return launch_pdl(q4_prologue_kernel, dim3(static_cast<unsigned>(p.B)), dim3(256), 0, stream, p);
+  return launch_pdl(q4_prologue_kernel, dim3(static_cast<unsigned>(p.B), static_cast<unsigned>((p.Hq + 2 * p.Hkv + 7) / 8)),
+                    dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_q4_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4AttnParams &p, int npad,
