@@ -383,7 +383,7 @@ int oracle_prefill_prologue(const oracle_geom_t *g, int T,
  * p = q_start[b] + i) and query head h (KV head floor(h / G)),
  *     out[b, i, h] = sum_{t <= p} softmax_t(q_rot[b, i, h] . K_t / sqrt(d)) V_t
  * over the cache after the prologue -- every earlier token and the token itself, none
- * after it.  out is [B, T, H_q, d]; or, when triples != NULL, one d-vector per listed
+ * after it (zeros for a sequence whose chunk is out of range).  out is [B, T, H_q, d]; or, when triples != NULL, one d-vector per listed
  * (b, i, h) in list order.  Returns the thread count used.                              */
 int oracle_prefill_attention(const oracle_geom_t *g, int T, const uint16_t *q_rot,
                              const uint16_t *k_cache, const uint16_t *v_cache,
@@ -409,6 +409,11 @@ int oracle_prefill_attention(const oracle_geom_t *g, int T, const uint16_t *q_ro
                 i = (int)((k / g->Hq) % T);
                 h = (int)(k % g->Hq);
             }
+            double *o = out + k * g->d;
+            if (q_start[b] < 0 || (long long)q_start[b] + T > g->max_seq) {  /* chunk out of range */
+                for (int e = 0; e < g->d; ++e) o[e] = 0.0;
+                continue;
+            }
             const int L = q_start[b] + i + 1;
             const int G = g->Hq / g->Hkv, kv = h / G;
             const double scale = 1.0 / sqrt((double)g->d);
@@ -423,7 +428,6 @@ int oracle_prefill_attention(const oracle_geom_t *g, int T, const uint16_t *q_ro
                 if (scores[t] > m) m = scores[t];
             }
             double l = 0.0;
-            double *o = out + k * g->d;
             for (int e = 0; e < g->d; ++e) o[e] = 0.0;
             for (int t = 0; t < L; ++t) {
                 double w = exp(scores[t] - m);
@@ -458,6 +462,10 @@ void oracle_prefill_blocked(const oracle_geom_t *g, int T, const uint16_t *q_rot
     const double scale = 1.0 / sqrt((double)d);
     int max_blocks = g->block_size > 0 ? (g->max_seq + g->block_size - 1) / g->block_size : 0;
     const int s0 = q_start[b];
+    if (s0 < 0 || (long long)s0 + T > g->max_seq) {  /* chunk out of range: zeros */
+        for (long long e = 0; e < (long long)T * d; ++e) out[e] = 0.0;
+        return;
+    }
     double *S = malloc(sizeof(double) * (size_t)qb * kt);
     double *m = malloc(sizeof(double) * qb), *l = malloc(sizeof(double) * qb);
     for (int i0 = 0; i0 < T; i0 += qb) {
