@@ -34,10 +34,15 @@ constexpr int kQ4StageBytes = 2 * kQ4TileBytes;          // K and V index tiles
 constexpr int kQ4BufBytes = 2 * kHalfTileBytes;          // one expanded bf16 tile (16 KiB)
 constexpr float kInvSqrtD = 0.08838834764831845f;        // 1 / sqrt(128)
 
-// Smem: [6 expanded tiles, one per consumer warp][6 stages][barriers][codebook][prefix]
+// Smem: [6 expanded tiles, one per consumer warp][6 stages][pair table, one copy per lane]
+// [per-stage scales][per-stage tile info][barriers][prefix]
 constexpr int kQ4OffBuf = 0;
 constexpr int kQ4OffStage = kConsumerWarps * kQ4BufBytes;
-constexpr int kQ4OffBar = kQ4OffStage + kStages * kQ4StageBytes;
+constexpr int kQ4OffPair = kQ4OffStage + kStages * kQ4StageBytes;
+constexpr int kQ4PairBytes = 256 * 32 * 4;
+constexpr int kQ4OffScale = kQ4OffPair + kQ4PairBytes;  // [stage][K, V][64] fp32
+constexpr int kQ4OffInfo = kQ4OffScale + kStages * 2 * kTile * 4;  // [stage] int4
+constexpr int kQ4OffBar = kQ4OffInfo + kStages * 16;
 static_assert(kQ4OffStage % 1024 == 0, "expanded tiles must keep 1024-byte alignment for the 128B swizzle");
 
 // Fast Walsh-Hadamard transform (Sylvester order) of a 128-vector held by a warp, lane l
@@ -57,6 +62,17 @@ __device__ __forceinline__ void fwht128(float (&v)[4], int lane) {
     }
   }
 }
+
+// 4-byte asynchronous global -> shared copy, and the arrive-on that fires on the barrier
+// once this thread's earlier copies have landed (no pending-count increment: the barrier's
+// expected count includes these arrivals)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void unpack4(uint2 w, float (&f)[4]) {
   f[0] = __uint_as_float(w.x << 16);
@@ -243,15 +259,18 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4OffBar);
   uint64_t *empty_bar = full_bar + kStages;
   // pair table: entry (a | b << 4) = bf16 c[a] | bf16 c[b] << 16, the codewords of two
-  // adjacent dims from their two nibbles
-  uint32_t *cpair = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [256]
-  uint32_t *pre = cpair + 256;                                           // [B + 1]
+  // adjacent dims from their two nibbles; 32 copies interleaved word by word, lane l
+  // reading copy l (word 32 e + l, always bank l), so random entries never conflict
+  uint32_t *cpair = reinterpret_cast<uint32_t *>(smem + kQ4OffPair);  // [256][32]
+  float *scl = reinterpret_cast<float *>(smem + kQ4OffScale);        // [stage][2][64]
+  int4 *info = reinterpret_cast<int4 *>(smem + kQ4OffInfo);           // [stage]
+  uint32_t *pre = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [B + 1]
   int32_t *Ls = reinterpret_cast<int32_t *>(pre + p.B + 1);            // [B]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&full_bar[s]), 1 + 32);  // the TMA issue + one arrive per producer lane
       mbar_init(smem_addr(&empty_bar[s]), 1);
     }
     fence_barrier_init();
@@ -260,8 +279,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
-  for (int e = tid; e < 256; e += blockDim.x)
-    cpair[e] = static_cast<uint32_t>(p.codebook[e & 15]) | (static_cast<uint32_t>(p.codebook[e >> 4]) << 16);
+  for (int e = tid; e < 256 * 32; e += blockDim.x) {
+    const int v = e >> 5;
+    cpair[e] = static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
+  }
   griddep_wait();  // the prologue kernel appended the new rows and wrote q~
   if (warp == 0) {  // tile prefix over the batch
     uint32_t run = 0;
@@ -302,29 +323,60 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    if (lane == 0) {
-      long long issued = 0;
-      bool ok = true;
-      for (long long i = 0; i < n && ok; ++i) {
-        int b, kv, j;
-        q4_locate(pre, Ls, p.B, xs + i, b, kv, j);
-        const int row = tile_row(b, j, true);
+    // Lane l looks up tile i0 + l of the next 32 (sequence, head, page, length), so that
+    // one page-table round trip serves 32 tiles; then per tile lane 0 stores the tile's
+    // info and issues the two index-tile TMAs, and every lane copies the scales of tokens
+    // l and l + 32 (the ones inside the sequence) with cp.async, whose arrivals complete
+    // the stage with the TMA bytes.
+    long long issued = 0;
+    bool ok = true;
+    for (long long i0 = 0; i0 < n && ok; i0 += 32) {
+      int mb = 0, mkv = 0, mrow = -kTile, mvalid = 0;
+      if (i0 + lane < n) {
+        int mj;
+        q4_locate(pre, Ls, p.B, xs + i0 + lane, mb, mkv, mj);
+        mrow = tile_row(mb, mj, true);
+        mvalid = min(kTile, Ls[mb] - mj * kTile);
+      }
+      const int cnt = static_cast<int>(min(32LL, n - i0));
+      for (int u = 0; u < cnt; ++u) {
+        const long long i = i0 + u;
+        const int b = __shfl_sync(0xffffffffu, mb, u), kv = __shfl_sync(0xffffffffu, mkv, u);
+        const int row = __shfl_sync(0xffffffffu, mrow, u), valid = __shfl_sync(0xffffffffu, mvalid, u);
         const int s = static_cast<int>(i % kStages);
         if (i >= kStages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kStages) - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint32_t fb = smem_addr(&full_bar[s]);
-        const uint32_t base = smem_addr(smem + kQ4OffStage + s * kQ4StageBytes);
-        mbar_arrive_expect_tx(fb, kQ4StageBytes);
-        tma_load_3d(base, &tmK, fb, 0, kv, row);
-        tma_load_3d(base + kQ4TileBytes, &tmV, fb, 0, kv, row);
+        if (lane == 0) {
+          info[s] = make_int4(b, kv, valid, row >= 0 ? 1 : 0);
+          const uint32_t base = smem_addr(smem + kQ4OffStage + s * kQ4StageBytes);
+          mbar_arrive_expect_tx(fb, kQ4StageBytes);
+          tma_load_3d(base, &tmK, fb, 0, kv, row);
+          tma_load_3d(base + kQ4TileBytes, &tmV, fb, 0, kv, row);
+        }
+        const uint32_t sdst = smem_addr(scl + s * 2 * kTile);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tok = lane + 32 * hh;
+          if (tok < valid && row >= 0) {
+            const long long r = (static_cast<long long>(row) + tok) * p.Hkv + kv;
+            cp_async4(sdst + 4 * tok, p.k_scale + r);
+            cp_async4(sdst + 4 * (kTile + tok), p.v_scale + r);
+          }
+        }
+        cp_async_arrive_noinc(fb);
         issued = i + 1;
       }
-      if (!ok) {
+    }
+    if (!ok) {
+      if (lane == 0) {
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
         for (long long ii = (issued > kStages ? issued - kStages : 0); ii < issued; ++ii)
           (void)mbar_wait(smem_addr(&full_bar[ii % kStages]), static_cast<uint32_t>((ii / kStages) & 1));
       }
     }
+    cp_async_wait_all();
     return;
   }
 
@@ -385,31 +437,59 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   };
   // Expands a 64 x 64-byte index tile into bf16 codewords, dims c and c + 64 of token t
   // from byte (t, c), in the two-panel 128-byte-swizzled layout of a TMA-loaded bf16 tile.
+  // Lane l takes the 16-byte pieces l, l + 32, ... (piece x: token x / 4, bytes
+  // 16 (x % 4) .. + 15, i.e. 16-byte chunks 2 (x % 4) and 2 (x % 4) + 1 of both panels),
+  // kPP pieces at a time in three phases -- load, look up, store -- so that their 16 kPP
+  // lookups are in flight together (two pieces with one head block; one with two, whose
+  // accumulators leave fewer registers).
+  constexpr int kPP = NT == 1 ? 2 : 1;
+  const uint32_t *cp_lane = cpair + lane;
   auto expand = [&](const uint8_t *idx) {
-#pragma unroll 4
-    for (int it = 0; it < kQ4TileBytes / 128; ++it) {
-      const int byte = (it * 32 + lane) * 4;
-      const int t = byte >> 6, c = byte & 63;
-      const uint32_t w4 = *reinterpret_cast<const uint32_t *>(idx + byte);
-      // bytes c + 2u, c + 2u + 1: low nibbles = dims (c + 2u, +1), high nibbles = dims + 64
-      uint32_t lo[2], hi[2];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t h2 = w4 >> (16 * u);
-        lo[u] = cpair[(h2 & 0x0fu) | ((h2 >> 4) & 0xf0u)];
-        hi[u] = cpair[((h2 >> 4) & 0x0fu) | ((h2 >> 8) & 0xf0u)];
+    for (int g = 0; g < 8 / kPP; ++g) {
+      uint4 wv[kPP];
+#pragma unroll
+      for (int q = 0; q < kPP; ++q) wv[q] = *reinterpret_cast<const uint4 *>(idx + ((kPP * g + q) * 32 + lane) * 16);
+      uint32_t lo[kPP][8], hi[kPP][8];
+#pragma unroll
+      for (int q = 0; q < kPP; ++q) {
+        const uint32_t wd[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            // bytes 4 k + 2 u and + 1: low nibbles = two adjacent dims, high nibbles = + 64
+            const uint32_t h2 = wd[k] >> (16 * u);
+            lo[q][2 * k + u] = cp_lane[((h2 & 0x0fu) | ((h2 >> 4) & 0xf0u)) << 5];
+            hi[q][2 * k + u] = cp_lane[(((h2 >> 4) & 0x0fu) | ((h2 >> 8) & 0xf0u)) << 5];
+          }
       }
-      const uint32_t off = swz128(t, c >> 3) + (c & 7) * 2;
-      *reinterpret_cast<uint2 *>(buf + off) = make_uint2(lo[0], lo[1]);
-      *reinterpret_cast<uint2 *>(buf + kHalfTileBytes + off) = make_uint2(hi[0], hi[1]);
+#pragma unroll
+      for (int q = 0; q < kPP; ++q) {
+        const int x = (kPP * g + q) * 32 + lane;
+        const int t = x >> 2, ch = 2 * (x & 3);
+        const uint32_t o0 = swz128(t, ch), o1 = swz128(t, ch + 1);
+        *reinterpret_cast<uint4 *>(buf + o0) = make_uint4(lo[q][0], lo[q][1], lo[q][2], lo[q][3]);
+        *reinterpret_cast<uint4 *>(buf + o1) = make_uint4(lo[q][4], lo[q][5], lo[q][6], lo[q][7]);
+        *reinterpret_cast<uint4 *>(buf + kHalfTileBytes + o0) = make_uint4(hi[q][0], hi[q][1], hi[q][2], hi[q][3]);
+        *reinterpret_cast<uint4 *>(buf + kHalfTileBytes + o1) = make_uint4(hi[q][4], hi[q][5], hi[q][6], hi[q][7]);
+      }
     }
   };
 
   uint32_t qh[8][NT][2], ql[8][NT][2];
   int cur_seg = -1;
   for (long long i = cw; i < n; i += kConsumerWarps) {
-    int b, kv, j;
-    q4_locate(pre, Ls, p.B, xs + i, b, kv, j);
+    const int s = static_cast<int>(i % kStages);
+    const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
+    __syncwarp();
+    if (!__all_sync(0xffffffffu, ready)) {
+      if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+      return;
+    }
+    const int4 ti = info[s];
+    const int b = ti.x, kv = ti.y, valid = ti.z;
+    const bool page_ok = ti.w != 0;
     const int sg = b * p.Hkv + kv;
     if (sg != cur_seg) {
       if (cur_seg >= 0) flush(cur_seg);
@@ -429,51 +509,31 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
           }
       }
     }
-    const int valid = min(kTile, Ls[b] - j * kTile);
-    // per-token scales of this lane's 8 tokens (16 mt + lane / 4 + 8 h); 0 past the length
-    const int row0 = tile_row(b, j, false);
+    // per-token scales of this lane's 8 tokens (16 mt + lane / 4 + 8 h), staged with the
+    // tile; 0 past the length and on a page outside the pool (its tiles read as zeros)
     float sk[4][2], sv[4][2];
-    {
-      // lane l loads tokens l and l + 32, then each lane takes its eight by shuffles
-      float k2[2], v2[2];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int tok = lane + 32 * hh;
-        const bool in = tok < valid && row0 >= 0;
-        const long long r = (static_cast<long long>(row0) + tok) * p.Hkv + kv;
-        k2[hh] = in ? p.k_scale[r] * p.scale_log2 : 0.f;
-        v2[hh] = in ? p.v_scale[r] : 0.f;
+        const int tok = 16 * mt + (lane >> 2) + 8 * hh;
+        const bool in = tok < valid && page_ok;
+        sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
+        sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
       }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int tok = 16 * mt + (lane >> 2) + 8 * hh;  // held by lane tok & 31, slot tok >> 5
-          const float ka = __shfl_sync(0xffffffffu, k2[0], tok & 31), kb = __shfl_sync(0xffffffffu, k2[1], tok & 31);
-          const float va = __shfl_sync(0xffffffffu, v2[0], tok & 31), vb = __shfl_sync(0xffffffffu, v2[1], tok & 31);
-          sk[mt][hh] = tok < 32 ? ka : kb;
-          sv[mt][hh] = tok < 32 ? va : vb;
-        }
-    }
-    const int s = static_cast<int>(i % kStages);
-    const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
-    __syncwarp();
-    if (!__all_sync(0xffffffffu, ready)) {
-      if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
-      return;
-    }
     const uint8_t *stage = smem + kQ4OffStage + s * kQ4StageBytes;
     expand(stage);
     __syncwarp();
 
-    // S^T = C_K q~^T (hi and lo parts of q~): 4 token blocks of 16 x NT head blocks of 8
-    float sacc[4][NT][4];
+    // S^T = C_K q~^T (hi and lo parts of q~; with one head block in two accumulators, so
+    // that the two mma chains interleave): 4 token blocks of 16 x NT head blocks of 8
+    float sacc[4][NT][4], sacl[4][NT][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sacl[mt][nt][e] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
@@ -487,9 +547,15 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
-          mma_bf16(sacc[mt][nt], a0, a1, a2, a3, ql[ks][nt][0], ql[ks][nt][1]);
+          mma_bf16(NT == 1 ? sacl[mt][nt] : sacc[mt][nt], a0, a1, a2, a3, ql[ks][nt][0], ql[ks][nt][1]);
         }
       }
+    if constexpr (NT == 1) {
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][0][e] += sacl[mt][0][e];
+    }
     __syncwarp();  // every lane's ldmatrix of C_K is done before C_V overwrites it
     expand(stage + kQ4TileBytes);
     __syncwarp();
@@ -571,7 +637,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 }
 
 size_t q4_attn_smem_bytes(int batch) {
-  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kStages + 4 * 256 + 4 * (batch + 1) + 4 * batch;
+  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kStages + 4 * (batch + 1) + 4 * batch;
 }
 
 cudaError_t q4_configure() {
