@@ -16,12 +16,13 @@
 //    kept as bf16 hi + lo (so that rounding q~ costs no accuracy); the new token's k row
 //    RoPE(RMSNorm(k_new)) and v row quantized and appended (R by a fast Walsh-Hadamard
 //    transform across the warp, the nearest level by the midpoint thresholds).
-//  * q4_attn_kernel: the split-KV attention of attention.cu -- the same worker partition,
-//    TMA producer, 6-stage ring and partial slots -- on 4 KB index tiles: the consumer warp
-//    that owns a stage expands its K tile into codewords (bf16, in the swizzled layout the
-//    mma code reads), runs S = K~ q~^T (hi and lo), scales each token's scores by its
-//    sigma_K, runs the online softmax, folds sigma_V into P, expands V the same way and
-//    accumulates O~ += C_V^T (P sigma_V)^T.
+//  * q4_attn_kernel: the split-KV attention of attention.cu -- the same worker partition
+//    and partial slots -- on 4 KB index tiles, through a 12-stage TMA ring whose stages
+//    also carry the tile's per-token scales (cp.async) and its (sequence, head, length).
+//    The consumer warp that owns a stage builds its mma fragments directly from a
+//    256-entry table of codeword pairs (no expanded tile in shared memory), runs
+//    S = K~ q~^T (hi and lo), scales each token's scores by its sigma_K, runs the online
+//    softmax, folds sigma_V into P and accumulates O~ += C_V^T (P sigma_V)^T.
 //  * q4_combine_kernel (combine.cu): the log-sum-exp merge, then R^T.
 #include "launch.h"
 
@@ -31,19 +32,18 @@ namespace {
 
 constexpr int kQ4TileBytes = kTile * 64;                 // 64 tokens x 64 bytes of indices
 constexpr int kQ4StageBytes = 2 * kQ4TileBytes;          // K and V index tiles
-constexpr int kQ4BufBytes = 2 * kHalfTileBytes;          // one expanded bf16 tile (16 KiB)
+constexpr int kQ4Stages = 2 * kConsumerWarps;          // ring depth: two stages per consumer warp
+static_assert(kQ4Stages % kConsumerWarps == 0, "each stage must belong to exactly one consumer warp");
 constexpr float kInvSqrtD = 0.08838834764831845f;        // 1 / sqrt(128)
 
-// Smem: [6 expanded tiles, one per consumer warp][6 stages][pair table, one copy per lane]
-// [per-stage scales][per-stage tile info][barriers][prefix]
-constexpr int kQ4OffBuf = 0;
-constexpr int kQ4OffStage = kConsumerWarps * kQ4BufBytes;
-constexpr int kQ4OffPair = kQ4OffStage + kStages * kQ4StageBytes;
+// Smem: [12 stages][pair table, one copy per lane][per-stage scales][per-stage tile info]
+// [barriers][prefix]
+constexpr int kQ4OffStage = 0;
+constexpr int kQ4OffPair = kQ4OffStage + kQ4Stages * kQ4StageBytes;
 constexpr int kQ4PairBytes = 256 * 32 * 4;
-constexpr int kQ4OffScale = kQ4OffPair + kQ4PairBytes;  // [stage][K, V][64] fp32
-constexpr int kQ4OffInfo = kQ4OffScale + kStages * 2 * kTile * 4;  // [stage] int4
-constexpr int kQ4OffBar = kQ4OffInfo + kStages * 16;
-static_assert(kQ4OffStage % 1024 == 0, "expanded tiles must keep 1024-byte alignment for the 128B swizzle");
+constexpr int kQ4OffScale = kQ4OffPair + kQ4PairBytes;               // [stage][K, V][64] fp32
+constexpr int kQ4OffInfo = kQ4OffScale + kQ4Stages * 2 * kTile * 4;  // [stage] int4
+constexpr int kQ4OffBar = kQ4OffInfo + kQ4Stages * 16;
 
 // Fast Walsh-Hadamard transform (Sylvester order) of a 128-vector held by a warp, lane l
 // holding dims 4 l .. 4 l + 3: bits 0-1 of the dim within the lane, bits 2-6 across lanes.
@@ -257,19 +257,19 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4OffBar);
-  uint64_t *empty_bar = full_bar + kStages;
+  uint64_t *empty_bar = full_bar + kQ4Stages;
   // pair table: entry (a | b << 4) = bf16 c[a] | bf16 c[b] << 16, the codewords of two
   // adjacent dims from their two nibbles; 32 copies interleaved word by word, lane l
   // reading copy l (word 32 e + l, always bank l), so random entries never conflict
   uint32_t *cpair = reinterpret_cast<uint32_t *>(smem + kQ4OffPair);  // [256][32]
   float *scl = reinterpret_cast<float *>(smem + kQ4OffScale);        // [stage][2][64]
   int4 *info = reinterpret_cast<int4 *>(smem + kQ4OffInfo);           // [stage]
-  uint32_t *pre = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [B + 1]
+  uint32_t *pre = reinterpret_cast<uint32_t *>(empty_bar + kQ4Stages);  // [B + 1]
   int32_t *Ls = reinterpret_cast<int32_t *>(pre + p.B + 1);            // [B]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kQ4Stages; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1 + 32);  // the TMA issue + one arrive per producer lane
       mbar_init(smem_addr(&empty_bar[s]), 1);
     }
@@ -343,8 +343,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         const long long i = i0 + u;
         const int b = __shfl_sync(0xffffffffu, mb, u), kv = __shfl_sync(0xffffffffu, mkv, u);
         const int row = __shfl_sync(0xffffffffu, mrow, u), valid = __shfl_sync(0xffffffffu, mvalid, u);
-        const int s = static_cast<int>(i % kStages);
-        if (i >= kStages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kStages) - 1) & 1));
+        const int s = static_cast<int>(i % kQ4Stages);
+        if (i >= kQ4Stages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kQ4Stages) - 1) & 1));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint32_t fb = smem_addr(&full_bar[s]);
@@ -372,8 +372,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     if (!ok) {
       if (lane == 0) {
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
-        for (long long ii = (issued > kStages ? issued - kStages : 0); ii < issued; ++ii)
-          (void)mbar_wait(smem_addr(&full_bar[ii % kStages]), static_cast<uint32_t>((ii / kStages) & 1));
+        for (long long ii = (issued > kQ4Stages ? issued - kQ4Stages : 0); ii < issued; ++ii)
+          (void)mbar_wait(smem_addr(&full_bar[ii % kQ4Stages]), static_cast<uint32_t>((ii / kQ4Stages) & 1));
       }
     }
     cp_async_wait_all();
@@ -381,9 +381,22 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   }
 
   // ------------------------------------------------------------------ consumer warps
+  // The mma fragments of the codeword tiles come straight from pair-table lookups, with no
+  // expanded tile in shared memory: each A register is two bf16 codewords, i.e. one
+  // lookup, once the dims are ordered so that the two nibbles of a lookup are
+  //  * for S = C_K q~^T (contraction over dims): the two nibbles of one index byte --
+  //    k-slot pair (2 c, 2 c + 1) of k-step ks for lane group c holds dims (j, j + 64) with
+  //    j = 16 c + 2 ks (and j + 1 for slots 8 + 2 c, +1), so a lane reads its token's 16
+  //    index bytes 16 c .. 16 c + 15 in one load and each byte is a table entry; q~ is
+  //    loaded in the same order;
+  //  * for O~^T = C_V^T (P sigma_V)^T (contraction over tokens): the same nibble of two
+  //    consecutive tokens -- row r of dim block md is dim 8 r + md (rows 8..15: 64 + 8 r
+  //    + md), so a lane reads 8 index bytes per token row and forms four entries per
+  //    word with two logic operations; the accumulator rows are written back in natural
+  //    dim order by the flush.
   const int cw = warp;
-  uint8_t *buf = smem + kQ4OffBuf + cw * kQ4BufBytes;  // this warp's expanded tile
-  const uint32_t bLo = smem_addr(buf), bHi = bLo + kHalfTileBytes;
+  const uint32_t *cp_lane = cpair + lane;
+  auto pair_entry = [&](uint32_t e) { return cp_lane[e << 5]; };
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -418,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int g = 8 * nt + 2 * (lane & 3) + (e & 1);
-          const int d = 16 * md + (lane >> 2) + ((e >> 1) << 3);
+          const int d = ((e >> 1) << 6) + 8 * (lane >> 2) + md;
           if (g < p.G) p.part_o[(base_row + g) * kHeadDim + d] = o[md][nt][e];
           o[md][nt][e] = 0.f;
         }
@@ -435,53 +448,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         l_run[nt][jj] = 0.f;
       }
   };
-  // Expands a 64 x 64-byte index tile into bf16 codewords, dims c and c + 64 of token t
-  // from byte (t, c), in the two-panel 128-byte-swizzled layout of a TMA-loaded bf16 tile.
-  // Lane l takes the 16-byte pieces l, l + 32, ... (piece x: token x / 4, bytes
-  // 16 (x % 4) .. + 15, i.e. 16-byte chunks 2 (x % 4) and 2 (x % 4) + 1 of both panels),
-  // kPP pieces at a time in three phases -- load, look up, store -- so that their 16 kPP
-  // lookups are in flight together (two pieces with one head block; one with two, whose
-  // accumulators leave fewer registers).
-  constexpr int kPP = NT == 1 ? 2 : 1;
-  const uint32_t *cp_lane = cpair + lane;
-  auto expand = [&](const uint8_t *idx) {
-#pragma unroll
-    for (int g = 0; g < 8 / kPP; ++g) {
-      uint4 wv[kPP];
-#pragma unroll
-      for (int q = 0; q < kPP; ++q) wv[q] = *reinterpret_cast<const uint4 *>(idx + ((kPP * g + q) * 32 + lane) * 16);
-      uint32_t lo[kPP][8], hi[kPP][8];
-#pragma unroll
-      for (int q = 0; q < kPP; ++q) {
-        const uint32_t wd[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            // bytes 4 k + 2 u and + 1: low nibbles = two adjacent dims, high nibbles = + 64
-            const uint32_t h2 = wd[k] >> (16 * u);
-            lo[q][2 * k + u] = cp_lane[((h2 & 0x0fu) | ((h2 >> 4) & 0xf0u)) << 5];
-            hi[q][2 * k + u] = cp_lane[(((h2 >> 4) & 0x0fu) | ((h2 >> 8) & 0xf0u)) << 5];
-          }
-      }
-#pragma unroll
-      for (int q = 0; q < kPP; ++q) {
-        const int x = (kPP * g + q) * 32 + lane;
-        const int t = x >> 2, ch = 2 * (x & 3);
-        const uint32_t o0 = swz128(t, ch), o1 = swz128(t, ch + 1);
-        *reinterpret_cast<uint4 *>(buf + o0) = make_uint4(lo[q][0], lo[q][1], lo[q][2], lo[q][3]);
-        *reinterpret_cast<uint4 *>(buf + o1) = make_uint4(lo[q][4], lo[q][5], lo[q][6], lo[q][7]);
-        *reinterpret_cast<uint4 *>(buf + kHalfTileBytes + o0) = make_uint4(hi[q][0], hi[q][1], hi[q][2], hi[q][3]);
-        *reinterpret_cast<uint4 *>(buf + kHalfTileBytes + o1) = make_uint4(hi[q][4], hi[q][5], hi[q][6], hi[q][7]);
-      }
-    }
-  };
 
+  const int r8 = lane >> 2, c4 = lane & 3;
   uint32_t qh[8][NT][2], ql[8][NT][2];
   int cur_seg = -1;
   for (long long i = cw; i < n; i += kConsumerWarps) {
-    const int s = static_cast<int>(i % kStages);
-    const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
+    const int s = static_cast<int>(i % kQ4Stages);
+    const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kQ4Stages) & 1));
     __syncwarp();
     if (!__all_sync(0xffffffffu, ready)) {
       if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
@@ -494,18 +467,22 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     if (sg != cur_seg) {
       if (cur_seg >= 0) flush(cur_seg);
       cur_seg = sg;
-      const int c2 = 2 * (lane & 3);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const int g = 8 * nt + (lane >> 2);
+        const int g = 8 * nt + r8;
         const long long row = (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            const int dd = 16 * ks + 8 * hf + c2;
-            qh[ks][nt][hf] = g < p.G ? *reinterpret_cast<const uint32_t *>(p.q_hi + row + dd) : 0u;
-            ql[ks][nt][hf] = g < p.G ? *reinterpret_cast<const uint32_t *>(p.q_lo + row + dd) : 0u;
+            const int j = 16 * c4 + 2 * ks + hf;  // dims j (low half) and j + 64 (high half)
+            uint32_t vh = 0u, vl = 0u;
+            if (g < p.G) {
+              vh = static_cast<uint32_t>(p.q_hi[row + j]) | (static_cast<uint32_t>(p.q_hi[row + j + 64]) << 16);
+              vl = static_cast<uint32_t>(p.q_lo[row + j]) | (static_cast<uint32_t>(p.q_lo[row + j + 64]) << 16);
+            }
+            qh[ks][nt][hf] = vh;
+            ql[ks][nt][hf] = vl;
           }
       }
     }
@@ -516,14 +493,13 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int tok = 16 * mt + (lane >> 2) + 8 * hh;
+        const int tok = 16 * mt + r8 + 8 * hh;
         const bool in = tok < valid && page_ok;
         sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
         sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
       }
-    const uint8_t *stage = smem + kQ4OffStage + s * kQ4StageBytes;
-    expand(stage);
-    __syncwarp();
+    const uint8_t *kt = smem + kQ4OffStage + s * kQ4StageBytes;  // [64 tokens][64 index bytes]
+    const uint8_t *vt = kt + kQ4TileBytes;
 
     // S^T = C_K q~^T (hi and lo parts of q~; with one head block in two accumulators, so
     // that the two mma chains interleave): 4 token blocks of 16 x NT head blocks of 8
@@ -535,31 +511,29 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sacl[mt][nt][e] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int mt = 0; mt < 4; ++mt) {
+      // tokens 16 mt + r (A rows 0-7) and + 8 (rows 8-15), index bytes 16 c .. 16 c + 15
+      const uint4 w0 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8) * 64 + 16 * c4);
+      const uint4 w1 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8 + 8) * 64 + 16 * c4);
+      const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const int qd = lane >> 3;
-        const int tok = 16 * mt + (lane & 7) + ((qd & 1) << 3);
-        const int chunk = 2 * ks + (qd >> 1);
-        const uint32_t addr = ((chunk >> 3) ? bHi : bLo) + swz128(tok, chunk & 7);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(addr, a0, a1, a2, a3);
+        const int wd = ks >> 1, sh = 16 * (ks & 1);  // bytes 2 ks and 2 ks + 1
+        const uint32_t a0 = pair_entry((x0[wd] >> sh) & 0xffu), a2 = pair_entry((x0[wd] >> (sh + 8)) & 0xffu);
+        const uint32_t a1 = pair_entry((x1[wd] >> sh) & 0xffu), a3 = pair_entry((x1[wd] >> (sh + 8)) & 0xffu);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
           mma_bf16(NT == 1 ? sacl[mt][nt] : sacc[mt][nt], a0, a1, a2, a3, ql[ks][nt][0], ql[ks][nt][1]);
         }
       }
+    }
     if constexpr (NT == 1) {
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[mt][0][e] += sacl[mt][0][e];
     }
-    __syncwarp();  // every lane's ldmatrix of C_K is done before C_V overwrites it
-    expand(stage + kQ4TileBytes);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));  // the index tiles are consumed
 
     // sigma_K * scale (log2 domain) per token, and the mask past the length
 #pragma unroll
@@ -614,30 +588,43 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         pl[mt][nt][0] = movmatrix_t(l01);
         pl[mt][nt][1] = movmatrix_t(l23);
       }
-    // O~^T += C_V^T (P sigma_V)^T : 8 dim blocks of 16 x 4 token k-steps
+    // O~^T += C_V^T (P sigma_V)^T: 4 token k-steps x 8 dim blocks of 16 (rows 8 r + md and
+    // 64 + 8 r + md); tokens t0, t0 + 1 (k-slots 2 c, +1) and t0 + 8, t0 + 9 (slots + 8)
 #pragma unroll
-    for (int md = 0; md < 8; ++md)
+    for (int mt = 0; mt < 4; ++mt) {
+      const int t0 = 16 * mt + 2 * c4;
+      const uint8_t *vr = vt + t0 * 64 + 8 * r8;
+      const uint2 y0 = *reinterpret_cast<const uint2 *>(vr), y1 = *reinterpret_cast<const uint2 *>(vr + 64);
+      const uint2 y2 = *reinterpret_cast<const uint2 *>(vr + 8 * 64), y3 = *reinterpret_cast<const uint2 *>(vr + 9 * 64);
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int qd = lane >> 3;
-        const int tok = 16 * mt + (lane & 7) + ((qd >> 1) << 3);
-        const int chunk = 2 * md + (qd & 1);
-        const uint32_t addr = ((chunk >> 3) ? bHi : bLo) + swz128(tok, chunk & 7);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(addr, a0, a1, a2, a3);
+      for (int hw = 0; hw < 2; ++hw) {
+        const uint32_t u0 = hw ? y0.y : y0.x, u1 = hw ? y1.y : y1.x, u2 = hw ? y2.y : y2.x, u3 = hw ? y3.y : y3.x;
+        // byte m of each: entry (nibble of token t) | (same nibble of token t + 1) << 4
+        const uint32_t lo01 = (u0 & 0x0f0f0f0fu) | ((u1 << 4) & 0xf0f0f0f0u);
+        const uint32_t hi01 = ((u0 >> 4) & 0x0f0f0f0fu) | (u1 & 0xf0f0f0f0u);
+        const uint32_t lo23 = (u2 & 0x0f0f0f0fu) | ((u3 << 4) & 0xf0f0f0f0u);
+        const uint32_t hi23 = ((u2 >> 4) & 0x0f0f0f0fu) | (u3 & 0xf0f0f0f0u);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
-          mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
+        for (int m = 0; m < 4; ++m) {
+          const int md = 4 * hw + m;
+          const uint32_t a0 = pair_entry((lo01 >> (8 * m)) & 0xffu), a1 = pair_entry((hi01 >> (8 * m)) & 0xffu);
+          const uint32_t a2 = pair_entry((lo23 >> (8 * m)) & 0xffu), a3 = pair_entry((hi23 >> (8 * m)) & 0xffu);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
+            mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
+          }
         }
       }
-    __syncwarp();  // the next tile's expansion overwrites C_V
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));  // the stage's index tiles are consumed
   }
   if (cur_seg >= 0) flush(cur_seg);
 }
 
 size_t q4_attn_smem_bytes(int batch) {
-  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kStages + 4 * (batch + 1) + 4 * batch;
+  return 1024 + static_cast<size_t>(kQ4OffBar) + 16 * kQ4Stages + 4 * (batch + 1) + 4 * batch;
 }
 
 cudaError_t q4_configure() {
