@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
                         const AttnParams p) {
   using C = Cfg<NT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smem = align_smem_1024(smem_raw);
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * C::kStageBytes);
   uint64_t *empty_bar = full_bar + kStages;
   uint32_t *pre = reinterpret_cast<uint32_t *>(empty_bar + kStages);  // [B + 1]

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     q4_attn_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const Q4AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smem = align_smem_1024(smem_raw);
   uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4OffBar);
   uint64_t *empty_bar = full_bar + kQ4Stages;
   // pair table: entry (a | b << 4) = bf16 c[a] | bf16 c[b] << 16, the codewords of two

@@ -102,6 +102,14 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory buffer advanced to a 1024-byte boundary (the period of the
+// 128-byte TMA swizzle) by pointer arithmetic on the buffer itself, so that the compiler
+// still sees the result as shared memory and emits shared-memory loads and stores for it
+// (an integer round trip would leave it a generic pointer).
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *raw) {
+  return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
