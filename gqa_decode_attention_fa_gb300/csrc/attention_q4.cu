@@ -395,8 +395,16 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   //    word with two logic operations; the accumulator rows are written back in natural
   //    dim order by the flush.
   const int cw = warp;
-  const uint32_t *cp_lane = cpair + lane;
-  auto pair_entry = [&](uint32_t e) { return cp_lane[e << 5]; };
+  // Entry of byte k of w in this lane's copy of the table: the byte moved down by a byte
+  // permute, then one shift-add onto the lane's 32-bit shared address.  The table is
+  // constant after the start-up barrier, so the load is a plain (reorderable) asm.
+  const uint32_t tbl_lane = smem_addr(cpair) + 4u * lane;
+  auto pair_entry = [&](uint32_t w, int k) {
+    const uint32_t e = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tbl_lane + (e << 7)));
+    return v;
+  };
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -518,9 +526,9 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        const int wd = ks >> 1, sh = 16 * (ks & 1);  // bytes 2 ks and 2 ks + 1
-        const uint32_t a0 = pair_entry((x0[wd] >> sh) & 0xffu), a2 = pair_entry((x0[wd] >> (sh + 8)) & 0xffu);
-        const uint32_t a1 = pair_entry((x1[wd] >> sh) & 0xffu), a3 = pair_entry((x1[wd] >> (sh + 8)) & 0xffu);
+        const int wd = ks >> 1, k0 = 2 * (ks & 1);  // bytes 2 ks and 2 ks + 1
+        const uint32_t a0 = pair_entry(x0[wd], k0), a2 = pair_entry(x0[wd], k0 + 1);
+        const uint32_t a1 = pair_entry(x1[wd], k0), a3 = pair_entry(x1[wd], k0 + 1);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
@@ -607,8 +615,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int md = 4 * hw + m;
-          const uint32_t a0 = pair_entry((lo01 >> (8 * m)) & 0xffu), a1 = pair_entry((hi01 >> (8 * m)) & 0xffu);
-          const uint32_t a2 = pair_entry((lo23 >> (8 * m)) & 0xffu), a3 = pair_entry((hi23 >> (8 * m)) & 0xffu);
+          const uint32_t a0 = pair_entry(lo01, m), a1 = pair_entry(hi01, m);
+          const uint32_t a2 = pair_entry(lo23, m), a3 = pair_entry(hi23, m);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);

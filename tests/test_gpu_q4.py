@@ -163,3 +163,39 @@ def test_q4_plan_reuse_and_determinism():
     plan.run_q4(w, out2)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+def test_q4_device_index_errors_are_flagged_not_faulted():
+    """Out-of-range positions, lengths and page ids set error bits and leave the other
+    sequences' outputs as they were; a length beyond the capacity zeroes that sequence's
+    output; nothing faults (the kernels bound-check; a page outside the pool reads as
+    zeros, scales included)."""
+    w = wl.make_q4(3, 10, 2, [100, 70, 5], paged=True, seed=24, max_seq=128, device="cuda")
+    ref = oracle_q4(w)
+    plan, out = run_gpu(w)
+    assert plan.device_errors() == 0
+    want = oracle_out_on(w, ref)
+    assert_out_close(out, want, "all valid")
+    # position == seq_len for sequence 1
+    w.positions[1] = 70
+    plan.run_q4(w, out)
+    torch.cuda.synchronize()
+    assert plan.device_errors() & binding.DEVERR_POSITION
+    assert_out_close(out[0:1], want[0:1], "valid sequence beside a bad position")
+    # seq_len beyond capacity for sequence 2
+    w.positions[1] = 69
+    w.seq_lens[2] = w.max_seq + 1
+    plan.run_q4(w, out)
+    torch.cuda.synchronize()
+    assert plan.device_errors() & binding.DEVERR_SEQLEN
+    assert torch.count_nonzero(out[2].float()) == 0
+    assert_out_close(out[0:1], want[0:1], "valid sequence beside a bad length")
+    # page id outside the pool for sequence 1's first page (its new row is on page 1)
+    w.seq_lens[2] = 5
+    w.page_table[1, 0] = 10 ** 6
+    plan.run_q4(w, out)
+    torch.cuda.synchronize()
+    assert plan.device_errors() & binding.DEVERR_PAGE
+    assert plan.device_errors() == 0  # cleared by the previous read
+    assert torch.all(torch.isfinite(out.float()))
+    assert_out_close(out[0:1], want[0:1], "valid sequence beside a bad page")
