@@ -649,7 +649,7 @@ extern "C" gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan, const void *q
   pp.max_blocks = plan->max_blocks;
   pp.num_blocks = paged ? d.num_cache_blocks : 0;
   pp.eps = eps;
-  if (launch_q4_prologue(pp, s) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_q4_prologue(pp, !rebuilt, s) != cudaSuccess) return GQA_ERR_CUDA;
 
   Q4AttnParams ap;
   memset(&ap, 0, sizeof ap);

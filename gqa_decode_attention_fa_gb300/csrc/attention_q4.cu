@@ -87,12 +87,20 @@ __device__ __forceinline__ void unpack4(uint2 w, float (&f)[4]) {
 // One warp per row: CTA (b, y) of 8 warps handles rows 8 y .. 8 y + 7 of sequence b's H_q
 // query rows, then its H_kv key rows, then its H_kv value rows.  Lane l holds dims 4 l .. 4 l + 3; the
 // RoPE partner of dim e (e +- 64) is in lane l ^ 16.
+// The kernel waits on the preceding kernel in the stream only at its end.  That kernel is
+// the previous step's combine (which lets this one start once the previous attention
+// kernel has finished, so the rotated-query buffer and the cache are free) or a kernel of
+// the caller (which has then finished); a RoPE table rebuild is ordered before it by a
+// plain launch.  The wait at the end keeps this grid from completing before the previous
+// combine has read its partials, which the next attention kernel overwrites.
 __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams p) {
-  griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.y * 8 + warp;  // this warp's row
-  if (r >= p.Hq + 2 * p.Hkv) return;
+  if (r >= p.Hq + 2 * p.Hkv) {
+    griddep_wait();
+    return;
+  }
   const int L = p.seq_lens[b], pos = p.positions[b];
   const bool len_ok = L >= 1 && L <= p.max_seq;
   const bool pos_ok = len_ok && pos >= 0 && pos < L;
@@ -228,6 +236,7 @@ __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams
       if (lane == 0) (is_k ? p.k_scale : p.v_scale)[crow_kv] = sigma;
     }
   }
+  griddep_wait();
 }
 
 // ----------------------------------------------------------------------------- attention
@@ -642,8 +651,8 @@ cudaError_t q4_configure() {
   return e;
 }
 
-cudaError_t launch_q4_prologue(const Q4PrologueParams &p, cudaStream_t stream) {
-  return launch_pdl(q4_prologue_kernel, dim3(static_cast<unsigned>(p.B), static_cast<unsigned>((p.Hq + 2 * p.Hkv + 7) / 8)),
+cudaError_t launch_q4_prologue(const Q4PrologueParams &p, bool pdl, cudaStream_t stream) {
+  return launch_ex(pdl, q4_prologue_kernel, dim3(static_cast<unsigned>(p.B), static_cast<unsigned>((p.Hq + 2 * p.Hkv + 7) / 8)),
                     dim3(256), 0, stream, p);
 }
 

@@ -86,7 +86,10 @@ struct Q4AttnParams {
   float scale_log2;
 };
 cudaError_t q4_configure();
-cudaError_t launch_q4_prologue(const Q4PrologueParams &p, cudaStream_t stream);
+// The 4-bit step's prologue reads the caller's inputs and the RoPE table before it waits on
+// the preceding kernel, so it is launched in plain stream order (`pdl` false) after a
+// RoPE table rebuild.
+cudaError_t launch_q4_prologue(const Q4PrologueParams &p, bool pdl, cudaStream_t stream);
 cudaError_t launch_q4_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4AttnParams &p, int npad,
                                 int num_workers, cudaStream_t stream);
 cudaError_t launch_q4_combine(const CombineParams &p, const int8_t *signs, cudaStream_t stream);

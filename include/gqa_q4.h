@@ -48,7 +48,11 @@ gqa_status_t gqa_q4_codebook(uint16_t *levels_bf16);
  *   out                     bf16 device [B, H_q, 128]
  * Three launches (prologue: rotated queries and the appended rows; split-KV attention on
  * the index tiles; combine and unrotation), programmatic stream serialization as for
- * gqa_decode_attn.  Errors: those of gqa_decode_attn; k_idx, v_idx 16-byte aligned,
+ * gqa_decode_attn: the prologue reads its inputs and the RoPE table and writes the
+ * rotated queries and the new rows before it waits on the preceding kernel (it waits at
+ * its end), so the same rule holds -- the kernel launched immediately before the call must
+ * not write the call's inputs if it triggers programmatic completion early; after a RoPE
+ * table rebuild the prologue is launched in plain stream order.  Errors: those of gqa_decode_attn; k_idx, v_idx 16-byte aligned,
  * scales and signs 4-byte aligned, else GQA_ERR_INVALID_ARG.
  */
 gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan,

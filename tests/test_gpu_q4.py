@@ -9,6 +9,7 @@ the packed indices equal the oracle's except where the exact rotated coordinate 
 binary64), and then the kernel's index is one of those two levels; the scale equals
 ||z|| / ||c[idx]|| for the kernel's own indices to 1e-5; every other row is untouched.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -199,3 +200,35 @@ def test_q4_device_index_errors_are_flagged_not_faulted():
     assert plan.device_errors() == 0  # cleared by the previous read
     assert torch.all(torch.isfinite(out.float()))
     assert_out_close(out[0:1], want[0:1], "valid sequence beside a bad page")
+
+
+def test_q4_back_to_back_steps_match_the_oracle():
+    """Four autoregressive steps enqueued back to back on one plan and stream, with no host
+    synchronisation between them: the lengths grow by one a step and every step brings
+    fresh q/k/v.  Each step's output is compared with the oracle's attention over the cache
+    the kernels left (later steps append only past this step's length).  The prologue
+    writes the rotated queries and the new rows before its grid-dependency wait, so this
+    checks that no step's kernels run into the previous step's reads."""
+    base = wl.make_q4(2, 40, 8, [130, 400], paged=True, seed=25, max_seq=448, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(26)
+    steps = []
+    for s in range(4):  # every input built before the first call
+        fresh = [torch.randn(t.shape, generator=gen, device="cuda").to(torch.bfloat16)
+                 for t in (base.q_new, base.k_new, base.v_new)]
+        steps.append(dataclasses.replace(base, q_new=fresh[0], k_new=fresh[1], v_new=fresh[2],
+                                         seq_lens=(base.seq_lens + s).contiguous(),
+                                         positions=(base.positions + s).contiguous()))
+    plan = binding.Plan(base.B, base.Hq, base.Hkv, base.max_seq, block_size=base.block_size,
+                        num_cache_blocks=base.num_blocks, seq_lens_host=base.seq_lens.cpu().numpy())
+    outs = [torch.full((base.B, base.Hq, base.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for _ in steps]
+    torch.cuda.synchronize()
+    for ws, out in zip(steps, outs):
+        plan.run_q4(ws, out)
+    torch.cuda.synchronize()
+    assert plan.device_errors() == 0
+    for s, (ws, out) in enumerate(zip(steps, outs)):
+        ref = oracle_q4(ws)
+        assert ref["status"] == 0
+        assert_out_close(out, oracle_out_on(ws, ref), f"step {s}")
