@@ -320,11 +320,11 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   const int W = gridDim.x, w = blockIdx.x;
   const long long xs = worker_begin(T, W, w), xe = worker_begin(T, W, w + 1);
   const long long n = xe - xs;
-  auto tile_row = [&](int b, int j, bool flag) {
+  auto tile_row = [&](int b, int j) {
     if (!p.paged) return b * p.max_seq + j * kTile;
     const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
     if (pg < 0 || pg >= p.num_blocks) {
-      if (flag) atomicOr(p.err, GQA_DEVERR_PAGE);
+      atomicOr(p.err, GQA_DEVERR_PAGE);
       return -kTile;  // the whole box out of bounds: TMA fills zeros
     }
     return pg * kTile;
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       if (i0 + lane < n) {
         int mj;
         q4_locate(pre, Ls, p.B, xs + i0 + lane, mb, mkv, mj);
-        mrow = tile_row(mb, mj, true);
+        mrow = tile_row(mb, mj);
         mvalid = min(kTile, Ls[mb] - mj * kTile);
       }
       const int cnt = static_cast<int>(min(32LL, n - i0));
