@@ -106,7 +106,9 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * gqa_plan_create -- the split planner.  Validates the geometry, chooses the number of
  * split-KV workers (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
  * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
- * per worker, ADR-0060 section 2.1 contiguous-block placement) and allocates the
+ * per worker, ADR-0060 section 2.1 contiguous-block placement: one worker per SM, at
+ * most one per tile, and a quarter of the tiles, rounded up, when the tiles fill the SMs
+ * three to four times over) and allocates the
  * workspace once, so no call allocates.  The workspace holds a copy of the rotated
  * queries, the fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats),
  * the RoPE tables (max_seq_len x 1.5 KiB), the first tiles each worker streamed at the
@@ -247,8 +249,8 @@ long long gqa_partition_describe(const int32_t *seq_lens_host, int batch, int nu
  *   max_seq_len * 1.5 KiB                       RoPE tables (binary64 and binary32, first)
  * + B * H_q * 256 B                             rotated queries
  * + (B * H_kv + W) * 6 * G * 520 B              fp32 (m, l, O) partials
- * each rounded up to 256 bytes, plus 256; W = desc->num_workers, or when 0 the SM count
- * capped at B * H_kv * ceil(max_seq_len / 64).  A geometry that needs more is rejected
+ * each rounded up to 256 bytes, plus 256; W = desc->num_workers, or when 0 the planner's
+ * count (as gqa_plan_create) for B * H_kv * ceil(max_seq_len / 64) tiles.  A geometry that needs more is rejected
  * with GQA_ERR_SCRATCH_LIMIT before anything is launched; use a plan for it.  (For example
  * B = 32, H_q = 40, H_kv = 8, max_seq_len = 8192 needs about 18 MiB; max_seq_len = 131072
  * does not fit whatever the batch.)
