@@ -51,3 +51,20 @@ def test_two_gloo_ranks_take_the_max_and_only_rank0_runs_the_reference():
     for rank in (0, 1):
         assert res[rank][0] == [2.0, 10.0, 3.5]
     assert res[1][1] is None   # a non-zero rank does no reference work and prints nothing
+
+
+def test_reference_arm_line_carries_the_contract_keys():
+    """The reference arm's JSON line (rank 0 of one): the metric and unit of our arm, the
+    workload, a cpu_baseline describing the oracle run and an e2e object with no
+    transfers."""
+    import json
+
+    args = argparse.Namespace(workload="qwen3-14b-tiny", steps=2, warmup=3)
+    r = json.loads(json.dumps(bench.run_reference(args, 0, 1)))
+    assert r["impl"] == "reference" and r["metric"] == bench.METRIC and r["unit"] == "us/step"
+    assert r["higher_is_better"] is False and r["n_gpus"] == 1
+    assert r["steps"] == 2 and r["warmup"] == 3 and r["config"] == {"workload": "qwen3-14b-tiny"}
+    assert r["value"] > 0 and r["ms_per_step"] == pytest.approx(r["value"] / 1e3, abs=1e-3)
+    cb = r["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == r["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert r["e2e"] == {"value": r["value"], "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
