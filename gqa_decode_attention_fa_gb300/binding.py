@@ -37,7 +37,7 @@ class GqaError(RuntimeError):
 class PlanDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "block_size", "max_seq_len",
-        "num_cache_blocks", "num_workers", "device")]
+        "num_cache_blocks", "num_workers", "device", "cluster_size")]
 
 
 class PrefillDesc(ctypes.Structure):
@@ -71,6 +71,12 @@ def load(build: bool = True):
         lib.gqa_plan_destroy.argtypes = [P]
         lib.gqa_plan_num_workers.argtypes = [P]
         lib.gqa_plan_num_workers.restype = I
+        lib.gqa_plan_describe.argtypes = [ctypes.POINTER(PlanDesc), P, I, P, P, P, P]
+        lib.gqa_plan_describe.restype = I
+        lib.gqa_plan_num_splits.argtypes = [P]
+        lib.gqa_plan_num_splits.restype = I
+        lib.gqa_plan_cluster_size.argtypes = [P]
+        lib.gqa_plan_cluster_size.restype = I
         lib.gqa_plan_workspace_bytes.argtypes = [P]
         lib.gqa_plan_workspace_bytes.restype = ctypes.c_size_t
         step = [P, P, P, P, P, P, P, P, P, P, P, F, F]
@@ -151,27 +157,48 @@ def partition_describe(seq_lens, num_kv_heads: int, max_seq_len: int, num_worker
     return int(T), rng
 
 
+GB300_SMS = 152
+GB300_CLUSTER_CAPACITY = (152, 76, 36, 15, 7)   # clusters of 1, 2, 4, 8, 16 CTAs resident at once
+
+
+def plan_describe(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *, block_size: int = 0,
+                  num_cache_blocks: int = 0, num_workers: int = 0, cluster_size: int = 0, seq_lens_host=None,
+                  num_sms: int = GB300_SMS, cluster_capacity=GB300_CLUSTER_CAPACITY, head_dim: int = 128):
+    """The planner's choices without a GPU (gqa_plan_describe): (workers, cluster size, splits)."""
+    desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+                    int(max_seq_len), int(num_cache_blocks), int(num_workers), 0, int(cluster_size))
+    sl = None if seq_lens_host is None else np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
+    cap = np.ascontiguousarray(np.asarray(cluster_capacity, dtype=np.int32))
+    out = np.zeros(3, dtype=np.int32)
+    _check(load().gqa_plan_describe(ctypes.byref(desc), None if sl is None else sl.ctypes.data, int(num_sms),
+                                    cap.ctypes.data, out[0:].ctypes.data, out[1:].ctypes.data,
+                                    out[2:].ctypes.data), "gqa_plan_describe")
+    return int(out[0]), int(out[1]), int(out[2])
+
+
 def decode_attn_static(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, q_new, k_new, v_new,
                        k_cache, v_cache, page_table, seq_lens, positions, q_norm_w, k_norm_w, rope_theta: float,
                        eps: float, out, *, block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128,
-                       num_workers: int = 0, device: int = 0, device_errors=None, stream=None):
+                       num_workers: int = 0, cluster_size: int = 0, device: int = 0, device_errors=None,
+                       stream=None):
     """One decode step through gqa_decode_attn_static: no plan, no device allocation; the
     workspace is the library's fixed static scratch of the device.  `device_errors` is an
     optional int32/uint32 device tensor of one element the kernels OR error bits into."""
     desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                    int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device))
+                    int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device), int(cluster_size))
     _check(load().gqa_decode_attn_static(
         ctypes.byref(desc), _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache),
         _dptr(page_table), _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta),
         float(eps), _dptr(out), _dptr(device_errors), _stream(stream)), "gqa_decode_attn_static")
 
 
-def decode_attn_static_workload(w, out, *, num_workers: int = 0, device: int = 0, device_errors=None, stream=None):
+def decode_attn_static_workload(w, out, *, num_workers: int = 0, cluster_size: int = 0, device: int = 0,
+                                device_errors=None, stream=None):
     """gqa_decode_attn_static on a workload's tensors (see workloads.Workload)."""
     decode_attn_static(w.B, w.Hq, w.Hkv, w.max_seq, w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, w.page_table,
                        w.seq_lens, w.positions, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out,
                        block_size=w.block_size, num_cache_blocks=w.num_blocks, num_workers=num_workers,
-                       device=device, device_errors=device_errors, stream=stream)
+                       cluster_size=cluster_size, device=device, device_errors=device_errors, stream=stream)
 
 
 def prefill_attn(batch: int, num_q_heads: int, num_kv_heads: int, chunk_len: int, max_seq_len: int, q_new, k_new,
@@ -206,10 +233,11 @@ class Plan:
 
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *,
                  block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128, num_workers: int = 0,
-                 device: int = 0, seq_lens_host=None):
+                 device: int = 0, seq_lens_host=None, cluster_size: int = 0):
         self._lib = load()
         self.desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                             int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device))
+                             int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device),
+                             int(cluster_size))
         sl = None
         if seq_lens_host is not None:
             sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
@@ -218,9 +246,10 @@ class Plan:
                                          ctypes.byref(self._h)), "gqa_plan_create")
 
     @classmethod
-    def for_workload(cls, w, num_workers: int = 0, device: int = 0) -> "Plan":
+    def for_workload(cls, w, num_workers: int = 0, device: int = 0, cluster_size: int = 0) -> "Plan":
         return cls(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
-                   num_workers=num_workers, device=device, seq_lens_host=w.seq_lens.cpu().numpy())
+                   num_workers=num_workers, device=device, seq_lens_host=w.seq_lens.cpu().numpy(),
+                   cluster_size=cluster_size)
 
     def close(self):
         if getattr(self, "_h", None) and self._h.value:
@@ -240,6 +269,15 @@ class Plan:
     @property
     def num_workers(self) -> int:
         return self._lib.gqa_plan_num_workers(self._h)
+
+    @property
+    def num_splits(self) -> int:
+        return self._lib.gqa_plan_num_splits(self._h)
+
+    @property
+    def cluster_size(self) -> int:
+        """The single-launch form's cluster size, 0 for split-KV + combine."""
+        return self._lib.gqa_plan_cluster_size(self._h)
 
     @property
     def workspace_bytes(self) -> int:

@@ -15,6 +15,8 @@ using namespace gqa;
 struct gqa_plan {
   gqa_plan_desc_t desc;
   int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0, combine_split = 1;
+  int csize = 0;   // single-launch form: CTAs per (sequence, KV head) cluster; 0: split-KV + combine
+  int nsplit = 0;  // KV splits of the longest (sequence, KV head) segment
   long long num_rows = 0;
   void *ws = nullptr;
   size_t ws_bytes = 0;
@@ -104,18 +106,53 @@ const float2 *rope_tab32_of(const gqa_plan_t *plan) {
   return reinterpret_cast<const float2 *>(plan->rope_tab + static_cast<size_t>(plan->desc.max_seq_len) * 64);
 }
 
-// The split planner: one worker CTA per SM (the kernel holds ~200 KiB of shared memory,
-// so one CTA fits an SM), never more workers than tiles.  Workers take equal contiguous
-// tile ranges.  One exception, measured: when the tiles fill every SM three to four times
-// over, about four tiles a worker beat one worker per SM -- one 4096-token sequence of 8
-// KV heads (512 tiles) took 8.8 us a step with 152 workers, 8.3 with 112, 8.0 with 128
-// and 7.9 with 96, and 9.4 with 76 (over six tiles a worker no longer fit its ring at
-// once).
+// The split-KV form's worker count.  A worker streams its tiles at a rate that does not
+// grow with fewer workers once the SMs are all busy, so the step takes about as long as
+// the longest worker's range: use the fewest workers that keep the longest range at its
+// minimum, ceil(T / SMs) tiles -- fewer workers also mean fewer partials to combine.
+// Measured on one 4096-token sequence of 8 KV heads (512 tiles, four a worker at most):
+// 128 workers 8.0 us a step, 152 workers 8.8 us (more partials, the same longest range).
 int plan_workers(int num_sms, long long total_tiles) {
-  long long w = num_sms;
-  if (total_tiles >= 3LL * num_sms && total_tiles < 4LL * num_sms) w = (total_tiles + 3) / 4;
-  if (total_tiles < w) w = total_tiles;
-  return w < 1 ? 1 : static_cast<int>(w);
+  if (total_tiles < 1) return 1;
+  const long long per = (total_tiles + num_sms - 1) / num_sms;  // the longest range's minimum
+  return static_cast<int>((total_tiles + per - 1) / per);
+}
+
+}  // namespace
+
+int gqa::plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long nseg,
+                        long long max_seg_tiles, long long total_tiles) {
+  auto cap = [&](int c) { return capacity[c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4]; };
+  if (forced < 0) return 0;
+  if (forced > 0) return cap(forced) >= 1 ? forced : -1;
+  if (num_workers > 0) return 0;           // an explicit worker count asks for the split-KV form
+  if (nseg > 2LL * num_sms) return 0;      // more than two waves of one-CTA segments
+  for (int c = 16; c >= 1; c >>= 1) {
+    if (c > 1 && c > max_seg_tiles) continue;        // no CTA without tiles
+    if (c > 1 && nseg * c > num_sms) continue;       // one CTA per SM ...
+    if (cap(c) < 1 || (c > 1 && cap(c) < nseg)) continue;  // ... and every cluster at once
+    // Enough CTAs to stream: 64 SMs nearly saturate HBM (about 105 GB/s each measured),
+    // or one CTA per tile already.
+    if (nseg * c < 64 && nseg * c < total_tiles) return 0;
+    return c;
+  }
+  return 0;
+}
+
+namespace {
+
+// Workers whose tile ranges touch the longest segment of a batch (the split form), for
+// gqa_plan_num_splits.
+int split_count(const int32_t *lens, int B, int Hkv, int max_seq, int W) {
+  long long T = 0, best_nt = -1, best_begin = 0;
+  for (int b = 0; b < B; ++b) {
+    long long L = lens ? lens[b] : max_seq;
+    L = L < 1 ? 1 : (L > max_seq ? max_seq : L);
+    const long long nt = (L + kTile - 1) / kTile;
+    if (nt > best_nt) best_nt = nt, best_begin = T;
+    T += Hkv * nt;
+  }
+  return worker_of(T, W, best_begin + best_nt - 1) - worker_of(T, W, best_begin) + 1;
 }
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.f; }
@@ -133,6 +170,8 @@ bool mapped_host(const void *h, void **d) {
     cudaGetLastError();
   return *d != nullptr;
 }
+
+bool valid_cluster_size(int c) { return c == -1 || c == 0 || c == 1 || c == 2 || c == 4 || c == 8 || c == 16; }
 
 // The kernels read and write whole 16-byte chunks of the bf16 tensors (and bulk-prefetch
 // them), and 4-byte words of the int32 ones; NULL passes (optional tensors).
@@ -202,9 +241,12 @@ gqa_status_t ensure_rope_table(const gqa_plan_t *plan, float theta, cudaStream_t
   return GQA_OK;
 }
 
+// The attention launch: the split-KV kernel (partials for gqa_combine) when `single_out`
+// is null, else the single-launch form writing the step's output there.
 gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k, const void *v, void *kc, void *vc,
                            const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
-                           float theta, float eps, cudaStream_t stream, bool host_inputs = false) {
+                           float theta, float eps, cudaStream_t stream, bool host_inputs = false,
+                           void *single_out = nullptr) {
   if (!device_args_aligned(q, k, v, kc, vc, qw, kw, pt, sl, pos)) return GQA_ERR_INVALID_ARG;
   bool rebuilt = false;
   gqa_status_t st = ensure_rope_table(plan, theta, stream, &rebuilt);
@@ -242,7 +284,16 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k,
   p.num_blocks = plan->desc.num_cache_blocks;
   p.eps = static_cast<double>(eps);
   p.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
-  return launch_attention(tk, tv, p, plan->npad, plan->W, !rebuilt, stream) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  cudaError_t e;
+  if (single_out) {
+    p.out = static_cast<uint16_t *>(single_out);
+    p.csize = plan->csize;
+    p.spec = nullptr;
+    e = launch_attention_cluster(tk, tv, p, plan->npad, !rebuilt, stream);
+  } else {
+    e = launch_attention(tk, tv, p, plan->npad, plan->W, !rebuilt, stream);
+  }
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
 gqa_status_t run_combine(const gqa_plan_t *plan, const int32_t *sl, void *out, cudaStream_t stream) {
@@ -266,18 +317,16 @@ gqa_status_t run_step(const gqa_plan_t *plan, const void *q, const void *k, cons
                       const int32_t *pt, const int32_t *sl, const int32_t *pos, const void *qw, const void *kw,
                       float theta, float eps, void *out, cudaStream_t stream, bool host_inputs = false) {
   if (!aligned(out, 16)) return GQA_ERR_INVALID_ARG;  // checked before anything is launched
-  gqa_status_t st = run_attention(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream, host_inputs);
-  if (st != GQA_OK) return st;
+  gqa_status_t st = run_attention(plan, q, k, v, kc, vc, pt, sl, pos, qw, kw, theta, eps, stream, host_inputs,
+                                  plan->csize > 0 ? out : nullptr);
+  if (st != GQA_OK || plan->csize > 0) return st;
   return run_combine(plan, sl, out, stream);
 }
 
-}  // namespace
-
-namespace gqa {
-
-gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay) {
+// Checks a geometry (all but the device index).
+gqa_status_t check_desc(const gqa_plan_desc_t &d) {
   if (d.batch < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.max_seq_len < 1 || d.num_workers < 0 ||
-      d.block_size < 0)
+      d.block_size < 0 || !valid_cluster_size(d.cluster_size))
     return GQA_ERR_INVALID_ARG;
   if (d.head_dim != GQA_HEAD_DIM || d.num_q_heads % d.num_kv_heads != 0 ||
       d.num_q_heads / d.num_kv_heads > GQA_MAX_GROUP || d.batch > GQA_MAX_BATCH ||
@@ -285,18 +334,71 @@ gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay)
     return GQA_ERR_UNSUPPORTED;
   const bool paged = d.block_size > 0;
   if (paged && d.num_cache_blocks < 1) return GQA_ERR_INVALID_ARG;
+  const long long max_blocks = (d.max_seq_len + kTile - 1) / kTile;
+  const long long num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile
+                                   : static_cast<long long>(d.batch) * d.max_seq_len;
+  if (num_rows > 0x7fffffffLL - kTile) return GQA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d.batch) * d.num_kv_heads * max_blocks > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+// The planner's decisions for a checked geometry on a device with `num_sms` SMs that can
+// hold capacity[k] clusters of 2^k single-launch CTAs at once: the split-KV worker count,
+// the step's form, the splits of the longest segment and the combine's shape.  Lengths
+// come from seq_lens_host (clamped to [1, max_seq_len]) or are max_seq_len.
+struct PlanChoice {
+  int W = 0, csize = 0, nsplit = 0, combine_split = 0;
+};
+gqa_status_t plan_choose(const gqa_plan_desc_t &d, const int32_t *seq_lens_host, int num_sms, const int *capacity,
+                         PlanChoice *out) {
+  long long total_tiles = 0, max_seg_tiles = 0;
+  for (int b = 0; b < d.batch; ++b) {
+    long long L = seq_lens_host ? seq_lens_host[b] : d.max_seq_len;
+    if (L < 1) L = 1;
+    if (L > d.max_seq_len) L = d.max_seq_len;
+    total_tiles += d.num_kv_heads * ((L + kTile - 1) / kTile);
+    max_seg_tiles = std::max(max_seg_tiles, (L + kTile - 1) / kTile);
+  }
+  PlanChoice c;
+  c.W = d.num_workers > 0 ? d.num_workers : plan_workers(num_sms, total_tiles);
+  c.combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, c.W, num_sms);
+  c.csize = plan_step_form(d.cluster_size, d.num_workers, num_sms, capacity,
+                           static_cast<long long>(d.batch) * d.num_kv_heads, max_seg_tiles, total_tiles);
+  if (c.csize < 0) return GQA_ERR_UNSUPPORTED;
+  c.nsplit = c.csize > 0 ? static_cast<int>(std::min<long long>(c.csize, max_seg_tiles))
+                         : split_count(seq_lens_host, d.batch, d.num_kv_heads, d.max_seq_len, c.W);
+  *out = c;
+  return GQA_OK;
+}
+
+// The current device's cluster capacities for a group size (attn_configure first).
+void device_capacity(int npad, int (&cap)[5]) {
+  for (int k = 0; k < 5; ++k) cap[k] = attn_cluster_capacity(npad, 1 << k);
+}
+
+}  // namespace
+
+namespace gqa {
+
+gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay) {
+  gqa_status_t st = check_desc(d);
+  if (st != GQA_OK) return st;
+  const bool paged = d.block_size > 0;
   const long long B = d.batch, Hkv = d.num_kv_heads;
   const long long max_blocks = (d.max_seq_len + kTile - 1) / kTile;
-  const long long num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile : B * d.max_seq_len;
-  if (num_rows > 0x7fffffffLL - kTile) return GQA_ERR_UNSUPPORTED;
-  if (B * Hkv * max_blocks > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
   StepLayout l;
   l.G = d.num_q_heads / d.num_kv_heads;
   l.npad = l.G <= 8 ? 8 : 16;
   l.max_blocks = static_cast<int>(max_blocks);
-  l.num_rows = num_rows;
-  l.W = d.num_workers > 0 ? d.num_workers : plan_workers(num_sms, B * Hkv * max_blocks);
-  l.combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, l.W, num_sms);
+  l.num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile : B * d.max_seq_len;
+  int cap[5];
+  device_capacity(l.npad, cap);
+  PlanChoice pc;
+  st = plan_choose(d, nullptr, num_sms, cap, &pc);
+  if (st != GQA_OK) return st;
+  l.W = pc.W;
+  l.combine_split = pc.combine_split;
+  l.csize = pc.csize;
   const long long slots = B * Hkv + l.W;
   l.tab_bytes = rope_tables_bytes(d.max_seq_len);
   l.off_q = l.tab_bytes;
@@ -320,6 +422,7 @@ gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *
   plan.W = lay.W;
   plan.max_blocks = lay.max_blocks;
   plan.combine_split = lay.combine_split;
+  plan.csize = lay.csize;
   plan.num_rows = lay.num_rows;
   char *c = static_cast<char *>(base);
   plan.rope_tab = reinterpret_cast<float4 *>(c);
@@ -342,20 +445,8 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   if (!desc || !plan) return GQA_ERR_INVALID_ARG;
   *plan = nullptr;
   const gqa_plan_desc_t &d = *desc;
-  if (d.batch < 1 || d.num_q_heads < 1 || d.num_kv_heads < 1 || d.max_seq_len < 1 || d.num_workers < 0 ||
-      d.block_size < 0)
-    return GQA_ERR_INVALID_ARG;
-  if (d.head_dim != GQA_HEAD_DIM || d.num_q_heads % d.num_kv_heads != 0 ||
-      d.num_q_heads / d.num_kv_heads > GQA_MAX_GROUP || d.batch > GQA_MAX_BATCH ||
-      (d.block_size != 0 && d.block_size != GQA_BLOCK_SIZE))
-    return GQA_ERR_UNSUPPORTED;
-  const bool paged = d.block_size > 0;
-  if (paged && d.num_cache_blocks < 1) return GQA_ERR_INVALID_ARG;
-  const long long max_blocks = (d.max_seq_len + kTile - 1) / kTile;
-  const long long num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile
-                                   : static_cast<long long>(d.batch) * d.max_seq_len;
-  if (num_rows > 0x7fffffffLL - kTile) return GQA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(d.batch) * d.num_kv_heads * max_blocks > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  gqa_status_t st = check_desc(d);
+  if (st != GQA_OK) return st;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) return GQA_ERR_CUDA;
   if (d.device < 0 || d.device >= ndev) return GQA_ERR_INVALID_ARG;
@@ -364,24 +455,30 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   if (!guard.ok) return GQA_ERR_CUDA;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess) return GQA_ERR_CUDA;
+  const int npad = d.num_q_heads / d.num_kv_heads <= 8 ? 8 : 16;
+  if (attn_configure(npad) != cudaSuccess) {
+    cudaGetLastError();
+    return GQA_ERR_CUDA;
+  }
+  int cap[5];
+  device_capacity(npad, cap);
+  PlanChoice pc;
+  st = plan_choose(d, seq_lens_host, sms, cap, &pc);
+  if (st != GQA_OK) return st;
 
   gqa_plan_t *p = new (std::nothrow) gqa_plan_t();
   if (!p) return GQA_ERR_WORKSPACE;
   p->desc = d;
   p->G = d.num_q_heads / d.num_kv_heads;
-  p->npad = p->G <= 8 ? 8 : 16;
+  p->npad = npad;
   p->num_sms = sms;
-  p->max_blocks = static_cast<int>(max_blocks);
-  p->num_rows = num_rows;
-  long long total_tiles = 0;
-  for (int b = 0; b < d.batch; ++b) {
-    long long L = seq_lens_host ? seq_lens_host[b] : d.max_seq_len;
-    if (L < 1) L = 1;
-    if (L > d.max_seq_len) L = d.max_seq_len;
-    total_tiles += d.num_kv_heads * ((L + kTile - 1) / kTile);
-  }
-  p->W = d.num_workers > 0 ? d.num_workers : plan_workers(sms, total_tiles);
-  p->combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, p->W, sms);
+  p->max_blocks = static_cast<int>((d.max_seq_len + kTile - 1) / kTile);
+  p->num_rows = d.block_size > 0 ? static_cast<long long>(d.num_cache_blocks) * kTile
+                                  : static_cast<long long>(d.batch) * d.max_seq_len;
+  p->W = pc.W;
+  p->combine_split = pc.combine_split;
+  p->csize = pc.csize;
+  p->nsplit = pc.nsplit;
 
   const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
   const long long slots = B * Hkv + p->W;
@@ -415,7 +512,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->q4_hi = reinterpret_cast<uint16_t *>(c); c += sz_q;
   p->q4_lo = reinterpret_cast<uint16_t *>(c); c += sz_q;
   if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess || cudaMemset(p->spec, 0xff, sz_spec) != cudaSuccess ||
-      attn_configure(p->npad) != cudaSuccess || q4_configure() != cudaSuccess ||
+      q4_configure() != cudaSuccess ||
       configure_small_kernels() != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
@@ -435,7 +532,25 @@ gqa_status_t gqa_plan_destroy(gqa_plan_t *plan) {
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
+gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_lens_host, int num_sms,
+                               const int *cluster_capacity, int *num_workers, int *cluster_size, int *num_splits) {
+  if (!desc || !cluster_capacity || num_sms < 1) return GQA_ERR_INVALID_ARG;
+  gqa_status_t st = check_desc(*desc);
+  if (st != GQA_OK) return st;
+  PlanChoice pc;
+  st = plan_choose(*desc, seq_lens_host, num_sms, cluster_capacity, &pc);
+  if (st != GQA_OK) return st;
+  if (num_workers) *num_workers = pc.W;
+  if (cluster_size) *cluster_size = pc.csize;
+  if (num_splits) *num_splits = pc.nsplit;
+  return GQA_OK;
+}
+
 int gqa_plan_num_workers(const gqa_plan_t *plan) { return plan ? plan->W : 0; }
+
+int gqa_plan_num_splits(const gqa_plan_t *plan) { return plan ? plan->nsplit : 0; }
+
+int gqa_plan_cluster_size(const gqa_plan_t *plan) { return plan ? plan->csize : 0; }
 
 size_t gqa_plan_workspace_bytes(const gqa_plan_t *plan) { return plan ? plan->ws_bytes : 0; }
 

@@ -85,17 +85,37 @@ __device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, 
 // as its exact value rounds (rotate_row_k), v = v_new, written to the token's cache row
 // (skipped when its page id is out of range; the producer flags that) and returned per
 // lane for the shared-memory patch.
-__device__ __forceinline__ void append_kv_row(const AttnParams &p, int kv, int lane, const KvRowIn &in,
-                                              uint16_t (&kz)[4], uint16_t (&vz)[4]) {
+__device__ __forceinline__ void rotated_kv_row(const AttnParams &p, const KvRowIn &in, uint16_t (&kz)[4],
+                                               uint16_t (&vz)[4]) {
   rotate_row_k(in.x, in.w, p.k_norm_w != nullptr, static_cast<float>(p.eps), in.cs0, in.cs1, kz);
 #pragma unroll
   for (int t = 0; t < 4; ++t) vz[t] = in.v[t];
+}
+__device__ __forceinline__ void store_kv_row(const AttnParams &p, int kv, int lane, const KvRowIn &in,
+                                             const uint16_t (&kz)[4], const uint16_t (&vz)[4]) {
   if (in.grow >= 0) {
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       p.k_cache[(in.grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = kz[t];
       p.v_cache[(in.grow * p.Hkv + kv) * kHeadDim + lane + 32 * t] = vz[t];
     }
+  }
+}
+__device__ __forceinline__ void append_kv_row(const AttnParams &p, int kv, int lane, const KvRowIn &in,
+                                              uint16_t (&kz)[4], uint16_t (&vz)[4]) {
+  rotated_kv_row(p, in, kz, vz);
+  store_kv_row(p, kv, lane, in, kz, vz);
+}
+// The same store from the packed form (two bf16 a register: dims l + 32 t, t = 0..3).
+__device__ __forceinline__ void store_packed_row(const AttnParams &p, int kv, int lane, long long grow,
+                                                 const uint32_t (&k2)[2], const uint32_t (&v2)[2]) {
+  if (grow < 0) return;
+  uint16_t *kr = p.k_cache + (grow * p.Hkv + kv) * kHeadDim + lane;
+  uint16_t *vr = p.v_cache + (grow * p.Hkv + kv) * kHeadDim + lane;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    kr[32 * t] = static_cast<uint16_t>(k2[t >> 1] >> (16 * (t & 1)));
+    vr[32 * t] = static_cast<uint16_t>(v2[t >> 1] >> (16 * (t & 1)));
   }
 }
 
@@ -137,18 +157,13 @@ __device__ __forceinline__ void load_q_inputs(const AttnParams &p, int b, int kv
     for (int hf = 0; hf < 2; ++hf) in.cs[ks][hf] = *reinterpret_cast<const float4 *>(cs + 16 * ks + 8 * hf + c2);
 }
 
-// `publish`: also store the rows, as plain [B, H_q, d] rows, to the workspace copy of the
-// rotated queries.
 template <int NT>
-__device__ __forceinline__ void rotate_q(const AttnParams &p, int b, int kv, int lane, bool publish,
-                                         const QIn<NT> &in, uint32_t (&qf)[8][NT][2]) {
-  const int c2 = 2 * (lane & 3);
+__device__ __forceinline__ void rotate_q(const AttnParams &p, int lane, const QIn<NT> &in, uint32_t (&qf)[8][NT][2]) {
   const float eps = static_cast<float>(p.eps);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int g = 8 * nt + (lane >> 2);
     const bool real = g < p.G;
-    const long long row = (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim;
     float ss = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
@@ -164,8 +179,7 @@ __device__ __forceinline__ void rotate_q(const AttnParams &p, int b, int kv, int
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int i = 16 * ks + 8 * hf + c2;  // pairs i, i + 1 (< 64)
+      for (int hf = 0; hf < 2; ++hf) {  // pairs i, i + 1 (< 64), i = 16 ks + 8 hf + 2 (l mod 4)
         float y0 = bf16_lo_to_float(in.x[nt][ks][hf]), y1 = bf16_hi_to_float(in.x[nt][ks][hf]);
         float p0 = bf16_lo_to_float(in.x[nt][ks + 4][hf]), p1 = bf16_hi_to_float(in.x[nt][ks + 4][hf]);
         if (p.q_norm_w) {
@@ -178,12 +192,164 @@ __device__ __forceinline__ void rotate_q(const AttnParams &p, int b, int kv, int
         if (!real) lo = hi = 0u;
         qf[ks][nt][hf] = lo;
         qf[ks + 4][nt][hf] = hi;
-        if (publish && real) {
-          *reinterpret_cast<uint32_t *>(p.q_rot + row + i) = lo;
-          *reinterpret_cast<uint32_t *>(p.q_rot + row + i + 64) = hi;
-        }
       }
   }
+}
+
+// Stores the rotated queries held in qf, as plain [B, H_q, d] rows, to the workspace copy
+// of the rotated queries (for tests and debugging; the kernel itself keeps q in registers).
+template <int NT>
+__device__ __forceinline__ void publish_q(const AttnParams &p, int b, int kv, int lane,
+                                          const uint32_t (&qf)[8][NT][2]) {
+  const int c2 = 2 * (lane & 3);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = 8 * nt + (lane >> 2);
+    if (g >= p.G) continue;
+    const long long row = (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int i = 16 * ks + 8 * hf + c2;
+        *reinterpret_cast<uint32_t *>(p.q_rot + row + i) = qf[ks][nt][hf];
+        *reinterpret_cast<uint32_t *>(p.q_rot + row + i + 64) = qf[ks + 4][nt][hf];
+      }
+  }
+}
+
+// Rows past L_b hold whatever the cache holds there; zero the V rows from `valid` on so
+// that P = 0 never meets a non-finite value.  Whole 128-byte rows, so the swizzle does not
+// matter.
+__device__ __forceinline__ void zero_v_tail(uint8_t *stage, int valid, int lane) {
+  uint4 *v0 = reinterpret_cast<uint4 *>(stage + 2 * kHalfTileBytes);
+  uint4 *v1 = reinterpret_cast<uint4 *>(stage + 3 * kHalfTileBytes);
+  const int nchunks = (kTile - valid) * 8;
+  for (int c = lane; c < nchunks; c += 32) {
+    v0[valid * 8 + c] = make_uint4(0, 0, 0, 0);
+    v1[valid * 8 + c] = make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+}
+
+// Writes an appended k/v row (lane l holds dims l + 32 t) into row r of a ring stage: the
+// TMA filled the stage from the cache before the row was appended.
+__device__ __forceinline__ void patch_row(uint8_t *stage, int r, const uint16_t (&kz)[4], const uint16_t (&vz)[4],
+                                          int lane) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int e = lane + 32 * t;
+    const uint32_t off = (e >> 6) * kHalfTileBytes + swz128(r, (e & 63) >> 3) + (e & 7) * 2;
+    *reinterpret_cast<uint16_t *>(stage + off) = kz[t];
+    *reinterpret_cast<uint16_t *>(stage + 2 * kHalfTileBytes + off) = vz[t];
+  }
+  __syncwarp();
+}
+
+
+// One 64-token tile of the recurrence for a warp's G heads, on a ring stage holding the
+// tile's K and V halves (128-byte swizzled): S^T = K_j q^T scaled to the log2 domain with
+// tokens >= valid masked to -inf, the online-softmax update of (m, l, O), and
+// O^T += V_j^T P^T with P split into bf16 hi + lo.
+template <int NT>
+__device__ __forceinline__ void tile_update(const uint8_t *stage, int valid, float scale_log2, int lane,
+                                            const uint32_t (&qf)[8][NT][2], float (&o)[8][NT][4],
+                                            float (&m_run)[NT][2], float (&l_run)[NT][2]) {
+  const uint32_t kLo = smem_addr(stage), kHi = kLo + kHalfTileBytes;
+  const uint32_t vLo = kLo + 2 * kHalfTileBytes, vHi = kLo + 3 * kHalfTileBytes;
+  // S^T = K_j q^T : 4 token blocks of 16 x NT head blocks of 8.
+  float sacc[4][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int qd = lane >> 3;
+      const int tok = 16 * mt + (lane & 7) + ((qd & 1) << 3);
+      const int chunk = 2 * ks + (qd >> 1);
+      const uint32_t addr = ((chunk >> 3) ? kHi : kLo) + swz128(tok, chunk & 7);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+    }
+
+  // scale (log2 domain) and mask tokens >= valid
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
+        sacc[mt][nt][e] = tok < valid ? sacc[mt][nt][e] * scale_log2 : -INFINITY;
+      }
+
+  // online-softmax update per head column
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sacc[mt][nt][jj], sacc[mt][nt][jj + 2]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[nt][jj], mx);
+      const float corr = fast_exp2(m_run[nt][jj] - m_new);  // 0 on the first tile
+      m_run[nt][jj] = m_new;
+      l_run[nt][jj] *= corr;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        o[md][nt][jj] *= corr;
+        o[md][nt][jj + 2] *= corr;
+      }
+    }
+
+  // P = 2^(s - m), split into bf16 hi + lo, transposed into B fragments of P^T
+  uint32_t ph[4][NT][2], pl[4][NT][2];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pv[e] = fast_exp2(sacc[mt][nt][e] - m_run[nt][e & 1]);
+        l_run[nt][e & 1] += pv[e];
+      }
+      const uint32_t h01 = pack_bf16(pv[0], pv[1]), h23 = pack_bf16(pv[2], pv[3]);
+      const uint32_t l01 = pack_bf16(pv[0] - bf16_lo_to_float(h01), pv[1] - bf16_hi_to_float(h01));
+      const uint32_t l23 = pack_bf16(pv[2] - bf16_lo_to_float(h23), pv[3] - bf16_hi_to_float(h23));
+      ph[mt][nt][0] = movmatrix_t(h01);
+      ph[mt][nt][1] = movmatrix_t(h23);
+      pl[mt][nt][0] = movmatrix_t(l01);
+      pl[mt][nt][1] = movmatrix_t(l23);
+    }
+
+  // O^T += V_j^T P^T : 8 dim blocks of 16 x 4 token k-steps
+#pragma unroll
+  for (int md = 0; md < 8; ++md)
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int qd = lane >> 3;
+      const int tok = 16 * mt + (lane & 7) + ((qd >> 1) << 3);
+      const int chunk = 2 * md + (qd & 1);
+      const uint32_t addr = ((chunk >> 3) ? vHi : vLo) + swz128(tok, chunk & 7);
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(addr, a0, a1, a2, a3);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
+        mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
+      }
+    }
 }
 
 template <int NT>
@@ -412,9 +578,12 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   // ------------------------------------------------------------------ consumer warps
   // Until griddep_wait() returns, the preceding kernel in the stream (the previous step's
-  // combine) may still be reading the partials, so those are written only after it;
-  // everything before it reads only the caller's inputs and the RoPE table and writes only
-  // the new cache rows, which that kernel does not touch.
+  // combine) may still be reading the partials, so those are written only after it.
+  // Everything before it reads only the caller's inputs and the RoPE table and writes only
+  // the new cache rows, which that kernel does not touch.  The workspace copy of the
+  // rotated queries is written after the wait too: a workspace laid out per call (the
+  // static-scratch entry point) can put this call's copy where the previous call's
+  // partials were.
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -480,31 +649,39 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   };
   int cur_seg = -1;
   if (q_b >= 0) {
-    if (Ps[q_b] >= 0) rotate_q<NT>(p, q_b, q_kv, lane, q_j == 0, qin, qf);
+    if (Ps[q_b] >= 0) rotate_q<NT>(p, lane, qin, qf);
     else zero_q();
     cur_seg = q_b * p.Hkv + q_kv;
   }
 
   // The new-token k/v rows this warp appends: the first two are computed now, while the
-  // first tiles are still in flight, written to the cache and kept packed in registers for
-  // the shared-memory patch; any further ones are computed when their tile arrives.
+  // first tiles are still in flight, kept packed in registers for the shared-memory patch
+  // and written to the cache right after the wait below (a preceding single-launch step
+  // may still be reading the rows a repeated position rewrites); any further ones are
+  // computed and written when their tile arrives.
   uint32_t ek0[2] = {0, 0}, ev0[2] = {0, 0}, ek1[2] = {0, 0}, ev1[2] = {0, 0};
+  long long grow0 = -1, grow1 = -1;
   if (ex0 >= 0) {
     uint16_t kz[4], vz[4];
-    append_kv_row(p, ex0_kv, lane, kin, kz, vz);
+    rotated_kv_row(p, kin, kz, vz);
+    grow0 = kin.grow;
     ek0[0] = kz[0] | (uint32_t(kz[1]) << 16), ek0[1] = kz[2] | (uint32_t(kz[3]) << 16);
     ev0[0] = vz[0] | (uint32_t(vz[1]) << 16), ev0[1] = vz[2] | (uint32_t(vz[3]) << 16);
   }
   if (ex1 >= 0) {
     uint16_t kz[4], vz[4];
     load_kv_row(p, ex1_b, ex1_kv, Ps[ex1_b], lane, kin);
-    append_kv_row(p, ex1_kv, lane, kin, kz, vz);
+    rotated_kv_row(p, kin, kz, vz);
+    grow1 = kin.grow;
     ek1[0] = kz[0] | (uint32_t(kz[1]) << 16), ek1[1] = kz[2] | (uint32_t(kz[3]) << 16);
     ev1[0] = vz[0] | (uint32_t(vz[1]) << 16), ev1[1] = vz[2] | (uint32_t(vz[3]) << 16);
   }
 
   griddep_wait();
   griddep_launch_dependents();
+  if (ex0 >= 0) store_packed_row(p, ex0_kv, lane, grow0, ek0, ev0);
+  if (ex1 >= 0) store_packed_row(p, ex1_kv, lane, grow1, ek1, ev1);
+  if (q_b >= 0 && q_j == 0 && Ps[q_b] >= 0) publish_q<NT>(p, q_b, q_kv, lane, qf);
 
   for (long long i = cw; i < n; i += kConsumerWarps) {
     int b, kv, j;
@@ -516,7 +693,8 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
       cur_seg = sg;
       if (pos_b >= 0) {
         load_q_inputs<NT>(p, b, kv, pos_b, lane, qin);
-        rotate_q<NT>(p, b, kv, lane, j == 0, qin, qf);
+        rotate_q<NT>(p, lane, qin, qf);
+        if (j == 0) publish_q<NT>(p, b, kv, lane, qf);
       } else {
         zero_q();
       }
@@ -530,22 +708,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
     }
     const int valid = min(kTile, Ls[b] - j * kTile);
     uint8_t *stage = smem + s * C::kStageBytes;
-    const uint32_t kLo = smem_addr(stage), kHi = kLo + kHalfTileBytes;
-    const uint32_t vLo = kLo + 2 * kHalfTileBytes, vHi = kLo + 3 * kHalfTileBytes;
-
-    if (valid < kTile) {
-      // Rows past L_b hold whatever the cache holds there; zero the V rows so that
-      // P = 0 never meets a non-finite value.  Whole 128-byte rows, so the swizzle
-      // does not matter.
-      uint4 *v0 = reinterpret_cast<uint4 *>(stage + 2 * kHalfTileBytes);
-      uint4 *v1 = reinterpret_cast<uint4 *>(stage + 3 * kHalfTileBytes);
-      const int nchunks = (kTile - valid) * 8;
-      for (int c = lane; c < nchunks; c += 32) {
-        v0[valid * 8 + c] = make_uint4(0, 0, 0, 0);
-        v1[valid * 8 + c] = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
+    if (valid < kTile) zero_v_tail(stage, valid, lane);
     // The tile holding sequence b's new token: the TMA filled this stage from the cache
     // before the row was appended, so patch the appended k and v rows into it.
     const bool holds_new = pos_b >= 0 && (pos_b >> 6) == j;
@@ -560,110 +723,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         load_kv_row(p, b, kv, pos_b, lane, kin);
         append_kv_row(p, kv, lane, kin, kz, vz);
       }
-      const int r = pos_b & (kTile - 1);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int e = lane + 32 * t;
-        const uint32_t off = (e >> 6) * kHalfTileBytes + swz128(r, (e & 63) >> 3) + (e & 7) * 2;
-        *reinterpret_cast<uint16_t *>(stage + off) = kz[t];
-        *reinterpret_cast<uint16_t *>(stage + 2 * kHalfTileBytes + off) = vz[t];
-      }
-      __syncwarp();
+      patch_row(stage, pos_b & (kTile - 1), kz, vz, lane);
     }
 
-    // S^T = K_j q^T : 4 token blocks of 16 x NT head blocks of 8.
-    float sacc[4][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int qd = lane >> 3;
-        const int tok = 16 * mt + (lane & 7) + ((qd & 1) << 3);
-        const int chunk = 2 * ks + (qd >> 1);
-        const uint32_t addr = ((chunk >> 3) ? kHi : kLo) + swz128(tok, chunk & 7);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(addr, a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
-      }
-
-    // scale (log2 domain) and mask tokens >= valid
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
-          sacc[mt][nt][e] = tok < valid ? sacc[mt][nt][e] * p.scale_log2 : -INFINITY;
-        }
-
-    // online-softmax update per head column
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sacc[mt][nt][jj], sacc[mt][nt][jj + 2]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[nt][jj], mx);
-        const float corr = fast_exp2(m_run[nt][jj] - m_new);  // 0 on the first tile
-        m_run[nt][jj] = m_new;
-        l_run[nt][jj] *= corr;
-#pragma unroll
-        for (int md = 0; md < 8; ++md) {
-          o[md][nt][jj] *= corr;
-          o[md][nt][jj + 2] *= corr;
-        }
-      }
-
-    // P = 2^(s - m), split into bf16 hi + lo, transposed into B fragments of P^T
-    uint32_t ph[4][NT][2], pl[4][NT][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          pv[e] = fast_exp2(sacc[mt][nt][e] - m_run[nt][e & 1]);
-          l_run[nt][e & 1] += pv[e];
-        }
-        const uint32_t h01 = pack_bf16(pv[0], pv[1]), h23 = pack_bf16(pv[2], pv[3]);
-        const uint32_t l01 = pack_bf16(pv[0] - bf16_lo_to_float(h01), pv[1] - bf16_hi_to_float(h01));
-        const uint32_t l23 = pack_bf16(pv[2] - bf16_lo_to_float(h23), pv[3] - bf16_hi_to_float(h23));
-        ph[mt][nt][0] = movmatrix_t(h01);
-        ph[mt][nt][1] = movmatrix_t(h23);
-        pl[mt][nt][0] = movmatrix_t(l01);
-        pl[mt][nt][1] = movmatrix_t(l23);
-      }
-
-    // O^T += V_j^T P^T : 8 dim blocks of 16 x 4 token k-steps
-#pragma unroll
-    for (int md = 0; md < 8; ++md)
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int qd = lane >> 3;
-        const int tok = 16 * mt + (lane & 7) + ((qd >> 1) << 3);
-        const int chunk = 2 * md + (qd & 1);
-        const uint32_t addr = ((chunk >> 3) ? vHi : vLo) + swz128(tok, chunk & 7);
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(addr, a0, a1, a2, a3);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
-          mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
-        }
-      }
+    tile_update<NT>(stage, valid, p.scale_log2, lane, qf, o, m_run, l_run);
 
     if (valid < kTile || holds_new) fence_proxy_async_smem();  // generic writes precede the next TMA here
     __syncwarp();
@@ -672,16 +735,429 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   if (cur_seg >= 0) flush(cur_seg);
 }
 
+// ------------------------------------------------------------------ single-launch form
+// The whole decode step in one launch, for batches with few (sequence, KV head) segments
+// (short and mid contexts of one or a few sequences, where the step is bound by latency):
+// one thread-block cluster of C = p.csize CTAs per segment.  CTA rank r of the cluster
+// streams the segment's tiles r, r + C, r + 2C, ... through the same producer / consumer
+// ring as the split-KV kernel and runs the same per-tile recurrence; the partials never
+// leave the chip.  Each CTA merges its six consumer warps' (m, l, O) in shared memory and
+// pushes the merged state to the cluster: CTA q owns dims [q 128/C, (q+1) 128/C) of the
+// segment's G heads, and every CTA stores its (m, l) and its O values for those dims into
+// CTA q's receive area with remote asynchronous stores that count their bytes on CTA q's
+// mbarrier.  CTA q waits for the C contributions, merges them in a fixed order (ADR-0060
+// section 4's merge) and writes its dims normalised in bf16.  No partials in HBM, no
+// second kernel and no grid-wide wait inside the step.
+//
+// Ordering with the neighbouring kernels in the stream (programmatic dependent launch):
+// the whole computation -- streaming the cache, the tiles, the merges -- runs without
+// waiting on the preceding kernel; only the writes to global memory wait for it: the
+// cache append (the preceding step may still read the row this one rewrites), the
+// rotated-query copy and `out` (it may write the same buffers).  The producer warp waits
+// first, appends the new row when this CTA holds it, fences it and lets the next kernel
+// launch, since the next step streams the cache before its own wait.  So the next step's
+// CTAs start as soon as this one's rows are in place and compute on the SMs this one
+// leaves free while it finishes; a step's time is about half its latency.
+//
+// Cluster protocol: every thread arrives on the cluster barrier once its CTA's mbarriers
+// are initialised and waits on it before the first remote store (so no store reaches an
+// uninitialised barrier), and arrives again once its CTA has received everything and waits
+// before leaving (so no CTA leaves while stores to or from it are in flight).  No thread
+// leaves early and every mbarrier wait is bounded, so a pipeline timeout cannot hang the
+// cluster.
+namespace {
+constexpr int kPartStride = 132;          // floats per (warp, head) partial row in shared memory
+// Receive area of the single-launch kernel, after the ring's barriers: (m, l) of every
+// sender and head, then O for the owned dims, [sender][head][128 / C].
+constexpr int kRecvMlFloats = GQA_MAX_GROUP * GQA_MAX_GROUP * 2;
+constexpr int kRecvOFloats = GQA_MAX_GROUP * kHeadDim;
+constexpr int kRecvOffset = kStages * 4 * kHalfTileBytes + 1024;   // from the aligned base
+constexpr size_t kClusterSmemBytes = 1024 + kRecvOffset + 4 * (kRecvMlFloats + kRecvOFloats);
+// Warps: the consumers, the producer, and an ordering warp that waits on the preceding
+// kernel, appends the new row (in the CTA whose tile holds it) and lets the next launch.
+constexpr int kOrderWarp = kConsumerWarps + 1;
+constexpr int kThreadsCluster = 32 * (kConsumerWarps + 2);
+}  // namespace
+
+template <int NT>
+__global__ void __launch_bounds__(kThreadsCluster, 1)
+    attn_cluster_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const AttnParams p) {
+  using Cf = Cfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align_smem_1024(smem_raw);
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kStages * Cf::kStageBytes);
+  uint64_t *empty_bar = full_bar + kStages;
+  uint64_t *recv_bar = empty_bar + kStages;
+  float *recv_ml = reinterpret_cast<float *>(smem + kRecvOffset);   // [C][G][2]
+  float *recv_o = recv_ml + kRecvMlFloats;                          // [C][G][128 / C]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = p.csize, dpr = kHeadDim / C;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int seg = static_cast<int>(blockIdx.x) / C;
+  const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
+  const bool producer = warp == kConsumerWarps;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_addr(recv_bar), 1);
+    fence_barrier_init();
+  }
+  if (producer && lane == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  // The segment's length and new-token position (one broadcast load per warp).
+  int L = p.seq_lens[b], pos = p.positions[b];
+  const int nt = tiles_of(L, p.max_seq);
+  if (nt == 0) {
+    if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_SEQLEN);
+    L = 0;
+    pos = -1;
+  } else if (pos < 0 || pos >= L) {
+    if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_POSITION);
+    pos = -1;
+  }
+  const int n = nt > rank ? (nt - rank + C - 1) / C : 0;  // local tile i is segment tile rank + C i
+  // The warp (of this CTA) whose tile holds the new token, or -1.
+  int owner = -1;
+  if (pos >= 0 && (pos >> 6) % C == rank) owner = ((pos >> 6) / C) % kConsumerWarps;
+  __syncthreads();  // barrier initialisation visible to the CTA
+  cluster_arrive();  // ... and to the cluster (waited for before the first remote store)
+
+  // Cache row of local tile i's first token (the TMA z coordinate); a page id outside the
+  // pool is flagged and read as a box wholly out of bounds (zeros).
+  auto tile_row = [&](int i) -> int {
+    const int j = rank + C * i;
+    if (p.paged) {
+      const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+      if (pg < 0 || pg >= p.num_blocks) {
+        atomicOr(p.err, GQA_DEVERR_PAGE);
+        return -kTile;
+      }
+      return pg * kTile;
+    }
+    return b * p.max_seq + j * kTile;
+  };
+
+  float o[8][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int md = 0; md < 8; ++md)
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[md][t][e] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      m_run[t][jj] = -INFINITY;
+      l_run[t][jj] = 0.f;
+    }
+
+  uint32_t qkeep[8][NT][2];  // warp 0 of rank 0: the rotated queries to publish
+  bool qpub = false;
+  if (warp == kOrderWarp) {
+    // ------------------------------------------------------------------ ordering warp
+    // Computes the new row (when this CTA's tiles hold it) while the preceding kernel
+    // drains, appends it once that kernel has completed, fences it and lets the next
+    // kernel launch.
+    KvRowIn kin;
+    uint16_t kz[4], vz[4];
+    if (owner >= 0) {
+      load_kv_row(p, b, kv, pos, lane, kin);
+      rotated_kv_row(p, kin, kz, vz);
+    }
+    griddep_wait();
+    if (owner >= 0) {
+      store_kv_row(p, kv, lane, kin, kz, vz);
+      __threadfence();
+    }
+    __syncwarp();
+    if (lane == 0) griddep_launch_dependents();
+  } else if (producer) {
+    // ---------------------------------------------------------------- producer warp
+    // The producer streams from the start and never waits on the preceding kernel: that
+    // kernel let this grid launch only after its own cache rows were appended and fenced
+    // (the single-launch kernel) or after the attention kernel it waits on had completed
+    // (the combine), and this step's own new row is patched into its tile by the consumer
+    // that owns it.
+    const int npre = n < kStages ? n : kStages;
+    int row = 0;
+    if (lane < npre) row = tile_row(lane);
+    for (int k = 0; k < npre; ++k) {
+      const int r_row = __shfl_sync(0xffffffffu, row, k);
+      if (lane == 0) {
+        const uint32_t fb = smem_addr(&full_bar[k]);
+        const uint32_t base = smem_addr(smem + k * Cf::kStageBytes);
+        mbar_arrive_expect_tx(fb, Cf::kStageBytes);
+        tma_load_3d(base, &tmK, fb, 0, kv, r_row);
+        tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, r_row);
+        tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, r_row);
+        tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
+      }
+    }
+    bool fail = false;
+    int issued = npre;
+    for (int i0 = npre; i0 < n && !fail; i0 += 32) {
+      row = i0 + lane < n ? tile_row(i0 + lane) : 0;
+      const int cnt = n - i0 < 32 ? n - i0 : 32;
+      for (int k = 0; k < cnt; ++k) {
+        const int r_row = __shfl_sync(0xffffffffu, row, k);
+        const int ii = i0 + k, s = ii % kStages;
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((ii / kStages) - 1) & 1));
+          if (ok) {
+            const uint32_t fb = smem_addr(&full_bar[s]);
+            const uint32_t base = smem_addr(smem + s * Cf::kStageBytes);
+            mbar_arrive_expect_tx(fb, Cf::kStageBytes);
+            tma_load_3d(base, &tmK, fb, 0, kv, r_row);
+            tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, r_row);
+            tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, r_row);
+            tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
+            issued = ii + 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          fail = true;
+          break;
+        }
+      }
+    }
+    if (fail && lane == 0) {
+      atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+      // no copy may still be landing in this CTA's shared memory when it is reused below
+      for (int ii = (issued > kStages ? issued - kStages : 0); ii < issued; ++ii)
+        (void)mbar_wait(smem_addr(&full_bar[ii % kStages]), static_cast<uint32_t>((ii / kStages) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ consumer warps
+    const int cw = warp;
+    const bool has_tiles = cw < n;
+    const int i_new = cw == owner ? (pos >> 6) / C : -1;  // local index of the new token's tile
+    QIn<NT> qin;
+    KvRowIn kin;
+    if (has_tiles && pos >= 0) load_q_inputs<NT>(p, b, kv, pos, lane, qin);
+    if (i_new >= 0) load_kv_row(p, b, kv, pos, lane, kin);
+    uint32_t qf[8][NT][2];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) qf[ks][t][0] = qf[ks][t][1] = 0u;
+    if (has_tiles && pos >= 0) rotate_q<NT>(p, lane, qin, qf);
+    uint16_t kz[4] = {0, 0, 0, 0}, vz[4] = {0, 0, 0, 0};
+    if (i_new >= 0) rotated_kv_row(p, kin, kz, vz);  // the same bits the producer appends
+    if (rank == 0 && cw == 0) {  // the rotated queries, published after the wait below
+      qpub = has_tiles && pos >= 0;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) qkeep[ks][t][0] = qf[ks][t][0], qkeep[ks][t][1] = qf[ks][t][1];
+    }
+
+    for (int i = cw; i < n; i += kConsumerWarps) {
+      const int s = i % kStages;
+      const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kStages) & 1));
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ready)) {
+        if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+        break;
+      }
+      const int valid = min(kTile, L - (rank + C * i) * kTile);
+      uint8_t *stage = smem + s * Cf::kStageBytes;
+      if (valid < kTile) zero_v_tail(stage, valid, lane);
+      if (i == i_new) patch_row(stage, pos & (kTile - 1), kz, vz, lane);
+      tile_update<NT>(stage, valid, p.scale_log2, lane, qf, o, m_run, l_run);
+      if (valid < kTile || i == i_new) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    }
+  }
+
+  // ------------------------------------------------------------------ merge
+  // Each consumer warp's (m, l) per head go to shared memory; once all are there, every
+  // warp rescales its own O (in registers) and l to the CTA's maximum m and stores them,
+  // so that the CTA's partial of an element is a plain sum over the six warps.
+  float *wpart = reinterpret_cast<float *>(smem);                          // [6][16][kPartStride]
+  float *wml = wpart + kConsumerWarps * GQA_MAX_GROUP * kPartStride;       // [6][16][2]
+  float *wm = wml + kConsumerWarps * GQA_MAX_GROUP * 2;                    // [6][16]
+  __syncthreads();  // every issued tile has been consumed: the ring is free
+  if (!producer && warp != kOrderWarp) {
+    const int cw = warp;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int g = 8 * t + 2 * lane + jj;
+        if (lane < 4 && g < p.G) wm[cw * GQA_MAX_GROUP + g] = m_run[t][jj];
+      }
+  }
+  __syncthreads();
+  if (!producer && warp != kOrderWarp) {
+    const int cw = warp;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int g = 8 * t + 2 * (lane & 3) + jj;  // the head column this lane holds
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, wm[c * GQA_MAX_GROUP + (g < p.G ? g : 0)]);
+        const float f = m_run[t][jj] == -INFINITY ? 0.f : exp2f(m_run[t][jj] - M);
+        float l = l_run[t][jj] * f;
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (lane < 4 && g < p.G) {
+          wml[(cw * GQA_MAX_GROUP + g) * 2 + 0] = M;
+          wml[(cw * GQA_MAX_GROUP + g) * 2 + 1] = l;
+        }
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          o[md][t][jj] *= f;
+          o[md][t][jj + 2] *= f;
+        }
+      }
+#pragma unroll
+    for (int md = 0; md < 8; ++md)
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int g = 8 * t + 2 * (lane & 3) + (e & 1);
+          const int d = 16 * md + (lane >> 2) + ((e >> 1) << 3);
+          if (g < p.G) wpart[(cw * GQA_MAX_GROUP + g) * kPartStride + d] = o[md][t][e];
+        }
+  }
+  __syncthreads();
+  // This CTA's partial per element -- (M, sum of the warps' rescaled l, sum of their
+  // rescaled O) -- pushed straight to the CTA that owns the element's dims.
+  const int E = p.G * kHeadDim;
+  const uint32_t bar_local = smem_addr(recv_bar);
+  if (tid == 0)  // this CTA's own receive phase: C senders x (G (m, l) pairs + G x dpr floats)
+    mbar_arrive_expect_tx(bar_local, static_cast<uint32_t>(C * p.G * (8 + 4 * dpr)));
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  for (int e = tid; e < E; e += kThreadsCluster) {
+    const int g = e >> 7, d = e & (kHeadDim - 1);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) acc += wpart[(c * GQA_MAX_GROUP + g) * kPartStride + d];
+    const int q = d / dpr, dd = d - q * dpr;
+    const uint32_t bar_q = mapa_shared(bar_local, q);
+    st_async_f32(mapa_shared(smem_addr(recv_o + (rank * p.G + g) * dpr + dd), q), acc, bar_q);
+    if (dd == 0) {
+      float den = 0.f;
+#pragma unroll
+      for (int c = 0; c < kConsumerWarps; ++c) den += wml[(c * GQA_MAX_GROUP + g) * 2 + 1];
+      st_async_v2f32(mapa_shared(smem_addr(recv_ml + (rank * p.G + g) * 2), q), wml[g * 2], den, bar_q);
+    }
+  }
+  // The owned dims: merge the C contributions and write them (global writes: after the
+  // preceding kernel has completed).
+  const bool got = mbar_wait(bar_local, 0);
+  if (!got && (tid & 31) == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+  cluster_arrive_relaxed();  // this CTA has received everything (or given up)
+  griddep_wait();
+  if (qpub) publish_q<NT>(p, b, kv, lane, qkeep);
+  for (int e = tid; e < p.G * dpr; e += kThreadsCluster) {
+    const int g = e / dpr, dd = e - g * dpr;
+    float mq[GQA_MAX_GROUP], lq[GQA_MAX_GROUP], oq[GQA_MAX_GROUP];
+#pragma unroll
+    for (int r = 0; r < GQA_MAX_GROUP; ++r) {
+      if (r < C) {
+        mq[r] = recv_ml[(r * p.G + g) * 2];
+        lq[r] = recv_ml[(r * p.G + g) * 2 + 1];
+        oq[r] = recv_o[(r * p.G + g) * dpr + dd];
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < GQA_MAX_GROUP; ++r)
+      if (r < C) M = fmaxf(M, mq[r]);
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < GQA_MAX_GROUP; ++r)
+        if (r < C) {
+          const float f = exp2f(mq[r] - M);
+          acc = fmaf(f, oq[r], acc);
+          den = fmaf(f, lq[r], den);
+        }
+    }
+    const float v = den > 0.f ? acc / den : 0.f;  // zeros for an invalid length (flagged above)
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    p.out[(static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim + rank * dpr + dd] =
+        *reinterpret_cast<const uint16_t *>(&h);
+  }
+  cluster_wait();  // every CTA has received everything: no store to or from this CTA is in flight
+}
+
 size_t attn_smem_bytes(int npad, int batch) {
   (void)npad;  // the rotated queries live in registers: the stage size does not depend on G
   const int stage = 4 * kHalfTileBytes;
   return 1024 + static_cast<size_t>(kStages) * stage + 16 * kStages + 4 * (batch + 1) + 8 * batch;
 }
 
+size_t attn_cluster_smem_bytes() { return kClusterSmemBytes; }
+
 cudaError_t attn_configure(int npad) {
   const int bytes = static_cast<int>(attn_smem_bytes(npad, GQA_MAX_BATCH));
-  if (npad == 8) return cudaFuncSetAttribute(attn_splitkv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  return cudaFuncSetAttribute(attn_splitkv_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const int cbytes = static_cast<int>(attn_cluster_smem_bytes());
+  void (*split)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_splitkv_kernel<1> : attn_splitkv_kernel<2>;
+  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+int attn_cluster_capacity(int npad, int csize) {
+  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(csize));
+  cfg.blockDim = dim3(kThreadsCluster);
+  cfg.dynamicSmemBytes = attn_cluster_smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, single, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_attention_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
+                                     bool pdl, cudaStream_t stream) {
+  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv * p.csize));
+  cfg.blockDim = dim3(kThreadsCluster);
+  cfg.dynamicSmemBytes = attn_cluster_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, single, tmK, tmV, p);
 }
 
 cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,

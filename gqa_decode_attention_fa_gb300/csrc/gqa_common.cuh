@@ -83,8 +83,10 @@ struct AttnParams {
   float *part_o;                            // [slots * kConsumerWarps * G][128]
   float *part_ml;                           // [slots * kConsumerWarps * G][2]  (m in log2 units, l)
   uint32_t *err;
+  uint16_t *out;                            // [B,Hq,d]: written by the single-launch form only
   int B, Hq, Hkv, G;
   int paged, max_seq, max_blocks, num_blocks;
+  int csize;                                // single-launch form: CTAs per segment (cluster size)
   double eps;
   float scale_log2;                         // log2(e) / sqrt(d)
 };
@@ -147,6 +149,39 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Thread-block clusters: every thread of every CTA of the cluster arrives (release) and
+// later waits (acquire); the wait returns once all of them have arrived.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// An arrive that orders nothing (no release): for a barrier whose only job is to keep
+// CTAs alive until every one of them has observed its own receptions complete.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+// Stores into another CTA's shared memory (a shared::cluster address) that count their
+// bytes on that CTA's mbarrier (also a shared::cluster address), from registers.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(addr), "f"(v),
+               "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v2f32(uint32_t addr, float a, float b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+               "f"(a), "f"(b), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
 }
 
 __device__ __forceinline__ void fence_barrier_init() {

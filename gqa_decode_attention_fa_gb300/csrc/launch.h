@@ -47,6 +47,21 @@ cudaError_t attn_configure(int npad);
 // when the preceding kernel may write any of them (a RoPE table rebuild).
 cudaError_t launch_attention(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
                              int num_workers, bool pdl, cudaStream_t stream);
+// The single-launch form of the step: B * H_kv clusters of p.csize CTAs, writing p.out.
+cudaError_t launch_attention_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
+                                     bool pdl, cudaStream_t stream);
+// How many clusters of `csize` CTAs of the single-launch kernel can be resident at once
+// on the current device (0: that cluster size cannot be launched).  attn_configure(npad)
+// must have run on the device first.
+int attn_cluster_capacity(int npad, int csize);
+// The step's form: the cluster size of the single-launch form, or 0 for split-KV +
+// combine.  `forced` is the caller's choice (gqa_plan_desc_t.cluster_size: 0 lets this
+// planner choose, -1 asks for split-KV + combine, else that cluster size); capacity[k] is
+// how many clusters of 2^k CTAs the device holds at once; max_seg_tiles is the tile count
+// of the longest (sequence, KV head) segment.  Returns -1 when a forced cluster size
+// cannot be launched.
+int plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long num_segments,
+                   long long max_seg_tiles, long long total_tiles);
 
 // The combine: split 0 runs one CTA per (sequence, KV head) segment, split 4, 2 or 1 that
 // many CTAs per query head; combine_split picks it from the geometry and worker count.
@@ -119,13 +134,15 @@ struct DeviceGuard {
 // 256-byte-aligned base.  The RoPE table comes first, so that its place does not depend on
 // the batch geometry and a table built by one call stays usable by the next.
 struct StepLayout {
-  int G = 0, npad = 0, W = 0, max_blocks = 0, combine_split = 1;
+  int G = 0, npad = 0, W = 0, max_blocks = 0, combine_split = 1, csize = 0;
   long long num_rows = 0;
   size_t tab_bytes = 0, off_q = 0, off_o = 0, off_ml = 0, off_err = 0, total = 0;
 };
 
 // Checks `d` as gqa_plan_create does (except the device index) and lays out its workspace;
-// the worker count is d.num_workers, else one per SM up to B * H_kv * ceil(max_seq/64).
+// the worker count is d.num_workers, else one per SM up to B * H_kv * ceil(max_seq/64),
+// and the step's form is planned for B sequences of max_seq_len tokens.  Needs the
+// device current and attn_configure run on it.
 gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay);
 
 // One decode step (split-KV attention with the prologue folded in -> combine) on the

@@ -83,15 +83,15 @@ extern "C" gqa_status_t gqa_decode_attn_static(const gqa_plan_desc_t *desc, cons
   if (!guard.ok) return GQA_ERR_CUDA;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess) return GQA_ERR_CUDA;
-  StepLayout lay;
-  gqa_status_t st = step_layout(d, sms, &lay);
-  if (st != GQA_OK) return st;
-  if (lay.total > GQA_STATIC_SCRATCH_BYTES) return GQA_ERR_SCRATCH_LIMIT;
 
   std::lock_guard<std::mutex> lk(g_mu);
   ScratchState &s = g_state[d.device];
-  st = set_up(s);
+  gqa_status_t st = set_up(s);  // before the layout: the step's form depends on the kernels' limits
   if (st != GQA_OK) return st;
+  StepLayout lay;
+  st = step_layout(d, sms, &lay);
+  if (st != GQA_OK) return st;
+  if (lay.total > GQA_STATIC_SCRATCH_BYTES) return GQA_ERR_SCRATCH_LIMIT;
   uint32_t *err = device_errors ? device_errors : reinterpret_cast<uint32_t *>(static_cast<char *>(s.base) + lay.off_err);
   // The binary32 table follows the binary64 one, so its place depends on max_seq_len:
   // reuse the tables only for the same theta and the same capacity.

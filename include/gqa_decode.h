@@ -16,7 +16,17 @@
  *   3. combine: the log-sum-exp merge of the partials, normalised once (ADR-0060
  *      section 4, merge()).
  * Steps 1 and 2 run in one kernel (the prologue folded into the attention kernel, as
- * the pages do); step 3 is a second kernel.
+ * the pages do).  The plan picks one of two forms for step 3 ("Qwen3-14B Optimization",
+ * section 2.1 "Then: buy it": delete a boundary; ADR-0060 section 9 item 5: short
+ * contexts are dominated by the reduce):
+ *   - split-KV + combine: the batch's KV tiles are cut into one contiguous range per SM
+ *     (ADR-0060 section 2.1) whatever the sequence boundaries, the partials go to the
+ *     workspace and a second kernel merges them.  For batches with many (sequence, KV
+ *     head) segments or long ones.
+ *   - single launch: one thread-block cluster of C CTAs per (sequence, KV head); the C
+ *     CTAs split its tiles, and their partials are merged on chip (shared memory, then
+ *     distributed shared memory across the cluster), so the step is one kernel.  For
+ *     batches whose segments fit the SMs C at a time with short to mid-length contexts.
  *
  * Conventions shared by every entry point
  *   - bf16 tensors are passed as pointers to 16-bit storage (IEEE bfloat16 bits).
@@ -30,14 +40,17 @@
  *     as synchronous.  Two calls that share a plan must not run concurrently (they
  *     share the plan's workspace); order them on one stream.
  *   - Kernels are launched with programmatic stream serialization: a kernel may start
- *     while the previous kernel on the stream drains.  The attention kernel reads its
- *     inputs (q/k/v_new, seq_lens, positions, page table, norm weights, the cache)
+ *     while the previous kernel on the stream drains.  The split-KV attention kernel reads
+ *     its inputs (q/k/v_new, seq_lens, positions, page table, norm weights, the cache)
  *     before it waits (griddepcontrol.wait) on that kernel, and writes the workspace
- *     only after; the combine waits before it reads anything.  So the kernel launched
- *     immediately before a step must not write the step's inputs if it triggers
- *     programmatic completion early (kernels launched without programmatic dependent
- *     launch, the usual case, never do).  After a RoPE table rebuild the attention kernel
- *     is launched in plain stream order.
+ *     only after; the combine reads only seq_lens before it waits.  The single-launch
+ *     kernel reads the same inputs before it waits, and writes the cache, the workspace
+ *     and `out` only after; it lets the next kernel launch once its cache rows are
+ *     appended (and fenced).  So the kernel launched immediately
+ *     before a step must not write the step's inputs if it triggers programmatic
+ *     completion early (kernels launched without programmatic dependent launch, the
+ *     usual case, never do).  After a RoPE table rebuild the attention kernel is launched
+ *     in plain stream order.
  *   - The first call with a given rope_theta (and the first after a different one)
  *     also launches, on the same stream, the build of the plan's RoPE tables:
  *     cos/sin(p * theta^(-2i/d)) for every p < max_seq_len in binary64 and rounded to
@@ -98,18 +111,32 @@ typedef struct gqa_plan_desc {
                              ignored (may be 0) when contiguous */
     int num_workers;      /* CTAs of the split-KV kernel; 0 lets the planner choose */
     int device;           /* CUDA device ordinal the plan and its calls run on */
+    int cluster_size;     /* the step's form: 0 lets the planner choose; -1 asks for the
+                             split-KV kernel + combine; 1, 2, 4, 8 or 16 asks for the
+                             single-launch form with that many CTAs per (sequence, KV head)
+                             cluster (GQA_ERR_UNSUPPORTED if the device cannot launch it).
+                             A non-zero num_workers with cluster_size 0 also means split-KV. */
 } gqa_plan_desc_t;
 
 typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp32 partials) */
 
 /*
- * gqa_plan_create -- the split planner.  Validates the geometry, chooses the number of
- * split-KV workers (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
- * long contexts many; here the whole batch's KV tiles are cut into one contiguous range
- * per worker, ADR-0060 section 2.1 contiguous-block placement: one worker per SM, at
- * most one per tile, and a quarter of the tiles, rounded up, when the tiles fill the SMs
- * three to four times over) and allocates the
- * workspace once, so no call allocates.  The workspace holds a copy of the rotated
+ * gqa_plan_create -- the split planner.  Validates the geometry, chooses the step's form
+ * and its splits (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
+ * long contexts many) and allocates the workspace once, so no call allocates.
+ *   - The single-launch form, for up to two waves of segments (B * H_kv <= 2 x SMs),
+ *     with the largest cluster size C in 16, 8, 4, 2 whose clusters all fit at once
+ *     (B * H_kv * C <= SMs, the device holds B * H_kv such clusters) and that does not
+ *     exceed the longest segment's tile count, else C = 1; provided the B * H_kv * C CTAs
+ *     can stream the cache (at least 64 of them, or one per tile).
+ *   - Otherwise split-KV + combine: the whole batch's T KV tiles are cut into one
+ *     contiguous range per worker (ADR-0060 section 2.1 contiguous-block placement); the
+ *     fewest workers that keep the longest range at ceil(T / SMs) tiles.
+ * gqa_plan_describe gives these choices for any device description, without a GPU.
+ * The scope table's scalar form gqa_plan_create(batch, num_q_heads, num_kv_heads,
+ * head_dim, block_size, max_seq_len, seq_lens_host, device, &plan) is this call with those
+ * fields in `desc` (plus the cache pool size, which the tensor maps need, and the two
+ * overrides); its gqa_plan_num_splits is declared below.  The workspace holds a copy of the rotated
  * queries, the fp32 (m, l, O) partials ((B*H_kv + workers) * 6 * G rows of 130 floats),
  * the RoPE tables (max_seq_len x 1.5 KiB), the first tiles each worker streamed at the
  * last call (contiguous caches: prefetched into L2 at the start of the next call) and
@@ -124,11 +151,38 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
 gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_lens_host,
                              gqa_plan_t **plan);
 
+/*
+ * gqa_plan_describe -- the planner's choices for a geometry on a described device, with
+ * no device work (for tests and tooling): the split-KV worker count, the step's form
+ * (cluster size, 0 for split-KV + combine) and the splits of the longest segment, as
+ * gqa_plan_create would make them.
+ *   desc, seq_lens_host : as for gqa_plan_create (desc->device is not used).
+ *   num_sms             : the device's SM count (>= 1).
+ *   cluster_capacity    : [5] how many clusters of 1, 2, 4, 8 and 16 single-launch CTAs
+ *                         the device holds at once (0: that size cannot be launched).
+ *   num_workers, cluster_size, num_splits : outputs; any may be NULL.
+ * Errors: those of gqa_plan_create's validation; GQA_ERR_UNSUPPORTED when a forced
+ * cluster size has capacity 0.
+ */
+gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_lens_host,
+                               int num_sms, const int *cluster_capacity, int *num_workers,
+                               int *cluster_size, int *num_splits);
+
 /* Frees the plan and its workspace (synchronous). NULL is accepted. */
 gqa_status_t gqa_plan_destroy(gqa_plan_t *plan);
 
-/* Number of split-KV workers (CTAs) the plan launches; 0 for a NULL plan. */
+/* Number of split-KV workers (CTAs) of the plan's split-KV kernel (the split-KV form, and
+ * gqa_attention_splitkv in either form); 0 for a NULL plan. */
 int gqa_plan_num_workers(const gqa_plan_t *plan);
+
+/* Number of KV splits of the longest (sequence, KV head) segment as planned: the cluster
+ * size in the single-launch form (at most the segment's tile count), else the number of
+ * split-KV workers whose ranges cover that segment.  0 for a NULL plan. */
+int gqa_plan_num_splits(const gqa_plan_t *plan);
+
+/* The step's form: the cluster size C of the single-launch form, or 0 for split-KV +
+ * combine; 0 for a NULL plan. */
+int gqa_plan_cluster_size(const gqa_plan_t *plan);
 
 /* Bytes of device workspace the plan owns; 0 for a NULL plan. */
 size_t gqa_plan_workspace_bytes(const gqa_plan_t *plan);
@@ -186,10 +240,11 @@ gqa_status_t gqa_decode_attn_host(const gqa_plan_t *plan,
                                   float rope_theta, float eps, void *out_host, void *stream);
 
 /*
- * The two launches of gqa_decode_attn, separately, for callers that schedule them
- * themselves (and for step-level tests and timing).  They communicate through the plan's
- * workspace and must be issued in this order on one stream; arguments are those of
- * gqa_decode_attn, and so are the errors.
+ * The two launches of the split-KV form of gqa_decode_attn, separately, for callers that
+ * schedule them themselves (and for step-level tests and timing); they run the split-KV
+ * form (the plan's worker count) whichever form gqa_decode_attn takes.  They communicate
+ * through the plan's workspace and must be issued in this order on one stream; arguments
+ * are those of gqa_decode_attn, and so are the errors.
  *   gqa_attention_splitkv: the prologue and the split-KV attention in one kernel.  Its
  *     consumer warps apply QK-norm + RoPE to the new queries (into registers, with a copy
  *     to the workspace), append the new k (QK-norm + RoPE) and v rows to the cache, and

@@ -26,7 +26,7 @@ def test_status_strings():
 
 def _create(**over):
     d = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=64, max_seq_len=128,
-             num_cache_blocks=4, num_workers=0, device=0)
+             num_cache_blocks=4, num_workers=0, device=0, cluster_size=0)
     d.update(over)
     desc = binding.PlanDesc(*[d[n] for n, _ in binding.PlanDesc._fields_])
     h = ctypes.c_void_p()
@@ -40,6 +40,9 @@ def _create(**over):
     (dict(num_workers=-1), binding.GQA_ERR_INVALID_ARG),
     (dict(block_size=-64), binding.GQA_ERR_INVALID_ARG),
     (dict(num_cache_blocks=0), binding.GQA_ERR_INVALID_ARG),
+    (dict(cluster_size=3), binding.GQA_ERR_INVALID_ARG),
+    (dict(cluster_size=32), binding.GQA_ERR_INVALID_ARG),
+    (dict(cluster_size=-2), binding.GQA_ERR_INVALID_ARG),
     (dict(head_dim=64), binding.GQA_ERR_UNSUPPORTED),
     (dict(num_q_heads=10, num_kv_heads=4), binding.GQA_ERR_UNSUPPORTED),   # H_q % H_kv != 0
     (dict(num_q_heads=34, num_kv_heads=2), binding.GQA_ERR_UNSUPPORTED),   # G = 17
@@ -63,6 +66,8 @@ def test_null_arguments_are_rejected():
     assert lib.gqa_combine(None, None, None, None) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_plan_destroy(None) == binding.GQA_OK
     assert lib.gqa_plan_num_workers(None) == 0
+    assert lib.gqa_plan_num_splits(None) == 0
+    assert lib.gqa_plan_cluster_size(None) == 0
     f = ctypes.c_uint32()
     assert lib.gqa_plan_device_errors(None, ctypes.byref(f), 0) == binding.GQA_ERR_INVALID_ARG
 

@@ -17,20 +17,26 @@ from _util import (K_WINDOW, Q_WINDOW, appended_rows, assert_out_close, check_ro
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(w, plan=None, num_workers=0):
-    plan = plan or binding.Plan.for_workload(w, num_workers=num_workers)
+# The step's two forms: 0 lets the planner choose (the single-launch form for the small
+# batches most tests use), -1 forces split-KV + combine.
+FORMS = [0, -1]
+
+
+def run_gpu(w, plan=None, num_workers=0, cluster_size=0):
+    plan = plan or binding.Plan.for_workload(w, num_workers=num_workers, cluster_size=cluster_size)
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     plan.run(w, out)
     torch.cuda.synchronize()
     return plan, out
 
 
-def full_check(w, num_workers=0, what=""):
+def full_check(w, num_workers=0, what="", cluster_size=0):
     """Run both sides on workload w (on the GPU) and check output, cache and q."""
     k0, v0 = bits(w.k_cache), bits(w.v_cache)
     ref = oracle_step(w)
     assert ref["status"] == 0
-    plan, out = run_gpu(w, num_workers=num_workers)
+    plan, out = run_gpu(w, num_workers=num_workers, cluster_size=cluster_size)
+    what = f"{what} [C={plan.cluster_size}]"
     assert plan.device_errors() == 0
     stats = assert_out_close(out, ref["out"], what)
     # cache: only the appended rows may change, V bit copies, K bit-exact (midpoint ties aside)
@@ -60,6 +66,27 @@ def full_check(w, num_workers=0, what=""):
 def test_named_workload_full_parity(name):
     w = wl.named(name, device="cuda")
     full_check(w, what=name)
+
+
+@pytest.mark.parametrize("name", ["qwen3-14b-tiny", "qwen3-14b-4k"])
+def test_named_short_workloads_in_the_split_form(name):
+    """The planner runs these in the single-launch form; the split-KV form must agree too."""
+    w = wl.named(name, device="cuda")
+    full_check(w, what=name, cluster_size=-1)
+
+
+@pytest.mark.parametrize("csize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("Hq,Hkv,lens,paged", [
+    (40, 8, [1000, 1, 64, 65], True),     # G = 5, ragged, single-token and page-edge lengths
+    (64, 8, [4096], False),               # G = 8
+    (32, 2, [700, 129], True),            # G = 16 (two head blocks)
+    (8, 8, [300, 2000], False),           # G = 1
+])
+def test_single_launch_cluster_sizes(csize, Hq, Hkv, lens, paged):
+    """Every cluster size of the single-launch form, forced, including sizes larger than a
+    short sequence's tile count (CTAs with no tiles) and non-portable 16-CTA clusters."""
+    w = wl.make(len(lens), Hq, Hkv, lens, paged=paged, seed=csize * 100 + Hq + len(lens), device="cuda")
+    full_check(w, what=f"C={csize} G={Hq // Hkv} lens={lens}", cluster_size=csize)
 
 
 def test_40_layer_sweep_parity():
@@ -99,17 +126,19 @@ def test_40_layer_sweep_parity():
 
 # ------------------------------------------------------------------ edge cases
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("lens", [[1], [2], [63], [64], [65], [127, 128, 129], [1, 64, 65, 300, 7]])
 @pytest.mark.parametrize("paged", [False, True])
-def test_ragged_tails_and_tiny_lengths(lens, paged):
+def test_ragged_tails_and_tiny_lengths(lens, paged, form):
     w = wl.make(len(lens), 10, 2, lens, paged=paged, seed=len(lens) * 7 + 1, device="cuda", extra_blocks=3)
-    full_check(w, what=f"lens={lens} paged={paged}")
+    full_check(w, what=f"lens={lens} paged={paged}", cluster_size=form)
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (8, 2), (10, 2), (16, 2), (24, 2), (32, 2), (64, 8)])
-def test_group_sizes(Hq, Hkv):
+def test_group_sizes(Hq, Hkv, form):
     w = wl.make(3, Hq, Hkv, [70, 200, 5], paged=True, seed=Hq + Hkv, device="cuda")
-    full_check(w, what=f"G={Hq // Hkv}")
+    full_check(w, what=f"G={Hq // Hkv}", cluster_size=form)
 
 
 @pytest.mark.parametrize("qk_norm", [False, True])
@@ -127,10 +156,11 @@ def test_one_sided_norm_weights():
     full_check(w, what="k norm only")
 
 
-def test_new_token_mid_sequence_and_capacity_not_a_tile_multiple():
+@pytest.mark.parametrize("form", FORMS)
+def test_new_token_mid_sequence_and_capacity_not_a_tile_multiple(form):
     w = wl.make(3, 10, 2, [100, 150, 37], paged=False, max_seq=150, positions=[10, 149, 0], seed=6,
                 device="cuda")
-    full_check(w, what="positions < L-1, max_seq=150")
+    full_check(w, what="positions < L-1, max_seq=150", cluster_size=form)
 
 
 @pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 151, 1000])
@@ -196,11 +226,12 @@ def test_plan_reused_across_changed_lengths():
         assert_out_close(out, ref["out"], f"lengths {ints(w.seq_lens).tolist()}")
 
 
-def test_step_replays_from_a_cuda_graph():
+@pytest.mark.parametrize("form", FORMS)
+def test_step_replays_from_a_cuda_graph(form):
     """After a first eager call (which builds the RoPE tables) the step can be captured into
     a CUDA graph; replays give the eager output bit for bit."""
     w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=15, device="cuda")
-    plan, out_eager = run_gpu(w)
+    plan, out_eager = run_gpu(w, cluster_size=form)
     out = torch.empty_like(out_eager)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -218,8 +249,9 @@ def test_step_replays_from_a_cuda_graph():
     assert plan.device_errors() == 0
 
 
-def test_determinism_bitwise():
-    w = wl.named("qwen3-14b-ragged", device="cuda")
+@pytest.mark.parametrize("name", ["qwen3-14b-ragged", "qwen3-14b-4k"])
+def test_determinism_bitwise(name):
+    w = wl.named(name, device="cuda")
     plan, out1 = run_gpu(w)
     out2 = torch.empty_like(out1)
     plan.run(w, out2)
@@ -228,9 +260,11 @@ def test_determinism_bitwise():
 
 
 def test_steps_equal_fused_call():
-    """The three step entry points in order give the fused call's output bit for bit."""
+    """In the split-KV form, the step's two launch entry points in order give the fused
+    call's output bit for bit."""
     w = wl.make(4, 40, 8, [500, 64, 1, 2000], paged=True, seed=11, device="cuda")
-    plan, out1 = run_gpu(w)
+    plan, out1 = run_gpu(w, cluster_size=-1)
+    assert plan.cluster_size == 0
     out2 = torch.empty_like(out1)
     plan.run_steps(w, out2)
     torch.cuda.synchronize()
@@ -255,12 +289,13 @@ def test_host_buffer_entry_point_matches_device_call(pinned):
     assert torch.equal(out1.cpu().view(torch.int16), out_h.view(torch.int16))
 
 
-def test_device_index_errors_are_flagged_not_faulted():
+@pytest.mark.parametrize("form", FORMS)
+def test_device_index_errors_are_flagged_not_faulted(form):
     """Out-of-range positions, lengths and page ids set error bits, zero that sequence's
     output and leave the others correct; nothing faults (the kernels bound-check)."""
     w = wl.make(3, 10, 2, [100, 70, 5], paged=True, seed=13, device="cuda", extra_blocks=2)
     ref = oracle_step(w)
-    plan = binding.Plan.for_workload(w)
+    plan = binding.Plan.for_workload(w, cluster_size=form)
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     # position == seq_len for sequence 1
     w.positions[1] = 70

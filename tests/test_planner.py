@@ -1,0 +1,90 @@
+"""The planner's choices (gqa_plan_describe: no device work) on GB300's description -- 152
+SMs, 152 / 76 / 36 / 15 / 7 resident clusters of 1 / 2 / 4 / 8 / 16 single-launch CTAs
+(cudaOccupancyMaxActiveClusters on the GPU) -- pinned for the five decode workloads, plus
+the rules behind them."""
+import math
+
+import pytest
+
+from gqa_decode_attention_fa_gb300 import binding, workloads as wl
+
+SMS = binding.GB300_SMS
+
+
+def describe(w, **kw):
+    return binding.plan_describe(w["B"], w["Hq"], w["Hkv"], w["max_seq"], block_size=w.get("block", 0),
+                                 num_cache_blocks=w.get("blocks", 0), seq_lens_host=w.get("lens"), **kw)
+
+
+WORKLOADS = {
+    # name: geometry, (split-KV workers, cluster size, splits of the longest segment)
+    "qwen3-14b-tiny": (dict(B=1, Hq=40, Hkv=8, max_seq=256, lens=[256]), (32, 4, 4)),
+    "qwen3-14b-4k": (dict(B=1, Hq=40, Hkv=8, max_seq=4096, lens=[4096]), (128, 8, 8)),
+    "qwen3-14b-ragged": (dict(B=32, Hq=40, Hkv=8, max_seq=8192, block=64, blocks=4000,
+                              lens=wl.ragged_lengths(32, 512, 8192, 0)), (152, 1, 1)),
+    "llama3-70b-128k": (dict(B=1, Hq=64, Hkv=8, max_seq=131072, lens=[131072]), (152, 8, 8)),
+    "qwen3-14b-40layer": (dict(B=8, Hq=40, Hkv=8, max_seq=32768, block=64, blocks=4096, lens=[32768] * 8),
+                          (152, 2, 2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_choices_on_the_five_workloads(name):
+    """Measured on GB300 (graph replay, consecutive steps on different caches, us/step,
+    single launch vs split-KV + combine): tiny 4.15 (C=4) vs 6.72; 4k 6.39 (C=8) vs 8.12;
+    ragged 81.6 (C=1) vs 95.1; 128k 79.5 (C=8) vs 82.9; one 40-layer layer 145.5 (C=2) vs
+    163.5 -- the planner takes the single launch with those cluster sizes."""
+    geom, want = WORKLOADS[name]
+    assert describe(geom) == want
+
+
+def test_split_form_workers_minimise_the_longest_range_then_the_workers():
+    """W = ceil(T / ceil(T / SMs)): the longest range is always ceil(T / SMs) tiles (the
+    minimum), no worker count below W achieves it, and the rule has no jump where an
+    older two-rule fit had one (3 and 4 x SMs)."""
+    prev_longest = 0
+    for T in list(range(1, 5 * SMS + 2)) + [1000, 5000, 10 ** 5]:
+        W, C, _ = binding.plan_describe(1, 8, 1, T * 64, cluster_size=-1)
+        assert C == 0 and 1 <= W <= SMS
+        longest = math.ceil(T / W)
+        assert longest == math.ceil(T / SMS)
+        assert W == 1 or math.ceil(T / (W - 1)) > longest
+        assert longest >= prev_longest
+        prev_longest = longest
+
+
+def test_cluster_size_rules():
+    g = dict(B=1, Hq=40, Hkv=8, max_seq=4096, lens=[4096])
+    # 8 segments of 64 tiles: 16-CTA clusters would need two waves (7 resident) -> 8
+    assert describe(g)[1] == 8
+    # with room for 8 clusters of 16, the largest size is taken
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=(152, 76, 38, 19, 9))[1] == 16
+    # never more CTAs per segment than the segment has tiles
+    assert binding.plan_describe(1, 40, 8, 100)[1] == 2
+    assert binding.plan_describe(1, 40, 8, 64)[1] == 1
+    # a long single segment would stream on 16 SMs: split-KV over every SM instead
+    assert binding.plan_describe(1, 8, 1, 131072)[1] == 0
+    # more than two waves of segments: split-KV
+    assert binding.plan_describe(64, 40, 8, 1024)[1] == 0
+    assert binding.plan_describe(38, 40, 8, 1024)[1] == 1
+    # explicit choices
+    assert binding.plan_describe(1, 40, 8, 4096, num_workers=64) == (64, 0, 8)
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_size=-1)[1] == 0
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_size=16)[1] == 16
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_size=2)[:2] == (128, 2)
+
+
+def test_forced_cluster_size_the_device_cannot_hold_is_rejected():
+    with pytest.raises(binding.GqaError) as e:
+        binding.plan_describe(1, 40, 8, 4096, cluster_size=16, cluster_capacity=(152, 76, 36, 15, 0))
+    assert e.value.status == binding.GQA_ERR_UNSUPPORTED
+    with pytest.raises(binding.GqaError) as e:
+        binding.plan_describe(1, 40, 8, 4096, cluster_size=3)
+    assert e.value.status == binding.GQA_ERR_INVALID_ARG
+
+
+def test_splits_follow_the_longest_segment():
+    # split form: workers whose ranges cover the longest segment (64 tiles over 128 workers' 512)
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_size=-1) == (128, 0, 16)
+    # single launch: the cluster size (16 segments: 8-CTA clusters would not all fit)
+    assert binding.plan_describe(2, 40, 8, 4096, seq_lens_host=[64, 4096]) == (130, 4, 4)

@@ -69,10 +69,34 @@ def test_static_entry_alternating_geometries_and_theta():
     assert int(errors.item()) == 0
 
 
+def test_static_entry_back_to_back_calls_with_growing_batch():
+    """Calls queued on one stream with no synchronisation between them, the same RoPE base
+    and capacity (so the second call reuses the tables and its kernels may start while the
+    first call's combine still runs) but a much larger batch, whose rotated-query region in
+    the shared scratch covers where the first call's partials lie.  Each output matches the
+    oracle."""
+    small = wl.make(1, 40, 8, [3000], paged=False, seed=25, max_seq=8192, device="cuda")
+    lens = wl.ragged_lengths(32, 512, 8192, seed=26)
+    big = wl.make(32, 40, 8, lens, paged=True, seed=26, max_seq=8192, device="cuda")
+    refs = [oracle_step(w) for w in (small, big, small)]
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.full((w.B, w.Hq, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+            for w in (small, big, small)]
+    # the first call on this geometry builds the tables; then three calls back to back
+    binding.decode_attn_static_workload(small, outs[0], device_errors=errors)
+    torch.cuda.synchronize()
+    for w, out in zip((small, big, small), outs):
+        binding.decode_attn_static_workload(w, out, device_errors=errors)
+    torch.cuda.synchronize()
+    assert int(errors.item()) == 0
+    for w, out, ref, tag in zip((small, big, small), outs, refs, ("B=1", "B=32", "B=1 again")):
+        assert_out_close(out, ref["out"], f"static back to back {tag}")
+
+
 def test_static_entry_rejects_geometry_beyond_scratch():
     w = wl.make(1, 8, 2, [100], paged=False, seed=24, device="cuda")
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
-    # a 131072-token capacity needs a 128 MiB RoPE table alone
+    # a 131072-token capacity needs 192 MiB of RoPE tables alone (1.5 KiB per position)
     with pytest.raises(binding.GqaError) as e:
         binding.decode_attn_static(1, 8, 2, 131072, w.q_new, w.k_new, w.v_new, w.k_cache, w.v_cache, None,
                                    w.seq_lens, w.positions, w.q_norm_w, w.k_norm_w, w.rope_theta, w.eps, out)
