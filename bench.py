@@ -5,12 +5,13 @@ One "step" is one pass of the whole hot path -- prologue (QK-norm + RoPE + cache
 split-KV attention, log-sum-exp combine -- over one decode batch of synthetic, seeded
 inputs already resident in HBM (for the 40-layer sweep: the 40 layers' calls).
 
-Prints ONE JSON line.  `value` is microseconds per step (lower is better); `roofline`
-reports the split-KV attention kernel's KV-read bandwidth (algorithmic bytes
-sum_b L_b * H_kv * d * 2 * 2 per launch over its CUDA-event duration) against the measured
-HBM copy peak; `e2e` is the same step through the host-buffer entry point with the
-per-step inputs copied in and the output copied out inside the timed region;
-`cpu_baseline` is the fp64 oracle timed on the host cores on a bounded sample.
+Prints ONE JSON line.  `value` is microseconds per step (lower is better), K steps timed
+as one CUDA graph replay with CUDA events; `roofline` reports the attention kernel's
+KV-read bandwidth (algorithmic bytes sum_b L_b * H_kv * d * 2 * 2 per launch, times the
+launches, over the timed region) against the measured HBM copy peak; `e2e` is the same
+step through the host-buffer entry point with the per-step inputs copied in and the
+output copied out inside the timed region; `cpu_baseline` is the fp64 oracle timed on
+the host cores on a bounded sample.  The headline workload is the 40-layer sweep.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -33,11 +34,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "qwen3-14b-4k"
+HEADLINE = "qwen3-14b-40layer"
 METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_splitkv_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_traffic.json")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -93,9 +94,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch (read + write) from the committed ncu capture of this
-    workload, if it was taken on the current kernel source; else None."""
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` (read + write) from the committed ncu capture of
+    this workload, if it was taken on the current kernel source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -104,7 +105,9 @@ def recorded_traffic(workload: str):
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
     rec = d.get("workloads", {}).get(workload)
-    return None if rec is None else int(rec["dram_bytes_per_launch"])
+    if rec is None or rec.get("kernel") != kernel:
+        return None
+    return int(rec["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -160,16 +163,23 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workloads
 
-def build_layers(name: str, device: str, l2_bytes: int):
+def build_layers(name: str, device: str, l2_bytes: int, layers: int = 0):
     """Per-step list of workloads: the 40 layers for the sweep, else one workload.  Small
-    caches are replicated into enough copies (> 3x L2) that every step reads from HBM; the
-    copies rotate across steps (as a model's layers do)."""
+    caches are replicated into enough copies (> 3x L2) that every step reads from HBM;
+    caches larger than 2x L2 get a second copy.  The copies rotate across steps (as a
+    model's layers do), so that consecutive steps -- which overlap on the device -- never
+    read the same cache.  `layers` > 0 cuts the 40-layer sweep to that many layers (for
+    profiling one layer under ncu)."""
     import torch
 
     from gqa_decode_attention_fa_gb300 import workloads as wl
 
     if name == "qwen3-14b-40layer":
-        return [[wl.named(name, device=device, layer=l) for l in range(wl.LAYERS_40)]], "inputs > L2 (1 GiB KV per layer)"
+        n = layers if layers > 0 else wl.LAYERS_40
+        ws = [wl.named(name, device=device, layer=l) for l in range(n)]
+        if n == 1:  # one layer: alternate with a second one
+            return [ws, [wl.named(name, device=device, layer=1)]], "inputs > L2 (1 GiB KV per layer, 2 layers alternating)"
+        return [ws], f"inputs > L2 (1 GiB KV per layer, {n} layers)"
     if name == "qwen3-14b-4k-decode":
         steps = wl.decode_sweep(device=device)
         kvb = sum(w.kv_bytes() for w in steps[-1])
@@ -177,9 +187,7 @@ def build_layers(name: str, device: str, l2_bytes: int):
                        f"autoregressive steps repeat (each rewrites the rows it appended)")
     w = wl.named(name, device=device)
     kvb = w.kv_bytes()
-    if kvb >= 2 * l2_bytes:
-        return [[w]], f"inputs > L2 ({kvb / 2**20:.0f} MiB KV per step)"
-    copies = int(math.ceil(3 * l2_bytes / kvb))
+    copies = 2 if kvb >= 2 * l2_bytes else int(math.ceil(3 * l2_bytes / kvb))
     sets = [[w]]
     for _ in range(copies - 1):
         c = wl.Workload(**{**w.__dict__})
@@ -187,6 +195,8 @@ def build_layers(name: str, device: str, l2_bytes: int):
         c.v_cache = w.v_cache.clone()
         sets.append([c])
     torch.cuda.synchronize()
+    if copies == 2 and kvb >= 2 * l2_bytes:
+        return sets, f"inputs > L2 ({kvb / 2**20:.0f} MiB KV per step, 2 cache copies alternating)"
     return sets, f"rotating {copies} cache copies ({copies * kvb / 2**20:.0f} MiB > 3x L2)"
 
 
@@ -194,7 +204,39 @@ def algorithmic_kv_bytes(layers) -> int:
     return sum(w.kv_bytes() for w in layers)
 
 
+def workload_config(name: str, layers: int = 0) -> dict:
+    """The workload's description (no device work): both arms print it in `config`."""
+    from gqa_decode_attention_fa_gb300 import workloads as wl
+
+    if name == "qwen3-14b-4k-decode":
+        return {"workload": name, "batch": 1, "q_heads": 40, "kv_heads": 8, "head_dim": 128,
+                "layers": wl.LAYERS_40, "seq_lens": f"{4096 - wl.DECODE_STEPS + 1}..4096 (one token per step)",
+                "cache": "contiguous", "parallelism": "replicas"}
+    geo = {"qwen3-14b-tiny": (1, 40, 8, 256, "contiguous"), "qwen3-14b-4k": (1, 40, 8, 4096, "contiguous"),
+           "qwen3-14b-ragged": (32, 40, 8, "ragged U[512,8192]", "paged-64"),
+           "llama3-70b-128k": (1, 64, 8, 131072, "contiguous"),
+           "qwen3-14b-40layer": (8, 40, 8, 32768, "paged-64")}[name]
+    n = (layers if layers > 0 else wl.LAYERS_40) if name == "qwen3-14b-40layer" else 1
+    return {"workload": name, "batch": geo[0], "q_heads": geo[1], "kv_heads": geo[2], "head_dim": 128,
+            "layers": n, "seq_lens": geo[3], "cache": geo[4], "parallelism": "replicas"}
+
+
+def percentiles(xs):
+    xs = sorted(xs)
+
+    def q(f):
+        if len(xs) == 1:
+            return xs[0]
+        i = f * (len(xs) - 1)
+        lo = int(math.floor(i))
+        return xs[lo] + (xs[min(lo + 1, len(xs) - 1)] - xs[lo]) * (i - lo)
+    return {"median": round(q(0.5), 3), "p10": round(q(0.1), 3), "p90": round(q(0.9), 3), "n": len(xs)}
+
+
 # ----------------------------------------------------------------------------- our arm
+
+INVOCATIONS = 20
+
 
 def run_ours(args, rank, world, local):
     import torch
@@ -206,34 +248,32 @@ def run_ours(args, rank, world, local):
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2**20)
     free, _ = torch.cuda.mem_get_info(local)
-    need = 48 * 2**30 if args.workload == "qwen3-14b-40layer" else 4 * 2**30
+    need = 48 * 2**30 if args.workload == "qwen3-14b-40layer" and args.layers == 0 else 4 * 2**30
     if free < need:
         raise SystemExit(f"bench: {free / 2**30:.1f} GiB free on {dev}, workload needs ~{need / 2**30:.0f} GiB")
-    sets, l2_note = build_layers(args.workload, dev, l2)
+    sets, l2_note = build_layers(args.workload, dev, l2, args.layers)
     first = sets[0][0]
     plan = binding.Plan(first.B, first.Hq, first.Hkv, first.max_seq, block_size=first.block_size,
                         num_cache_blocks=max(w.num_blocks for s in sets for w in s), device=local,
                         seq_lens_host=first.seq_lens.cpu().numpy())
     outs = [torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev) for w in sets[0]]
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream(device=dev)
     kv_per_step = sum(algorithmic_kv_bytes(s) for s in sets) // len(sets)  # mean over the step list
-    launches_per_step = 2 * len(sets[0])
+    single = plan.cluster_size > 0
+    launches_per_layer = 1 if single else 2
+    launches_per_step = launches_per_layer * len(sets[0])
+    form = (f"single launch, clusters of {plan.cluster_size} CTAs per (sequence, KV head)" if single
+            else f"split-KV ({plan.num_workers} workers) + combine")
 
     def step(k):
         """One decode step through the fused entry point (prologue, attention, combine)."""
         for li, w in enumerate(sets[k % len(sets)]):
             plan.run(w, outs[li], stream)
 
-    def step_timed(k, ev_pairs):
-        """The same step through its two launch entry points with CUDA events around the
-        split-KV attention launch (events between launches cost the overlap of consecutive
-        launches, so this pass gives the attention kernel's own duration)."""
-        for li, w in enumerate(sets[k % len(sets)]):
-            plan.run_steps(w, outs[li], stream, between=lambda i, li=li: ev_pairs[li][i].record(stream))
-
     barrier = (lambda: torch.distributed.barrier()) if world > 1 else (lambda: None)
     K, W = args.steps, args.warmup
-    with ClockSampler(local) as clk:
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    with torch.cuda.stream(stream), ClockSampler(local) as clk:
         # warm-up: at least W steps and at least --warmup-seconds of GPU work so the clock
         # record covers the loaded state
         t0 = time.perf_counter()
@@ -242,35 +282,59 @@ def run_ours(args, rank, world, local):
             step(done)
             done += 1
             if done % 64 == 0:
-                torch.cuda.synchronize()
-        torch.cuda.synchronize()
-        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                stream.synchronize()
+        stream.synchronize()
+        graph = None
+        if args.launch == "graph":
+            # the K steps captured once (their launches keep their programmatic dependencies)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for k in range(K):
+                    step(k)
+            graph.replay()
+            stream.synchronize()
+
+        def region():
+            a, b = ev(), ev()
+            a.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for k in range(K):
+                    step(k)
+            b.record(stream)
+            return a, b
+
         barrier()
         torch.cuda.synchronize()
-        e_start.record(stream)
+        e_start, e_end = region()
+        torch.cuda.synchronize()
+        barrier()
+        # the same K steps again as separate invocations: their spread
+        inv = []
+        for _ in range(INVOCATIONS):
+            a, b = region()
+            inv.append((a, b))
+        # and launched eagerly (host launch rate included)
+        a_eager, b_eager = ev(), ev()
+        a_eager.record(stream)
         for k in range(K):
             step(k)
-        e_end.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        # second timed pass: the attention kernel's own duration per launch
-        attn_events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                        for _ in sets[0]] for _ in range(K)]
-        for k in range(K):
-            step_timed(k, attn_events[k])
+        b_eager.record(stream)
         torch.cuda.synchronize()
     clocks = clk.result
     region_ms = e_start.elapsed_time(e_end)
-    attn_ms = [a.elapsed_time(b) for per in attn_events for a, b in per]
+    inv_us = [a.elapsed_time(b) * 1e3 / K for a, b in inv]
+    eager_us = a_eager.elapsed_time(b_eager) * 1e3 / K
+    del graph
     if plan.device_errors() != 0:
         raise SystemExit("bench: device error flags set during the timed region")
 
     # e2e: host buffers through gqa_decode_attn_host, inputs in / output out every step
-    import torch as _t
     host = []
     for w in sets[0]:
         host.append({k: getattr(w, k).cpu().pin_memory() for k in ("q_new", "k_new", "v_new", "seq_lens", "positions")})
-    out_h = [_t.empty((w.B, w.Hq, w.d), dtype=_t.bfloat16).pin_memory() for w in sets[0]]
+    out_h = [torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16).pin_memory() for w in sets[0]]
     h2d = sum(sum(t.numel() * t.element_size() for t in h.values()) for h in host)
     d2h = sum(t.numel() * t.element_size() for t in out_h)
 
@@ -298,10 +362,15 @@ def run_ours(args, rank, world, local):
         us_step, e2e_us = max_over_ranks([us_step, e2e_us], dev)
 
     peak, peak_src = hbm_peak()
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
     kv_per_launch = kv_per_step / len(sets[0])
-    achieved = kv_per_launch / (attn_avg_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    per_launch_us = us_step / len(sets[0]) if single else None
+    kernel = "attn_cluster_kernel" if single else "attn_splitkv_kernel"
+    achieved = kv_per_step / (us_step * 1e-6) / 1e9
+    traffic = recorded_traffic(args.workload, kernel)
+    config = workload_config(args.workload, args.layers)
+    config.update({"parallelism": f"replicas x{world}", "l2": l2_note, "form": form,
+                   "launch": (f"CUDA graph of the {K} timed steps (programmatic dependent launches kept)"
+                              if args.launch == "graph" else "eager launches")})
     result = {
         "metric": METRIC,
         "value": round(us_step, 3),
@@ -315,26 +384,28 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the named workload)",
-        "config": {"workload": args.workload, "batch": first.B, "q_heads": first.Hq, "kv_heads": first.Hkv,
-                   "head_dim": first.d, "layers": len(sets[0]),
-                   "seq_lens": "ragged U[512,8192]" if first.B > 1 and args.workload == "qwen3-14b-ragged"
-                   else (f"{int(sets[0][0].seq_lens[0])}..{int(sets[-1][0].seq_lens[0])} (one token per step)"
-                         if len(sets) > 1 and args.workload == "qwen3-14b-4k-decode"
-                         else int(first.seq_lens[0].item())),
-                   "cache": "paged-64" if first.paged else "contiguous", "l2": l2_note,
-                   "workers": plan.num_workers, "parallelism": f"replicas x{world}"},
+        "config": config,
         "kv_bytes_per_step": kv_per_step,
         "kv_gbs": round(kv_per_step / (us_step * 1e-6) / 1e9, 1),
-        "roofline": {"bound": "hbm", "kernel": "attn_splitkv_kernel", "achieved": round(achieved, 1),
+        "invocations": {**percentiles(inv_us), "unit": "us/step",
+                        "how": f"{INVOCATIONS} further timed regions of the same {K} steps"},
+        "eager_us_per_step": round(eager_us, 3),
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "frac_of_8TBs": round(achieved / 8000.0, 4), "avg_launch_us": round(attn_avg_ms * 1e3, 3),
+                     "frac_of_8TBs": round(achieved / 8000.0, 4),
+                     "per_launch_us": None if per_launch_us is None else round(per_launch_us, 3),
                      "algorithmic_bytes_per_launch": int(kv_per_launch),
+                     "note": ("one kernel per layer; consecutive launches overlap (programmatic dependent "
+                              "launch), so a launch's share of the timed region is the region over the launches"
+                              if single else
+                              "two kernels per layer (attention, combine); achieved is over the whole step"),
                      "traffic": traffic},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
-        "gpu_launches_note": "split-KV attention (prologue folded in) + combine per layer (the RoPE table kernel "
-                             "runs once per theta, before the timed region)",
+        "gpu_launches_note": (f"{launches_per_layer} kernel(s) per layer (" +
+                              ("the single-launch step" if single else "split-KV attention + combine") +
+                              "); the RoPE table kernel runs once per theta, before the timed region"),
         "clocks": clocks,
     }
     return result, sets
@@ -395,7 +466,8 @@ Q4 = ("qwen3-14b-4k-q4", "qwen3-14b-ragged-q4")
 
 def run_q4(name: str, steps: int, warmup: int, local: int):
     """The decode step over a 4-bit cache (gqa_decode_attn_q4: prologue, attention on the
-    index tiles, combine), K steps back to back between CUDA events after warm-up.  Caches
+    index tiles, combine), K steps as one CUDA graph replay between CUDA events after
+    warm-up.  Caches
     smaller than twice L2 are replicated (> 3x L2 of copies, rotated across steps) so that
     every step reads from HBM.  Roofline: the cache bytes a step reads (64 index bytes + a
     4-byte scale per token, KV head and tensor) over the step's time."""
@@ -420,17 +492,23 @@ def run_q4(name: str, steps: int, warmup: int, local: int):
     plan = binding.Plan(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
                         device=local, seq_lens_host=w.seq_lens.cpu().numpy())
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream()
-    for k in range(max(3, warmup)):
-        plan.run_q4(sets[k % len(sets)], out, stream)
-    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        a.record(stream)
-        for k in range(steps):
+    with torch.cuda.stream(stream), ClockSampler(local) as clk:
+        for k in range(max(3, warmup)):
             plan.run_q4(sets[k % len(sets)], out, stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()  # the timed steps captured once, as for the bf16 cache
+        with torch.cuda.graph(graph, stream=stream):
+            for k in range(steps):
+                plan.run_q4(sets[k % len(sets)], out, stream)
+        graph.replay()
+        stream.synchronize()
+        a.record(stream)
+        graph.replay()
         b.record(stream)
-        torch.cuda.synchronize()
+        stream.synchronize()
+        del graph
     if plan.device_errors() != 0:
         raise SystemExit("bench: device error flags set during the 4-bit-cache steps")
     us = a.elapsed_time(b) * 1e3 / steps
@@ -444,9 +522,10 @@ def run_q4(name: str, steps: int, warmup: int, local: int):
             "l2": l2_note, "steps": steps, "workers": plan.num_workers, "clocks_sm_mhz": clk.result["sm_mhz"]}
 
 
-def cpu_baseline(name: str, budget_s: float = 12.0):
+def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0):
     """The fp64 oracle, as it stands, on the host cores: whole decode steps of the workload
-    (for the 40-layer sweep: whole layers, scaled by 40) until ~budget_s of CPU time."""
+    (for the 40-layer sweep: whole layers, scaled by the step's layer count) until
+    ~budget_s of CPU time."""
     import oracle
     from gqa_decode_attention_fa_gb300 import workloads as wl
     from gqa_decode_attention_fa_gb300.workloads import bits, ints
@@ -465,8 +544,8 @@ def cpu_baseline(name: str, budget_s: float = 12.0):
         if time.perf_counter() - t_all > budget_s or len(times) >= 200:
             break
     per_unit = statistics.median(times)
-    layers = wl.LAYERS_40 if name == "qwen3-14b-40layer" else 1
-    unit = "layer" if layers > 1 else "step"
+    layers = (layers or wl.LAYERS_40) if name == "qwen3-14b-40layer" else 1
+    unit = "layer" if name == "qwen3-14b-40layer" else "step"
     return {"value": round(per_unit * layers * 1e6, 1), "unit": "us/step", "cores": int(r["threads"]),
             "kind": "oracle",
             "sample": f"{len(times)} full {unit}(s) of {name} in fp64 (median), x{layers} per step"}
@@ -480,7 +559,7 @@ def run_reference(args, rank, world):
     from gqa_decode_attention_fa_gb300 import workloads as wl
     from gqa_decode_attention_fa_gb300.workloads import bits, ints
 
-    layers = wl.LAYERS_40 if args.workload == "qwen3-14b-40layer" else 1
+    layers = (getattr(args, "layers", 0) or wl.LAYERS_40) if args.workload == "qwen3-14b-40layer" else 1
     w = wl.named(args.workload, device="cpu")
     g = oracle.geom(w.B, w.Hq, w.Hkv, w.d, w.block_size, w.max_seq, w.num_rows)
     a = [bits(w.q_new), bits(w.k_new), bits(w.v_new), bits(w.k_cache), bits(w.v_cache), ints(w.page_table),
@@ -507,7 +586,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload},
+        "config": workload_config(args.workload, getattr(args, "layers", 0)),
         "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -524,9 +603,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--warmup-seconds", type=float, default=0.3,
                     help="keep warming up for at least this long (so the clock record sees the loaded GPU)")
-    ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-ragged,llama3-70b-128k,qwen3-14b-40layer,"
+    ap.add_argument("--by-config", default="qwen3-14b-tiny,qwen3-14b-4k,qwen3-14b-ragged,llama3-70b-128k,"
                                            "qwen3-14b-4k-decode," + PREFILL + "," + ",".join(Q4),
                     help="other workloads to time (GPU only) into the line's by_config; '' for none")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="cut the 40-layer sweep to this many layers (for profiling one layer); 0 = all 40")
+    ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
+                    help="time the K steps as one CUDA graph replay (default) or as eager launches")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.warmup < 3:
@@ -547,7 +630,7 @@ def main():
     del sets
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args.workload)
+        result["cpu_baseline"] = cpu_baseline(args.workload, layers=result["config"]["layers"])
     by = {}
     for name in [n for n in args.by_config.split(",") if n and n != args.workload]:
         if name == PREFILL:
@@ -558,14 +641,14 @@ def main():
             by[name] = run_q4(name, min(args.steps, 50), args.warmup, local)
             torch.cuda.empty_cache()
             continue
-        sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50)})
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50), "layers": 0})
         r, s = run_ours(sub, rank, world, local)
         del s
         torch.cuda.empty_cache()
-        by[name] = {"us_per_step": r["value"], "kv_gbs": r["kv_gbs"], "attn_gbs": r["roofline"]["achieved"],
-                    "frac": r["roofline"]["frac"], "frac_of_8TBs": r["roofline"]["frac_of_8TBs"],
-                    "attn_us": r["roofline"]["avg_launch_us"], "e2e_us": r["e2e"]["value"],
-                    "steps": r["steps"], "l2": r["config"]["l2"], "clocks_sm_mhz": r["clocks"]["sm_mhz"]}
+        by[name] = {"us_per_step": r["value"], "eager_us_per_step": r["eager_us_per_step"],
+                    "invocations": r["invocations"], "kv_gbs": r["kv_gbs"], "roofline": r["roofline"],
+                    "e2e_us": r["e2e"]["value"], "steps": r["steps"], "form": r["config"]["form"],
+                    "l2": r["config"]["l2"], "clocks_sm_mhz": r["clocks"]["sm_mhz"]}
     if by:
         result["by_config"] = by
     if rank == 0:

@@ -63,7 +63,8 @@ def test_reference_arm_line_carries_the_contract_keys():
     r = json.loads(json.dumps(bench.run_reference(args, 0, 1)))
     assert r["impl"] == "reference" and r["metric"] == bench.METRIC and r["unit"] == "us/step"
     assert r["higher_is_better"] is False and r["n_gpus"] == 1
-    assert r["steps"] == 2 and r["warmup"] == 3 and r["config"] == {"workload": "qwen3-14b-tiny"}
+    assert r["steps"] == 2 and r["warmup"] == 3 and r["config"] == bench.workload_config("qwen3-14b-tiny")
+    assert r["config"]["workload"] == "qwen3-14b-tiny" and r["config"]["layers"] == 1
     assert r["value"] > 0 and r["ms_per_step"] == pytest.approx(r["value"] / 1e3, abs=1e-3)
     cb = r["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == r["value"] and cb["cores"] >= 1 and cb["sample"]
