@@ -16,6 +16,7 @@ struct gqa_plan {
   gqa_plan_desc_t desc;
   int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0, combine_split = 1;
   int csize = 0;   // single-launch form: CTAs per (sequence, KV head) cluster; 0: split-KV + combine
+  int spec_tiles = 0;  // tiles of the longest segment as planned
   int nsplit = 0;  // KV splits of the longest (sequence, KV head) segment
   long long num_rows = 0;
   void *ws = nullptr;
@@ -288,6 +289,7 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k,
   if (single_out) {
     p.out = static_cast<uint16_t *>(single_out);
     p.csize = plan->csize;
+    p.spec_tiles = plan->spec_tiles;
     p.spec = nullptr;
     e = launch_attention_cluster(tk, tv, p, plan->npad, !rebuilt, stream);
   } else {
@@ -347,7 +349,7 @@ gqa_status_t check_desc(const gqa_plan_desc_t &d) {
 // the step's form, the splits of the longest segment and the combine's shape.  Lengths
 // come from seq_lens_host (clamped to [1, max_seq_len]) or are max_seq_len.
 struct PlanChoice {
-  int W = 0, csize = 0, nsplit = 0, combine_split = 0;
+  int W = 0, csize = 0, nsplit = 0, combine_split = 0, max_seg_tiles = 0;
 };
 gqa_status_t plan_choose(const gqa_plan_desc_t &d, const int32_t *seq_lens_host, int num_sms, const int *capacity,
                          PlanChoice *out) {
@@ -365,6 +367,7 @@ gqa_status_t plan_choose(const gqa_plan_desc_t &d, const int32_t *seq_lens_host,
   c.csize = plan_step_form(d.cluster_size, d.num_workers, num_sms, capacity,
                            static_cast<long long>(d.batch) * d.num_kv_heads, max_seg_tiles, total_tiles);
   if (c.csize < 0) return GQA_ERR_UNSUPPORTED;
+  c.max_seg_tiles = static_cast<int>(max_seg_tiles);
   c.nsplit = c.csize > 0 ? static_cast<int>(std::min<long long>(c.csize, max_seg_tiles))
                          : split_count(seq_lens_host, d.batch, d.num_kv_heads, d.max_seq_len, c.W);
   *out = c;
@@ -399,6 +402,7 @@ gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay)
   l.W = pc.W;
   l.combine_split = pc.combine_split;
   l.csize = pc.csize;
+  l.spec_tiles = pc.max_seg_tiles;
   const long long slots = B * Hkv + l.W;
   l.tab_bytes = rope_tables_bytes(d.max_seq_len);
   l.off_q = l.tab_bytes;
@@ -423,6 +427,7 @@ gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *
   plan.max_blocks = lay.max_blocks;
   plan.combine_split = lay.combine_split;
   plan.csize = lay.csize;
+  plan.spec_tiles = lay.spec_tiles;
   plan.num_rows = lay.num_rows;
   char *c = static_cast<char *>(base);
   plan.rope_tab = reinterpret_cast<float4 *>(c);
@@ -479,6 +484,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->combine_split = pc.combine_split;
   p->csize = pc.csize;
   p->nsplit = pc.nsplit;
+  p->spec_tiles = pc.max_seg_tiles;
 
   const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
   const long long slots = B * Hkv + p->W;

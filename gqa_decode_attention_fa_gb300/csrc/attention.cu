@@ -772,7 +772,20 @@ constexpr int kPartStride = 132;          // floats per (warp, head) partial row
 constexpr int kRecvMlFloats = GQA_MAX_GROUP * GQA_MAX_GROUP * 2;
 constexpr int kRecvOFloats = GQA_MAX_GROUP * kHeadDim;
 constexpr int kRecvOffset = kStages * 4 * kHalfTileBytes + 1024;   // from the aligned base
-constexpr size_t kClusterSmemBytes = 1024 + kRecvOffset + 4 * (kRecvMlFloats + kRecvOFloats);
+constexpr int kKvRowOffset = kRecvOffset + 4 * (kRecvMlFloats + kRecvOFloats);  // the appended k/v row
+constexpr size_t kClusterSmemBytes = 1024 + kKvRowOffset + 2 * kHeadDim * 2;
+
+// Barrier 1 hands the appended k/v row from the ordering warp to the consumer warp whose
+// tile holds it (the ordering warp arrives, that consumer waits).
+__device__ __forceinline__ void kvrow_arrive() { asm volatile("bar.arrive 1, 64;" ::: "memory"); }
+__device__ __forceinline__ void kvrow_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// Barrier 2: the producer warp arrives once the ring's barriers are initialised; the
+// consumer warps wait for it before their first wait on a ring stage.
+constexpr int kRingReadyThreads = 32 * (kConsumerWarps + 1);
+__device__ __forceinline__ void ring_ready_arrive() {
+  asm volatile("bar.arrive 2, %0;" ::"n"(kRingReadyThreads) : "memory");
+}
+__device__ __forceinline__ void ring_ready_sync() { asm volatile("bar.sync 2, %0;" ::"n"(kRingReadyThreads) : "memory"); }
 // Warps: the consumers, the producer, and an ordering warp that waits on the preceding
 // kernel, appends the new row (in the CTA whose tile holds it) and lets the next launch.
 constexpr int kOrderWarp = kConsumerWarps + 1;
@@ -798,19 +811,61 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   const int seg = static_cast<int>(blockIdx.x) / C;
   const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
   const bool producer = warp == kConsumerWarps;
+  uint16_t *kvrow = reinterpret_cast<uint16_t *>(smem + kKvRowOffset);  // [2][128]: k, v
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), 1);
+  // Cache row of local tile i's first token (the TMA z coordinate); a page id outside the
+  // pool reads as a box wholly out of bounds (zeros) and is flagged when `flag`.
+  auto tile_row = [&](int i, bool flag) -> int {
+    const int j = rank + C * i;
+    if (p.paged) {
+      const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+      if (pg < 0 || pg >= p.num_blocks) {
+        if (flag) atomicOr(p.err, GQA_DEVERR_PAGE);
+        return -kTile;
+      }
+      return pg * kTile;
     }
-    mbar_init(smem_addr(recv_bar), 1);
-    fence_barrier_init();
+    return b * p.max_seq + j * kTile;
+  };
+  auto issue = [&](int s, int r_row) {  // one tile into stage s (lane 0 of the producer)
+    const uint32_t fb = smem_addr(&full_bar[s]);
+    const uint32_t base = smem_addr(smem + s * Cf::kStageBytes);
+    mbar_arrive_expect_tx(fb, Cf::kStageBytes);
+    tma_load_3d(base, &tmK, fb, 0, kv, r_row);
+    tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, r_row);
+    tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, r_row);
+    tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
+  };
+
+  // The producer initialises the barriers and, before the segment's length is known, loads
+  // the first tiles the plan expects this CTA to stream (a tile's cache row does not depend
+  // on the length); tiles that turn out to lie past the length are waited for and dropped.
+  int nspec = 0, spec_row = 0;
+  if (producer) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(smem_addr(&full_bar[s]), 1);
+        mbar_init(smem_addr(&empty_bar[s]), 1);
+      }
+      mbar_init(smem_addr(recv_bar), 1);
+      fence_barrier_init();
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
+    const int st = p.spec_tiles < p.max_blocks ? p.spec_tiles : p.max_blocks;
+    nspec = st > rank ? (st - rank + C - 1) / C : 0;
+    nspec = nspec < kStages ? nspec : kStages;
+    if (lane < nspec) spec_row = tile_row(lane, false);
+    __syncwarp();
+    for (int k = 0; k < nspec; ++k) {
+      const int r_row = __shfl_sync(0xffffffffu, spec_row, k);
+      if (lane == 0) issue(k, r_row);
+    }
+    ring_ready_arrive();
   }
-  if (producer && lane == 0) {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
+  // The cluster barrier's first phase: every CTA's barriers are initialised (the producer's
+  // lane 0 arrives after its initialisation; it is waited for before the first remote store).
+  cluster_arrive();
   // The segment's length and new-token position (one broadcast load per warp).
   int L = p.seq_lens[b], pos = p.positions[b];
   const int nt = tiles_of(L, p.max_seq);
@@ -826,23 +881,6 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   // The warp (of this CTA) whose tile holds the new token, or -1.
   int owner = -1;
   if (pos >= 0 && (pos >> 6) % C == rank) owner = ((pos >> 6) / C) % kConsumerWarps;
-  __syncthreads();  // barrier initialisation visible to the CTA
-  cluster_arrive();  // ... and to the cluster (waited for before the first remote store)
-
-  // Cache row of local tile i's first token (the TMA z coordinate); a page id outside the
-  // pool is flagged and read as a box wholly out of bounds (zeros).
-  auto tile_row = [&](int i) -> int {
-    const int j = rank + C * i;
-    if (p.paged) {
-      const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
-      if (pg < 0 || pg >= p.num_blocks) {
-        atomicOr(p.err, GQA_DEVERR_PAGE);
-        return -kTile;
-      }
-      return pg * kTile;
-    }
-    return b * p.max_seq + j * kTile;
-  };
 
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
@@ -872,6 +910,12 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     if (owner >= 0) {
       load_kv_row(p, b, kv, pos, lane, kin);
       rotated_kv_row(p, kin, kz, vz);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        kvrow[lane + 32 * t] = kz[t];
+        kvrow[kHeadDim + lane + 32 * t] = vz[t];
+      }
+      kvrow_arrive();  // the owning consumer warp patches its tile with these
     }
     griddep_wait();
     if (owner >= 0) {
@@ -888,24 +932,17 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     // (the combine), and this step's own new row is patched into its tile by the consumer
     // that owns it.
     const int npre = n < kStages ? n : kStages;
+    if (lane < nspec && lane < n && spec_row < 0) atomicOr(p.err, GQA_DEVERR_PAGE);  // now known to be read
     int row = 0;
-    if (lane < npre) row = tile_row(lane);
-    for (int k = 0; k < npre; ++k) {
+    if (lane >= nspec && lane < npre) row = tile_row(lane, true);
+    for (int k = nspec; k < npre; ++k) {
       const int r_row = __shfl_sync(0xffffffffu, row, k);
-      if (lane == 0) {
-        const uint32_t fb = smem_addr(&full_bar[k]);
-        const uint32_t base = smem_addr(smem + k * Cf::kStageBytes);
-        mbar_arrive_expect_tx(fb, Cf::kStageBytes);
-        tma_load_3d(base, &tmK, fb, 0, kv, r_row);
-        tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, r_row);
-        tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, r_row);
-        tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
-      }
+      if (lane == 0) issue(k, r_row);
     }
     bool fail = false;
-    int issued = npre;
+    int issued = npre > nspec ? npre : nspec;
     for (int i0 = npre; i0 < n && !fail; i0 += 32) {
-      row = i0 + lane < n ? tile_row(i0 + lane) : 0;
+      row = i0 + lane < n ? tile_row(i0 + lane, true) : 0;
       const int cnt = n - i0 < 32 ? n - i0 : 32;
       for (int k = 0; k < cnt; ++k) {
         const int r_row = __shfl_sync(0xffffffffu, row, k);
@@ -914,13 +951,7 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
         if (lane == 0) {
           ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((ii / kStages) - 1) & 1));
           if (ok) {
-            const uint32_t fb = smem_addr(&full_bar[s]);
-            const uint32_t base = smem_addr(smem + s * Cf::kStageBytes);
-            mbar_arrive_expect_tx(fb, Cf::kStageBytes);
-            tma_load_3d(base, &tmK, fb, 0, kv, r_row);
-            tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, r_row);
-            tma_load_3d(base + 2 * kHalfTileBytes, &tmV, fb, 0, kv, r_row);
-            tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
+            issue(s, r_row);
             issued = ii + 1;
           }
         }
@@ -931,10 +962,13 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
         }
       }
     }
-    if (fail && lane == 0) {
-      atomicOr(p.err, GQA_DEVERR_TIMEOUT);
-      // no copy may still be landing in this CTA's shared memory when it is reused below
-      for (int ii = (issued > kStages ? issued - kStages : 0); ii < issued; ++ii)
+    if (lane == 0) {
+      if (fail) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+      // No copy may still be landing in this CTA's shared memory when it is reused below:
+      // after a failure, the last ring's worth; else the speculative tiles past the length,
+      // which no consumer waits for.
+      const int from = fail ? (issued > kStages ? issued - kStages : 0) : n;
+      for (int ii = from; ii < issued; ++ii)
         (void)mbar_wait(smem_addr(&full_bar[ii % kStages]), static_cast<uint32_t>((ii / kStages) & 1));
     }
     __syncwarp();
@@ -944,17 +978,14 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     const bool has_tiles = cw < n;
     const int i_new = cw == owner ? (pos >> 6) / C : -1;  // local index of the new token's tile
     QIn<NT> qin;
-    KvRowIn kin;
     if (has_tiles && pos >= 0) load_q_inputs<NT>(p, b, kv, pos, lane, qin);
-    if (i_new >= 0) load_kv_row(p, b, kv, pos, lane, kin);
     uint32_t qf[8][NT][2];
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
       for (int t = 0; t < NT; ++t) qf[ks][t][0] = qf[ks][t][1] = 0u;
     if (has_tiles && pos >= 0) rotate_q<NT>(p, lane, qin, qf);
-    uint16_t kz[4] = {0, 0, 0, 0}, vz[4] = {0, 0, 0, 0};
-    if (i_new >= 0) rotated_kv_row(p, kin, kz, vz);  // the same bits the producer appends
+    ring_ready_sync();  // the ring's barriers are initialised
     if (rank == 0 && cw == 0) {  // the rotated queries, published after the wait below
       qpub = has_tiles && pos >= 0;
 #pragma unroll
@@ -974,7 +1005,13 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
       const int valid = min(kTile, L - (rank + C * i) * kTile);
       uint8_t *stage = smem + s * Cf::kStageBytes;
       if (valid < kTile) zero_v_tail(stage, valid, lane);
-      if (i == i_new) patch_row(stage, pos & (kTile - 1), kz, vz, lane);
+      if (i == i_new) {  // the appended row, from the ordering warp
+        kvrow_sync();
+        uint16_t kz[4], vz[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) kz[t] = kvrow[lane + 32 * t], vz[t] = kvrow[kHeadDim + lane + 32 * t];
+        patch_row(stage, pos & (kTile - 1), kz, vz, lane);
+      }
       tile_update<NT>(stage, valid, p.scale_log2, lane, qf, o, m_run, l_run);
       if (valid < kTile || i == i_new) fence_proxy_async_smem();
       __syncwarp();
@@ -1067,30 +1104,21 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   cluster_arrive_relaxed();  // this CTA has received everything (or given up)
   griddep_wait();
   if (qpub) publish_q<NT>(p, b, kv, lane, qkeep);
+  // (Code that runs once per launch is kept compact: on a latency-bound step its
+  // instruction fetches, not its arithmetic, set the time.)
   for (int e = tid; e < p.G * dpr; e += kThreadsCluster) {
     const int g = e / dpr, dd = e - g * dpr;
-    float mq[GQA_MAX_GROUP], lq[GQA_MAX_GROUP], oq[GQA_MAX_GROUP];
-#pragma unroll
-    for (int r = 0; r < GQA_MAX_GROUP; ++r) {
-      if (r < C) {
-        mq[r] = recv_ml[(r * p.G + g) * 2];
-        lq[r] = recv_ml[(r * p.G + g) * 2 + 1];
-        oq[r] = recv_o[(r * p.G + g) * dpr + dd];
-      }
-    }
     float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < GQA_MAX_GROUP; ++r)
-      if (r < C) M = fmaxf(M, mq[r]);
+#pragma unroll 1
+    for (int r = 0; r < C; ++r) M = fmaxf(M, recv_ml[(r * p.G + g) * 2]);
     float acc = 0.f, den = 0.f;
     if (M != -INFINITY) {
-#pragma unroll
-      for (int r = 0; r < GQA_MAX_GROUP; ++r)
-        if (r < C) {
-          const float f = exp2f(mq[r] - M);
-          acc = fmaf(f, oq[r], acc);
-          den = fmaf(f, lq[r], den);
-        }
+#pragma unroll 1
+      for (int r = 0; r < C; ++r) {
+        const float f = exp2f(recv_ml[(r * p.G + g) * 2] - M);
+        acc = fmaf(f, recv_o[(r * p.G + g) * dpr + dd], acc);
+        den = fmaf(f, recv_ml[(r * p.G + g) * 2 + 1], den);
+      }
     }
     const float v = den > 0.f ? acc / den : 0.f;  // zeros for an invalid length (flagged above)
     const __nv_bfloat16 h = __float2bfloat16_rn(v);

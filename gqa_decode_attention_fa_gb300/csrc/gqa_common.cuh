@@ -87,6 +87,9 @@ struct AttnParams {
   int B, Hq, Hkv, G;
   int paged, max_seq, max_blocks, num_blocks;
   int csize;                                // single-launch form: CTAs per segment (cluster size)
+  int spec_tiles;                           // single-launch form: tiles of the longest segment the
+                                            // plan expects (its first tiles are loaded before the
+                                            // length is read)
   double eps;
   float scale_log2;                         // log2(e) / sqrt(d)
 };

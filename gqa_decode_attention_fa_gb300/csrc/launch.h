@@ -134,7 +134,7 @@ struct DeviceGuard {
 // 256-byte-aligned base.  The RoPE table comes first, so that its place does not depend on
 // the batch geometry and a table built by one call stays usable by the next.
 struct StepLayout {
-  int G = 0, npad = 0, W = 0, max_blocks = 0, combine_split = 1, csize = 0;
+  int G = 0, npad = 0, W = 0, max_blocks = 0, combine_split = 1, csize = 0, spec_tiles = 0;
   long long num_rows = 0;
   size_t tab_bytes = 0, off_q = 0, off_o = 0, off_ml = 0, off_err = 0, total = 0;
 };
