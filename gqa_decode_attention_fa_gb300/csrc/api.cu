@@ -747,6 +747,40 @@ extern "C" gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan, const void *q
   if (!encode_u8_map(&tk, 3, k_idx, dims, strides, box) || !encode_u8_map(&tv, 3, v_idx, dims, strides, box))
     return GQA_ERR_CUDA;
 
+  if (plan->csize > 0) {  // the single-launch form
+    Q4ClusterParams cp;
+    memset(&cp, 0, sizeof cp);
+    cp.seq_lens = seq_lens;
+    cp.positions = positions;
+    cp.page_table = page_table;
+    cp.q_new = static_cast<const uint16_t *>(q_new);
+    cp.k_new = static_cast<const uint16_t *>(k_new);
+    cp.v_new = static_cast<const uint16_t *>(v_new);
+    cp.q_norm_w = static_cast<const uint16_t *>(q_norm_w);
+    cp.k_norm_w = static_cast<const uint16_t *>(k_norm_w);
+    cp.rope_tab32 = rope_tab32_of(plan);
+    cp.signs = rot_signs;
+    cp.codebook = static_cast<const uint16_t *>(codebook);
+    cp.k_idx = k_idx;
+    cp.v_idx = v_idx;
+    cp.k_scale = k_scale;
+    cp.v_scale = v_scale;
+    cp.out = static_cast<uint16_t *>(out);
+    cp.err = plan->err;
+    cp.B = d.batch;
+    cp.Hq = d.num_q_heads;
+    cp.Hkv = d.num_kv_heads;
+    cp.G = plan->G;
+    cp.paged = paged ? 1 : 0;
+    cp.max_seq = d.max_seq_len;
+    cp.max_blocks = plan->max_blocks;
+    cp.num_blocks = paged ? d.num_cache_blocks : 0;
+    cp.csize = plan->csize;
+    cp.eps = eps;
+    cp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
+    return launch_q4_cluster(tk, tv, cp, plan->npad, !rebuilt, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  }
+
   Q4PrologueParams pp;
   memset(&pp, 0, sizeof pp);
   pp.seq_lens = seq_lens;

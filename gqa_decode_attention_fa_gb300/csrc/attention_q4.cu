@@ -81,6 +81,112 @@ __device__ __forceinline__ void unpack4(uint2 w, float (&f)[4]) {
   f[3] = __uint_as_float(w.y & 0xffff0000u);
 }
 
+// Per-warp constants of the 4-bit row arithmetic, lane l holding dims 4 l .. 4 l + 3: the
+// RoPE (cos, sin) of those dims' pairs at a position, the rotation's signs, the codebook
+// and the midpoints between consecutive levels (exact in binary32).
+struct Q4RowConsts {
+  float cs_c[4], cs_s[4], sg[4], cb[16], thr[15];
+};
+__device__ __forceinline__ void q4_row_consts(const float2 *rope_tab32, int pos, const int8_t *signs,
+                                              const uint16_t *codebook, int lane, Q4RowConsts &k) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    k.cs_c[u] = 1.f;
+    k.cs_s[u] = 0.f;
+  }
+  if (pos >= 0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 t = rope_tab32[static_cast<long long>(pos) * 64 + 4 * (lane & 15) + u];
+      k.cs_c[u] = t.x;
+      k.cs_s[u] = t.y;
+    }
+  }
+  const char4 s4 = reinterpret_cast<const char4 *>(signs)[lane];
+  k.sg[0] = s4.x;
+  k.sg[1] = s4.y;
+  k.sg[2] = s4.z;
+  k.sg[3] = s4.w;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) k.cb[j] = __uint_as_float(static_cast<uint32_t>(codebook[j]) << 16);
+#pragma unroll
+  for (int j = 0; j < 15; ++j) k.thr[j] = 0.5f * (k.cb[j] + k.cb[j + 1]);
+}
+
+// RMSNorm (optional weight) and RoPE of a bf16 row, binary32; the RoPE partner of dim e
+// (e +- 64) is in lane l ^ 16.
+__device__ __forceinline__ void q4_norm_rope(const uint16_t *src, const uint16_t *w, float eps, const Q4RowConsts &k,
+                                             int lane, float (&z)[4]) {
+  float x[4], y[4], ss = 0.f;
+  unpack4(reinterpret_cast<const uint2 *>(src)[lane], x);
+  float wv[4] = {1.f, 1.f, 1.f, 1.f};
+  if (w) unpack4(reinterpret_cast<const uint2 *>(w)[lane], wv);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    ss = fmaf(x[u], x[u], ss);
+    y[u] = x[u] * wv[u];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rn = w ? 1.0f / sqrtf(ss * (1.0f / 128.0f) + eps) : 1.0f;
+  const bool first_half = lane < 16;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float yp = __shfl_xor_sync(0xffffffffu, y[u], 16);
+    z[u] = rn * (first_half ? fmaf(y[u], k.cs_c[u], -yp * k.cs_s[u]) : fmaf(y[u], k.cs_c[u], yp * k.cs_s[u]));
+  }
+}
+
+// Quantizes a row z: t = sqrt(d) R z / ||z||, idx = the nearest level (the lower one on a
+// tie); the indices packed into bytes 4 l .. 4 l + 3 (lanes < 16) and sigma.
+__device__ __forceinline__ void q4_quantize(const float (&z)[4], const Q4RowConsts &k, int lane, uint32_t &packed,
+                                            float &sigma) {
+  float ss = 0.f, y[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    ss = fmaf(z[u], z[u], ss);
+    y[u] = k.sg[u] * z[u];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float s = sqrtf(ss);
+  fwht128(y, lane);  // H D z = sqrt(d) R z
+  int idx[4];
+  float cn = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float t = s > 0.f ? y[u] / s : 0.f;  // sqrt(d) (R z)_i / ||z||
+    int j = 0;
+    float cj = k.cb[0];  // the chosen level, selected in registers (no indexed local array)
+#pragma unroll
+    for (int q = 0; q < 15; ++q) {
+      const bool above = k.thr[q] < t;
+      j += above ? 1 : 0;
+      cj = above ? k.cb[q + 1] : cj;
+    }
+    idx[u] = j;
+    cn = fmaf(cj, cj, cn);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cn += __shfl_xor_sync(0xffffffffu, cn, o);
+  sigma = s > 0.f ? s / sqrtf(cn) : 0.f;
+  const uint32_t mine = idx[0] | (idx[1] << 8) | (idx[2] << 16) | (idx[3] << 24);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, mine, 16);  // dims + 64 from lane l + 16
+  packed = mine | (hi << 4);
+}
+
+// q~ = R bf16(z) = H D bf16(z) / sqrt(d) (q is a bf16 activation), in place.
+__device__ __forceinline__ void q4_rotate_query(float (&z)[4], const Q4RowConsts &k, int lane) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const __nv_bfloat16 zq = __float2bfloat16_rn(z[u]);
+    z[u] = k.sg[u] * __bfloat162float(zq);
+  }
+  fwht128(z, lane);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) z[u] *= kInvSqrtD;
+}
+
 }  // namespace
 
 // ----------------------------------------------------------------------------- prologue
@@ -118,96 +224,16 @@ __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams
       crow = static_cast<long long>(b) * p.max_seq + pos;
     }
   }
-  const bool first_half = lane < 16;
-  float cs_c[4] = {1.f, 1.f, 1.f, 1.f}, cs_s[4] = {0.f, 0.f, 0.f, 0.f};
-  if (pos_ok) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float2 t = p.rope_tab32[static_cast<long long>(pos) * 64 + 4 * (lane & 15) + u];
-      cs_c[u] = t.x;
-      cs_s[u] = t.y;
-    }
-  }
-  float sg[4];
-  {
-    const char4 s4 = reinterpret_cast<const char4 *>(p.signs)[lane];
-    sg[0] = s4.x;
-    sg[1] = s4.y;
-    sg[2] = s4.z;
-    sg[3] = s4.w;
-  }
-  // codebook and the midpoints between consecutive levels (exact in binary32)
-  float cb[16], thr[15];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) cb[j] = __uint_as_float(static_cast<uint32_t>(p.codebook[j]) << 16);
-#pragma unroll
-  for (int j = 0; j < 15; ++j) thr[j] = 0.5f * (cb[j] + cb[j + 1]);
-
-  // RMSNorm (optional weight) and RoPE of a row, binary32
-  auto norm_rope = [&](const uint16_t *src, const uint16_t *w, float (&z)[4]) {
-    float x[4], y[4], ss = 0.f;
-    unpack4(reinterpret_cast<const uint2 *>(src)[lane], x);
-    float wv[4] = {1.f, 1.f, 1.f, 1.f};
-    if (w) unpack4(reinterpret_cast<const uint2 *>(w)[lane], wv);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      ss = fmaf(x[u], x[u], ss);
-      y[u] = x[u] * wv[u];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rn = w ? 1.0f / sqrtf(ss * (1.0f / 128.0f) + p.eps) : 1.0f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float yp = __shfl_xor_sync(0xffffffffu, y[u], 16);
-      z[u] = rn * (first_half ? fmaf(y[u], cs_c[u], -yp * cs_s[u]) : fmaf(y[u], cs_c[u], yp * cs_s[u]));
-    }
-  };
-  // quantize a row z: indices packed into bytes 4 l .. 4 l + 3 (lanes < 16) and sigma
-  auto quantize = [&](const float (&z)[4], uint32_t &packed, float &sigma) {
-    float ss = 0.f, y[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      ss = fmaf(z[u], z[u], ss);
-      y[u] = sg[u] * z[u];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float s = sqrtf(ss);
-    fwht128(y, lane);  // H D z = sqrt(d) R z
-    int idx[4];
-    float cn = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float t = s > 0.f ? y[u] / s : 0.f;  // sqrt(d) (R z)_i / ||z||
-      int k = 0;
-#pragma unroll
-      for (int j = 0; j < 15; ++j) k += thr[j] < t ? 1 : 0;
-      idx[u] = k;
-      cn = fmaf(cb[k], cb[k], cn);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cn += __shfl_xor_sync(0xffffffffu, cn, o);
-    sigma = s > 0.f ? s / sqrtf(cn) : 0.f;
-    uint32_t mine = idx[0] | (idx[1] << 8) | (idx[2] << 16) | (idx[3] << 24);
-    const uint32_t hi = __shfl_xor_sync(0xffffffffu, mine, 16);  // dims + 64 from lane l + 16
-    packed = mine | (hi << 4);
-  };
+  Q4RowConsts kc;
+  q4_row_consts(p.rope_tab32, pos_ok ? pos : -1, p.signs, p.codebook, lane, kc);
 
   {
     if (r < p.Hq) {
       const long long row = static_cast<long long>(b) * p.Hq + r;
       float z[4] = {0.f, 0.f, 0.f, 0.f};
       if (pos_ok) {
-        norm_rope(p.q_new + row * kHeadDim, p.q_norm_w, z);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // q~ = R z = H D z / sqrt(d)
-          const __nv_bfloat16 zq = __float2bfloat16_rn(z[u]);  // q is a bf16 activation
-          z[u] = sg[u] * __bfloat162float(zq);
-        }
-        fwht128(z, lane);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) z[u] *= kInvSqrtD;
+        q4_norm_rope(p.q_new + row * kHeadDim, p.q_norm_w, p.eps, kc, lane, z);
+        q4_rotate_query(z, kc, lane);
       }
       uint32_t h[2], l[2];
 #pragma unroll
@@ -223,13 +249,13 @@ __global__ void __launch_bounds__(256) q4_prologue_kernel(const Q4PrologueParams
       const long long nrow = static_cast<long long>(b) * p.Hkv + kv;
       float z[4];
       if (is_k) {
-        norm_rope(p.k_new + nrow * kHeadDim, p.k_norm_w, z);
+        q4_norm_rope(p.k_new + nrow * kHeadDim, p.k_norm_w, p.eps, kc, lane, z);
       } else {
         unpack4(reinterpret_cast<const uint2 *>(p.v_new + nrow * kHeadDim)[lane], z);
       }
       uint32_t packed;
       float sigma;
-      quantize(z, packed, sigma);
+      q4_quantize(z, kc, lane, packed, sigma);
       const long long crow_kv = crow * p.Hkv + kv;
       uint8_t *dst = (is_k ? p.k_idx : p.v_idx) + crow_kv * 64;
       if (lane < 16) reinterpret_cast<uint32_t *>(dst)[lane] = packed;
@@ -258,6 +284,144 @@ __device__ __forceinline__ void q4_locate(const uint32_t *pre, const int32_t *Ls
 }
 
 }  // namespace
+
+// One 64-token index tile of the 4-bit recurrence for a warp's G heads: kt holds the K and
+// V index tiles ([64 tokens][64 bytes] each), sk / sv the tokens' sigma_K * scale (log2
+// domain) and sigma_V for this lane's 8 tokens (16 mt + lane / 4 + 8 h), 0 past the
+// length.  S = C_K q~^T with q~ as bf16 hi + lo, the online-softmax update of (m, l, O~)
+// and O~^T += C_V^T (P sigma_V)^T, with the mma fragments built from pair-table lookups
+// (the dim orders are described at the consumer loop of q4_attn_kernel).
+template <int NT>
+__device__ __forceinline__ void q4_tile_update(const uint8_t *kt, int valid, const float (&sk)[4][2],
+                                               const float (&sv)[4][2], uint32_t tbl_lane, int lane,
+                                               const uint32_t (&qh)[8][NT][2], const uint32_t (&ql)[8][NT][2],
+                                               float (&o)[8][NT][4], float (&m_run)[NT][2], float (&l_run)[NT][2]) {
+  const int r8 = lane >> 2, c4 = lane & 3;
+  auto pair_entry = [&](uint32_t w, int k) {
+    const uint32_t e = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
+    uint32_t v;
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tbl_lane + (e << 7)));
+    return v;
+  };
+  const uint8_t *vt = kt + kQ4TileBytes;
+
+  // S^T = C_K q~^T (hi and lo parts of q~; with one head block in two accumulators, so
+  // that the two mma chains interleave): 4 token blocks of 16 x NT head blocks of 8
+  float sacc[4][NT][4], sacl[4][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sacl[mt][nt][e] = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    // tokens 16 mt + r (A rows 0-7) and + 8 (rows 8-15), index bytes 16 c .. 16 c + 15
+    const uint4 w0 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8) * 64 + 16 * c4);
+    const uint4 w1 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8 + 8) * 64 + 16 * c4);
+    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int wd = ks >> 1, k0 = 2 * (ks & 1);  // bytes 2 ks and 2 ks + 1
+      const uint32_t a0 = pair_entry(x0[wd], k0), a2 = pair_entry(x0[wd], k0 + 1);
+      const uint32_t a1 = pair_entry(x1[wd], k0), a3 = pair_entry(x1[wd], k0 + 1);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
+        mma_bf16(NT == 1 ? sacl[mt][nt] : sacc[mt][nt], a0, a1, a2, a3, ql[ks][nt][0], ql[ks][nt][1]);
+      }
+    }
+  }
+  if constexpr (NT == 1) {
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[mt][0][e] += sacl[mt][0][e];
+  }
+
+  // sigma_K * scale (log2 domain) per token, and the mask past the length
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
+        sacc[mt][nt][e] = tok < valid ? sacc[mt][nt][e] * sk[mt][e >> 1] : -INFINITY;
+      }
+  // online-softmax update per head column
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sacc[mt][nt][jj], sacc[mt][nt][jj + 2]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run[nt][jj], mx);
+      const float corr = fast_exp2(m_run[nt][jj] - m_new);  // 0 on the first tile
+      m_run[nt][jj] = m_new;
+      l_run[nt][jj] *= corr;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        o[md][nt][jj] *= corr;
+        o[md][nt][jj + 2] *= corr;
+      }
+    }
+  // P = 2^(s - m) (l sums P), then P sigma_V split into bf16 hi + lo, transposed into B
+  // fragments of (P sigma_V)^T
+  uint32_t ph[4][NT][2], pl[4][NT][2];
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pe = fast_exp2(sacc[mt][nt][e] - m_run[nt][e & 1]);
+        l_run[nt][e & 1] += pe;
+        pv[e] = pe * sv[mt][e >> 1];
+      }
+      const uint32_t h01 = pack_bf16(pv[0], pv[1]), h23 = pack_bf16(pv[2], pv[3]);
+      const uint32_t l01 = pack_bf16(pv[0] - bf16_lo_to_float(h01), pv[1] - bf16_hi_to_float(h01));
+      const uint32_t l23 = pack_bf16(pv[2] - bf16_lo_to_float(h23), pv[3] - bf16_hi_to_float(h23));
+      ph[mt][nt][0] = movmatrix_t(h01);
+      ph[mt][nt][1] = movmatrix_t(h23);
+      pl[mt][nt][0] = movmatrix_t(l01);
+      pl[mt][nt][1] = movmatrix_t(l23);
+    }
+  // O~^T += C_V^T (P sigma_V)^T: 4 token k-steps x 8 dim blocks of 16 (rows 8 r + md and
+  // 64 + 8 r + md); tokens t0, t0 + 1 (k-slots 2 c, +1) and t0 + 8, t0 + 9 (slots + 8)
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    const int t0 = 16 * mt + 2 * c4;
+    const uint8_t *vr = vt + t0 * 64 + 8 * r8;
+    const uint2 y0 = *reinterpret_cast<const uint2 *>(vr), y1 = *reinterpret_cast<const uint2 *>(vr + 64);
+    const uint2 y2 = *reinterpret_cast<const uint2 *>(vr + 8 * 64), y3 = *reinterpret_cast<const uint2 *>(vr + 9 * 64);
+#pragma unroll
+    for (int hw = 0; hw < 2; ++hw) {
+      const uint32_t u0 = hw ? y0.y : y0.x, u1 = hw ? y1.y : y1.x, u2 = hw ? y2.y : y2.x, u3 = hw ? y3.y : y3.x;
+      // byte m of each: entry (nibble of token t) | (same nibble of token t + 1) << 4
+      const uint32_t lo01 = (u0 & 0x0f0f0f0fu) | ((u1 << 4) & 0xf0f0f0f0u);
+      const uint32_t hi01 = ((u0 >> 4) & 0x0f0f0f0fu) | (u1 & 0xf0f0f0f0u);
+      const uint32_t lo23 = (u2 & 0x0f0f0f0fu) | ((u3 << 4) & 0xf0f0f0f0u);
+      const uint32_t hi23 = ((u2 >> 4) & 0x0f0f0f0fu) | (u3 & 0xf0f0f0f0u);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int md = 4 * hw + m;
+        const uint32_t a0 = pair_entry(lo01, m), a1 = pair_entry(hi01, m);
+        const uint32_t a2 = pair_entry(lo23, m), a3 = pair_entry(hi23, m);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
+          mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
+        }
+      }
+    }
+  }
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kThreadsAttn, 1)
@@ -408,12 +572,6 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
   // permute, then one shift-add onto the lane's 32-bit shared address.  The table is
   // constant after the start-up barrier, so the load is a plain (reorderable) asm.
   const uint32_t tbl_lane = smem_addr(cpair) + 4u * lane;
-  auto pair_entry = [&](uint32_t w, int k) {
-    const uint32_t e = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
-    uint32_t v;
-    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tbl_lane + (e << 7)));
-    return v;
-  };
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -515,129 +673,427 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
         sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
       }
-    const uint8_t *kt = smem + kQ4OffStage + s * kQ4StageBytes;  // [64 tokens][64 index bytes]
-    const uint8_t *vt = kt + kQ4TileBytes;
-
-    // S^T = C_K q~^T (hi and lo parts of q~; with one head block in two accumulators, so
-    // that the two mma chains interleave): 4 token blocks of 16 x NT head blocks of 8
-    float sacc[4][NT][4], sacl[4][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sacl[mt][nt][e] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      // tokens 16 mt + r (A rows 0-7) and + 8 (rows 8-15), index bytes 16 c .. 16 c + 15
-      const uint4 w0 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8) * 64 + 16 * c4);
-      const uint4 w1 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8 + 8) * 64 + 16 * c4);
-      const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int wd = ks >> 1, k0 = 2 * (ks & 1);  // bytes 2 ks and 2 ks + 1
-        const uint32_t a0 = pair_entry(x0[wd], k0), a2 = pair_entry(x0[wd], k0 + 1);
-        const uint32_t a1 = pair_entry(x1[wd], k0), a3 = pair_entry(x1[wd], k0 + 1);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
-          mma_bf16(NT == 1 ? sacl[mt][nt] : sacc[mt][nt], a0, a1, a2, a3, ql[ks][nt][0], ql[ks][nt][1]);
-        }
-      }
-    }
-    if constexpr (NT == 1) {
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][0][e] += sacl[mt][0][e];
-    }
-
-    // sigma_K * scale (log2 domain) per token, and the mask past the length
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = 16 * mt + (lane >> 2) + ((e >> 1) << 3);
-          sacc[mt][nt][e] = tok < valid ? sacc[mt][nt][e] * sk[mt][e >> 1] : -INFINITY;
-        }
-    // online-softmax update per head column
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(sacc[mt][nt][jj], sacc[mt][nt][jj + 2]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float m_new = fmaxf(m_run[nt][jj], mx);
-        const float corr = fast_exp2(m_run[nt][jj] - m_new);  // 0 on the first tile
-        m_run[nt][jj] = m_new;
-        l_run[nt][jj] *= corr;
-#pragma unroll
-        for (int md = 0; md < 8; ++md) {
-          o[md][nt][jj] *= corr;
-          o[md][nt][jj + 2] *= corr;
-        }
-      }
-    // P = 2^(s - m) (l sums P), then P sigma_V split into bf16 hi + lo, transposed into B
-    // fragments of (P sigma_V)^T
-    uint32_t ph[4][NT][2], pl[4][NT][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pe = fast_exp2(sacc[mt][nt][e] - m_run[nt][e & 1]);
-          l_run[nt][e & 1] += pe;
-          pv[e] = pe * sv[mt][e >> 1];
-        }
-        const uint32_t h01 = pack_bf16(pv[0], pv[1]), h23 = pack_bf16(pv[2], pv[3]);
-        const uint32_t l01 = pack_bf16(pv[0] - bf16_lo_to_float(h01), pv[1] - bf16_hi_to_float(h01));
-        const uint32_t l23 = pack_bf16(pv[2] - bf16_lo_to_float(h23), pv[3] - bf16_hi_to_float(h23));
-        ph[mt][nt][0] = movmatrix_t(h01);
-        ph[mt][nt][1] = movmatrix_t(h23);
-        pl[mt][nt][0] = movmatrix_t(l01);
-        pl[mt][nt][1] = movmatrix_t(l23);
-      }
-    // O~^T += C_V^T (P sigma_V)^T: 4 token k-steps x 8 dim blocks of 16 (rows 8 r + md and
-    // 64 + 8 r + md); tokens t0, t0 + 1 (k-slots 2 c, +1) and t0 + 8, t0 + 9 (slots + 8)
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const int t0 = 16 * mt + 2 * c4;
-      const uint8_t *vr = vt + t0 * 64 + 8 * r8;
-      const uint2 y0 = *reinterpret_cast<const uint2 *>(vr), y1 = *reinterpret_cast<const uint2 *>(vr + 64);
-      const uint2 y2 = *reinterpret_cast<const uint2 *>(vr + 8 * 64), y3 = *reinterpret_cast<const uint2 *>(vr + 9 * 64);
-#pragma unroll
-      for (int hw = 0; hw < 2; ++hw) {
-        const uint32_t u0 = hw ? y0.y : y0.x, u1 = hw ? y1.y : y1.x, u2 = hw ? y2.y : y2.x, u3 = hw ? y3.y : y3.x;
-        // byte m of each: entry (nibble of token t) | (same nibble of token t + 1) << 4
-        const uint32_t lo01 = (u0 & 0x0f0f0f0fu) | ((u1 << 4) & 0xf0f0f0f0u);
-        const uint32_t hi01 = ((u0 >> 4) & 0x0f0f0f0fu) | (u1 & 0xf0f0f0f0u);
-        const uint32_t lo23 = (u2 & 0x0f0f0f0fu) | ((u3 << 4) & 0xf0f0f0f0u);
-        const uint32_t hi23 = ((u2 >> 4) & 0x0f0f0f0fu) | (u3 & 0xf0f0f0f0u);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int md = 4 * hw + m;
-          const uint32_t a0 = pair_entry(lo01, m), a1 = pair_entry(hi01, m);
-          const uint32_t a2 = pair_entry(lo23, m), a3 = pair_entry(hi23, m);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
-            mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
-          }
-        }
-      }
-    }
+    q4_tile_update<NT>(smem + kQ4OffStage + s * kQ4StageBytes, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run,
+                       l_run);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));  // the stage's index tiles are consumed
   }
   if (cur_seg >= 0) flush(cur_seg);
+}
+
+// ------------------------------------------------------------------ single-launch form
+// The whole 4-bit step in one launch, as the bf16 step's single-launch form (attention.cu):
+// one thread-block cluster of C CTAs per (sequence, KV head), CTA rank r streaming the
+// segment's index tiles r, r + C, ...  The prologue is folded in: the consumer warps
+// compute the segment's rotated queries q~ into shared memory, and an ordering warp
+// quantizes the new k and v rows, hands them to the consumer whose tile holds them, waits
+// on the preceding kernel, appends them, fences them and lets the next kernel launch.  The
+// merge is partitioned by query head (CTA q owns the heads g with g mod C = q): every CTA
+// pushes its partial of a head to the head's owner with remote st.async stores counted on
+// the owner's mbarrier, and the owner merges the C contributions, rotates the row back
+// (R^T: a Walsh-Hadamard transform across a warp) and writes it in bf16.  The ordering and
+// cluster protocol are the bf16 kernel's: only the global writes (the append and `out`)
+// wait on the preceding kernel, no thread leaves early, every mbarrier wait is bounded.
+namespace {
+constexpr int kQ4COrderWarp = kConsumerWarps + 1;
+constexpr int kQ4CThreads = 32 * (kConsumerWarps + 2);
+constexpr int kQ4CPartStride = 132;                                       // floats per (warp, head) row
+constexpr int kQ4COffStage = 0;                                           // [12][K, V][64 tokens][64 B]
+constexpr int kQ4COffPair = kQ4COffStage + kQ4Stages * kQ4StageBytes;     // pair table, 32 copies
+constexpr int kQ4COffScale = kQ4COffPair + kQ4PairBytes;                  // [12][K, V][64] fp32
+constexpr int kQ4COffInfo = kQ4COffScale + kQ4Stages * 2 * kTile * 4;     // [12] page inside the pool
+constexpr int kQ4COffQ = kQ4COffInfo + 64;                                // [hi, lo][16][128] bf16 q~
+constexpr int kQ4COffNew = kQ4COffQ + 2 * GQA_MAX_GROUP * kHeadDim * 2;   // new K, V index rows, sigmas
+constexpr int kQ4COffRecv = kQ4COffNew + 256;                             // [C x owned][2] then [..][128]
+constexpr int kQ4CRecvRows = 2 * GQA_MAX_GROUP;                           // C x ceil(G / C) <= G + C - 1
+constexpr int kQ4COffBar = kQ4COffRecv + kQ4CRecvRows * (2 + kHeadDim) * 4;
+constexpr size_t kQ4CSmemBytes = 1024 + kQ4COffBar + 8 * (2 * kQ4Stages + 1);
+static_assert(kConsumerWarps * GQA_MAX_GROUP * kQ4CPartStride * 4 + 2 * kConsumerWarps * GQA_MAX_GROUP * 4 * 2 <=
+                  kQ4Stages * kQ4StageBytes,
+              "the merge's warp partials must fit in the ring");
+
+// Barrier 1: the ordering warp hands the new rows to the consumer whose tile holds them;
+// barrier 2: the consumer warps' rotated queries are in shared memory.
+__device__ __forceinline__ void q4c_newrow_arrive() { asm volatile("bar.arrive 1, 64;" ::: "memory"); }
+__device__ __forceinline__ void q4c_newrow_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+__device__ __forceinline__ void q4c_consumers_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+}
+// Heads of a segment owned by cluster rank q: g = q, q + C, ...
+__device__ __forceinline__ int q4c_owned(int G, int C, int q) { return q < G ? (G - q + C - 1) / C : 0; }
+}  // namespace
+
+template <int NT>
+__global__ void __launch_bounds__(kQ4CThreads, 1)
+    q4_cluster_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const Q4ClusterParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align_smem_1024(smem_raw);
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4COffBar);
+  uint64_t *empty_bar = full_bar + kQ4Stages;
+  uint64_t *recv_bar = empty_bar + kQ4Stages;
+  uint32_t *cpair = reinterpret_cast<uint32_t *>(smem + kQ4COffPair);  // [256][32]
+  float *scl = reinterpret_cast<float *>(smem + kQ4COffScale);        // [stage][2][64]
+  int *pinfo = reinterpret_cast<int *>(smem + kQ4COffInfo);           // [stage]
+  uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + kQ4COffQ);      // [2][16][128]
+  uint32_t *newrow = reinterpret_cast<uint32_t *>(smem + kQ4COffNew);  // K words [16], V words [16], sigmas
+  float *recv_ml = reinterpret_cast<float *>(smem + kQ4COffRecv);     // [C x owned][2]
+  float *recv_o = recv_ml + 2 * kQ4CRecvRows;                         // [C x owned][128]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = p.csize;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int seg = static_cast<int>(blockIdx.x) / C;
+  const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
+  const bool producer = warp == kConsumerWarps;
+
+  if (producer && lane == 0) {
+    for (int s = 0; s < kQ4Stages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1 + 32);  // the TMA issue + one arrive per producer lane
+      mbar_init(smem_addr(&empty_bar[s]), 1);
+    }
+    mbar_init(smem_addr(recv_bar), 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  for (int e = tid; e < 256 * 32; e += kQ4CThreads) {
+    const int v = e >> 5;
+    cpair[e] = static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
+  }
+  int L = p.seq_lens[b], pos = p.positions[b];
+  const int nt = tiles_of(L, p.max_seq);
+  if (nt == 0) {
+    if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_SEQLEN);
+    L = 0;
+    pos = -1;
+  } else if (pos < 0 || pos >= L) {
+    if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_POSITION);
+    pos = -1;
+  }
+  const int n = nt > rank ? (nt - rank + C - 1) / C : 0;  // local tile i is segment tile rank + C i
+  int owner = -1;  // the consumer warp whose tile holds the new token
+  if (pos >= 0 && (pos >> 6) % C == rank) owner = ((pos >> 6) / C) % kConsumerWarps;
+  __syncthreads();   // barriers and the pair table ready in the CTA
+  cluster_arrive();  // ... and the receive barrier for the cluster
+
+  const uint32_t tbl_lane = smem_addr(cpair) + 4u * lane;
+  float o[8][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+  for (int md = 0; md < 8; ++md)
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[md][t][e] = 0.f;
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      m_run[t][jj] = -INFINITY;
+      l_run[t][jj] = 0.f;
+    }
+
+  if (warp == kQ4COrderWarp) {
+    // ------------------------------------------------------------------ ordering warp
+    Q4RowConsts kc;
+    uint32_t pk = 0, pv = 0;
+    float sgk = 0.f, sgv = 0.f;
+    long long crow = -1;
+    if (owner >= 0) {
+      q4_row_consts(p.rope_tab32, pos, p.signs, p.codebook, lane, kc);
+      const long long nrow = static_cast<long long>(b) * p.Hkv + kv;
+      float z[4];
+      q4_norm_rope(p.k_new + nrow * kHeadDim, p.k_norm_w, p.eps, kc, lane, z);
+      q4_quantize(z, kc, lane, pk, sgk);
+      unpack4(reinterpret_cast<const uint2 *>(p.v_new + nrow * kHeadDim)[lane], z);
+      q4_quantize(z, kc, lane, pv, sgv);
+      if (lane < 16) {
+        newrow[lane] = pk;
+        newrow[16 + lane] = pv;
+      }
+      if (lane == 0) {
+        newrow[32] = __float_as_uint(sgk);
+        newrow[33] = __float_as_uint(sgv);
+      }
+      if (p.paged) {
+        const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + (pos >> 6)];
+        if (pg >= 0 && pg < p.num_blocks) crow = static_cast<long long>(pg) * kTile + (pos & (kTile - 1));
+      } else {
+        crow = static_cast<long long>(b) * p.max_seq + pos;
+      }
+      q4c_newrow_arrive();
+    }
+    griddep_wait();
+    if (crow >= 0) {
+      const long long r = crow * p.Hkv + kv;
+      if (lane < 16) {
+        reinterpret_cast<uint32_t *>(p.k_idx + r * 64)[lane] = pk;
+        reinterpret_cast<uint32_t *>(p.v_idx + r * 64)[lane] = pv;
+      }
+      if (lane == 0) {
+        p.k_scale[r] = sgk;
+        p.v_scale[r] = sgv;
+      }
+      __threadfence();
+    }
+    __syncwarp();
+    if (lane == 0) griddep_launch_dependents();
+  } else if (producer) {
+    // ---------------------------------------------------------------- producer warp
+    // Index tiles by TMA; each lane copies the scales of tokens l and l + 32 (inside the
+    // sequence) with cp.async, whose arrivals complete the stage with the TMA bytes.
+    bool ok = true;
+    int issued = 0;
+    for (int i0 = 0; i0 < n && ok; i0 += 32) {
+      int mrow = -kTile, mok = 0;
+      if (i0 + lane < n) {
+        const int j = rank + C * (i0 + lane);
+        if (p.paged) {
+          const int pg = p.page_table[static_cast<long long>(b) * p.max_blocks + j];
+          if (pg >= 0 && pg < p.num_blocks) mrow = pg * kTile, mok = 1;
+          else atomicOr(p.err, GQA_DEVERR_PAGE);
+        } else {
+          mrow = b * p.max_seq + j * kTile;
+          mok = 1;
+        }
+      }
+      const int cnt = n - i0 < 32 ? n - i0 : 32;
+      for (int u = 0; u < cnt; ++u) {
+        const int i = i0 + u;
+        const int row = __shfl_sync(0xffffffffu, mrow, u), pok = __shfl_sync(0xffffffffu, mok, u);
+        const int valid = min(kTile, L - (rank + C * i) * kTile);
+        const int s = i % kQ4Stages;
+        if (i >= kQ4Stages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kQ4Stages) - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint32_t fb = smem_addr(&full_bar[s]);
+        if (lane == 0) {
+          pinfo[s] = pok;
+          const uint32_t base = smem_addr(smem + kQ4COffStage + s * kQ4StageBytes);
+          mbar_arrive_expect_tx(fb, kQ4StageBytes);
+          tma_load_3d(base, &tmK, fb, 0, kv, row);
+          tma_load_3d(base + kQ4TileBytes, &tmV, fb, 0, kv, row);
+        }
+        const uint32_t sdst = smem_addr(scl + s * 2 * kTile);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tok = lane + 32 * hh;
+          if (tok < valid && pok) {
+            const long long r = (static_cast<long long>(row) + tok) * p.Hkv + kv;
+            cp_async4(sdst + 4 * tok, p.k_scale + r);
+            cp_async4(sdst + 4 * (kTile + tok), p.v_scale + r);
+          }
+        }
+        cp_async_arrive_noinc(fb);
+        issued = i + 1;
+      }
+    }
+    if (lane == 0 && !ok) {
+      atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+      for (int ii = (issued > kQ4Stages ? issued - kQ4Stages : 0); ii < issued; ++ii)
+        (void)mbar_wait(smem_addr(&full_bar[ii % kQ4Stages]), static_cast<uint32_t>((ii / kQ4Stages) & 1));
+    }
+    cp_async_wait_all();
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ consumer warps
+    const int cw = warp, r8 = lane >> 2, c4 = lane & 3;
+    // the segment's rotated queries q~ (hi + lo), one head a warp at a time
+    {
+      Q4RowConsts kc;
+      q4_row_consts(p.rope_tab32, pos, p.signs, p.codebook, lane, kc);
+      for (int g = cw; g < p.G; g += kConsumerWarps) {
+        float z[4] = {0.f, 0.f, 0.f, 0.f};
+        if (pos >= 0) {
+          q4_norm_rope(p.q_new + (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim, p.q_norm_w, p.eps, kc,
+                       lane, z);
+          q4_rotate_query(z, kc, lane);
+        }
+        uint32_t h[2], l[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          h[u] = pack_bf16(z[2 * u], z[2 * u + 1]);
+          l[u] = pack_bf16(z[2 * u] - bf16_lo_to_float(h[u]), z[2 * u + 1] - bf16_hi_to_float(h[u]));
+        }
+        reinterpret_cast<uint2 *>(qbuf + g * kHeadDim)[lane] = make_uint2(h[0], h[1]);
+        reinterpret_cast<uint2 *>(qbuf + (GQA_MAX_GROUP + g) * kHeadDim)[lane] = make_uint2(l[0], l[1]);
+      }
+    }
+    q4c_consumers_sync();
+    uint32_t qh[8][NT][2], ql[8][NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int g = 8 * t + r8;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int j = 16 * c4 + 2 * ks + hf;  // dims j (low half) and j + 64 (high half)
+          uint32_t vh = 0u, vl = 0u;
+          if (g < p.G) {
+            vh = static_cast<uint32_t>(qbuf[g * kHeadDim + j]) | (static_cast<uint32_t>(qbuf[g * kHeadDim + j + 64]) << 16);
+            vl = static_cast<uint32_t>(qbuf[(GQA_MAX_GROUP + g) * kHeadDim + j]) |
+                 (static_cast<uint32_t>(qbuf[(GQA_MAX_GROUP + g) * kHeadDim + j + 64]) << 16);
+          }
+          qh[ks][t][hf] = vh;
+          ql[ks][t][hf] = vl;
+        }
+    }
+    const int i_new = cw == owner ? (pos >> 6) / C : -1;
+    for (int i = cw; i < n; i += kConsumerWarps) {
+      const int s = i % kQ4Stages;
+      const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kQ4Stages) & 1));
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ready)) {
+        if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+        break;
+      }
+      const int valid = min(kTile, L - (rank + C * i) * kTile);
+      const bool page_ok = pinfo[s] != 0;
+      uint8_t *kt = smem + kQ4COffStage + s * kQ4StageBytes;
+      if (i == i_new) {  // the new row, from the ordering warp, into its place in the stage
+        q4c_newrow_sync();
+        const int r = pos & (kTile - 1);
+        if (lane < 16) {
+          reinterpret_cast<uint32_t *>(kt + r * 64)[lane] = newrow[lane];
+          reinterpret_cast<uint32_t *>(kt + kQ4TileBytes + r * 64)[lane] = newrow[16 + lane];
+        }
+        if (lane == 0) {
+          scl[s * 2 * kTile + r] = __uint_as_float(newrow[32]);
+          scl[s * 2 * kTile + kTile + r] = __uint_as_float(newrow[33]);
+        }
+        __syncwarp();
+      }
+      float sk[4][2], sv[4][2];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int tok = 16 * mt + r8 + 8 * hh;
+          const bool in = tok < valid && page_ok;
+          sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
+          sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
+        }
+      q4_tile_update<NT>(kt, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run, l_run);
+      if (i == i_new) fence_proxy_async_smem();  // generic writes precede the next TMA into the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+    }
+  }
+
+  // ------------------------------------------------------------------ merge
+  float *wpart = reinterpret_cast<float *>(smem);                           // [6][16][132]
+  float *wml = wpart + kConsumerWarps * GQA_MAX_GROUP * kQ4CPartStride;     // [6][16][2]
+  float *wm = wml + kConsumerWarps * GQA_MAX_GROUP * 2;                     // [6][16]
+  __syncthreads();  // every issued tile has been consumed: the ring is free
+  const bool consumer = !producer && warp != kQ4COrderWarp;
+  if (consumer) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int g = 8 * t + 2 * lane + jj;
+        if (lane < 4 && g < p.G) wm[warp * GQA_MAX_GROUP + g] = m_run[t][jj];
+      }
+  }
+  __syncthreads();
+  if (consumer) {
+    const int cw = warp;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int g = 8 * t + 2 * (lane & 3) + jj;
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, wm[c * GQA_MAX_GROUP + (g < p.G ? g : 0)]);
+        const float f = m_run[t][jj] == -INFINITY ? 0.f : exp2f(m_run[t][jj] - M);
+        float l = l_run[t][jj] * f;
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (lane < 4 && g < p.G) {
+          wml[(cw * GQA_MAX_GROUP + g) * 2 + 0] = M;
+          wml[(cw * GQA_MAX_GROUP + g) * 2 + 1] = l;
+        }
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          o[md][t][jj] *= f;
+          o[md][t][jj + 2] *= f;
+        }
+      }
+#pragma unroll
+    for (int md = 0; md < 8; ++md)
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int g = 8 * t + 2 * (lane & 3) + (e & 1);
+          const int d = ((e >> 1) << 6) + 8 * (lane >> 2) + md;  // natural dim order
+          if (g < p.G) wpart[(cw * GQA_MAX_GROUP + g) * kQ4CPartStride + d] = o[md][t][e];
+        }
+  }
+  __syncthreads();
+  const int own = q4c_owned(p.G, C, rank);
+  const uint32_t bar_local = smem_addr(recv_bar);
+  if (tid == 0) mbar_arrive_expect_tx(bar_local, static_cast<uint32_t>(C * own * (8 + 4 * kHeadDim)));
+  cluster_wait();  // every CTA of the cluster has initialised its barriers
+  for (int e = tid; e < p.G * kHeadDim; e += kQ4CThreads) {
+    const int g = e >> 7, d = e & (kHeadDim - 1);
+    const int q = g % C, slot = g / C, own_q = q4c_owned(p.G, C, q);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) acc += wpart[(c * GQA_MAX_GROUP + g) * kQ4CPartStride + d];
+    const uint32_t bar_q = mapa_shared(bar_local, q);
+    const int rrow = rank * own_q + slot;
+    st_async_f32(mapa_shared(smem_addr(recv_o + rrow * kHeadDim + d), q), acc, bar_q);
+    if (d == 0) {
+      float den = 0.f;
+#pragma unroll
+      for (int c = 0; c < kConsumerWarps; ++c) den += wml[(c * GQA_MAX_GROUP + g) * 2 + 1];
+      st_async_v2f32(mapa_shared(smem_addr(recv_ml + rrow * 2), q), wml[g * 2], den, bar_q);
+    }
+  }
+  const bool got = mbar_wait(bar_local, 0);
+  if (!got && lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+  cluster_arrive_relaxed();  // this CTA has received everything (or given up)
+  griddep_wait();
+  // the owned heads: merge, rotate back (R^T o = D H o / sqrt(d)) and write; a warp a head
+  for (int slot = warp; slot < own; slot += kQ4CThreads / 32) {
+    const int g = rank + C * slot;
+    float M = -INFINITY;
+#pragma unroll 1
+    for (int r = 0; r < C; ++r) M = fmaxf(M, recv_ml[(r * own + slot) * 2]);
+    float v[4] = {0.f, 0.f, 0.f, 0.f}, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll 1
+      for (int r = 0; r < C; ++r) {
+        const int rr = r * own + slot;
+        const float f = exp2f(recv_ml[rr * 2] - M);
+        const float4 x = reinterpret_cast<const float4 *>(recv_o + rr * kHeadDim)[lane];
+        v[0] = fmaf(f, x.x, v[0]);
+        v[1] = fmaf(f, x.y, v[1]);
+        v[2] = fmaf(f, x.z, v[2]);
+        v[3] = fmaf(f, x.w, v[3]);
+        den = fmaf(f, recv_ml[rr * 2 + 1], den);
+      }
+    }
+    const float inv = den > 0.f ? 1.0f / den : 0.f;  // zeros for an invalid length (flagged above)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] *= inv;
+    fwht128(v, lane);
+    const char4 s4 = reinterpret_cast<const char4 *>(p.signs)[lane];
+    const float sg[4] = {static_cast<float>(s4.x), static_cast<float>(s4.y), static_cast<float>(s4.z),
+                         static_cast<float>(s4.w)};
+    uint32_t w2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      w2[u] = pack_bf16(sg[2 * u] * v[2 * u] * kInvSqrtD, sg[2 * u + 1] * v[2 * u + 1] * kInvSqrtD);
+    reinterpret_cast<uint2 *>(p.out + (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim)[lane] =
+        make_uint2(w2[0], w2[1]);
+  }
+  cluster_wait();  // every CTA has received everything: no store to or from this CTA is in flight
 }
 
 size_t q4_attn_smem_bytes(int batch) {
@@ -648,7 +1104,32 @@ cudaError_t q4_configure() {
   const int bytes = static_cast<int>(q4_attn_smem_bytes(GQA_MAX_BATCH));
   cudaError_t e = cudaFuncSetAttribute(q4_attn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(q4_attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const int cbytes = static_cast<int>(kQ4CSmemBytes);
+  for (void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) : {q4_cluster_kernel<1>, q4_cluster_kernel<2>}) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
   return e;
+}
+
+cudaError_t launch_q4_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4ClusterParams &p, int npad,
+                              bool pdl, cudaStream_t stream) {
+  void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) = npad == 8 ? q4_cluster_kernel<1> : q4_cluster_kernel<2>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv * p.csize));
+  cfg.blockDim = dim3(kQ4CThreads);
+  cfg.dynamicSmemBytes = kQ4CSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k, tmK, tmV, p);
 }
 
 cudaError_t launch_q4_prologue(const Q4PrologueParams &p, bool pdl, cudaStream_t stream) {

@@ -100,7 +100,25 @@ struct Q4AttnParams {
   int B, Hq, Hkv, G, paged, max_seq, max_blocks, num_blocks;
   float scale_log2;
 };
+// The single-launch form of the 4-bit step (attention_q4.cu): prologue, attention and the
+// merge with unrotation in one kernel, a cluster of csize CTAs per (sequence, KV head).
+struct Q4ClusterParams {
+  const int32_t *seq_lens, *positions, *page_table;
+  const uint16_t *q_new, *k_new, *v_new;    // [B,Hq,d], [B,Hkv,d], [B,Hkv,d]
+  const uint16_t *q_norm_w, *k_norm_w;      // [d] or null
+  const float2 *rope_tab32;                 // [max_seq][64] (cos, sin), binary32
+  const int8_t *signs;                      // [d] +-1
+  const uint16_t *codebook;                 // [16] bf16 levels, ascending
+  uint8_t *k_idx, *v_idx;                   // [rows,Hkv,d/2] packed indices
+  float *k_scale, *v_scale;                 // [rows,Hkv]
+  uint16_t *out;                            // [B,Hq,d]
+  uint32_t *err;
+  int B, Hq, Hkv, G, paged, max_seq, max_blocks, num_blocks, csize;
+  float eps, scale_log2;
+};
 cudaError_t q4_configure();
+cudaError_t launch_q4_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4ClusterParams &p, int npad,
+                              bool pdl, cudaStream_t stream);
 // The 4-bit step's prologue reads the caller's inputs and the RoPE table before it waits on
 // the preceding kernel, so it is launched in plain stream order (`pdl` false) after a
 // RoPE table rebuild.

@@ -46,13 +46,17 @@ gqa_status_t gqa_q4_codebook(uint16_t *levels_bf16);
  *   rot_signs               int8 device [128], each +1 or -1 (the diagonal D of R)
  *   codebook                bf16 device [16] levels, ascending
  *   out                     bf16 device [B, H_q, 128]
- * Three launches (prologue: rotated queries and the appended rows; split-KV attention on
- * the index tiles; combine and unrotation), programmatic stream serialization as for
- * gqa_decode_attn: the prologue reads its inputs and the RoPE table and writes the
- * rotated queries and the new rows before it waits on the preceding kernel (it waits at
- * its end), so the same rule holds -- the kernel launched immediately before the call must
- * not write the call's inputs if it triggers programmatic completion early; after a RoPE
- * table rebuild the prologue is launched in plain stream order.  Errors: those of gqa_decode_attn; k_idx, v_idx 16-byte aligned,
+ * The plan's form decides the launches (gqa_plan_cluster_size): in the single-launch form
+ * one kernel per step (a cluster per (sequence, KV head); the rotated queries and the new
+ * rows computed in it, the partials merged and rotated back on chip; the new rows, and
+ * `out`, written only after the preceding kernel has completed); in the split-KV form three
+ * (prologue: rotated queries and the appended rows; split-KV attention on the index tiles;
+ * combine and unrotation).  Programmatic stream serialization as for gqa_decode_attn: the
+ * first kernel reads its inputs and the RoPE table before it waits on the preceding
+ * kernel (the split form's prologue also writes the rotated queries and the new rows, and
+ * waits at its end), so the same rule holds -- the kernel launched immediately before the
+ * call must not write the call's inputs if it triggers programmatic completion early;
+ * after a RoPE table rebuild the first kernel is launched in plain stream order.  Errors: those of gqa_decode_attn; k_idx, v_idx 16-byte aligned,
  * scales and signs 4-byte aligned, else GQA_ERR_INVALID_ARG.
  */
 gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan,

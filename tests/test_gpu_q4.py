@@ -48,9 +48,13 @@ def oracle_out_on(w, ref, pairs=None):
                                pairs=pairs)
 
 
-def run_gpu(w):
+# 0: the planner's form (the single-launch form for these small batches), -1: split-KV
+FORMS = [0, -1]
+
+
+def run_gpu(w, cluster_size=0):
     plan = binding.Plan(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
-                        seq_lens_host=w.seq_lens.cpu().numpy())
+                        seq_lens_host=w.seq_lens.cpu().numpy(), cluster_size=cluster_size)
     out = torch.full((w.B, w.Hq, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
     plan.run_q4(w, out)
     torch.cuda.synchronize()
@@ -119,18 +123,20 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("form", FORMS + [1, 2, 16])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_q4_parity(name):
+def test_q4_parity(name, form):
     B, Hq, Hkv, lens, max_seq, paged, norm = CASES[name]
     w = wl.make_q4(B, Hq, Hkv, lens, paged=paged, seed=21, qk_norm=norm, max_seq=max_seq, device="cuda", name=name)
     k0, v0, ks0, vs0 = np_u8(w.k_idx), np_u8(w.v_idx), np_u8(w.k_scale), np_u8(w.v_scale)
     ref = oracle_q4(w)
     assert ref["status"] == 0
-    plan, out = run_gpu(w)
+    plan, out = run_gpu(w, cluster_size=form)
+    name = f"{name} [C={plan.cluster_size}]"
     assert plan.device_errors() == 0
     assert check_appended(w, k0, v0, ks0, vs0, ref) <= 2
     want = oracle_out_on(w, ref)
-    if name == "single-token":
+    if name.startswith("single-token"):
         # a one-token context returns its dequantized v row itself, entries up to ~4, where
         # one bf16 rounding alone can exceed 1e-2: allow it per element (2^-7 |ref|)
         got = out.float().cpu().double().numpy()
@@ -155,25 +161,27 @@ def test_q4_full_size_ragged_on_sampled_heads():
     assert max_abs <= 1e-2 and rel <= 2e-3, (max_abs, rel)
 
 
-def test_q4_plan_reuse_and_determinism():
+@pytest.mark.parametrize("form", FORMS)
+def test_q4_plan_reuse_and_determinism(form):
     """Two calls on one plan with the same inputs give the same bits (the second rewrites
     the same rows)."""
     w = wl.make_q4(2, 40, 8, [300, 1000], paged=True, seed=23, max_seq=1024, device="cuda")
-    plan, out1 = run_gpu(w)
+    plan, out1 = run_gpu(w, cluster_size=form)
     out2 = torch.empty_like(out1)
     plan.run_q4(w, out2)
     torch.cuda.synchronize()
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-def test_q4_device_index_errors_are_flagged_not_faulted():
+@pytest.mark.parametrize("form", FORMS)
+def test_q4_device_index_errors_are_flagged_not_faulted(form):
     """Out-of-range positions, lengths and page ids set error bits and leave the other
     sequences' outputs as they were; a length beyond the capacity zeroes that sequence's
     output; nothing faults (the kernels bound-check; a page outside the pool reads as
     zeros, scales included)."""
     w = wl.make_q4(3, 10, 2, [100, 70, 5], paged=True, seed=24, max_seq=128, device="cuda")
     ref = oracle_q4(w)
-    plan, out = run_gpu(w)
+    plan, out = run_gpu(w, cluster_size=form)
     assert plan.device_errors() == 0
     want = oracle_out_on(w, ref)
     assert_out_close(out, want, "all valid")
@@ -202,13 +210,14 @@ def test_q4_device_index_errors_are_flagged_not_faulted():
     assert_out_close(out[0:1], want[0:1], "valid sequence beside a bad page")
 
 
-def test_q4_back_to_back_steps_match_the_oracle():
+@pytest.mark.parametrize("form", FORMS)
+def test_q4_back_to_back_steps_match_the_oracle(form):
     """Four autoregressive steps enqueued back to back on one plan and stream, with no host
     synchronisation between them: the lengths grow by one a step and every step brings
     fresh q/k/v.  Each step's output is compared with the oracle's attention over the cache
-    the kernels left (later steps append only past this step's length).  The prologue
-    writes the rotated queries and the new rows before its grid-dependency wait, so this
-    checks that no step's kernels run into the previous step's reads."""
+    the kernels left (later steps append only past this step's length).  Consecutive steps
+    overlap on the device, so this checks that no step's kernels run into the previous
+    step's reads and that each step sees the rows the previous one appended."""
     base = wl.make_q4(2, 40, 8, [130, 400], paged=True, seed=25, max_seq=448, device="cuda")
     gen = torch.Generator(device="cuda")
     gen.manual_seed(26)
@@ -220,7 +229,8 @@ def test_q4_back_to_back_steps_match_the_oracle():
                                          seq_lens=(base.seq_lens + s).contiguous(),
                                          positions=(base.positions + s).contiguous()))
     plan = binding.Plan(base.B, base.Hq, base.Hkv, base.max_seq, block_size=base.block_size,
-                        num_cache_blocks=base.num_blocks, seq_lens_host=base.seq_lens.cpu().numpy())
+                        num_cache_blocks=base.num_blocks, seq_lens_host=base.seq_lens.cpu().numpy(),
+                        cluster_size=form)
     outs = [torch.full((base.B, base.Hq, base.d), float("nan"), dtype=torch.bfloat16, device="cuda")
             for _ in steps]
     torch.cuda.synchronize()
