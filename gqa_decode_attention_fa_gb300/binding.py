@@ -73,6 +73,8 @@ def load(build: bool = True):
         lib.gqa_plan_num_workers.restype = I
         lib.gqa_plan_describe.argtypes = [ctypes.POINTER(PlanDesc), P, I, P, P, P, P]
         lib.gqa_plan_describe.restype = I
+        lib.gqa_plan_set_ordered_start.argtypes = [P, I]
+        lib.gqa_plan_set_ordered_start.restype = I
         lib.gqa_plan_num_splits.argtypes = [P]
         lib.gqa_plan_num_splits.restype = I
         lib.gqa_plan_cluster_size.argtypes = [P]
@@ -269,6 +271,10 @@ class Plan:
     @property
     def num_workers(self) -> int:
         return self._lib.gqa_plan_num_workers(self._h)
+
+    def set_ordered_start(self, ordered: bool = True):
+        """Launch each step's first kernel in plain stream order (gqa_plan_set_ordered_start)."""
+        _check(self._lib.gqa_plan_set_ordered_start(self._h, int(bool(ordered))), "gqa_plan_set_ordered_start")
 
     @property
     def num_splits(self) -> int:

@@ -17,6 +17,9 @@ struct gqa_plan {
   int G = 0, npad = 0, W = 0, num_sms = 0, max_blocks = 0, combine_split = 1;
   int csize = 0;   // single-launch form: CTAs per (sequence, KV head) cluster; 0: split-KV + combine
   int spec_tiles = 0;  // tiles of the longest segment as planned
+  // launch the first kernel of a step in plain stream order (it then starts only once the
+  // preceding kernel has completed), for callers whose preceding kernels trigger early
+  bool ordered_first = false;
   int nsplit = 0;  // KV splits of the longest (sequence, KV head) segment
   long long num_rows = 0;
   void *ws = nullptr;
@@ -291,9 +294,9 @@ gqa_status_t run_attention(const gqa_plan_t *plan, const void *q, const void *k,
     p.csize = plan->csize;
     p.spec_tiles = plan->spec_tiles;
     p.spec = nullptr;
-    e = launch_attention_cluster(tk, tv, p, plan->npad, !rebuilt, stream);
+    e = launch_attention_cluster(tk, tv, p, plan->npad, !rebuilt && !plan->ordered_first, stream);
   } else {
-    e = launch_attention(tk, tv, p, plan->npad, plan->W, !rebuilt, stream);
+    e = launch_attention(tk, tv, p, plan->npad, plan->W, !rebuilt && !plan->ordered_first, stream);
   }
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -552,6 +555,12 @@ gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_l
   return GQA_OK;
 }
 
+gqa_status_t gqa_plan_set_ordered_start(gqa_plan_t *plan, int ordered) {
+  if (!plan) return GQA_ERR_INVALID_ARG;
+  plan->ordered_first = ordered != 0;
+  return GQA_OK;
+}
+
 int gqa_plan_num_workers(const gqa_plan_t *plan) { return plan ? plan->W : 0; }
 
 int gqa_plan_num_splits(const gqa_plan_t *plan) { return plan ? plan->nsplit : 0; }
@@ -778,7 +787,8 @@ extern "C" gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan, const void *q
     cp.csize = plan->csize;
     cp.eps = eps;
     cp.scale_log2 = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(kHeadDim)));
-    return launch_q4_cluster(tk, tv, cp, plan->npad, !rebuilt, s) == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    return launch_q4_cluster(tk, tv, cp, plan->npad, !rebuilt && !plan->ordered_first, s) == cudaSuccess ? GQA_OK
+                                                                                                    : GQA_ERR_CUDA;
   }
 
   Q4PrologueParams pp;
@@ -809,7 +819,7 @@ extern "C" gqa_status_t gqa_decode_attn_q4(const gqa_plan_t *plan, const void *q
   pp.max_blocks = plan->max_blocks;
   pp.num_blocks = paged ? d.num_cache_blocks : 0;
   pp.eps = eps;
-  if (launch_q4_prologue(pp, !rebuilt, s) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_q4_prologue(pp, !rebuilt && !plan->ordered_first, s) != cudaSuccess) return GQA_ERR_CUDA;
 
   Q4AttnParams ap;
   memset(&ap, 0, sizeof ap);

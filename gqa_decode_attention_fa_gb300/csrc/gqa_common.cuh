@@ -211,6 +211,14 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// Bulk copy global -> this CTA's shared memory of `bytes` (both addresses 16-byte aligned,
+// a multiple of 16 bytes), completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)

@@ -70,6 +70,8 @@ constexpr int kPfMaxSplit = 4;                  // KV parts of one split query t
 // A partial is column-major, [130][128 rows] floats: O columns, then m, then l, so that the
 // softmax warps (thread = row) write and read it in coalesced 128-byte lines.
 constexpr int kPartFloats = (kHeadDim + 2) * kPfRows;
+// The prologue holds a token's H_q + 2 H_kv rows in shared memory (256 B each).
+constexpr int kRopeMaxSmem = 200 * 1024;
 static_assert(kPfCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two prefill CTAs must share an SM");
 static_assert(kPfCtasPerSm * kPfTmemCols <= 512, "tensor memory of the co-resident CTAs");
 
@@ -114,41 +116,64 @@ __device__ __forceinline__ long long cache_row_of(const PrefillParams &p, int b,
 }  // namespace
 
 // ------------------------------------------------------------------------------ prologue
-// One CTA per chunk token (blockIdx.x = b * T + i); warp w rotates rows w, w + 8, ... of
-// the token's H_q query heads followed by its H_kv key heads (lane l holds dims l + 32 t).
+// One CTA per chunk token (blockIdx.x = b * T + i).  The token's query, key and value rows
+// are contiguous in q/k/v_new, so one bulk copy each brings them into shared memory while
+// the CTA computes cos/sin of the token's position; then warp w rotates rows w, w + 8, ...
+// of the H_q query heads followed by the H_kv key heads (lane l holds dims l + 32 t) from
+// shared memory.  The inputs are read before the wait on the preceding kernel; `out` and the
+// cache are written after it.
 __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p) {
   __shared__ float4 cs[kHeadDim / 2];  // (cos_hi, sin_hi, cos_lo, sin_lo) of pair i
-  griddep_wait();
+  __shared__ __align__(8) uint64_t rows_bar;
+  extern __shared__ __align__(16) uint8_t rope_rows[];  // [H_q + 2 H_kv][128] bf16: q, k, v rows
   griddep_launch_dependents();
   const int b = blockIdx.x / p.T, i = blockIdx.x - b * p.T;
-  if (blockIdx.x == 0)  // the merge tickets start at zero (a merge also returns its ticket to zero)
-    for (int r = threadIdx.x; r < p.ntail; r += blockDim.x) p.ticket[r] = 0;
   const int s = p.q_start[b];
-  if (!chunk_ok(p, s)) {
-    // a chunk outside [0, max_seq_len): flagged, nothing appended, zeros for its output
-    // (the attention kernel gives it no work)
-    if (i == 0 && threadIdx.x == 0) atomicOr(p.err, s < 0 ? GQA_DEVERR_POSITION : GQA_DEVERR_SEQLEN);
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<long long>(b) * p.T + i) * p.Hq * kHeadDim);
-    for (int c = threadIdx.x; c < p.Hq * kHeadDim / 8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
-    return;
+  const bool ok = chunk_ok(p, s);
+  const long long tok = static_cast<long long>(b) * p.T + i;
+  const uint32_t qbytes = static_cast<uint32_t>(p.Hq) * kHeadDim * 2, kvbytes = static_cast<uint32_t>(p.Hkv) * kHeadDim * 2;
+  const uint32_t bar = smem_addr(&rows_bar);
+  if (threadIdx.x == 0 && ok) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, qbytes + 2 * kvbytes);
+    bulk_load(smem_addr(rope_rows), p.q_new + tok * p.Hq * kHeadDim, qbytes, bar);
+    bulk_load(smem_addr(rope_rows) + qbytes, p.k_new + tok * p.Hkv * kHeadDim, kvbytes, bar);
+    bulk_load(smem_addr(rope_rows) + qbytes + kvbytes, p.v_new + tok * p.Hkv * kHeadDim, kvbytes, bar);
   }
   const int pos = s + i;
-  if (threadIdx.x < kHeadDim / 2) {
+  if (ok && threadIdx.x < kHeadDim / 2) {
     double sv, cv;
     sincos(static_cast<double>(pos) * p.inv_freq[threadIdx.x], &sv, &cv);
     const float ch = static_cast<float>(cv), sh = static_cast<float>(sv);
     cs[threadIdx.x] = make_float4(ch, sh, static_cast<float>(cv - ch), static_cast<float>(sv - sh));
   }
-  __syncthreads();
+  griddep_wait();  // `out` and the cache rows are written below
+  if (blockIdx.x == 0)  // the merge tickets start at zero (a merge also returns its ticket to zero)
+    for (int r = threadIdx.x; r < p.ntail; r += blockDim.x) p.ticket[r] = 0;
+  if (!ok) {
+    // a chunk outside [0, max_seq_len): flagged, nothing appended, zeros for its output
+    // (the attention kernel gives it no work)
+    if (i == 0 && threadIdx.x == 0) atomicOr(p.err, s < 0 ? GQA_DEVERR_POSITION : GQA_DEVERR_SEQLEN);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out + tok * p.Hq * kHeadDim);
+    for (int c = threadIdx.x; c < p.Hq * kHeadDim / 8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  __syncthreads();  // cos/sin (and the barrier's initialisation) visible
+  const bool landed = mbar_wait(bar, 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long tok = static_cast<long long>(b) * p.T + i;
+  if (!__all_sync(0xffffffffu, landed)) {  // the row copies never arrived: flag, write nothing
+    if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
+    return;
+  }
   const long long crow = cache_row_of(p, b, pos);
   if (crow < 0 && threadIdx.x == 0) atomicOr(p.err, GQA_DEVERR_PAGE);
   const float4 c0 = cs[lane], c1 = cs[lane + 32];
+  const uint16_t *rq = reinterpret_cast<const uint16_t *>(rope_rows);
   for (int r = warp; r < p.Hq + p.Hkv; r += 8) {
     if (r < p.Hq) {
       // query row: binary32, one bf16 rounding (it is not stored in the cache)
-      const uint16_t *src = p.q_new + (tok * p.Hq + r) * kHeadDim;
+      const uint16_t *src = rq + r * kHeadDim;
       float y[4], ss = 0.f;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -170,8 +195,8 @@ __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p
       }
     } else if (crow >= 0) {
       const int kv = r - p.Hq;
-      const uint16_t *ksrc = p.k_new + (tok * p.Hkv + kv) * kHeadDim;
-      const uint16_t *vsrc = p.v_new + (tok * p.Hkv + kv) * kHeadDim;
+      const uint16_t *ksrc = rq + (p.Hq + kv) * kHeadDim;
+      const uint16_t *vsrc = rq + (p.Hq + p.Hkv + kv) * kHeadDim;
       uint16_t x[4], w[4], kz[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -648,6 +673,8 @@ gqa_status_t check_desc(const gqa_prefill_desc_t &d) {
   const long long rows = d.block_size > 0 ? static_cast<long long>(d.num_cache_blocks) * kTile
                                           : static_cast<long long>(d.batch) * d.max_seq_len;
   if (rows > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  if (static_cast<long long>(d.num_q_heads + 2 * d.num_kv_heads) * kHeadDim * 2 > kRopeMaxSmem)
+    return GQA_ERR_UNSUPPORTED;  // a token's rows must fit the prologue's shared memory
   return GQA_OK;
 }
 
@@ -696,6 +723,8 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
     if (!pd.configured) {
       void *part = nullptr, *ticket = nullptr;
       if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(prefill_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRopeMaxSmem) !=
               cudaSuccess ||
           cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
@@ -785,7 +814,9 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
     return GQA_ERR_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_pdl(prefill_rope_kernel, dim3(static_cast<unsigned>(p.B * p.T)), dim3(256), 0, s, p) != cudaSuccess)
+  const size_t rope_smem = static_cast<size_t>(p.Hq + 2 * p.Hkv) * kHeadDim * 2;
+  if (launch_pdl(prefill_rope_kernel, dim3(static_cast<unsigned>(p.B * p.T)), dim3(256), rope_smem, s, p) !=
+      cudaSuccess)
     return GQA_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(p.ndp + p.ntail * p.ksplit);
   if (launch_pdl(prefill_attn_kernel, dim3(grid), dim3(kPfThreads), static_cast<size_t>(kSmemBytes), s, tq, tk, tv,

@@ -168,6 +168,19 @@ gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_l
                                int num_sms, const int *cluster_capacity, int *num_workers,
                                int *cluster_size, int *num_splits);
 
+/*
+ * gqa_plan_set_ordered_start -- with `ordered` non-zero, the first kernel of each step on
+ * this plan (gqa_decode_attn, gqa_decode_attn_host, gqa_attention_splitkv,
+ * gqa_decode_attn_q4) is launched in plain stream order: it starts only once the kernel
+ * before it on the stream has completed and its writes are visible, and so may follow a
+ * caller kernel that triggers programmatic completion early while writing the step's
+ * inputs (the precondition above).  The kernels within a step, and consecutive steps of
+ * this library, keep their programmatic dependent launches.  0 (the default) restores the
+ * overlapped start.  Returns GQA_ERR_INVALID_ARG for a NULL plan.  Not synchronised with
+ * calls in flight: set it between steps.
+ */
+gqa_status_t gqa_plan_set_ordered_start(gqa_plan_t *plan, int ordered);
+
 /* Frees the plan and its workspace (synchronous). NULL is accepted. */
 gqa_status_t gqa_plan_destroy(gqa_plan_t *plan);
 

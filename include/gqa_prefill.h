@@ -70,12 +70,15 @@ typedef struct gqa_prefill_desc {
  *                 page id outside the pool appends nothing there and reads that page as zeros.
  *   stream     cudaStream_t as void*
  * Launches two kernels with programmatic stream serialization: the prologue kernel (one
- * CTA per chunk token) waits for the preceding kernel in the stream before it reads
- * anything; the attention kernel waits for the prologue kernel.
+ * CTA per chunk token) reads q/k/v_new, q_start and the page table before it waits for the
+ * preceding kernel in the stream, and writes `out` and the cache only after; so the kernel
+ * launched immediately before the call must not write those inputs if it triggers
+ * programmatic completion early.  The attention kernel waits for the prologue kernel.
  * Errors: GQA_ERR_INVALID_ARG (NULL desc or tensor, page_table given for a contiguous cache
  * or missing for a paged one, misaligned tensor, bad sizes, rope_theta <= 0, eps < 0 or not
  * finite), GQA_ERR_UNSUPPORTED (head_dim != 128, H_q % H_kv != 0, G > 16, block_size other
- * than 0 or 64, more than 2^31 cache rows), GQA_ERR_CUDA (set-up or launch failure).
+ * than 0 or 64, more than 2^31 cache rows, (H_q + 2 H_kv) x 256 B above 200 KiB), GQA_ERR_CUDA
+ * (set-up or launch failure).
  */
 gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc,
                               const void *q_new, const void *k_new, const void *v_new,

@@ -67,6 +67,7 @@ def test_null_arguments_are_rejected():
     assert lib.gqa_plan_destroy(None) == binding.GQA_OK
     assert lib.gqa_plan_num_workers(None) == 0
     assert lib.gqa_plan_num_splits(None) == 0
+    assert lib.gqa_plan_set_ordered_start(None, 1) == binding.GQA_ERR_INVALID_ARG
     assert lib.gqa_plan_cluster_size(None) == 0
     f = ctypes.c_uint32()
     assert lib.gqa_plan_device_errors(None, ctypes.byref(f), 0) == binding.GQA_ERR_INVALID_ARG

@@ -24,15 +24,18 @@ def _bf16(gen, shape, device):
     return torch.randn(shape, generator=gen, dtype=torch.float32).to(torch.bfloat16).to(device)
 
 
-@pytest.mark.parametrize("form", [0, -1, 16])
+@pytest.mark.parametrize("form,ordered", [(0, False), (-1, False), (16, False), (0, True), (-1, True)])
 @pytest.mark.parametrize("paged", [False, True])
-def test_back_to_back_autoregressive_steps(paged, form):
+def test_back_to_back_autoregressive_steps(paged, form, ordered):
     """form: the planner's choice (the single-launch form here), split-KV + combine, and the
-    single-launch form with 16-CTA clusters."""
+    single-launch form with 16-CTA clusters; ordered: each step's first kernel launched in
+    plain stream order (gqa_plan_set_ordered_start)."""
     lens0 = [130, 70, 600]  # no sequence crosses a 64-token page in STEPS steps
     w = wl.make(3, 40, 8, lens0, paged=paged, max_seq=640, seed=41, device="cuda")
     plan = binding.Plan(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
                         cluster_size=form)
+    if ordered:
+        plan.set_ordered_start(True)
     gen = torch.Generator().manual_seed(42)
     steps = []
     for t in range(STEPS):
