@@ -160,7 +160,8 @@ def partition_describe(seq_lens, num_kv_heads: int, max_seq_len: int, num_worker
 
 
 GB300_SMS = 152
-GB300_CLUSTER_CAPACITY = (152, 76, 36, 15, 7)   # clusters of 1, 2, 4, 8, 16 CTAs resident at once
+# clusters of 1, 2, ..., 16 single-launch CTAs resident at once on GB300 (cudaOccupancyMaxActiveClusters)
+GB300_CLUSTER_CAPACITY = (152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7)
 
 
 def plan_describe(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *, block_size: int = 0,
@@ -171,6 +172,8 @@ def plan_describe(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: 
                     int(max_seq_len), int(num_cache_blocks), int(num_workers), 0, int(cluster_size))
     sl = None if seq_lens_host is None else np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     cap = np.ascontiguousarray(np.asarray(cluster_capacity, dtype=np.int32))
+    if cap.shape != (16,):
+        raise ValueError("cluster_capacity: 16 counts, for clusters of 1 .. 16 CTAs")
     out = np.zeros(3, dtype=np.int32)
     _check(load().gqa_plan_describe(ctypes.byref(desc), None if sl is None else sl.ctypes.data, int(num_sms),
                                     cap.ctypes.data, out[0:].ctypes.data, out[1:].ctypes.data,

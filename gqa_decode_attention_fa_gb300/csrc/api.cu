@@ -126,7 +126,7 @@ int plan_workers(int num_sms, long long total_tiles) {
 
 int gqa::plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long nseg,
                         long long max_seg_tiles, long long total_tiles) {
-  auto cap = [&](int c) { return capacity[c == 1 ? 0 : c == 2 ? 1 : c == 4 ? 2 : c == 8 ? 3 : 4]; };
+  auto cap = [&](int c) { return capacity[c - 1]; };
   if (forced < 0) return 0;
   if (forced > 0) return cap(forced) >= 1 ? forced : -1;
   if (num_workers > 0) return 0;           // an explicit worker count asks for the split-KV form
@@ -175,7 +175,7 @@ bool mapped_host(const void *h, void **d) {
   return *d != nullptr;
 }
 
-bool valid_cluster_size(int c) { return c == -1 || c == 0 || c == 1 || c == 2 || c == 4 || c == 8 || c == 16; }
+bool valid_cluster_size(int c) { return c >= -1 && c <= 16; }
 
 // The kernels read and write whole 16-byte chunks of the bf16 tensors (and bulk-prefetch
 // them), and 4-byte words of the int32 ones; NULL passes (optional tensors).
@@ -348,7 +348,7 @@ gqa_status_t check_desc(const gqa_plan_desc_t &d) {
 }
 
 // The planner's decisions for a checked geometry on a device with `num_sms` SMs that can
-// hold capacity[k] clusters of 2^k single-launch CTAs at once: the split-KV worker count,
+// hold capacity[c - 1] clusters of c single-launch CTAs at once (c = 1 .. 16): the split-KV worker count,
 // the step's form, the splits of the longest segment and the combine's shape.  Lengths
 // come from seq_lens_host (clamped to [1, max_seq_len]) or are max_seq_len.
 struct PlanChoice {
@@ -377,9 +377,10 @@ gqa_status_t plan_choose(const gqa_plan_desc_t &d, const int32_t *seq_lens_host,
   return GQA_OK;
 }
 
-// The current device's cluster capacities for a group size (attn_configure first).
-void device_capacity(int npad, int (&cap)[5]) {
-  for (int k = 0; k < 5; ++k) cap[k] = attn_cluster_capacity(npad, 1 << k);
+// The current device's cluster capacities for a group size, clusters of 1 .. 16 CTAs
+// (attn_configure first).
+void device_capacity(int npad, int (&cap)[16]) {
+  for (int k = 0; k < 16; ++k) cap[k] = attn_cluster_capacity(npad, k + 1);
 }
 
 }  // namespace
@@ -397,7 +398,7 @@ gqa_status_t step_layout(const gqa_plan_desc_t &d, int num_sms, StepLayout *lay)
   l.npad = l.G <= 8 ? 8 : 16;
   l.max_blocks = static_cast<int>(max_blocks);
   l.num_rows = paged ? static_cast<long long>(d.num_cache_blocks) * kTile : B * d.max_seq_len;
-  int cap[5];
+  int cap[16];
   device_capacity(l.npad, cap);
   PlanChoice pc;
   st = plan_choose(d, nullptr, num_sms, cap, &pc);
@@ -468,7 +469,7 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
     cudaGetLastError();
     return GQA_ERR_CUDA;
   }
-  int cap[5];
+  int cap[16];
   device_capacity(npad, cap);
   PlanChoice pc;
   st = plan_choose(d, seq_lens_host, sms, cap, &pc);

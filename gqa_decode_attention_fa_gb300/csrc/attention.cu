@@ -806,8 +806,10 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   float *recv_o = recv_ml + kRecvMlFloats;                          // [C][G][128 / C]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = p.csize, dpr = kHeadDim / C;
+  const int C = p.csize;
   const int rank = static_cast<int>(cluster_ctarank());
+  // CTA q owns dims [q * 128 / C, (q + 1) * 128 / C) of the segment's heads
+  const int d0 = rank * kHeadDim / C, nd = (rank + 1) * kHeadDim / C - d0;
   const int seg = static_cast<int>(blockIdx.x) / C;
   const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
   const bool producer = warp == kConsumerWarps;
@@ -1079,17 +1081,18 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   // rescaled O) -- pushed straight to the CTA that owns the element's dims.
   const int E = p.G * kHeadDim;
   const uint32_t bar_local = smem_addr(recv_bar);
-  if (tid == 0)  // this CTA's own receive phase: C senders x (G (m, l) pairs + G x dpr floats)
-    mbar_arrive_expect_tx(bar_local, static_cast<uint32_t>(C * p.G * (8 + 4 * dpr)));
+  if (tid == 0)  // this CTA's own receive phase: C senders x (G (m, l) pairs + G x nd floats)
+    mbar_arrive_expect_tx(bar_local, static_cast<uint32_t>(C * p.G * (8 + 4 * nd)));
   cluster_wait();  // every CTA of the cluster has initialised its barriers
   for (int e = tid; e < E; e += kThreadsCluster) {
     const int g = e >> 7, d = e & (kHeadDim - 1);
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < kConsumerWarps; ++c) acc += wpart[(c * GQA_MAX_GROUP + g) * kPartStride + d];
-    const int q = d / dpr, dd = d - q * dpr;
+    const int q = ((d + 1) * C - 1) / kHeadDim;  // the owner of dim d
+    const int dq = q * kHeadDim / C, ndq = (q + 1) * kHeadDim / C - dq, dd = d - dq;
     const uint32_t bar_q = mapa_shared(bar_local, q);
-    st_async_f32(mapa_shared(smem_addr(recv_o + (rank * p.G + g) * dpr + dd), q), acc, bar_q);
+    st_async_f32(mapa_shared(smem_addr(recv_o + (rank * p.G + g) * ndq + dd), q), acc, bar_q);
     if (dd == 0) {
       float den = 0.f;
 #pragma unroll
@@ -1106,8 +1109,8 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   if (qpub) publish_q<NT>(p, b, kv, lane, qkeep);
   // (Code that runs once per launch is kept compact: on a latency-bound step its
   // instruction fetches, not its arithmetic, set the time.)
-  for (int e = tid; e < p.G * dpr; e += kThreadsCluster) {
-    const int g = e / dpr, dd = e - g * dpr;
+  for (int e = tid; e < p.G * nd; e += kThreadsCluster) {
+    const int g = e / nd, dd = e - g * nd;
     float M = -INFINITY;
 #pragma unroll 1
     for (int r = 0; r < C; ++r) M = fmaxf(M, recv_ml[(r * p.G + g) * 2]);
@@ -1116,13 +1119,13 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
 #pragma unroll 1
       for (int r = 0; r < C; ++r) {
         const float f = exp2f(recv_ml[(r * p.G + g) * 2] - M);
-        acc = fmaf(f, recv_o[(r * p.G + g) * dpr + dd], acc);
+        acc = fmaf(f, recv_o[(r * p.G + g) * nd + dd], acc);
         den = fmaf(f, recv_ml[(r * p.G + g) * 2 + 1], den);
       }
     }
     const float v = den > 0.f ? acc / den : 0.f;  // zeros for an invalid length (flagged above)
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    p.out[(static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim + rank * dpr + dd] =
+    p.out[(static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim + d0 + dd] =
         *reinterpret_cast<const uint16_t *>(&h);
   }
   cluster_wait();  // every CTA has received everything: no store to or from this CTA is in flight

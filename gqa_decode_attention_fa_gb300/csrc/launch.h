@@ -56,8 +56,8 @@ cudaError_t launch_attention_cluster(const CUtensorMap &tmK, const CUtensorMap &
 int attn_cluster_capacity(int npad, int csize);
 // The step's form: the cluster size of the single-launch form, or 0 for split-KV +
 // combine.  `forced` is the caller's choice (gqa_plan_desc_t.cluster_size: 0 lets this
-// planner choose, -1 asks for split-KV + combine, else that cluster size); capacity[k] is
-// how many clusters of 2^k CTAs the device holds at once; max_seg_tiles is the tile count
+// planner choose, -1 asks for split-KV + combine, else that cluster size); capacity[c - 1]
+// is how many clusters of c CTAs the device holds at once (c = 1 .. 16); max_seg_tiles is the tile count
 // of the longest (sequence, KV head) segment.  Returns -1 when a forced cluster size
 // cannot be launched.
 int plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long num_segments,

@@ -112,10 +112,10 @@ typedef struct gqa_plan_desc {
     int num_workers;      /* CTAs of the split-KV kernel; 0 lets the planner choose */
     int device;           /* CUDA device ordinal the plan and its calls run on */
     int cluster_size;     /* the step's form: 0 lets the planner choose; -1 asks for the
-                             split-KV kernel + combine; 1, 2, 4, 8 or 16 asks for the
-                             single-launch form with that many CTAs per (sequence, KV head)
-                             cluster (GQA_ERR_UNSUPPORTED if the device cannot launch it).
-                             A non-zero num_workers with cluster_size 0 also means split-KV. */
+                             split-KV kernel + combine; 1 .. 16 asks for the single-launch
+                             form with that many CTAs per (sequence, KV head) cluster
+                             (GQA_ERR_UNSUPPORTED if the device cannot launch it).  A
+                             non-zero num_workers with cluster_size 0 also means split-KV. */
 } gqa_plan_desc_t;
 
 typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp32 partials) */
@@ -158,8 +158,8 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
  * gqa_plan_create would make them.
  *   desc, seq_lens_host : as for gqa_plan_create (desc->device is not used).
  *   num_sms             : the device's SM count (>= 1).
- *   cluster_capacity    : [5] how many clusters of 1, 2, 4, 8 and 16 single-launch CTAs
- *                         the device holds at once (0: that size cannot be launched).
+ *   cluster_capacity    : [16] how many clusters of 1, 2, ..., 16 single-launch CTAs the
+ *                         device holds at once (0: that size cannot be launched).
  *   num_workers, cluster_size, num_splits : outputs; any may be NULL.
  * Errors: those of gqa_plan_create's validation; GQA_ERR_UNSUPPORTED when a forced
  * cluster size has capacity 0.

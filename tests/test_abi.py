@@ -40,7 +40,7 @@ def _create(**over):
     (dict(num_workers=-1), binding.GQA_ERR_INVALID_ARG),
     (dict(block_size=-64), binding.GQA_ERR_INVALID_ARG),
     (dict(num_cache_blocks=0), binding.GQA_ERR_INVALID_ARG),
-    (dict(cluster_size=3), binding.GQA_ERR_INVALID_ARG),
+    (dict(cluster_size=17), binding.GQA_ERR_INVALID_ARG),
     (dict(cluster_size=32), binding.GQA_ERR_INVALID_ARG),
     (dict(cluster_size=-2), binding.GQA_ERR_INVALID_ARG),
     (dict(head_dim=64), binding.GQA_ERR_UNSUPPORTED),

@@ -75,7 +75,7 @@ def test_named_short_workloads_in_the_split_form(name):
     full_check(w, what=name, cluster_size=-1)
 
 
-@pytest.mark.parametrize("csize", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("csize", [1, 2, 3, 4, 8, 10, 16])
 @pytest.mark.parametrize("Hq,Hkv,lens,paged", [
     (40, 8, [1000, 1, 64, 65], True),     # G = 5, ragged, single-token and page-edge lengths
     (64, 8, [4096], False),               # G = 8
@@ -83,8 +83,9 @@ def test_named_short_workloads_in_the_split_form(name):
     (8, 8, [300, 2000], False),           # G = 1
 ])
 def test_single_launch_cluster_sizes(csize, Hq, Hkv, lens, paged):
-    """Every cluster size of the single-launch form, forced, including sizes larger than a
-    short sequence's tile count (CTAs with no tiles) and non-portable 16-CTA clusters."""
+    """Cluster sizes of the single-launch form, forced, including sizes that do not divide
+    the 128 dims (uneven dim slices), sizes larger than a short sequence's tile count (CTAs
+    with no tiles) and non-portable 16-CTA clusters."""
     w = wl.make(len(lens), Hq, Hkv, lens, paged=paged, seed=csize * 100 + Hq + len(lens), device="cuda")
     full_check(w, what=f"C={csize} G={Hq // Hkv} lens={lens}", cluster_size=csize)
 

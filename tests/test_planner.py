@@ -1,7 +1,7 @@
 """The planner's choices (gqa_plan_describe: no device work) on GB300's description -- 152
-SMs, 152 / 76 / 36 / 15 / 7 resident clusters of 1 / 2 / 4 / 8 / 16 single-launch CTAs
-(cudaOccupancyMaxActiveClusters on the GPU) -- pinned for the five decode workloads, plus
-the rules behind them."""
+SMs; 152 / 76 / 46 / 36 / 28 / 23 / 15 / 15 / 15 / 13 / 8 / 8 / 7 / 7 / 7 / 7 resident
+clusters of 1 .. 16 single-launch CTAs (cudaOccupancyMaxActiveClusters on the GPU) --
+pinned for the five decode workloads, plus the rules behind them."""
 import math
 
 import pytest
@@ -58,7 +58,8 @@ def test_cluster_size_rules():
     # 8 segments of 64 tiles: 16-CTA clusters would need two waves (7 resident) -> 8
     assert describe(g)[1] == 8
     # with room for 8 clusters of 16, the largest size is taken
-    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=(152, 76, 38, 19, 9))[1] == 16
+    roomy = (152, 76, 50, 38, 30, 25, 21, 19, 16, 15, 13, 12, 11, 10, 10, 9)
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=roomy)[1] == 16
     # never more CTAs per segment than the segment has tiles
     assert binding.plan_describe(1, 40, 8, 100)[1] == 2
     assert binding.plan_describe(1, 40, 8, 64)[1] == 1
@@ -76,11 +77,14 @@ def test_cluster_size_rules():
 
 def test_forced_cluster_size_the_device_cannot_hold_is_rejected():
     with pytest.raises(binding.GqaError) as e:
-        binding.plan_describe(1, 40, 8, 4096, cluster_size=16, cluster_capacity=(152, 76, 36, 15, 0))
+        binding.plan_describe(1, 40, 8, 4096, cluster_size=16,
+                              cluster_capacity=binding.GB300_CLUSTER_CAPACITY[:15] + (0,))
     assert e.value.status == binding.GQA_ERR_UNSUPPORTED
     with pytest.raises(binding.GqaError) as e:
-        binding.plan_describe(1, 40, 8, 4096, cluster_size=3)
+        binding.plan_describe(1, 40, 8, 4096, cluster_size=17)
     assert e.value.status == binding.GQA_ERR_INVALID_ARG
+    # any size the device holds may be forced, powers of two or not
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_size=10)[1] == 10
 
 
 def test_splits_follow_the_longest_segment():
