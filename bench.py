@@ -86,26 +86,60 @@ def bf16_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "attn_cluster_kernel": ("attention.cu", "gqa_common.cuh", "rowmath.cuh"),
+    "attn_splitkv_kernel": ("attention.cu", "gqa_common.cuh", "rowmath.cuh"),
+    "q4_cluster_kernel": ("attention_q4.cu", "gqa_common.cuh", "launch.h"),
+}
+
+
+def _code_only(src: str) -> str:
+    """C/CUDA source with comments removed and whitespace runs collapsed (string and
+    character literals kept verbatim), so that editing a comment does not change the
+    hash of a kernel's code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_hash(kernel: str = "attn_cluster_kernel"):
+    """Hash of the code (comments and layout excluded) of the files `kernel` is built from."""
     h = hashlib.sha256()
-    for name in ("attention.cu", "gqa_common.cuh", "rowmath.cuh"):
-        with open(os.path.join(ROOT, "gqa_decode_attention_fa_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "gqa_decode_attention_fa_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` (read + write) from the committed ncu capture of
-    this workload, if it was taken on the current kernel source; else None."""
+    this workload, if it was taken on the kernel's current source; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_hash") != kernel_source_hash():
-        return None
     rec = d.get("workloads", {}).get(workload)
-    if rec is None or rec.get("kernel") != kernel:
+    if rec is None or rec.get("kernel") != kernel or kernel not in KERNEL_SOURCES:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -516,12 +550,16 @@ def run_q4(name: str, steps: int, warmup: int, local: int):
     us = a.elapsed_time(b) * 1e3 / steps
     peak, src = hbm_peak()
     gbs = kvb / (us * 1e-6) / 1e9
+    single = plan.cluster_size > 0
+    kernel = "q4_cluster_kernel" if single else "q4 prologue + attention + combine (whole step)"
     return {"us_per_step": round(us, 3), "kv_bytes_per_step": kvb, "kv_gbs": round(gbs, 1),
             "bf16_cache_bytes_per_step": int(w.seq_lens.long().sum().item()) * w.Hkv * w.d * 2 * 2,
-            "roofline": {"bound": "hbm", "kernel": "q4 prologue + attention + combine (whole step)",
-                         "achieved": round(gbs, 1), "peak": peak, "peak_source": src, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4)},
-            "l2": l2_note, "steps": steps, "workers": plan.num_workers, "clocks_sm_mhz": clk.result["sm_mhz"]}
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(gbs, 1), "peak": peak,
+                         "peak_source": src, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "traffic": recorded_traffic(name, kernel) if single else None},
+            "form": (f"single launch, clusters of {plan.cluster_size} CTAs per (sequence, KV head)" if single
+                     else f"split-KV ({plan.num_workers} workers): prologue, attention, combine"),
+            "l2": l2_note, "steps": steps, "clocks_sm_mhz": clk.result["sm_mhz"]}
 
 
 def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0):

@@ -11,7 +11,9 @@
 // R is orthogonal, so the step never unrotates a cache row: with q~ = R q,
 //   q . x^_t = sigma_t (q~ . c[idx_t])   and   sum_t p_t x^_t = R^T sum_t p_t sigma_t c[idx_t],
 // i.e. the scores and the value sum run on the raw codewords in the rotated domain, and
-// the merged output row is rotated back once, by the combine.  Three kernels:
+// the merged output row is rotated back once.  Two forms, as for the bf16 cache: the
+// single-launch form (q4_cluster_kernel, at the end of this file: the whole step in one
+// launch, the merge on chip) and the split-KV form's three kernels:
 //  * q4_prologue_kernel (one warp per row): q~ = R RoPE(RMSNorm(q_new)) in binary32,
 //    kept as bf16 hi + lo (so that rounding q~ costs no accuracy); the new token's k row
 //    RoPE(RMSNorm(k_new)) and v row quantized and appended (R by a fast Walsh-Hadamard
