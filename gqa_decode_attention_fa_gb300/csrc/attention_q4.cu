@@ -293,16 +293,28 @@ __device__ __forceinline__ void q4_locate(const uint32_t *pre, const int32_t *Ls
 // length.  S = C_K q~^T with q~ as bf16 hi + lo, the online-softmax update of (m, l, O~)
 // and O~^T += C_V^T (P sigma_V)^T, with the mma fragments built from pair-table lookups
 // (the dim orders are described at the consumer loop of q4_attn_kernel).
-template <int NT>
+//
+// The pair table holds one copy of its 256 entries per lane.  kWide = false: entry e of
+// lane l at tbl + 128 e (tbl = the table's shared address + 4 l), so a lookup is a byte
+// permute, a shift-add and the load.  kWide = true: the table starts on a 64 KiB boundary T
+// of the shared window with entries 256 bytes apart, tbl = T + 4 l, and one byte permute
+// that puts the index byte into bits 8-15 of tbl gives the address (T has zero low 16 bits
+// and lies below 2^18), so a lookup is two instructions.
+template <int NT, bool kWide>
 __device__ __forceinline__ void q4_tile_update(const uint8_t *kt, int valid, const float (&sk)[4][2],
-                                               const float (&sv)[4][2], uint32_t tbl_lane, int lane,
+                                               const float (&sv)[4][2], uint32_t tbl, int lane,
                                                const uint32_t (&qh)[8][NT][2], const uint32_t (&ql)[8][NT][2],
                                                float (&o)[8][NT][4], float (&m_run)[NT][2], float (&l_run)[NT][2]) {
   const int r8 = lane >> 2, c4 = lane & 3;
   auto pair_entry = [&](uint32_t w, int k) {
-    const uint32_t e = __byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k));
+    uint32_t a;
+    if constexpr (kWide) {
+      a = __byte_perm(w, tbl, 0x7604u | (static_cast<uint32_t>(k) << 4));  // bytes: tbl.0, w.k, tbl.2, tbl.3
+    } else {
+      a = tbl + (__byte_perm(w, 0u, 0x4440u | static_cast<uint32_t>(k)) << 7);
+    }
     uint32_t v;
-    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(tbl_lane + (e << 7)));
+    asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
   };
   const uint8_t *vt = kt + kQ4TileBytes;
@@ -316,17 +328,23 @@ __device__ __forceinline__ void q4_tile_update(const uint8_t *kt, int valid, con
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = sacl[mt][nt][e] = 0.f;
+  // tokens 16 mt + r (A rows 0-7) and + 8 (rows 8-15), index bytes 16 c .. 16 c + 15; the
+  // token blocks innermost, so that consecutive mma feed different accumulators
+  uint32_t xk[4][2][4];
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
-    // tokens 16 mt + r (A rows 0-7) and + 8 (rows 8-15), index bytes 16 c .. 16 c + 15
     const uint4 w0 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8) * 64 + 16 * c4);
     const uint4 w1 = *reinterpret_cast<const uint4 *>(kt + (16 * mt + r8 + 8) * 64 + 16 * c4);
-    const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+    xk[mt][0][0] = w0.x, xk[mt][0][1] = w0.y, xk[mt][0][2] = w0.z, xk[mt][0][3] = w0.w;
+    xk[mt][1][0] = w1.x, xk[mt][1][1] = w1.y, xk[mt][1][2] = w1.z, xk[mt][1][3] = w1.w;
+  }
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int wd = ks >> 1, k0 = 2 * (ks & 1);  // bytes 2 ks and 2 ks + 1
-      const uint32_t a0 = pair_entry(x0[wd], k0), a2 = pair_entry(x0[wd], k0 + 1);
-      const uint32_t a1 = pair_entry(x1[wd], k0), a3 = pair_entry(x1[wd], k0 + 1);
+  for (int ks = 0; ks < 8; ++ks) {
+    const int wd = ks >> 1, k0 = 2 * (ks & 1);  // bytes 2 ks and 2 ks + 1
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint32_t a0 = pair_entry(xk[mt][0][wd], k0), a2 = pair_entry(xk[mt][0][wd], k0 + 1);
+      const uint32_t a1 = pair_entry(xk[mt][1][wd], k0), a3 = pair_entry(xk[mt][1][wd], k0 + 1);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         mma_bf16(sacc[mt][nt], a0, a1, a2, a3, qh[ks][nt][0], qh[ks][nt][1]);
@@ -410,16 +428,22 @@ __device__ __forceinline__ void q4_tile_update(const uint8_t *kt, int valid, con
       const uint32_t hi01 = ((u0 >> 4) & 0x0f0f0f0fu) | (u1 & 0xf0f0f0f0u);
       const uint32_t lo23 = (u2 & 0x0f0f0f0fu) | ((u3 << 4) & 0xf0f0f0f0u);
       const uint32_t hi23 = ((u2 >> 4) & 0x0f0f0f0fu) | (u3 & 0xf0f0f0f0u);
+      // the four dim blocks' hi products, then their lo products (no accumulator is
+      // used by two consecutive mma)
+      uint32_t av[4][4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int md = 4 * hw + m;
-        const uint32_t a0 = pair_entry(lo01, m), a1 = pair_entry(hi01, m);
-        const uint32_t a2 = pair_entry(lo23, m), a3 = pair_entry(hi23, m);
+        av[m][0] = pair_entry(lo01, m), av[m][1] = pair_entry(hi01, m);
+        av[m][2] = pair_entry(lo23, m), av[m][3] = pair_entry(hi23, m);
+      }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16(o[md][nt], a0, a1, a2, a3, ph[mt][nt][0], ph[mt][nt][1]);
-          mma_bf16(o[md][nt], a0, a1, a2, a3, pl[mt][nt][0], pl[mt][nt][1]);
-        }
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          mma_bf16(o[4 * hw + m][nt], av[m][0], av[m][1], av[m][2], av[m][3], ph[mt][nt][0], ph[mt][nt][1]);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          mma_bf16(o[4 * hw + m][nt], av[m][0], av[m][1], av[m][2], av[m][3], pl[mt][nt][0], pl[mt][nt][1]);
       }
     }
   }
@@ -675,7 +699,7 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
         sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
         sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
       }
-    q4_tile_update<NT>(smem + kQ4OffStage + s * kQ4StageBytes, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run,
+    q4_tile_update<NT, false>(smem + kQ4OffStage + s * kQ4StageBytes, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run,
                        l_run);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));  // the stage's index tiles are consumed
@@ -697,49 +721,84 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 // cluster protocol are the bf16 kernel's: only the global writes (the append and `out`)
 // wait on the preceding kernel, no thread leaves early, every mbarrier wait is bounded.
 namespace {
-constexpr int kQ4COrderWarp = kConsumerWarps + 1;
-constexpr int kQ4CThreads = 32 * (kConsumerWarps + 2);
 constexpr int kQ4CPartStride = 132;                                       // floats per (warp, head) row
-constexpr int kQ4COffStage = 0;                                           // [12][K, V][64 tokens][64 B]
-constexpr int kQ4COffPair = kQ4COffStage + kQ4Stages * kQ4StageBytes;     // pair table, 32 copies
-constexpr int kQ4COffScale = kQ4COffPair + kQ4PairBytes;                  // [12][K, V][64] fp32
-constexpr int kQ4COffInfo = kQ4COffScale + kQ4Stages * 2 * kTile * 4;     // [12] page inside the pool
-constexpr int kQ4COffQ = kQ4COffInfo + 64;                                // [hi, lo][16][128] bf16 q~
-constexpr int kQ4COffNew = kQ4COffQ + 2 * GQA_MAX_GROUP * kHeadDim * 2;   // new K, V index rows, sigmas
-constexpr int kQ4COffRecv = kQ4COffNew + 256;                             // [C x owned][2] then [..][128]
+constexpr int kQ4CTableBytes = 65536;
 constexpr int kQ4CRecvRows = 2 * GQA_MAX_GROUP;                           // C x ceil(G / C) <= G + C - 1
-constexpr int kQ4COffBar = kQ4COffRecv + kQ4CRecvRows * (2 + kHeadDim) * 4;
-constexpr size_t kQ4CSmemBytes = 1024 + kQ4COffBar + 8 * (2 * kQ4Stages + 1);
-static_assert(kConsumerWarps * GQA_MAX_GROUP * kQ4CPartStride * 4 + 2 * kConsumerWarps * GQA_MAX_GROUP * 4 * 2 <=
-                  kQ4Stages * kQ4StageBytes,
-              "the merge's warp partials must fit in the ring");
+// Warps and shared memory of q4_cluster_kernel<NT>: six consumer warps, a producer warp
+// and an ordering warp; a ring of two stages per consumer warp (a stage is always consumed
+// by the same warp, so that a warp never waits on a stage barrier two phases ahead).
+// (Eight consumer warps with sixteen stages measured slower: 70.8 against 65.0 us on the
+// ragged 4-bit batch.)
+//
+// Layout.  The pair table (the wide form of q4_tile_update: 256 entries x 256 bytes) starts
+// at T, the first 64 KiB boundary of the shared window at or after the 1024-aligned base A.
+// The ring's stages fill [A, T) as far as whole stages fit (n1 of them, n1 <= 7 because
+// T - A < 64 KiB) and continue after the table; the rest follows them:
+//   [stages 0 .. n1-1][unused < 8 KiB][table, 64 KiB][stages n1 .. 11][misc]
+// with misc = [scales][tile info][q~][new rows][receive area][barriers].  The whole layout
+// takes at most 64 KiB + 12 stages + 7 KiB + misc from A.  After the tile loop the table's
+// space holds the merge's warp partials.
+template <int NT>
+struct Q4C {
+  static constexpr int kWarps = kConsumerWarps;
+  static constexpr int kStages = 2 * kWarps;
+  static constexpr int kOrderWarp = kWarps + 1;
+  static constexpr int kThreads = 32 * (kWarps + 2);
+  static constexpr int kMiscScale = 0;                                           // [stage][K, V][64] fp32
+  static constexpr int kMiscInfo = kMiscScale + kStages * 2 * kTile * 4;         // [stage] page inside the pool
+  static constexpr int kMiscQ = kMiscInfo + 4 * kStages;                         // [hi, lo][16][128] bf16 q~
+  static constexpr int kMiscNew = kMiscQ + 2 * GQA_MAX_GROUP * kHeadDim * 2;     // new K, V index rows, sigmas
+  static constexpr int kMiscRecv = kMiscNew + 256;                               // [C x owned][2], [..][128]
+  static constexpr int kMiscBar = kMiscRecv + kQ4CRecvRows * (2 + kHeadDim) * 4;
+  static constexpr int kMiscBytes = kMiscBar + 8 * (2 * kStages + 1);
+  static constexpr size_t kSmemBytes =
+      1024 + kQ4CTableBytes + kStages * kQ4StageBytes + (kQ4StageBytes - 1024) + kMiscBytes;
+  // the merge's partials: [W][16][132] O, [W][16][2] (m, l), [W][16] m
+  static constexpr int kPartBytes = kWarps * GQA_MAX_GROUP * (kQ4CPartStride + 2 + 1) * 4;
+  static_assert(kMiscQ % 16 == 0 && kMiscRecv % 16 == 0 && kMiscBar % 8 == 0, "misc alignment");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kPartBytes <= kQ4CTableBytes, "the partials fit in the table's space");
+};
 
 // Barrier 1: the ordering warp hands the new rows to the consumer whose tile holds them;
 // barrier 2: the consumer warps' rotated queries are in shared memory.
 __device__ __forceinline__ void q4c_newrow_arrive() { asm volatile("bar.arrive 1, 64;" ::: "memory"); }
 __device__ __forceinline__ void q4c_newrow_sync() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+template <int W>
 __device__ __forceinline__ void q4c_consumers_sync() {
-  asm volatile("bar.sync 2, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+  asm volatile("bar.sync 2, %0;" ::"n"(32 * W) : "memory");
 }
 // Heads of a segment owned by cluster rank q: g = q, q + C, ...
 __device__ __forceinline__ int q4c_owned(int G, int C, int q) { return q < G ? (G - q + C - 1) / C : 0; }
 }  // namespace
 
 template <int NT>
-__global__ void __launch_bounds__(kQ4CThreads, 1)
+__global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
     q4_cluster_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const Q4ClusterParams p) {
+  using K = Q4C<NT>;
+  constexpr int kW = K::kWarps, kS = K::kStages, kThreads = K::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align_smem_1024(smem_raw);
-  uint64_t *full_bar = reinterpret_cast<uint64_t *>(smem + kQ4COffBar);
-  uint64_t *empty_bar = full_bar + kQ4Stages;
-  uint64_t *recv_bar = empty_bar + kQ4Stages;
-  uint32_t *cpair = reinterpret_cast<uint32_t *>(smem + kQ4COffPair);  // [256][32]
-  float *scl = reinterpret_cast<float *>(smem + kQ4COffScale);        // [stage][2][64]
-  int *pinfo = reinterpret_cast<int *>(smem + kQ4COffInfo);           // [stage]
-  uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + kQ4COffQ);      // [2][16][128]
-  uint32_t *newrow = reinterpret_cast<uint32_t *>(smem + kQ4COffNew);  // K words [16], V words [16], sigmas
-  float *recv_ml = reinterpret_cast<float *>(smem + kQ4COffRecv);     // [C x owned][2]
+  // the layout described above (the same in every CTA of the launch)
+  const uint32_t base_a = smem_addr(smem);
+  const uint32_t region1 = ((base_a + 0xFFFFu) & ~0xFFFFu) - base_a;   // T - A
+  const int n1 = static_cast<int>(region1 / kQ4StageBytes);            // stages before the table (< 8)
+  uint8_t *table = smem + region1;
+  uint8_t *region2 = table + kQ4CTableBytes;
+  uint8_t *misc = region2 + (kS - n1) * kQ4StageBytes;
+  auto stage_ptr = [&](int s) -> uint8_t * {
+    return s < n1 ? smem + s * kQ4StageBytes : region2 + (s - n1) * kQ4StageBytes;
+  };
+  uint64_t *full_bar = reinterpret_cast<uint64_t *>(misc + K::kMiscBar);
+  uint64_t *empty_bar = full_bar + kS;
+  uint64_t *recv_bar = empty_bar + kS;
+  uint32_t *cpair = reinterpret_cast<uint32_t *>(table);              // [256][64]: lane copies in [0, 32)
+  float *scl = reinterpret_cast<float *>(misc + K::kMiscScale);       // [stage][2][64]
+  int *pinfo = reinterpret_cast<int *>(misc + K::kMiscInfo);          // [stage]
+  uint16_t *qbuf = reinterpret_cast<uint16_t *>(misc + K::kMiscQ);     // [2][16][128]
+  uint32_t *newrow = reinterpret_cast<uint32_t *>(misc + K::kMiscNew); // K words [16], V words [16], sigmas
+  float *recv_ml = reinterpret_cast<float *>(misc + K::kMiscRecv);    // [C x owned][2]
   float *recv_o = recv_ml + 2 * kQ4CRecvRows;                         // [C x owned][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -747,10 +806,10 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
   const int rank = static_cast<int>(cluster_ctarank());
   const int seg = static_cast<int>(blockIdx.x) / C;
   const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
-  const bool producer = warp == kConsumerWarps;
+  const bool producer = warp == kW;
 
   if (producer && lane == 0) {
-    for (int s = 0; s < kQ4Stages; ++s) {
+    for (int s = 0; s < kS; ++s) {
       mbar_init(smem_addr(&full_bar[s]), 1 + 32);  // the TMA issue + one arrive per producer lane
       mbar_init(smem_addr(&empty_bar[s]), 1);
     }
@@ -759,9 +818,10 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
-  for (int e = tid; e < 256 * 32; e += kQ4CThreads) {
+  for (int e = tid; e < 256 * 32; e += kThreads) {
     const int v = e >> 5;
-    cpair[e] = static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
+    cpair[v * 64 + (e & 31)] =
+        static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
   }
   int L = p.seq_lens[b], pos = p.positions[b];
   const int nt = tiles_of(L, p.max_seq);
@@ -775,11 +835,11 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
   }
   const int n = nt > rank ? (nt - rank + C - 1) / C : 0;  // local tile i is segment tile rank + C i
   int owner = -1;  // the consumer warp whose tile holds the new token
-  if (pos >= 0 && (pos >> 6) % C == rank) owner = ((pos >> 6) / C) % kConsumerWarps;
+  if (pos >= 0 && (pos >> 6) % C == rank) owner = ((pos >> 6) / C) % kW;
   __syncthreads();   // barriers and the pair table ready in the CTA
   cluster_arrive();  // ... and the receive barrier for the cluster
 
-  const uint32_t tbl_lane = smem_addr(cpair) + 4u * lane;
+  const uint32_t tbl_lane = smem_addr(cpair) + 4u * lane;  // T + 4 lane: the wide table
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
@@ -796,7 +856,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
       l_run[t][jj] = 0.f;
     }
 
-  if (warp == kQ4COrderWarp) {
+  if (warp == K::kOrderWarp) {
     // ------------------------------------------------------------------ ordering warp
     Q4RowConsts kc;
     uint32_t pk = 0, pv = 0;
@@ -865,14 +925,14 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
         const int i = i0 + u;
         const int row = __shfl_sync(0xffffffffu, mrow, u), pok = __shfl_sync(0xffffffffu, mok, u);
         const int valid = min(kTile, L - (rank + C * i) * kTile);
-        const int s = i % kQ4Stages;
-        if (i >= kQ4Stages) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kQ4Stages) - 1) & 1));
+        const int s = i % kS;
+        if (i >= kS) ok = mbar_wait(smem_addr(&empty_bar[s]), static_cast<uint32_t>(((i / kS) - 1) & 1));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         const uint32_t fb = smem_addr(&full_bar[s]);
         if (lane == 0) {
           pinfo[s] = pok;
-          const uint32_t base = smem_addr(smem + kQ4COffStage + s * kQ4StageBytes);
+          const uint32_t base = smem_addr(stage_ptr(s));
           mbar_arrive_expect_tx(fb, kQ4StageBytes);
           tma_load_3d(base, &tmK, fb, 0, kv, row);
           tma_load_3d(base + kQ4TileBytes, &tmV, fb, 0, kv, row);
@@ -893,8 +953,8 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
     }
     if (lane == 0 && !ok) {
       atomicOr(p.err, GQA_DEVERR_TIMEOUT);
-      for (int ii = (issued > kQ4Stages ? issued - kQ4Stages : 0); ii < issued; ++ii)
-        (void)mbar_wait(smem_addr(&full_bar[ii % kQ4Stages]), static_cast<uint32_t>((ii / kQ4Stages) & 1));
+      for (int ii = (issued > kS ? issued - kS : 0); ii < issued; ++ii)
+        (void)mbar_wait(smem_addr(&full_bar[ii % kS]), static_cast<uint32_t>((ii / kS) & 1));
     }
     cp_async_wait_all();
     __syncwarp();
@@ -905,7 +965,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
     {
       Q4RowConsts kc;
       q4_row_consts(p.rope_tab32, pos, p.signs, p.codebook, lane, kc);
-      for (int g = cw; g < p.G; g += kConsumerWarps) {
+      for (int g = cw; g < p.G; g += kW) {
         float z[4] = {0.f, 0.f, 0.f, 0.f};
         if (pos >= 0) {
           q4_norm_rope(p.q_new + (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim, p.q_norm_w, p.eps, kc,
@@ -922,7 +982,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
         reinterpret_cast<uint2 *>(qbuf + (GQA_MAX_GROUP + g) * kHeadDim)[lane] = make_uint2(l[0], l[1]);
       }
     }
-    q4c_consumers_sync();
+    q4c_consumers_sync<kW>();
     uint32_t qh[8][NT][2], ql[8][NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -943,9 +1003,9 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
         }
     }
     const int i_new = cw == owner ? (pos >> 6) / C : -1;
-    for (int i = cw; i < n; i += kConsumerWarps) {
-      const int s = i % kQ4Stages;
-      const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kQ4Stages) & 1));
+    for (int i = cw; i < n; i += kW) {
+      const int s = i % kS;
+      const bool ready = mbar_wait(smem_addr(&full_bar[s]), static_cast<uint32_t>((i / kS) & 1));
       __syncwarp();
       if (!__all_sync(0xffffffffu, ready)) {
         if (lane == 0) atomicOr(p.err, GQA_DEVERR_TIMEOUT);
@@ -953,7 +1013,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
       }
       const int valid = min(kTile, L - (rank + C * i) * kTile);
       const bool page_ok = pinfo[s] != 0;
-      uint8_t *kt = smem + kQ4COffStage + s * kQ4StageBytes;
+      uint8_t *kt = stage_ptr(s);
       if (i == i_new) {  // the new row, from the ordering warp, into its place in the stage
         q4c_newrow_sync();
         const int r = pos & (kTile - 1);
@@ -977,7 +1037,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
           sk[mt][hh] = in ? scl[s * 2 * kTile + tok] * p.scale_log2 : 0.f;
           sv[mt][hh] = in ? scl[s * 2 * kTile + kTile + tok] : 0.f;
         }
-      q4_tile_update<NT>(kt, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run, l_run);
+      q4_tile_update<NT, true>(kt, valid, sk, sv, tbl_lane, lane, qh, ql, o, m_run, l_run);
       if (i == i_new) fence_proxy_async_smem();  // generic writes precede the next TMA into the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
@@ -985,11 +1045,11 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
   }
 
   // ------------------------------------------------------------------ merge
-  float *wpart = reinterpret_cast<float *>(smem);                           // [6][16][132]
-  float *wml = wpart + kConsumerWarps * GQA_MAX_GROUP * kQ4CPartStride;     // [6][16][2]
-  float *wm = wml + kConsumerWarps * GQA_MAX_GROUP * 2;                     // [6][16]
-  __syncthreads();  // every issued tile has been consumed: the ring is free
-  const bool consumer = !producer && warp != kQ4COrderWarp;
+  float *wpart = reinterpret_cast<float *>(table);  // [W][16][132], over the table
+  float *wml = wpart + kW * GQA_MAX_GROUP * kQ4CPartStride;  // [W][16][2]
+  float *wm = wml + kW * GQA_MAX_GROUP * 2;                  // [W][16]
+  __syncthreads();  // every issued tile has been consumed: the table is no longer read
+  const bool consumer = !producer && warp != K::kOrderWarp;
   if (consumer) {
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -1009,7 +1069,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
         const int g = 8 * t + 2 * (lane & 3) + jj;
         float M = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kConsumerWarps; ++c) M = fmaxf(M, wm[c * GQA_MAX_GROUP + (g < p.G ? g : 0)]);
+        for (int c = 0; c < kW; ++c) M = fmaxf(M, wm[c * GQA_MAX_GROUP + (g < p.G ? g : 0)]);
         const float f = m_run[t][jj] == -INFINITY ? 0.f : exp2f(m_run[t][jj] - M);
         float l = l_run[t][jj] * f;
         l += __shfl_xor_sync(0xffffffffu, l, 4);
@@ -1041,19 +1101,19 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
   const uint32_t bar_local = smem_addr(recv_bar);
   if (tid == 0) mbar_arrive_expect_tx(bar_local, static_cast<uint32_t>(C * own * (8 + 4 * kHeadDim)));
   cluster_wait();  // every CTA of the cluster has initialised its barriers
-  for (int e = tid; e < p.G * kHeadDim; e += kQ4CThreads) {
+  for (int e = tid; e < p.G * kHeadDim; e += kThreads) {
     const int g = e >> 7, d = e & (kHeadDim - 1);
     const int q = g % C, slot = g / C, own_q = q4c_owned(p.G, C, q);
     float acc = 0.f;
 #pragma unroll
-    for (int c = 0; c < kConsumerWarps; ++c) acc += wpart[(c * GQA_MAX_GROUP + g) * kQ4CPartStride + d];
+    for (int c = 0; c < kW; ++c) acc += wpart[(c * GQA_MAX_GROUP + g) * kQ4CPartStride + d];
     const uint32_t bar_q = mapa_shared(bar_local, q);
     const int rrow = rank * own_q + slot;
     st_async_f32(mapa_shared(smem_addr(recv_o + rrow * kHeadDim + d), q), acc, bar_q);
     if (d == 0) {
       float den = 0.f;
 #pragma unroll
-      for (int c = 0; c < kConsumerWarps; ++c) den += wml[(c * GQA_MAX_GROUP + g) * 2 + 1];
+      for (int c = 0; c < kW; ++c) den += wml[(c * GQA_MAX_GROUP + g) * 2 + 1];
       st_async_v2f32(mapa_shared(smem_addr(recv_ml + rrow * 2), q), wml[g * 2], den, bar_q);
     }
   }
@@ -1062,7 +1122,7 @@ __global__ void __launch_bounds__(kQ4CThreads, 1)
   cluster_arrive_relaxed();  // this CTA has received everything (or given up)
   griddep_wait();
   // the owned heads: merge, rotate back (R^T o = D H o / sqrt(d)) and write; a warp a head
-  for (int slot = warp; slot < own; slot += kQ4CThreads / 32) {
+  for (int slot = warp; slot < own; slot += kThreads / 32) {
     const int g = rank + C * slot;
     float M = -INFINITY;
 #pragma unroll 1
@@ -1106,21 +1166,23 @@ cudaError_t q4_configure() {
   const int bytes = static_cast<int>(q4_attn_smem_bytes(GQA_MAX_BATCH));
   cudaError_t e = cudaFuncSetAttribute(q4_attn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(q4_attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  const int cbytes = static_cast<int>(kQ4CSmemBytes);
-  for (void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) : {q4_cluster_kernel<1>, q4_cluster_kernel<2>}) {
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  void (*ck[2])(CUtensorMap, CUtensorMap, Q4ClusterParams) = {q4_cluster_kernel<1>, q4_cluster_kernel<2>};
+  const int cbytes[2] = {static_cast<int>(Q4C<1>::kSmemBytes), static_cast<int>(Q4C<2>::kSmemBytes)};
+  for (int i = 0; i < 2; ++i) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ck[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes[i]);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ck[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
   return e;
 }
 
 cudaError_t launch_q4_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4ClusterParams &p, int npad,
                               bool pdl, cudaStream_t stream) {
-  void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) = npad == 8 ? q4_cluster_kernel<1> : q4_cluster_kernel<2>;
+  const bool one = npad == 8;
+  void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) = one ? q4_cluster_kernel<1> : q4_cluster_kernel<2>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv * p.csize));
-  cfg.blockDim = dim3(kQ4CThreads);
-  cfg.dynamicSmemBytes = kQ4CSmemBytes;
+  cfg.blockDim = dim3(one ? Q4C<1>::kThreads : Q4C<2>::kThreads);
+  cfg.dynamicSmemBytes = one ? Q4C<1>::kSmemBytes : Q4C<2>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
