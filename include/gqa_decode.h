@@ -125,10 +125,11 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * and its splits (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
  * long contexts many) and allocates the workspace once, so no call allocates.
  *   - The single-launch form, for up to two waves of segments (B * H_kv <= 2 x SMs),
- *     with the largest cluster size C in 16, 8, 4, 2 whose clusters all fit at once
- *     (B * H_kv * C <= SMs, the device holds B * H_kv such clusters) and that does not
- *     exceed the longest segment's tile count, else C = 1; provided the B * H_kv * C CTAs
- *     can stream the cache (at least 64 of them, or one per tile).
+ *     with the largest cluster size C (2 .. 16, at most the longest segment's tile count,
+ *     B * H_kv * C <= SMs) for which the device holds the clusters of two consecutive
+ *     steps at once (2 B * H_kv of them), else of one step (B * H_kv), else C = 1;
+ *     provided the B * H_kv * C CTAs can stream the cache (at least 48 of them, or one
+ *     per tile).
  *   - Otherwise split-KV + combine: the whole batch's T KV tiles are cut into one
  *     contiguous range per worker (ADR-0060 section 2.1 contiguous-block placement); the
  *     fewest workers that keep the longest range at ceil(T / SMs) tiles.

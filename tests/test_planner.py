@@ -19,10 +19,10 @@ def describe(w, **kw):
 WORKLOADS = {
     # name: geometry, (split-KV workers, cluster size, splits of the longest segment)
     "qwen3-14b-tiny": (dict(B=1, Hq=40, Hkv=8, max_seq=256, lens=[256]), (32, 4, 4)),
-    "qwen3-14b-4k": (dict(B=1, Hq=40, Hkv=8, max_seq=4096, lens=[4096]), (128, 8, 8)),
+    "qwen3-14b-4k": (dict(B=1, Hq=40, Hkv=8, max_seq=4096, lens=[4096]), (128, 6, 6)),
     "qwen3-14b-ragged": (dict(B=32, Hq=40, Hkv=8, max_seq=8192, block=64, blocks=4000,
                               lens=wl.ragged_lengths(32, 512, 8192, 0)), (152, 1, 1)),
-    "llama3-70b-128k": (dict(B=1, Hq=64, Hkv=8, max_seq=131072, lens=[131072]), (152, 8, 8)),
+    "llama3-70b-128k": (dict(B=1, Hq=64, Hkv=8, max_seq=131072, lens=[131072]), (152, 6, 6)),
     "qwen3-14b-40layer": (dict(B=8, Hq=40, Hkv=8, max_seq=32768, block=64, blocks=4096, lens=[32768] * 8),
                           (152, 2, 2)),
 }
@@ -31,9 +31,10 @@ WORKLOADS = {
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_choices_on_the_five_workloads(name):
     """Measured on GB300 (graph replay, consecutive steps on different caches, us/step,
-    single launch vs split-KV + combine): tiny 4.15 (C=4) vs 6.72; 4k 6.39 (C=8) vs 8.12;
-    ragged 81.6 (C=1) vs 95.1; 128k 79.5 (C=8) vs 82.9; one 40-layer layer 145.5 (C=2) vs
-    163.5 -- the planner takes the single launch with those cluster sizes."""
+    single launch vs split-KV + combine): tiny 4.15 (C=4) vs 6.72; 4k 5.86 (C=6; 6.22 with
+    C=8) vs 8.12; ragged 81.6 (C=1) vs 95.1; 128k 78.4 (C=6; 80.0 with C=8) vs 82.9; one
+    40-layer layer 145.5 (C=2) vs 163.5 -- the planner takes the single launch with those
+    cluster sizes."""
     geom, want = WORKLOADS[name]
     assert describe(geom) == want
 
@@ -55,16 +56,31 @@ def test_split_form_workers_minimise_the_longest_range_then_the_workers():
 
 def test_cluster_size_rules():
     g = dict(B=1, Hq=40, Hkv=8, max_seq=4096, lens=[4096])
-    # 8 segments of 64 tiles: 16-CTA clusters would need two waves (7 resident) -> 8
-    assert describe(g)[1] == 8
-    # with room for 8 clusters of 16, the largest size is taken
+    # 8 segments of 64 tiles: GB300 holds 15 clusters of 7 or 8 CTAs, 23 of 6, so 6 is the
+    # largest size with two consecutive steps' 16 clusters resident at once
+    assert describe(g)[1] == 6
+    # with room for 16 clusters of 9, that size is taken
     roomy = (152, 76, 50, 38, 30, 25, 21, 19, 16, 15, 13, 12, 11, 10, 10, 9)
-    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=roomy)[1] == 16
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=roomy)[1] == 9
+    # 64 segments: no size above 1 holds two steps (128 clusters); 2 holds one step
+    assert binding.plan_describe(8, 40, 8, 32768)[1] == 2
+    # 40 segments: 3-CTA clusters hold one step (46 >= 40) with 120 CTAs
+    assert binding.plan_describe(5, 40, 8, 4096)[1] == 3
+    # 16 segments: 4-CTA clusters hold two steps (36 >= 32)
+    assert binding.plan_describe(2, 40, 8, 4096)[1] == 4
+    # a device holding no cluster above 5 CTAs: 5 (40 CTAs, below 48, for 512 tiles) gives
+    # way to the split form; with no more tiles than CTAs (5 a segment), to the single launch
+    none_above_5 = (152, 76, 46, 36, 28) + (0,) * 11
+    assert binding.plan_describe(1, 40, 8, 4096, cluster_capacity=none_above_5)[1] == 0
+    assert binding.plan_describe(1, 40, 8, 320, cluster_capacity=none_above_5)[1] == 5
     # never more CTAs per segment than the segment has tiles
     assert binding.plan_describe(1, 40, 8, 100)[1] == 2
     assert binding.plan_describe(1, 40, 8, 64)[1] == 1
     # a long single segment would stream on 16 SMs: split-KV over every SM instead
     assert binding.plan_describe(1, 8, 1, 131072)[1] == 0
+    # two long segments on 32 SMs (below 48): split-KV; three on 48 SMs: single launch
+    assert binding.plan_describe(1, 16, 2, 131072)[1] == 0
+    assert binding.plan_describe(1, 24, 3, 131072)[1] == 16
     # more than two waves of segments: split-KV
     assert binding.plan_describe(64, 40, 8, 1024)[1] == 0
     assert binding.plan_describe(38, 40, 8, 1024)[1] == 1
