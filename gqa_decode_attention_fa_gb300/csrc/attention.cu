@@ -62,7 +62,8 @@ struct KvRowIn {
   long long grow;             // cache row of the new token; -1 when its page is out of range
 };
 
-__device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, int pos, int lane, KvRowIn &in) {
+// The inputs of the new row that do not depend on its position (k_new, v_new, k_norm_w) ...
+__device__ __forceinline__ void load_kv_inputs(const AttnParams &p, int b, int kv, int lane, KvRowIn &in) {
   const long long nrow = (static_cast<long long>(b) * p.Hkv + kv) * kHeadDim;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -70,6 +71,9 @@ __device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, 
     in.v[t] = p.v_new[nrow + lane + 32 * t];
     in.w[t] = p.k_norm_w ? p.k_norm_w[lane + 32 * t] : uint16_t(0);
   }
+}
+// ... and those that do (the RoPE table row, the cache row).
+__device__ __forceinline__ void load_kv_place(const AttnParams &p, int b, int pos, int lane, KvRowIn &in) {
   in.cs0 = p.rope_dw[static_cast<long long>(pos) * 64 + lane];
   in.cs1 = p.rope_dw[static_cast<long long>(pos) * 64 + lane + 32];
   in.grow = -1;
@@ -79,6 +83,10 @@ __device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, 
   } else {
     in.grow = static_cast<long long>(b) * p.max_seq + pos;
   }
+}
+__device__ __forceinline__ void load_kv_row(const AttnParams &p, int b, int kv, int pos, int lane, KvRowIn &in) {
+  load_kv_inputs(p, b, kv, lane, in);
+  load_kv_place(p, b, pos, lane, in);
 }
 
 // Appends one new token for KV head kv: k = RoPE_pos(RMSNorm(k_new)) rounded once to bf16
@@ -132,8 +140,9 @@ struct QIn {
   float4 cs[4][2];       // (cos, sin) of pairs i and i + 1, i = 16 ks + 8 hf + 2 (l mod 4), ks < 4
 };
 
+// The query rows and q_norm_w (independent of the position) ...
 template <int NT>
-__device__ __forceinline__ void load_q_inputs(const AttnParams &p, int b, int kv, int pos, int lane, QIn<NT> &in) {
+__device__ __forceinline__ void load_q_rows(const AttnParams &p, int b, int kv, int lane, QIn<NT> &in) {
   const int c2 = 2 * (lane & 3);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -150,11 +159,21 @@ __device__ __forceinline__ void load_q_inputs(const AttnParams &p, int b, int kv
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
       in.w[ks][hf] = p.q_norm_w ? *reinterpret_cast<const uint32_t *>(p.q_norm_w + 16 * ks + 8 * hf + c2) : 0u;
+}
+// ... and the RoPE table row of the position.
+template <int NT>
+__device__ __forceinline__ void load_q_rope(const AttnParams &p, int pos, int lane, QIn<NT> &in) {
+  const int c2 = 2 * (lane & 3);
   const float2 *cs = p.rope_tab32 + static_cast<long long>(pos) * 64;
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) in.cs[ks][hf] = *reinterpret_cast<const float4 *>(cs + 16 * ks + 8 * hf + c2);
+}
+template <int NT>
+__device__ __forceinline__ void load_q_inputs(const AttnParams &p, int b, int kv, int pos, int lane, QIn<NT> &in) {
+  load_q_rows<NT>(p, b, kv, lane, in);
+  load_q_rope<NT>(p, pos, lane, in);
 }
 
 template <int NT>
@@ -863,6 +882,10 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     tma_load_3d(base + 3 * kHalfTileBytes, &tmV, fb, 64, kv, r_row);
   };
 
+  // The plan's expectation of the segment's tiles (the longest segment of the lengths it
+  // was made with) and of this CTA's share.
+  const int st_all = p.spec_tiles < p.max_blocks ? p.spec_tiles : p.max_blocks;
+  const int st_cta = st_all > rank ? (st_all - rank + C - 1) / C : 0;
   // The producer initialises the barriers and, before the segment's length is known, loads
   // the first tiles the plan expects this CTA to stream (a tile's cache row does not depend
   // on the length); tiles that turn out to lie past the length are waited for and dropped.
@@ -878,9 +901,7 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
     }
-    const int st = p.spec_tiles < p.max_blocks ? p.spec_tiles : p.max_blocks;
-    const int st_local = st > rank ? (st - rank + C - 1) / C : 0;  // this CTA's expected tiles
-    nspec = st_local < kStages ? st_local : kStages;
+    nspec = st_cta < kStages ? st_cta : kStages;
     if (lane < nspec) spec_row = tile_row(lane, false);
     __syncwarp();
     for (int k = 0; k < nspec; ++k) {
@@ -891,16 +912,23 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     // step) also prefetches the tiles past the ring into L2, which then arrive from L2 as
     // stages free instead of starting a DRAM round trip then.  (Measured on a 4k step: 5.87
     // -> 5.46 us; prefetching one ring ahead all along slowed the bandwidth-bound steps.)
-    if (st_local > kStages && st_local <= 2 * kStages)
+    if (st_cta > kStages && st_cta <= 2 * kStages)
       spec_prefetch_l2(&tmK, &tmV, p.paged ? p.page_table : nullptr, p.max_blocks, p.num_blocks, p.max_seq, b, kv,
-                       rank, C, kStages, st_local, lane);
+                       rank, C, kStages, st_cta, lane);
     ring_ready_arrive();
   }
   // The cluster barrier's first phase: every CTA's barriers are initialised (the producer's
   // lane 0 arrives after its initialisation; it is waited for before the first remote store).
   cluster_arrive();
-  // The segment's length and new-token position (one broadcast load per warp).
+  // The segment's length and new-token position (one broadcast load per warp), then the
+  // inputs that do not depend on the position -- the queries (consumer warps), the new k
+  // and v rows (ordering warp) -- requested before the position arrives, so that the
+  // latencies overlap (a layer's inputs are usually not in L2 when its kernel starts).
   int L = p.seq_lens[b], pos = p.positions[b];
+  QIn<NT> qin;
+  KvRowIn kin;
+  if (warp < kConsumerWarps) load_q_rows<NT>(p, b, kv, lane, qin);
+  else if (warp == kOrderWarp) load_kv_inputs(p, b, kv, lane, kin);
   const int nt = tiles_of(L, p.max_seq);
   if (nt == 0) {
     if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_SEQLEN);
@@ -938,10 +966,9 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     // Computes the new row (when this CTA's tiles hold it) while the preceding kernel
     // drains, appends it once that kernel has completed, fences it and lets the next
     // kernel launch.
-    KvRowIn kin;
     uint16_t kz[4], vz[4];
     if (owner >= 0) {
-      load_kv_row(p, b, kv, pos, lane, kin);
+      load_kv_place(p, b, pos, lane, kin);
       rotated_kv_row(p, kin, kz, vz);
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -1010,8 +1037,7 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
     const int cw = warp;
     const bool has_tiles = cw < n;
     const int i_new = cw == owner ? (pos >> 6) / C : -1;  // local index of the new token's tile
-    QIn<NT> qin;
-    if (has_tiles && pos >= 0) load_q_inputs<NT>(p, b, kv, pos, lane, qin);
+    if (has_tiles && pos >= 0) load_q_rope<NT>(p, pos, lane, qin);
     uint32_t qf[8][NT][2];
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
