@@ -115,12 +115,12 @@ __device__ __forceinline__ void q4_row_consts(const float2 *rope_tab32, int pos,
   for (int j = 0; j < 15; ++j) k.thr[j] = 0.5f * (k.cb[j] + k.cb[j + 1]);
 }
 
-// RMSNorm (optional weight) and RoPE of a bf16 row, binary32; the RoPE partner of dim e
-// (e +- 64) is in lane l ^ 16.
-__device__ __forceinline__ void q4_norm_rope(const uint16_t *src, const uint16_t *w, float eps, const Q4RowConsts &k,
-                                             int lane, float (&z)[4]) {
+// RMSNorm (optional weight) and RoPE of a bf16 row whose dims 4 l .. 4 l + 3 lane l holds
+// (`bits`), binary32; the RoPE partner of dim e (e +- 64) is in lane l ^ 16.
+__device__ __forceinline__ void q4_norm_rope(uint2 bits, const uint16_t *w, float eps, const Q4RowConsts &k, int lane,
+                                             float (&z)[4]) {
   float x[4], y[4], ss = 0.f;
-  unpack4(reinterpret_cast<const uint2 *>(src)[lane], x);
+  unpack4(bits, x);
   float wv[4] = {1.f, 1.f, 1.f, 1.f};
   if (w) unpack4(reinterpret_cast<const uint2 *>(w)[lane], wv);
 #pragma unroll
@@ -137,6 +137,10 @@ __device__ __forceinline__ void q4_norm_rope(const uint16_t *src, const uint16_t
     const float yp = __shfl_xor_sync(0xffffffffu, y[u], 16);
     z[u] = rn * (first_half ? fmaf(y[u], k.cs_c[u], -yp * k.cs_s[u]) : fmaf(y[u], k.cs_c[u], yp * k.cs_s[u]));
   }
+}
+__device__ __forceinline__ void q4_norm_rope(const uint16_t *src, const uint16_t *w, float eps, const Q4RowConsts &k,
+                                             int lane, float (&z)[4]) {
+  q4_norm_rope(reinterpret_cast<const uint2 *>(src)[lane], w, eps, k, lane, z);
 }
 
 // Quantizes a row z: t = sqrt(d) R z / ||z||, idx = the nearest level (the lower one on a
@@ -818,12 +822,26 @@ __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
   }
+  // The segment's length and new-token position, then the rows that do not depend on the
+  // position -- a consumer warp's first query head, the ordering warp's new k and v rows --
+  // requested before the pair table is built, so that their latencies overlap it.
+  int L = p.seq_lens[b], pos = p.positions[b];
+  uint2 xraw = make_uint2(0u, 0u), vraw = make_uint2(0u, 0u);
+  {
+    const long long krow = (static_cast<long long>(b) * p.Hkv + kv) * kHeadDim;
+    if (warp < kW && warp < p.G) {
+      xraw = reinterpret_cast<const uint2 *>(p.q_new + (static_cast<long long>(b) * p.Hq + kv * p.G + warp) *
+                                                           kHeadDim)[lane];
+    } else if (warp == K::kOrderWarp) {
+      xraw = reinterpret_cast<const uint2 *>(p.k_new + krow)[lane];
+      vraw = reinterpret_cast<const uint2 *>(p.v_new + krow)[lane];
+    }
+  }
   for (int e = tid; e < 256 * 32; e += kThreads) {
     const int v = e >> 5;
     cpair[v * 64 + (e & 31)] =
         static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
   }
-  int L = p.seq_lens[b], pos = p.positions[b];
   const int nt = tiles_of(L, p.max_seq);
   if (nt == 0) {
     if (tid == 0 && rank == 0 && kv == 0) atomicOr(p.err, GQA_DEVERR_SEQLEN);
@@ -864,11 +882,10 @@ __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
     long long crow = -1;
     if (owner >= 0) {
       q4_row_consts(p.rope_tab32, pos, p.signs, p.codebook, lane, kc);
-      const long long nrow = static_cast<long long>(b) * p.Hkv + kv;
       float z[4];
-      q4_norm_rope(p.k_new + nrow * kHeadDim, p.k_norm_w, p.eps, kc, lane, z);
+      q4_norm_rope(xraw, p.k_norm_w, p.eps, kc, lane, z);
       q4_quantize(z, kc, lane, pk, sgk);
-      unpack4(reinterpret_cast<const uint2 *>(p.v_new + nrow * kHeadDim)[lane], z);
+      unpack4(vraw, z);
       q4_quantize(z, kc, lane, pv, sgv);
       if (lane < 16) {
         newrow[lane] = pk;
@@ -968,8 +985,10 @@ __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
       for (int g = cw; g < p.G; g += kW) {
         float z[4] = {0.f, 0.f, 0.f, 0.f};
         if (pos >= 0) {
-          q4_norm_rope(p.q_new + (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim, p.q_norm_w, p.eps, kc,
-                       lane, z);
+          const uint2 bits = g == cw ? xraw
+                                     : reinterpret_cast<const uint2 *>(
+                                           p.q_new + (static_cast<long long>(b) * p.Hq + kv * p.G + g) * kHeadDim)[lane];
+          q4_norm_rope(bits, p.q_norm_w, p.eps, kc, lane, z);
           q4_rotate_query(z, kc, lane);
         }
         uint32_t h[2], l[2];
