@@ -37,7 +37,7 @@ class GqaError(RuntimeError):
 class PlanDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "num_q_heads", "num_kv_heads", "head_dim", "block_size", "max_seq_len",
-        "num_cache_blocks", "num_workers", "device", "cluster_size")]
+        "num_cache_blocks", "num_workers", "device", "cluster_size", "ordered_start")]
 
 
 class PrefillDesc(ctypes.Structure):
@@ -166,10 +166,12 @@ GB300_CLUSTER_CAPACITY = (152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7
 
 def plan_describe(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *, block_size: int = 0,
                   num_cache_blocks: int = 0, num_workers: int = 0, cluster_size: int = 0, seq_lens_host=None,
-                  num_sms: int = GB300_SMS, cluster_capacity=GB300_CLUSTER_CAPACITY, head_dim: int = 128):
+                  num_sms: int = GB300_SMS, cluster_capacity=GB300_CLUSTER_CAPACITY, head_dim: int = 128,
+                  ordered_start: bool = False):
     """The planner's choices without a GPU (gqa_plan_describe): (workers, cluster size, splits)."""
     desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                    int(max_seq_len), int(num_cache_blocks), int(num_workers), 0, int(cluster_size))
+                    int(max_seq_len), int(num_cache_blocks), int(num_workers), 0, int(cluster_size),
+                    int(bool(ordered_start)))
     sl = None if seq_lens_host is None else np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))
     cap = np.ascontiguousarray(np.asarray(cluster_capacity, dtype=np.int32))
     if cap.shape != (16,):
@@ -185,12 +187,13 @@ def decode_attn_static(batch: int, num_q_heads: int, num_kv_heads: int, max_seq_
                        k_cache, v_cache, page_table, seq_lens, positions, q_norm_w, k_norm_w, rope_theta: float,
                        eps: float, out, *, block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128,
                        num_workers: int = 0, cluster_size: int = 0, device: int = 0, device_errors=None,
-                       stream=None):
+                       stream=None, ordered_start: bool = False):
     """One decode step through gqa_decode_attn_static: no plan, no device allocation; the
     workspace is the library's fixed static scratch of the device.  `device_errors` is an
     optional int32/uint32 device tensor of one element the kernels OR error bits into."""
     desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
-                    int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device), int(cluster_size))
+                    int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device), int(cluster_size),
+                    int(bool(ordered_start)))
     _check(load().gqa_decode_attn_static(
         ctypes.byref(desc), _dptr(q_new), _dptr(k_new), _dptr(v_new), _dptr(k_cache), _dptr(v_cache),
         _dptr(page_table), _dptr(seq_lens), _dptr(positions), _dptr(q_norm_w), _dptr(k_norm_w), float(rope_theta),
@@ -238,11 +241,11 @@ class Plan:
 
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, max_seq_len: int, *,
                  block_size: int = 0, num_cache_blocks: int = 0, head_dim: int = 128, num_workers: int = 0,
-                 device: int = 0, seq_lens_host=None, cluster_size: int = 0):
+                 device: int = 0, seq_lens_host=None, cluster_size: int = 0, ordered_start: bool = False):
         self._lib = load()
         self.desc = PlanDesc(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
                              int(max_seq_len), int(num_cache_blocks), int(num_workers), int(device),
-                             int(cluster_size))
+                             int(cluster_size), int(bool(ordered_start)))
         sl = None
         if seq_lens_host is not None:
             sl = np.ascontiguousarray(np.asarray(seq_lens_host, dtype=np.int32))

@@ -20,6 +20,8 @@ struct gqa_plan {
   // launch the first kernel of a step in plain stream order (it then starts only once the
   // preceding kernel has completed), for callers whose preceding kernels trigger early
   bool ordered_first = false;
+  // the planner's form and splits for overlapping [0] and ordered [1] starts
+  int csize_by_start[2] = {0, 0}, nsplit_by_start[2] = {0, 0};
   int nsplit = 0;  // KV splits of the longest (sequence, KV head) segment
   long long num_rows = 0;
   void *ws = nullptr;
@@ -125,25 +127,39 @@ int plan_workers(int num_sms, long long total_tiles) {
 }  // namespace
 
 int gqa::plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long nseg,
-                        long long max_seg_tiles, long long total_tiles) {
+                        long long max_seg_tiles, long long total_tiles, bool ordered) {
   auto cap = [&](int c) { return capacity[c - 1]; };
   if (forced < 0) return 0;
   if (forced > 0) return cap(forced) >= 1 ? forced : -1;
   if (num_workers > 0) return 0;           // an explicit worker count asks for the split-KV form
   if (nseg > 2LL * num_sms) return 0;      // more than two waves of one-CTA segments
-  // The largest cluster size whose clusters the device holds for two consecutive steps at
-  // once (the next step's CTAs then start while this one finishes), else for one step; a
-  // tile for every CTA and at most one CTA per SM.  (Measured on GB300, where 15 clusters of
-  // 8 fit: 8 segments take 6-CTA clusters, 5.86 us a 4k step against 6.22 with 8.)
-  int best = 1;
-  for (int need = 2; need >= 1 && best == 1; --need)
-    for (int c = 16; c >= 2; --c) {
-      if (c > max_seg_tiles || nseg * c > num_sms) continue;
-      if (cap(c) >= need * nseg) {
-        best = c;
-        break;
-      }
+  // The largest cluster size (a tile for every CTA, at most one CTA per SM) whose clusters
+  // the device holds at once for `need2` steps' worth of segments (need2 / 2 steps), or 1.
+  auto largest = [&](long long need2) {
+    for (int c = 16; c >= 2; --c)
+      if (c <= max_seg_tiles && nseg * c <= num_sms && 2LL * cap(c) >= need2 * nseg) return c;
+    return 1;
+  };
+  int best;
+  if (ordered) {
+    best = largest(2);  // a step runs alone: the most CTAs streaming
+  } else {
+    // Steps overlap.  Short segments (a CTA streams at most two rings of tiles; the step
+    // is latency-bound): room for two consecutive steps, so that the next step's CTAs
+    // start as this one finishes.  Long segments (bandwidth-bound): room for one and a half
+    // steps, else one -- more CTAs streaming while part of the next step already runs.
+    // Measured on GB300 (15 clusters of 8 fit, 13 of 10, 23 of 6), 8 segments: a 4k step
+    // 5.35 us with clusters of 6, 5.56 with 10, 5.85 with 8; 8k / 16k / 128k contexts
+    // 7.82 / 12.1 / 75.5 us with 10, against 7.98 / 13.0 / 78.6 with 6.
+    const int c2 = largest(4);
+    const long long per_cta = (max_seg_tiles + c2 - 1) / c2;
+    if (c2 > 1 && per_cta <= 2LL * kStages) {
+      best = c2;
+    } else {
+      best = largest(3);
+      if (best == 1) best = largest(2);
     }
+  }
   if (best == 1 && cap(1) < 1) return 0;
   // Enough CTAs to stream: 48 SMs nearly saturate HBM (6.85 TB/s measured on a 128k
   // sequence, about 140 GB/s each), or one CTA per tile already.
@@ -376,7 +392,8 @@ gqa_status_t plan_choose(const gqa_plan_desc_t &d, const int32_t *seq_lens_host,
   c.W = d.num_workers > 0 ? d.num_workers : plan_workers(num_sms, total_tiles);
   c.combine_split = combine_split(d.batch, d.num_q_heads, d.num_kv_heads, c.W, num_sms);
   c.csize = plan_step_form(d.cluster_size, d.num_workers, num_sms, capacity,
-                           static_cast<long long>(d.batch) * d.num_kv_heads, max_seg_tiles, total_tiles);
+                           static_cast<long long>(d.batch) * d.num_kv_heads, max_seg_tiles, total_tiles,
+                           d.ordered_start != 0);
   if (c.csize < 0) return GQA_ERR_UNSUPPORTED;
   c.max_seg_tiles = static_cast<int>(max_seg_tiles);
   c.nsplit = c.csize > 0 ? static_cast<int>(std::min<long long>(c.csize, max_seg_tiles))
@@ -441,6 +458,7 @@ gqa_status_t run_step_at(const gqa_plan_desc_t &d, const StepLayout &lay, void *
   plan.csize = lay.csize;
   plan.spec_tiles = lay.spec_tiles;
   plan.num_rows = lay.num_rows;
+  plan.ordered_first = d.ordered_start != 0;
   char *c = static_cast<char *>(base);
   plan.rope_tab = reinterpret_cast<float4 *>(c);
   plan.q_rot = reinterpret_cast<uint16_t *>(c + lay.off_q);
@@ -479,8 +497,12 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   }
   int cap[16];
   device_capacity(npad, cap);
-  PlanChoice pc;
+  PlanChoice pc, pc_other;
   st = plan_choose(d, seq_lens_host, sms, cap, &pc);
+  if (st != GQA_OK) return st;
+  gqa_plan_desc_t d_other = d;
+  d_other.ordered_start = d.ordered_start ? 0 : 1;
+  st = plan_choose(d_other, seq_lens_host, sms, cap, &pc_other);
   if (st != GQA_OK) return st;
 
   gqa_plan_t *p = new (std::nothrow) gqa_plan_t();
@@ -497,6 +519,10 @@ gqa_status_t gqa_plan_create(const gqa_plan_desc_t *desc, const int32_t *seq_len
   p->csize = pc.csize;
   p->nsplit = pc.nsplit;
   p->spec_tiles = pc.max_seg_tiles;
+  p->ordered_first = d.ordered_start != 0;
+  const int mine = p->ordered_first ? 1 : 0;
+  p->csize_by_start[mine] = pc.csize, p->nsplit_by_start[mine] = pc.nsplit;
+  p->csize_by_start[1 - mine] = pc_other.csize, p->nsplit_by_start[1 - mine] = pc_other.nsplit;
 
   const long long B = d.batch, Hq = d.num_q_heads, Hkv = d.num_kv_heads;
   const long long slots = B * Hkv + p->W;
@@ -567,6 +593,9 @@ gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_l
 gqa_status_t gqa_plan_set_ordered_start(gqa_plan_t *plan, int ordered) {
   if (!plan) return GQA_ERR_INVALID_ARG;
   plan->ordered_first = ordered != 0;
+  // the planner's form for the new setting (the workspace holds either form's partials)
+  plan->csize = plan->csize_by_start[plan->ordered_first ? 1 : 0];
+  plan->nsplit = plan->nsplit_by_start[plan->ordered_first ? 1 : 0];
   return GQA_OK;
 }
 

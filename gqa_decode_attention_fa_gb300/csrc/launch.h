@@ -58,10 +58,11 @@ int attn_cluster_capacity(int npad, int csize);
 // combine.  `forced` is the caller's choice (gqa_plan_desc_t.cluster_size: 0 lets this
 // planner choose, -1 asks for split-KV + combine, else that cluster size); capacity[c - 1]
 // is how many clusters of c CTAs the device holds at once (c = 1 .. 16); max_seg_tiles is the tile count
-// of the longest (sequence, KV head) segment.  Returns -1 when a forced cluster size
-// cannot be launched.
+// of the longest (sequence, KV head) segment; `ordered`: consecutive steps do not overlap
+// (gqa_plan_desc_t.ordered_start).  Returns -1 when a forced cluster size cannot be
+// launched.
 int plan_step_form(int forced, int num_workers, int num_sms, const int *capacity, long long num_segments,
-                   long long max_seg_tiles, long long total_tiles);
+                   long long max_seg_tiles, long long total_tiles, bool ordered);
 
 // The combine: split 0 runs one CTA per (sequence, KV head) segment, split 4, 2 or 1 that
 // many CTAs per query head; combine_split picks it from the geometry and worker count.

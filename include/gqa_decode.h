@@ -116,6 +116,11 @@ typedef struct gqa_plan_desc {
                              form with that many CTAs per (sequence, KV head) cluster
                              (GQA_ERR_UNSUPPORTED if the device cannot launch it).  A
                              non-zero num_workers with cluster_size 0 also means split-KV. */
+    int ordered_start;    /* 0: a step's first kernel may start while the kernel before it
+                             on the stream drains, so consecutive steps overlap; non-zero:
+                             it is launched in plain stream order (the initial setting of
+                             gqa_plan_set_ordered_start, which see).  The planner sizes the
+                             clusters for the setting. */
 } gqa_plan_desc_t;
 
 typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp32 partials) */
@@ -124,12 +129,15 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * gqa_plan_create -- the split planner.  Validates the geometry, chooses the step's form
  * and its splits (ADR-0060 sections 5.3 and 9 item 5: short contexts want few splits,
  * long contexts many) and allocates the workspace once, so no call allocates.
- *   - The single-launch form, for up to two waves of segments (B * H_kv <= 2 x SMs),
- *     with the largest cluster size C (2 .. 16, at most the longest segment's tile count,
- *     B * H_kv * C <= SMs) for which the device holds the clusters of two consecutive
- *     steps at once (2 B * H_kv of them), else of one step (B * H_kv), else C = 1;
- *     provided the B * H_kv * C CTAs can stream the cache (at least 48 of them, or one
- *     per tile).
+ *   - The single-launch form, for up to two waves of segments (B * H_kv <= 2 x SMs).
+ *     Its cluster size C (2 .. 16, at most the longest segment's tile count,
+ *     B * H_kv * C <= SMs; else C = 1) is the largest for which the device holds at once
+ *     the clusters of: with overlapping steps (ordered_start 0) and short segments (a CTA
+ *     streams at most two rings of tiles), two consecutive steps (2 B * H_kv clusters), so
+ *     that the next step's CTAs start as this one finishes; with overlapping steps and long
+ *     segments, one and a half steps, else one; with ordered starts (a step runs alone),
+ *     one step, the most CTAs streaming.  Provided the B * H_kv * C CTAs can stream the
+ *     cache (at least 48 of them, or one per tile).
  *   - Otherwise split-KV + combine: the whole batch's T KV tiles are cut into one
  *     contiguous range per worker (ADR-0060 section 2.1 contiguous-block placement); the
  *     fewest workers that keep the longest range at ceil(T / SMs) tiles.
@@ -175,10 +183,12 @@ gqa_status_t gqa_plan_describe(const gqa_plan_desc_t *desc, const int32_t *seq_l
  * gqa_decode_attn_q4) is launched in plain stream order: it starts only once the kernel
  * before it on the stream has completed and its writes are visible, and so may follow a
  * caller kernel that triggers programmatic completion early while writing the step's
- * inputs (the precondition above).  The kernels within a step, and consecutive steps of
- * this library, keep their programmatic dependent launches.  0 (the default) restores the
- * overlapped start.  Returns GQA_ERR_INVALID_ARG for a NULL plan.  Not synchronised with
- * calls in flight: set it between steps.
+ * inputs (the precondition above).  The kernels within a step keep their programmatic
+ * dependent launches; consecutive steps no longer overlap, so the plan switches to the
+ * cluster size the planner takes for a step that runs alone (unless the plan was created
+ * with an explicit cluster_size or num_workers).  0 restores the overlapped start and its
+ * cluster size.  Returns GQA_ERR_INVALID_ARG for a NULL plan.  Not synchronised with calls
+ * in flight: set it between steps.
  */
 gqa_status_t gqa_plan_set_ordered_start(gqa_plan_t *plan, int ordered);
 

@@ -26,7 +26,7 @@ def test_status_strings():
 
 def _create(**over):
     d = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=64, max_seq_len=128,
-             num_cache_blocks=4, num_workers=0, device=0, cluster_size=0)
+             num_cache_blocks=4, num_workers=0, device=0, cluster_size=0, ordered_start=0)
     d.update(over)
     desc = binding.PlanDesc(*[d[n] for n, _ in binding.PlanDesc._fields_])
     h = ctypes.c_void_p()

@@ -61,3 +61,22 @@ def test_back_to_back_autoregressive_steps(paged, form, ordered):
         kc, vc = ref["k_cache"], ref["v_cache"]
     np.testing.assert_array_equal(bits(w.v_cache), vc)
     np.testing.assert_array_equal(bits(w.k_cache), kc)
+
+
+def test_ordered_start_switches_to_the_planners_size_for_a_step_alone():
+    """gqa_plan_set_ordered_start re-selects the cluster size: the same as a plan created
+    with ordered_start, and back again when cleared; an explicit size is kept."""
+    for lens in ([4096], [131072], [256]):
+        kw = dict(seq_lens_host=np.asarray(lens, dtype=np.int32))
+        overl = binding.Plan(1, 40, 8, max(lens), **kw)
+        ordered = binding.Plan(1, 40, 8, max(lens), ordered_start=True, **kw)
+        c_overl, c_ordered = overl.cluster_size, ordered.cluster_size
+        overl.set_ordered_start(True)
+        assert overl.cluster_size == c_ordered
+        overl.set_ordered_start(False)
+        assert overl.cluster_size == c_overl
+        forced = binding.Plan(1, 40, 8, max(lens), cluster_size=2, **kw)
+        forced.set_ordered_start(True)
+        assert forced.cluster_size == 2
+        for p in (overl, ordered, forced):
+            p.close()
