@@ -835,7 +835,9 @@ __device__ __noinline__ void spec_prefetch_l2(const CUtensorMap *tmK, const CUte
   }
 }
 
-template <int NT>
+// kOrder: the launch order of the segments comes from p.seg_order (a separate instance, so
+// that the launches without it keep their start-up path unchanged).
+template <int NT, bool kOrder>
 __global__ void __launch_bounds__(kThreadsCluster, 1)
     attn_cluster_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const AttnParams p) {
@@ -853,7 +855,9 @@ __global__ void __launch_bounds__(kThreadsCluster, 1)
   const int rank = static_cast<int>(cluster_ctarank());
   // CTA q owns dims [q * 128 / C, (q + 1) * 128 / C) of the segment's heads
   const int d0 = rank * kHeadDim / C, nd = (rank + 1) * kHeadDim / C - d0;
-  const int seg = static_cast<int>(blockIdx.x) / C;
+  // the cluster's segment: launch order longest first when the plan gives one (a batch of
+  // more clusters than the device holds at once then ends with its short segments)
+  const int seg = kOrder ? p.seg_order[blockIdx.x / C] : static_cast<int>(blockIdx.x) / C;
   const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
   const bool producer = warp == kConsumerWarps;
   uint16_t *kvrow = reinterpret_cast<uint16_t *>(smem + kKvRowOffset);  // [2][128]: k, v
@@ -1196,19 +1200,29 @@ size_t attn_smem_bytes(int npad, int batch) {
 
 size_t attn_cluster_smem_bytes() { return kClusterSmemBytes; }
 
+namespace {
+using ClusterKernel = void (*)(CUtensorMap, CUtensorMap, AttnParams);
+ClusterKernel cluster_kernel(int npad, bool order) {
+  if (npad == 8) return order ? attn_cluster_kernel<1, true> : attn_cluster_kernel<1, false>;
+  return order ? attn_cluster_kernel<2, true> : attn_cluster_kernel<2, false>;
+}
+}  // namespace
+
 cudaError_t attn_configure(int npad) {
   const int bytes = static_cast<int>(attn_smem_bytes(npad, GQA_MAX_BATCH));
   const int cbytes = static_cast<int>(attn_cluster_smem_bytes());
   void (*split)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_splitkv_kernel<1> : attn_splitkv_kernel<2>;
-  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  for (bool order : {false, true}) {
+    const ClusterKernel single = cluster_kernel(npad, order);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(single, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
   return e;
 }
 
 int attn_cluster_capacity(int npad, int csize) {
-  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
+  const ClusterKernel single = cluster_kernel(npad, false);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(csize));
   cfg.blockDim = dim3(kThreadsCluster);
@@ -1230,7 +1244,7 @@ int attn_cluster_capacity(int npad, int csize) {
 
 cudaError_t launch_attention_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnParams &p, int npad,
                                      bool pdl, cudaStream_t stream) {
-  void (*single)(CUtensorMap, CUtensorMap, AttnParams) = npad == 8 ? attn_cluster_kernel<1> : attn_cluster_kernel<2>;
+  const ClusterKernel single = cluster_kernel(npad, p.seg_order != nullptr);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv * p.csize));
   cfg.blockDim = dim3(kThreadsCluster);

@@ -776,7 +776,8 @@ __device__ __forceinline__ void q4c_consumers_sync() {
 __device__ __forceinline__ int q4c_owned(int G, int C, int q) { return q < G ? (G - q + C - 1) / C : 0; }
 }  // namespace
 
-template <int NT>
+// kOrder: the launch order of the segments comes from p.seg_order.
+template <int NT, bool kOrder>
 __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
     q4_cluster_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const Q4ClusterParams p) {
@@ -808,7 +809,7 @@ __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = p.csize;
   const int rank = static_cast<int>(cluster_ctarank());
-  const int seg = static_cast<int>(blockIdx.x) / C;
+  const int seg = kOrder ? p.seg_order[blockIdx.x / C] : static_cast<int>(blockIdx.x) / C;
   const int b = seg / p.Hkv, kv = seg - b * p.Hkv;
   const bool producer = warp == kW;
 
@@ -1185,9 +1186,11 @@ cudaError_t q4_configure() {
   const int bytes = static_cast<int>(q4_attn_smem_bytes(GQA_MAX_BATCH));
   cudaError_t e = cudaFuncSetAttribute(q4_attn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(q4_attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  void (*ck[2])(CUtensorMap, CUtensorMap, Q4ClusterParams) = {q4_cluster_kernel<1>, q4_cluster_kernel<2>};
-  const int cbytes[2] = {static_cast<int>(Q4C<1>::kSmemBytes), static_cast<int>(Q4C<2>::kSmemBytes)};
-  for (int i = 0; i < 2; ++i) {
+  void (*ck[4])(CUtensorMap, CUtensorMap, Q4ClusterParams) = {q4_cluster_kernel<1, false>, q4_cluster_kernel<2, false>,
+                                                              q4_cluster_kernel<1, true>, q4_cluster_kernel<2, true>};
+  const int cbytes[4] = {static_cast<int>(Q4C<1>::kSmemBytes), static_cast<int>(Q4C<2>::kSmemBytes),
+                         static_cast<int>(Q4C<1>::kSmemBytes), static_cast<int>(Q4C<2>::kSmemBytes)};
+  for (int i = 0; i < 4; ++i) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ck[i], cudaFuncAttributeMaxDynamicSharedMemorySize, cbytes[i]);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ck[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
@@ -1197,7 +1200,10 @@ cudaError_t q4_configure() {
 cudaError_t launch_q4_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4ClusterParams &p, int npad,
                               bool pdl, cudaStream_t stream) {
   const bool one = npad == 8;
-  void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) = one ? q4_cluster_kernel<1> : q4_cluster_kernel<2>;
+  const bool order = p.seg_order != nullptr;
+  void (*k)(CUtensorMap, CUtensorMap, Q4ClusterParams) =
+      one ? (order ? q4_cluster_kernel<1, true> : q4_cluster_kernel<1, false>)
+          : (order ? q4_cluster_kernel<2, true> : q4_cluster_kernel<2, false>);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.B * p.Hkv * p.csize));
   cfg.blockDim = dim3(one ? Q4C<1>::kThreads : Q4C<2>::kThreads);

@@ -90,6 +90,8 @@ struct AttnParams {
   int spec_tiles;                           // single-launch form: tiles of the longest segment the
                                             // plan expects (its first tiles are loaded before the
                                             // length is read)
+  const int32_t *seg_order;                 // single-launch form: cluster i streams segment
+                                            // seg_order[i] (b H_kv + kv), or i when null
   double eps;
   float scale_log2;                         // log2(e) / sqrt(d)
 };

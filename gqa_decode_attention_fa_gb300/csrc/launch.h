@@ -116,6 +116,7 @@ struct Q4ClusterParams {
   uint32_t *err;
   int B, Hq, Hkv, G, paged, max_seq, max_blocks, num_blocks, csize;
   float eps, scale_log2;
+  const int32_t *seg_order;                 // cluster i streams segment seg_order[i], or i when null
 };
 cudaError_t q4_configure();
 cudaError_t launch_q4_cluster(const CUtensorMap &tmK, const CUtensorMap &tmV, const Q4ClusterParams &p, int npad,

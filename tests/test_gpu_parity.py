@@ -22,20 +22,22 @@ pytestmark = pytest.mark.gpu
 FORMS = [0, -1]
 
 
-def run_gpu(w, plan=None, num_workers=0, cluster_size=0):
+def run_gpu(w, plan=None, num_workers=0, cluster_size=0, ordered_start=False):
     plan = plan or binding.Plan.for_workload(w, num_workers=num_workers, cluster_size=cluster_size)
+    if ordered_start:
+        plan.set_ordered_start(True)
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.bfloat16, device="cuda")
     plan.run(w, out)
     torch.cuda.synchronize()
     return plan, out
 
 
-def full_check(w, num_workers=0, what="", cluster_size=0):
+def full_check(w, num_workers=0, what="", cluster_size=0, ordered_start=False):
     """Run both sides on workload w (on the GPU) and check output, cache and q."""
     k0, v0 = bits(w.k_cache), bits(w.v_cache)
     ref = oracle_step(w)
     assert ref["status"] == 0
-    plan, out = run_gpu(w, num_workers=num_workers, cluster_size=cluster_size)
+    plan, out = run_gpu(w, num_workers=num_workers, cluster_size=cluster_size, ordered_start=ordered_start)
     what = f"{what} [C={plan.cluster_size}]"
     assert plan.device_errors() == 0
     stats = assert_out_close(out, ref["out"], what)
@@ -66,6 +68,14 @@ def full_check(w, num_workers=0, what="", cluster_size=0):
 def test_named_workload_full_parity(name):
     w = wl.named(name, device="cuda")
     full_check(w, what=name)
+
+
+@pytest.mark.parametrize("name", ["qwen3-14b-4k", "qwen3-14b-ragged"])
+def test_named_workloads_with_ordered_starts(name):
+    """Ordered starts re-select the cluster size (12 on the 4k step) and, for the ragged
+    batch (more one-CTA clusters than SMs), launch its segments longest first."""
+    w = wl.named(name, device="cuda")
+    full_check(w, what=f"{name} ordered", ordered_start=True)
 
 
 @pytest.mark.parametrize("name", ["qwen3-14b-tiny", "qwen3-14b-4k"])
