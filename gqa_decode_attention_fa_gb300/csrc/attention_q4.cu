@@ -411,19 +411,28 @@ __device__ __forceinline__ void q4_tile_update(const uint8_t *kt, int valid, con
       const uint32_t h01 = pack_bf16(pv[0], pv[1]), h23 = pack_bf16(pv[2], pv[3]);
       const uint32_t l01 = pack_bf16(pv[0] - bf16_lo_to_float(h01), pv[1] - bf16_hi_to_float(h01));
       const uint32_t l23 = pack_bf16(pv[2] - bf16_lo_to_float(h23), pv[3] - bf16_hi_to_float(h23));
-      ph[mt][nt][0] = movmatrix_t(h01);
-      ph[mt][nt][1] = movmatrix_t(h23);
-      pl[mt][nt][0] = movmatrix_t(l01);
-      pl[mt][nt][1] = movmatrix_t(l23);
+      // lanes with odd c hold their two k-slots (tokens) swapped, as their V index rows are
+      // loaded below (both mma operands of a k-slot pair come from lanes of the same c)
+      const uint32_t sw = (c4 & 1) ? 0x1032u : 0x3210u;
+      ph[mt][nt][0] = __byte_perm(movmatrix_t(h01), 0u, sw);
+      ph[mt][nt][1] = __byte_perm(movmatrix_t(h23), 0u, sw);
+      pl[mt][nt][0] = __byte_perm(movmatrix_t(l01), 0u, sw);
+      pl[mt][nt][1] = __byte_perm(movmatrix_t(l23), 0u, sw);
     }
   // O~^T += C_V^T (P sigma_V)^T: 4 token k-steps x 8 dim blocks of 16 (rows 8 r + md and
-  // 64 + 8 r + md); tokens t0, t0 + 1 (k-slots 2 c, +1) and t0 + 8, t0 + 9 (slots + 8)
+  // 64 + 8 r + md); tokens t0, t0 + 1 (k-slots 2 c, +1) and t0 + 8, t0 + 9 (slots + 8).
+  // Lanes with odd c take the rows of a token pair in the other order (t0 + 1 first), so
+  // that each 8-byte load touches two even and two odd 64-byte rows, i.e. all 32 banks;
+  // their P fragments were swapped to match.
+  const int tswap = c4 & 1;
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
     const int t0 = 16 * mt + 2 * c4;
     const uint8_t *vr = vt + t0 * 64 + 8 * r8;
-    const uint2 y0 = *reinterpret_cast<const uint2 *>(vr), y1 = *reinterpret_cast<const uint2 *>(vr + 64);
-    const uint2 y2 = *reinterpret_cast<const uint2 *>(vr + 8 * 64), y3 = *reinterpret_cast<const uint2 *>(vr + 9 * 64);
+    const uint2 y0 = *reinterpret_cast<const uint2 *>(vr + tswap * 64);
+    const uint2 y1 = *reinterpret_cast<const uint2 *>(vr + (1 - tswap) * 64);
+    const uint2 y2 = *reinterpret_cast<const uint2 *>(vr + (8 + tswap) * 64);
+    const uint2 y3 = *reinterpret_cast<const uint2 *>(vr + (9 - tswap) * 64);
 #pragma unroll
     for (int hw = 0; hw < 2; ++hw) {
       const uint32_t u0 = hw ? y0.y : y0.x, u1 = hw ? y1.y : y1.x, u2 = hw ? y2.y : y2.x, u3 = hw ? y3.y : y3.x;
