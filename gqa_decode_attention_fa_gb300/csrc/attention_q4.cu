@@ -847,10 +847,19 @@ __global__ void __launch_bounds__(Q4C<NT>::kThreads, 1)
       vraw = reinterpret_cast<const uint2 *>(p.v_new + krow)[lane];
     }
   }
-  for (int e = tid; e < 256 * 32; e += kThreads) {
-    const int v = e >> 5;
-    cpair[v * 64 + (e & 31)] =
-        static_cast<uint32_t>(p.codebook[v & 15]) | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
+  {
+    // the pair table: entry v = (c[v & 15], c[v >> 4]) in each lane's copy, four copies
+    // (16 bytes) a store; thread t writes entries v = t / 8 + 32 k (k < 8), copies
+    // 4 (t mod 8) .. + 3, so its low codeword c[(t / 8) mod 16] is the same for all eight
+    static_assert(kThreads == 256, "pair-table build layout");
+    const int c0 = 4 * (tid & 7);
+    const uint32_t lo = p.codebook[(tid >> 3) & 15];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int v = (tid >> 3) + 32 * k;
+      const uint32_t e = lo | (static_cast<uint32_t>(p.codebook[v >> 4]) << 16);
+      *reinterpret_cast<uint4 *>(&cpair[v * 64 + c0]) = make_uint4(e, e, e, e);
+    }
   }
   const int nt = tiles_of(L, p.max_seq);
   if (nt == 0) {
