@@ -597,12 +597,12 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 
   // ------------------------------------------------------------------ consumer warps
   // Until griddep_wait() returns, the preceding kernel in the stream (the previous step's
-  // combine) may still be reading the partials, so those are written only after it.
-  // Everything before it reads only the caller's inputs and the RoPE table and writes only
-  // the new cache rows, which that kernel does not touch.  The workspace copy of the
-  // rotated queries is written after the wait too: a workspace laid out per call (the
-  // static-scratch entry point) can put this call's copy where the previous call's
-  // partials were.
+  // combine) may still be reading the partials, so nothing is written before it: the work
+  // before the wait only reads (the caller's inputs, the RoPE table, the cache) and
+  // computes the first new rows.  The new cache rows, the workspace copy of the rotated
+  // queries and the partials are all written after it -- a workspace laid out per call
+  // (the static-scratch entry point) can put this call's copy where the previous call's
+  // partials were, and the preceding step may still read a row this one rewrites.
   float o[8][NT][4];
   float m_run[NT][2], l_run[NT][2];
 #pragma unroll
