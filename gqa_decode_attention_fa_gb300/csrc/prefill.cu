@@ -9,7 +9,7 @@
 // heads of a KV head share one operand (section 5.4: "GQA batches the group's query heads
 // along the same axis as decode").
 //
-// Two kernels:
+// Two kernels, and a third when query tiles are cut into KV parts:
 //  * prefill_rope_kernel: one CTA per chunk token.  cos/sin of the token's position in
 //    binary64, the rotated queries (binary32, rounded once to bf16) written to `out`, which
 //    holds them until the attention kernel has read them, and the appended k row
@@ -28,6 +28,9 @@
 //    other's tensor work.  The running maximum is raised lazily: O in
 //    tensor memory is rescaled only when a row's maximum grows by more than 2^8, so P stays
 //    below 256 and most tiles need no rescale.
+//  * prefill_merge_kernel: the KV parts of the cut query tiles (see the work items below)
+//    leave fp32 partials; one CTA per (cut tile, 16 dims) merges them after the attention
+//    kernel (M = max m_k, out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k).
 #include <math.h>
 #include <string.h>
 
@@ -66,7 +69,7 @@ constexpr int kOffBar = kOffKV + kPfStages * kStageBytes;
 constexpr int kNumBars = 1 + 4 * kPfStages + 2 + 2 + 1 + 1;
 constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
 constexpr int kPfMaxSlots = 320;                // split-tile partials the static scratch holds
-constexpr int kPfMaxSplit = 4;                  // KV parts of one split query tile
+constexpr int kPfMaxSplit = 8;                  // KV parts of one split query tile
 // A partial is column-major, [130][128 rows] floats: O columns, then m, then l, so that the
 // softmax warps (thread = row) write and read it in coalesced 128-byte lines.
 constexpr int kPartFloats = (kHeadDim + 2) * kPfRows;
@@ -92,11 +95,10 @@ struct PrefillParams {
   float eps, scale_log2;
   double inv_freq[kHeadDim / 2];
   // Work items (CTAs): ndp whole query tiles, then ntail tiles cut into ksplit KV parts
-  // each; a cut tile's parts leave fp32 partials in part[ntail * ksplit][kPartFloats] and
-  // the last to finish (ticket[tail index]) merges them.
+  // each; a cut tile's parts leave fp32 partials in part[ntail * ksplit][kPartFloats],
+  // which prefill_merge_kernel merges.
   int ndp, ntail, ksplit;
   float *part;
-  unsigned int *ticket;
 };
 
 namespace {
@@ -149,8 +151,6 @@ __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p
     cs[threadIdx.x] = make_float4(ch, sh, static_cast<float>(cv - ch), static_cast<float>(sv - sh));
   }
   griddep_wait();  // `out` and the cache rows are written below
-  if (blockIdx.x == 0)  // the merge tickets start at zero (a merge also returns its ticket to zero)
-    for (int r = threadIdx.x; r < p.ntail; r += blockDim.x) p.ticket[r] = 0;
   if (!ok) {
     // a chunk outside [0, max_seq_len): flagged, nothing appended, zeros for its output
     // (the attention kernel gives it no work)
@@ -232,7 +232,6 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
-  int *merge_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -553,13 +552,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         }
       }
     } else if (nt > 0) {
-      // A part of a cut tile: leave (O, m, l) in its slot, take the tile's ticket; the last
-      // of its non-empty parts merges them: M = max m_k,
-      // out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k.
-      const int r = tile - p.ndp;
-      auto slot = [&](int pt) { return p.part + (static_cast<long long>(r) * p.ksplit + pt) * kPartFloats; };
-      auto part_has_tiles = [&](int pt) { return n * pt / p.ksplit < n * (pt + 1) / p.ksplit; };
-      float *mine = slot(part);
+      // A part of a cut tile: leave (O, m, l) in its slot for prefill_merge_kernel.
+      float *mine = p.part + (static_cast<long long>(tile - p.ndp) * p.ksplit + part) * kPartFloats;
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float o[32];
@@ -575,64 +569,6 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       }
       mine[kHeadDim * kPfRows + row] = m_run;
       mine[(kHeadDim + 1) * kPfRows + row] = have_o ? l_run : 0.f;
-      __threadfence();
-      asm volatile("bar.sync 1, %0;" ::"n"(kPfRows) : "memory");  // the four softmax warps
-      if (row == 0) {
-        int np = 0;
-        for (int pt = 0; pt < p.ksplit; ++pt) np += part_has_tiles(pt) ? 1 : 0;
-        const unsigned prev = atomicAdd(&p.ticket[r], 1u);
-        const bool last = prev == static_cast<unsigned>(np - 1);
-        if (last) {
-          __threadfence();
-          p.ticket[r] = 0;  // ready for the next call
-        }
-        *merge_flag = last ? 1 : 0;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kPfRows) : "memory");
-      if (*merge_flag) {
-        // weight of part pt for this row: 2^(m_pt - M) / L (0 for an empty part or a row
-        // the part did not see)
-        float wgt[kPfMaxSplit];
-        float M = -INFINITY, L = 0.f;
-#pragma unroll
-        for (int pt = 0; pt < kPfMaxSplit; ++pt) {
-          wgt[pt] = 0.f;
-          if (pt < p.ksplit && part_has_tiles(pt)) {
-            const float lv = __ldcg(slot(pt) + (kHeadDim + 1) * kPfRows + row);
-            const float mv = __ldcg(slot(pt) + kHeadDim * kPfRows + row);
-            wgt[pt] = lv > 0.f ? mv : -INFINITY;  // m for now
-            if (lv > 0.f) M = fmaxf(M, mv);
-          } else {
-            wgt[pt] = -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int pt = 0; pt < kPfMaxSplit; ++pt) {
-          if (wgt[pt] != -INFINITY) {
-            const float f = fast_exp2(wgt[pt] - M);
-            L += f * __ldcg(slot(pt) + (kHeadDim + 1) * kPfRows + row);
-            wgt[pt] = f;
-          } else {
-            wgt[pt] = 0.f;
-          }
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-        for (int pt = 0; pt < kPfMaxSplit; ++pt) wgt[pt] *= inv;
-        for (int c8 = 0; c8 < kHeadDim / 8; ++c8) {
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int pt = 0; pt < kPfMaxSplit; ++pt) {
-            if (wgt[pt] == 0.f) continue;
-            const float *pp = slot(pt) + (8 * c8) * kPfRows + row;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wgt[pt], __ldcg(pp + e * kPfRows), acc[e]);
-          }
-          if (in_block)
-            reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
-                                                            pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
-        }
-      }
     }
   }
 
@@ -648,6 +584,58 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   }
 }
 
+// ------------------------------------------------------------------------------ merge
+// One CTA per (cut query tile r, 16 dims), four threads per row of the tile's 128-row M
+// tile (row = token-in-block * G + head, as in the attention kernel), four dims each.  It
+// waits for the attention kernel, weighs the non-empty parts of its row --
+// w_k = 2^(m_k - M) / L with M = max m_k, L = sum 2^(m_k - M) l_k -- and writes its dims of
+// the row in bf16.  A thread's loads of all parts are issued before the sums.
+constexpr int kPfMergeDims = 16;                     // dims a merge CTA covers
+constexpr int kPfMergeThreads = kPfRows * (kPfMergeDims / 4);
+__global__ void __launch_bounds__(kPfMergeThreads) prefill_merge_kernel(const PrefillParams p) {
+  griddep_wait();  // the attention kernel's partials
+  const int r = static_cast<int>(blockIdx.x);
+  const int row = static_cast<int>(threadIdx.x) % kPfRows;
+  const int d0 = kPfMergeDims * static_cast<int>(blockIdx.y) + 4 * (static_cast<int>(threadIdx.x) / kPfRows);
+  const int tile = p.ndp + r;
+  const int bk = p.B * p.Hkv;
+  const int qb = p.nqb - 1 - tile / bk;
+  const int rem = tile % bk;
+  const int b = rem / p.Hkv, kv = rem - b * p.Hkv;
+  const int t0 = qb * p.Tt, t_end = min(t0 + p.Tt, p.T);
+  const int s0 = p.q_start[b];
+  if (!chunk_ok(p, s0)) return;  // the prologue wrote this chunk's zeros
+  const int n = (s0 + t_end - 1) / kTile + 1;  // the tile's KV tiles, cut into ksplit parts
+  const int tl = row / p.G, g = row - tl * p.G, t = t0 + tl;
+  if (!(tl < p.Tt && t < t_end)) return;
+  auto slot = [&](int pt) { return p.part + (static_cast<long long>(r) * p.ksplit + pt) * kPartFloats; };
+  float mv[kPfMaxSplit], lv[kPfMaxSplit], x[kPfMaxSplit][4];
+#pragma unroll
+  for (int pt = 0; pt < kPfMaxSplit; ++pt) {  // every load first: (m, l) and the four dims
+    const bool has = pt < p.ksplit && n * pt / p.ksplit < n * (pt + 1) / p.ksplit;
+    const float *sp = slot(pt < p.ksplit ? pt : 0);
+    mv[pt] = has ? __ldcg(sp + kHeadDim * kPfRows + row) : -INFINITY;
+    lv[pt] = has ? __ldcg(sp + (kHeadDim + 1) * kPfRows + row) : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[pt][e] = has ? __ldcg(sp + (d0 + e) * kPfRows + row) : 0.f;
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int pt = 0; pt < kPfMaxSplit; ++pt)
+    if (lv[pt] > 0.f) M = fmaxf(M, mv[pt]);  // a part that saw none of the row's keys has l = 0
+  float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int pt = 0; pt < kPfMaxSplit; ++pt) {
+    const float f = lv[pt] > 0.f ? fast_exp2(mv[pt] - M) : 0.f;
+    L += f * lv[pt];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[e] = fmaf(f, x[pt][e], acc[e]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint16_t *dst = p.out + ((static_cast<long long>(b) * p.T + t) * p.Hq + kv * p.G + g) * kHeadDim + d0;
+  *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+}
+
 // --------------------------------------------------------------------------- host side
 
 namespace {
@@ -657,7 +645,6 @@ struct PfDevice {
   bool configured = false;
   int sms = 0;
   float *part = nullptr;
-  unsigned int *ticket = nullptr;
 };
 PfDevice g_pf_dev[64];
 
@@ -684,9 +671,8 @@ bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 
 // A per-call error word when the caller passes none (nothing reads it).
 static __device__ uint32_t g_prefill_err_sink;
-// Partials of the query tiles cut into KV parts, and their merge tickets.
+// Partials of the query tiles cut into KV parts.
 static __device__ __align__(16) float g_pf_part[kPfMaxSlots * kPartFloats];
-static __device__ unsigned int g_pf_ticket[kPfMaxSlots];
 
 }  // namespace gqa
 
@@ -721,7 +707,7 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
     std::lock_guard<std::mutex> lk(g_pf_mu);
     PfDevice &pd = g_pf_dev[d.device];
     if (!pd.configured) {
-      void *part = nullptr, *ticket = nullptr;
+      void *part = nullptr;
       if (cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
               cudaSuccess ||
           cudaFuncSetAttribute(prefill_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRopeMaxSmem) !=
@@ -729,13 +715,11 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
           cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
           cudaDeviceGetAttribute(&pd.sms, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess ||
-          cudaGetSymbolAddress(&part, g_pf_part) != cudaSuccess ||
-          cudaGetSymbolAddress(&ticket, g_pf_ticket) != cudaSuccess) {
+          cudaGetSymbolAddress(&part, g_pf_part) != cudaSuccess) {
         cudaGetLastError();
         return GQA_ERR_CUDA;
       }
       pd.part = static_cast<float *>(part);
-      pd.ticket = static_cast<unsigned int *>(ticket);
       pd.configured = true;
     }
     dev = pd;
@@ -764,7 +748,6 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   p.out = static_cast<uint16_t *>(out);
   p.err = err;
   p.part = dev.part;
-  p.ticket = dev.ticket;
   p.B = d.batch;
   p.T = d.chunk_len;
   p.Hq = d.num_q_heads;
@@ -821,6 +804,9 @@ extern "C" gqa_status_t gqa_prefill_attn(const gqa_prefill_desc_t *desc, const v
   const unsigned grid = static_cast<unsigned>(p.ndp + p.ntail * p.ksplit);
   if (launch_pdl(prefill_attn_kernel, dim3(grid), dim3(kPfThreads), static_cast<size_t>(kSmemBytes), s, tq, tk, tv,
                  p) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  if (p.ntail > 0 && launch_pdl(prefill_merge_kernel, dim3(static_cast<unsigned>(p.ntail), kHeadDim / kPfMergeDims),
+                                dim3(kPfMergeThreads), 0, s, p) != cudaSuccess)
     return GQA_ERR_CUDA;
   return GQA_OK;
 }
