@@ -109,6 +109,32 @@ def test_prefill_parity(name):
     check_cache(w, k0, v0, ref)
 
 
+def test_v_values_far_from_unit_scale():
+    """P V keeps V's bf16 range: KV head 2's values scaled by 2^-20 (every value far below
+    fp16's normal range), KV head 5 holding 70000 in a cache row and -1e6 in a chunk row
+    (beyond fp16's largest), the other heads ordinary.  Every KV head but 5 is held to the
+    relative L2 bound on its own scale; head 5's outputs, up to ~10^4, element by element to
+    one bf16 step of the exact value plus 10^-3 of the head's largest."""
+    B, Hq, Hkv, T = 1, 40, 8, 77
+    w = wl.make_prefill(B, Hq, Hkv, T, [130], paged=False, seed=5, max_seq=256, device="cuda", name="v-range")
+    w.v_cache[:, :, 2] *= 2.0 ** -20
+    w.v_new[:, :, 2] *= 2.0 ** -20
+    w.v_cache[0, 10, 5, 7] = 70000.0
+    w.v_new[0, 40, 5, 100] = -1e6
+    ref = oracle_prefill(w)
+    assert ref["status"] == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, err)
+    assert int(err.item()) == 0
+    g = out.float().cpu().double().numpy().reshape(T, Hkv, Hq // Hkv, w.d)
+    r = ref["out"].reshape(T, Hkv, Hq // Hkv, w.d)
+    assert np.all(np.isfinite(g))
+    rels = {kv: float(np.linalg.norm(g[:, kv] - r[:, kv]) / np.linalg.norm(r[:, kv])) for kv in range(Hkv) if kv != 5}
+    assert max(rels.values()) <= 2e-3, rels
+    big = np.abs(r[:, 5])
+    assert np.all(np.abs(g[:, 5] - r[:, 5]) <= 2.0 ** -8 * big + 1e-3 * big.max())
+
+
 def test_prompt_fed_in_chunks_matches_one_call():
     """A 300-token prompt through three calls (128 + 128 + 44 tokens, each on the cache the
     previous one left) gives the outputs of the oracle's single 300-token chunk."""
