@@ -52,9 +52,10 @@ def oracle_out_on(w, ref, pairs=None):
 FORMS = [0, -1]
 
 
-def run_gpu(w, cluster_size=0):
+def run_gpu(w, cluster_size=0, ordered_start=False):
     plan = binding.Plan(w.B, w.Hq, w.Hkv, w.max_seq, block_size=w.block_size, num_cache_blocks=w.num_blocks,
-                        seq_lens_host=w.seq_lens.cpu().numpy(), cluster_size=cluster_size)
+                        seq_lens_host=w.seq_lens.cpu().numpy(), cluster_size=cluster_size,
+                        ordered_start=ordered_start)
     out = torch.full((w.B, w.Hq, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
     plan.run_q4(w, out)
     torch.cuda.synchronize()
@@ -159,6 +160,23 @@ def test_q4_full_size_ragged_on_sampled_heads():
     got = torch.stack([out[int(b), int(h)] for b, h in pairs])
     max_abs, rel = out_errors(got, oracle_out_on(w, ref, pairs=pairs))
     assert max_abs <= 1e-2 and rel <= 2e-3, (max_abs, rel)
+
+
+@pytest.mark.parametrize("ordered", [False, True])
+def test_q4_more_segments_than_one_wave(ordered):
+    """192 (sequence, KV head) segments of 1..600 tokens -- more one-CTA clusters than the GPU
+    holds at once, so that they launch longest first in the plan's order -- with overlapping
+    and with ordered starts: every output and appended row against the oracle."""
+    lens = wl.ragged_lengths(24, 1, 600, seed=27)
+    w = wl.make_q4(24, 16, 8, lens, paged=True, seed=27, max_seq=640, device="cuda", name="one-cta-waves")
+    k0, v0, ks0, vs0 = np_u8(w.k_idx), np_u8(w.v_idx), np_u8(w.k_scale), np_u8(w.v_scale)
+    ref = oracle_q4(w)
+    assert ref["status"] == 0
+    plan, out = run_gpu(w, ordered_start=ordered)
+    assert plan.cluster_size == 1
+    assert plan.device_errors() == 0
+    assert check_appended(w, k0, v0, ks0, vs0, ref) <= 8
+    assert_out_close(out, oracle_out_on(w, ref), f"one-CTA waves, ordered={ordered}")
 
 
 @pytest.mark.parametrize("form", FORMS)
