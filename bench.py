@@ -592,10 +592,13 @@ def run_q4(name: str, steps: int, warmup: int, local: int):
             "l2": l2_note, "steps": steps, "clocks_sm_mhz": clk.result["sm_mhz"]}
 
 
-def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0):
-    """The fp64 oracle, as it stands, on the host cores: whole decode steps of the workload
-    (for the 40-layer sweep: whole layers, scaled by the step's layer count) until
-    ~budget_s of CPU time."""
+_ORACLE_CORES = []  # the oracle's thread count before anything changed it
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0, threads: int = 0):
+    """The fp64 oracle, as it stands, on the host cores (all of them, or `threads`): whole
+    decode steps of the workload (for the 40-layer sweep: whole layers, scaled by the step's
+    layer count) until ~budget_s of CPU time."""
     import oracle
     from gqa_decode_attention_fa_gb300 import workloads as wl
     from gqa_decode_attention_fa_gb300.workloads import bits, ints
@@ -604,7 +607,9 @@ def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0):
     args = [bits(w.q_new), bits(w.k_new), bits(w.v_new), bits(w.k_cache), bits(w.v_cache), ints(w.page_table),
             ints(w.seq_lens), ints(w.positions), bits(w.q_norm_w), bits(w.k_norm_w), w.rope_theta, w.eps]
     g = oracle.geom(w.B, w.Hq, w.Hkv, w.d, w.block_size, w.max_seq, w.num_rows)
-    threads = oracle.max_threads()
+    if not _ORACLE_CORES:
+        _ORACLE_CORES.append(oracle.max_threads())
+    oracle.set_threads(threads or _ORACLE_CORES[0])
     times = []
     t_all = time.perf_counter()
     while True:
@@ -613,6 +618,7 @@ def cpu_baseline(name: str, budget_s: float = 12.0, layers: int = 0):
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all > budget_s or len(times) >= 200:
             break
+    oracle.set_threads(_ORACLE_CORES[0])  # leave the oracle on all cores
     per_unit = statistics.median(times)
     layers = (layers or wl.LAYERS_40) if name == "qwen3-14b-40layer" else 1
     unit = "layer" if name == "qwen3-14b-40layer" else "step"
@@ -720,6 +726,11 @@ def main():
                     "invocations": r["invocations"], "kv_gbs": r["kv_gbs"], "roofline": r["roofline"],
                     "e2e_us": r["e2e"]["value"], "steps": r["steps"], "form": r["config"]["form"],
                     "l2": r["config"]["l2"], "clocks_sm_mhz": r["clocks"]["sm_mhz"]}
+        if rank == 0 and not args.no_cpu_baseline:
+            # the oracle on all host cores, and on one core for the two short steps
+            by[name]["cpu_baseline"] = cpu_baseline(name, budget_s=3.0)
+            if name in ("qwen3-14b-tiny", "qwen3-14b-4k"):
+                by[name]["cpu_baseline_1_core"] = cpu_baseline(name, budget_s=3.0, threads=1)
     if by:
         result["by_config"] = by
     if rank == 0:
