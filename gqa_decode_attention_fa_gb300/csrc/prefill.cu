@@ -121,10 +121,10 @@ __device__ __forceinline__ long long cache_row_of(const PrefillParams &p, int b,
 // One CTA per chunk token (blockIdx.x = b * T + i).  The token's query, key and value rows
 // are contiguous in q/k/v_new, so one bulk copy each brings them into shared memory while
 // the CTA computes cos/sin of the token's position; then warp w rotates rows w, w + 8, ...
-// of the H_q query heads followed by the H_kv key heads (lane l holds dims l + 32 t) from
-// shared memory.  The inputs are read before the wait on the preceding kernel; `out` and the
+// of the H_q query heads followed by the H_kv key heads (lane l holds dims 2l, 2l + 1,
+// 2l + 64, 2l + 65) from shared memory.  The inputs are read before the wait on the preceding kernel; `out` and the
 // cache are written after it.
-__global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(256, 6) prefill_rope_kernel(const PrefillParams p) {
   __shared__ float4 cs[kHeadDim / 2];  // (cos_hi, sin_hi, cos_lo, sin_lo) of pair i
   __shared__ __align__(8) uint64_t rows_bar;
   extern __shared__ __align__(16) uint8_t rope_rows[];  // [H_q + 2 H_kv][128] bf16: q, k, v rows
@@ -168,49 +168,59 @@ __global__ void __launch_bounds__(256) prefill_rope_kernel(const PrefillParams p
   }
   const long long crow = cache_row_of(p, b, pos);
   if (crow < 0 && threadIdx.x == 0) atomicOr(p.err, GQA_DEVERR_PAGE);
-  const float4 c0 = cs[lane], c1 = cs[lane + 32];
-  const uint16_t *rq = reinterpret_cast<const uint16_t *>(rope_rows);
+  // Lane l holds dims 2l, 2l + 1 and their RoPE partners 2l + 64, 2l + 65 of a row (one
+  // 32-bit word each half), so that a row is read and written in two 32-bit accesses a lane
+  // and both pairs stay in the lane.
+  const float4 c0 = cs[2 * lane], c1 = cs[2 * lane + 1];
+  const uint32_t *rw = reinterpret_cast<const uint32_t *>(rope_rows);  // [row][64] bf16 pairs
+  uint32_t qw0 = 0u, qw1 = 0u, kw0 = 0u, kw1 = 0u;  // the norm weights of the lane's dims
+  if (p.q_norm_w) {
+    qw0 = reinterpret_cast<const uint32_t *>(p.q_norm_w)[lane];
+    qw1 = reinterpret_cast<const uint32_t *>(p.q_norm_w)[32 + lane];
+  }
+  if (p.k_norm_w) {
+    kw0 = reinterpret_cast<const uint32_t *>(p.k_norm_w)[lane];
+    kw1 = reinterpret_cast<const uint32_t *>(p.k_norm_w)[32 + lane];
+  }
   for (int r = warp; r < p.Hq + p.Hkv; r += 8) {
     if (r < p.Hq) {
       // query row: binary32, one bf16 rounding (it is not stored in the cache)
-      const uint16_t *src = rq + r * kHeadDim;
-      float y[4], ss = 0.f;
+      const uint32_t a = rw[r * 64 + lane], c = rw[r * 64 + 32 + lane];
+      const float x[4] = {bf16_lo_to_float(a), bf16_hi_to_float(a), bf16_lo_to_float(c), bf16_hi_to_float(c)};
+      float ss = 0.f;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float x = bf16_bits_to_float(src[lane + 32 * t]);
-        ss = fmaf(x, x, ss);
-        y[t] = p.q_norm_w ? x * bf16_bits_to_float(p.q_norm_w[lane + 32 * t]) : x;
+      for (int t = 0; t < 4; ++t) ss = fmaf(x[t], x[t], ss);
+      float y[4];
+      if (p.q_norm_w) {
+        y[0] = x[0] * bf16_lo_to_float(qw0), y[1] = x[1] * bf16_hi_to_float(qw0);
+        y[2] = x[2] * bf16_lo_to_float(qw1), y[3] = x[3] * bf16_hi_to_float(qw1);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) y[t] = x[t];
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const float rn = p.q_norm_w ? 1.0f / sqrtf(ss * (1.0f / 128.0f) + p.eps) : 1.0f;
-      uint16_t *dst = p.out + (tok * p.Hq + r) * kHeadDim;
       const float z0 = rn * fmaf(y[0], c0.x, -y[2] * c0.y), z2 = rn * fmaf(y[2], c0.x, y[0] * c0.y);
       const float z1 = rn * fmaf(y[1], c1.x, -y[3] * c1.y), z3 = rn * fmaf(y[3], c1.x, y[1] * c1.y);
-      const float z[4] = {z0, z1, z2, z3};
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(z[t]);
-        dst[lane + 32 * t] = *reinterpret_cast<const uint16_t *>(&h);
-      }
+      uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + (tok * p.Hq + r) * kHeadDim);
+      dst[lane] = pack_bf16(z0, z1);
+      dst[32 + lane] = pack_bf16(z2, z3);
     } else if (crow >= 0) {
       const int kv = r - p.Hq;
-      const uint16_t *ksrc = rq + (p.Hq + kv) * kHeadDim;
-      const uint16_t *vsrc = rq + (p.Hq + p.Hkv + kv) * kHeadDim;
-      uint16_t x[4], w[4], kz[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        x[t] = ksrc[lane + 32 * t];
-        w[t] = p.k_norm_w ? p.k_norm_w[lane + 32 * t] : uint16_t(0);
-      }
+      const uint32_t a = rw[(p.Hq + kv) * 64 + lane], c = rw[(p.Hq + kv) * 64 + 32 + lane];
+      const uint16_t x[4] = {static_cast<uint16_t>(a & 0xffffu), static_cast<uint16_t>(a >> 16),
+                             static_cast<uint16_t>(c & 0xffffu), static_cast<uint16_t>(c >> 16)};
+      const uint16_t w[4] = {static_cast<uint16_t>(kw0 & 0xffffu), static_cast<uint16_t>(kw0 >> 16),
+                             static_cast<uint16_t>(kw1 & 0xffffu), static_cast<uint16_t>(kw1 >> 16)};
+      uint16_t kz[4];
       rotate_row_k(x, w, p.k_norm_w != nullptr, p.eps, c0, c1, kz);
-      uint16_t *kd = p.k_cache + (crow * p.Hkv + kv) * kHeadDim;
-      uint16_t *vd = p.v_cache + (crow * p.Hkv + kv) * kHeadDim;
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        kd[lane + 32 * t] = kz[t];
-        vd[lane + 32 * t] = vsrc[lane + 32 * t];
-      }
+      uint32_t *kd = reinterpret_cast<uint32_t *>(p.k_cache + (crow * p.Hkv + kv) * kHeadDim);
+      uint32_t *vd = reinterpret_cast<uint32_t *>(p.v_cache + (crow * p.Hkv + kv) * kHeadDim);
+      kd[lane] = static_cast<uint32_t>(kz[0]) | (static_cast<uint32_t>(kz[1]) << 16);
+      kd[32 + lane] = static_cast<uint32_t>(kz[2]) | (static_cast<uint32_t>(kz[3]) << 16);
+      vd[lane] = rw[(p.Hq + p.Hkv + kv) * 64 + lane];
+      vd[32 + lane] = rw[(p.Hq + p.Hkv + kv) * 64 + 32 + lane];
     }
   }
 }

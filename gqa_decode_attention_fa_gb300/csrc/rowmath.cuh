@@ -71,9 +71,10 @@ __device__ __forceinline__ uint16_t round_dw_bf16(dw z) {
 }
 
 // One warp computes RoPE_pos(RMSNorm(x, w)) of a 128-dim bf16 row x and rounds each element
-// once to bf16.  Lane l holds dims {l, l+32, l+64, l+96} of x (and of w, when has_w), so the
-// RoPE pairs (l, l+64) and (l+32, l+96) stay in the lane; out[t] is dim l + 32 t.  cs0/cs1
-// are the double-word (cos_hi, sin_hi, cos_lo, sin_lo) of the angles of pairs l and l+32.
+// once to bf16.  Each lane holds four dims of x (and of w, when has_w) as two RoPE pairs:
+// x[0] with its partner x[2], x[1] with x[3] (the decode step: dims l, l+32, l+64, l+96; the
+// prefill prologue: 2l, 2l+1, 2l+64, 2l+65); out[t] is the dim of x[t].  cs0/cs1 are the
+// double-word (cos_hi, sin_hi, cos_lo, sin_lo) of the angles of the pairs of x[0] and x[1].
 //   ss = sum x^2: the squares are exact in binary32 (8-bit significands) and are summed in
 //     double-word, in the lane and over the shuffle tree (every lane gets the same sum);
 //   r = 1/sqrt(ss/128 + eps): a correctly rounded binary32 seed and one Newton step in
