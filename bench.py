@@ -726,7 +726,8 @@ def main():
                     "invocations": r["invocations"], "kv_gbs": r["kv_gbs"], "roofline": r["roofline"],
                     "e2e_us": r["e2e"]["value"], "steps": r["steps"], "form": r["config"]["form"],
                     "l2": r["config"]["l2"], "clocks_sm_mhz": r["clocks"]["sm_mhz"]}
-        if rank == 0 and not args.no_cpu_baseline:
+        from gqa_decode_attention_fa_gb300 import workloads as wl
+        if rank == 0 and not args.no_cpu_baseline and name in wl.WORKLOADS:
             # the oracle on all host cores, and on one core for the two short steps
             by[name]["cpu_baseline"] = cpu_baseline(name, budget_s=3.0)
             if name in ("qwen3-14b-tiny", "qwen3-14b-4k"):
