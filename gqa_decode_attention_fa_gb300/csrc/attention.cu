@@ -1,4 +1,7 @@
-// Split-KV decode attention over a bf16 KV cache (sm_103a).
+// Decode attention over a bf16 KV cache (sm_103a): the split-KV kernel (a worker
+// partition of the batch's tiles, partials merged by the combine kernel) and, further
+// down, the single-launch kernel (a thread-block cluster per segment, merged on chip),
+// which share the producer / consumer ring and the per-tile recurrence.
 //
 // What it computes -- for each query head h of sequence b, over its KV tiles -- is the
 // FlashAttention per-tile recurrence of "ADR-0060: AHBM GQA Fused Attention Kernel
@@ -755,9 +758,10 @@ __global__ void __launch_bounds__(kThreadsAttn, 1)
 }
 
 // ------------------------------------------------------------------ single-launch form
-// The whole decode step in one launch, for batches with few (sequence, KV head) segments
-// (short and mid contexts of one or a few sequences, where the step is bound by latency):
-// one thread-block cluster of C = p.csize CTAs per segment.  CTA rank r of the cluster
+// The whole decode step in one launch: one thread-block cluster of C = p.csize CTAs per
+// (sequence, KV head) segment -- several CTAs per segment for a few long sequences, C = 1
+// for batches with more segments than SMs (then, when the clusters come in more than one
+// wave and the plan gives an order, the segments start longest first).  CTA rank r of the cluster
 // streams the segment's tiles r, r + C, r + 2C, ... through the same producer / consumer
 // ring as the split-KV kernel and runs the same per-tile recurrence; the partials never
 // leave the chip.  Each CTA merges its six consumer warps' (m, l, O) in shared memory and
