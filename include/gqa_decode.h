@@ -151,8 +151,11 @@ typedef struct gqa_plan gqa_plan_t; /* opaque; owns the workspace (rotated q, fp
  * last call (contiguous caches: prefetched into L2 at the start of the next call) and
  * staging buffers for gqa_decode_attn_host.
  *   desc          : geometry (copied).
- *   seq_lens_host : optional host array [B] of expected lengths used only to size the
- *                   worker count; NULL plans for B sequences of max_seq_len tokens.
+ *   seq_lens_host : optional host array [B] of expected lengths, used to choose the form,
+ *                   the worker count and the cluster size, and to order the segments
+ *                   longest first when the clusters come in more than one wave; NULL
+ *                   plans for B sequences of max_seq_len tokens.  Other lengths at call
+ *                   time are computed correctly, only possibly with a worse choice.
  *   plan          : receives the new plan.
  * Errors: GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE.
  * Synchronous (allocates device memory).
