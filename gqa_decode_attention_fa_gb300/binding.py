@@ -20,7 +20,7 @@ from . import build as _build
 (GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED, GQA_ERR_CUDA, GQA_ERR_WORKSPACE,
  GQA_ERR_SCRATCH_LIMIT) = range(6)
 STATIC_SCRATCH_BYTES = 32 << 20
-DEVERR_POSITION, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_POSITION, DEVERR_SEQLEN, DEVERR_PAGE, DEVERR_TIMEOUT, DEVERR_LAUNCH = 0x1, 0x2, 0x4, 0x8, 0x10
 HEADER = os.path.join(_build.ROOT, "include", "gqa_decode.h")
 HEADERS = _build.HEADERS
 

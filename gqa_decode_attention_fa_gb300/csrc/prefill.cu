@@ -16,7 +16,8 @@
 //    (double-word arithmetic, rounded to bf16 as the exact value rounds) and v row.
 //  * prefill_attn_kernel: one CTA per (sequence, KV head, block of Tt = 128 / G chunk
 //    tokens); its 128-row M tile stacks those tokens' G heads.  A TMA warp streams 64-token
-//    K/V tiles into a 2-stage ring (K and V released separately); an MMA warp issues
+//    K tiles into a 2-stage ring and V tiles into a 3-stage one (a K tile is released once
+//    S has used it, a V tile after P V); an MMA warp issues
 //    S = Q K^T (M = 128, N = 64, K = 128) into tensor memory (two S buffers) and
 //    O += P V (N = 128, K = 64) into a tensor-memory accumulator, P read from tensor
 //    memory; four softmax warps own one row each per thread (tensor-memory lane = row),
@@ -45,7 +46,8 @@ namespace gqa {
 
 namespace {
 
-constexpr int kPfStages = 2;                    // K/V ring depth (K and V released separately)
+constexpr int kPfKStages = 2;                   // K ring depth (a K tile is released once S has used it)
+constexpr int kPfVStages = 3;                   // V ring depth (a V tile is released after P V)
 constexpr int kPfSoftmaxWarps = 4;              // one row per thread, 128 rows
 constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 2);  // + TMA warp + MMA warp
 constexpr int kPfProducerWarp = kPfSoftmaxWarps;
@@ -60,14 +62,17 @@ constexpr uint32_t kTmemO = 128;
 constexpr float kRescaleLog2 = 8.f;             // lazy rescale threshold (P <= 2^8)
 
 constexpr int kQBytes = 2 * kPfRows * kHalfRowBytes;     // 32 KiB: two 64-dim panels
-constexpr int kStageBytes = 4 * kHalfTileBytes;           // 32 KiB: K lo, K hi, V lo, V hi
+constexpr int kKvTileBytes = 2 * kHalfTileBytes;          // 16 KiB: a K or V tile's two 64-dim halves
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffBar = kOffKV + kPfStages * kStageBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + kPfKStages * kKvTileBytes;
+constexpr int kOffBar = kOffV + kPfVStages * kKvTileBytes;
+// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
 // o_done, drain
-constexpr int kNumBars = 1 + 4 * kPfStages + 2 + 2 + 1 + 1;
-constexpr int kSmemBytes = 1024 + kOffBar + 8 * kNumBars + 16;
+constexpr int kNumBars = 1 + 2 * kPfKStages + 2 * kPfVStages + 2 + 2 + 1 + 1;
+// The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle needs it);
+// the kernel checks it rather than reserving slack, so that two CTAs fit an SM.
+constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 16;
 constexpr int kPfMaxSlots = 320;                // split-tile partials the static scratch holds
 constexpr int kPfMaxSplit = 8;                  // KV parts of one split query tile
 // A partial is column-major, [130][128 rows] floats: O columns, then m, then l, so that the
@@ -76,6 +81,7 @@ constexpr int kPartFloats = (kHeadDim + 2) * kPfRows;
 // The prologue holds a token's H_q + 2 H_kv rows in shared memory (256 B each).
 constexpr int kRopeMaxSmem = 200 * 1024;
 static_assert(kPfCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "two prefill CTAs must share an SM");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kKvTileBytes % 1024 == 0, "swizzled tiles 1024-aligned");
 static_assert(kPfCtasPerSm * kPfTmemCols <= 512, "tensor memory of the co-resident CTAs");
 
 }  // namespace
@@ -229,15 +235,19 @@ __global__ void __launch_bounds__(256, 6) prefill_rope_kernel(const PrefillParam
 __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align_smem_1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if ((smem_addr(smem_raw) & 1023u) != 0u) {  // a launch assumption broken: no work at all
+    if (threadIdx.x == 0) atomicOr(p.err, GQA_DEVERR_LAUNCH);
+    return;
+  }
+  uint8_t *smem = smem_raw;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   uint64_t *q_full = bars;
   uint64_t *k_full = bars + 1;
-  uint64_t *k_empty = k_full + kPfStages;
-  uint64_t *v_full = k_empty + kPfStages;
-  uint64_t *v_empty = v_full + kPfStages;
-  uint64_t *s_full = v_empty + kPfStages;
+  uint64_t *k_empty = k_full + kPfKStages;
+  uint64_t *v_full = k_empty + kPfKStages;
+  uint64_t *v_empty = v_full + kPfVStages;
+  uint64_t *s_full = v_empty + kPfVStages;
   uint64_t *p_full = s_full + 2;
   uint64_t *o_done = p_full + 2;
   uint64_t *drain = o_done + 1;
@@ -295,7 +305,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
   const int j0 = split ? n * part / p.ksplit : 0, j1 = split ? n * (part + 1) / p.ksplit : n;
   const int nt = j1 - j0;
   uint8_t *const qs = smem + kOffQ;
-  auto stage_ptr = [&](int s) { return smem + kOffKV + s * kStageBytes; };
+  auto k_ptr = [&](int s) { return smem + kOffK + s * kKvTileBytes; };
+  auto v_ptr = [&](int s) { return smem + kOffV + s * kKvTileBytes; };
 
   if (warp == kPfProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
@@ -319,11 +330,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       bool ok = true;
       // i counts the item's KV tiles (stages and phases), j = j0 + i is the tile
       auto load_k = [&](int i) -> bool {
-        const int s = i % kPfStages;
-        if (i >= kPfStages && !mbar_wait(smem_addr(&k_empty[s]), static_cast<uint32_t>((i / kPfStages - 1) & 1)))
+        const int s = i % kPfKStages;
+        if (i >= kPfKStages && !mbar_wait(smem_addr(&k_empty[s]), static_cast<uint32_t>((i / kPfKStages - 1) & 1)))
           return false;
         const int row = row_of(j0 + i);
-        const uint32_t fb = smem_addr(&k_full[s]), base = smem_addr(stage_ptr(s));
+        const uint32_t fb = smem_addr(&k_full[s]), base = smem_addr(k_ptr(s));
         mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
         tma_load_3d(base, &tmK, fb, 0, kv, row);
         tma_load_3d(base + kHalfTileBytes, &tmK, fb, 64, kv, row);
@@ -331,11 +342,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         return true;
       };
       auto load_v = [&](int i) -> bool {
-        const int s = i % kPfStages;
-        if (i >= kPfStages && !mbar_wait(smem_addr(&v_empty[s]), static_cast<uint32_t>((i / kPfStages - 1) & 1)))
+        const int s = i % kPfVStages;
+        if (i >= kPfVStages && !mbar_wait(smem_addr(&v_empty[s]), static_cast<uint32_t>((i / kPfVStages - 1) & 1)))
           return false;
         const int row = row_of(j0 + i);
-        const uint32_t fb = smem_addr(&v_full[s]), base = smem_addr(stage_ptr(s)) + 2 * kHalfTileBytes;
+        const uint32_t fb = smem_addr(&v_full[s]), base = smem_addr(v_ptr(s));
         mbar_arrive_expect_tx(fb, 2 * kHalfTileBytes);
         tma_load_3d(base, &tmV, fb, 0, kv, row);
         tma_load_3d(base + kHalfTileBytes, &tmV, fb, 64, kv, row);
@@ -351,10 +362,10 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
         // Do not leave while copies into this CTA's shared memory may still be in flight.
         (void)mbar_wait(smem_addr(q_full), 0);
-        for (int j = (kissued > kPfStages ? kissued - kPfStages : 0); j < kissued; ++j)
-          (void)mbar_wait(smem_addr(&k_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
-        for (int j = (vissued > kPfStages ? vissued - kPfStages : 0); j < vissued; ++j)
-          (void)mbar_wait(smem_addr(&v_full[j % kPfStages]), static_cast<uint32_t>((j / kPfStages) & 1));
+        for (int j = (kissued > kPfKStages ? kissued - kPfKStages : 0); j < kissued; ++j)
+          (void)mbar_wait(smem_addr(&k_full[j % kPfKStages]), static_cast<uint32_t>((j / kPfKStages) & 1));
+        for (int j = (vissued > kPfVStages ? vissued - kPfVStages : 0); j < vissued; ++j)
+          (void)mbar_wait(smem_addr(&v_full[j % kPfVStages]), static_cast<uint32_t>((j / kPfVStages) & 1));
       }
     }
   } else if (warp == kPfMmaWarp) {
@@ -369,11 +380,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       // O += P_t V_t (hi then lo part of P, read from tensor memory), then release V_t
       // and mark O current.
       auto issue_pv = [&](int t) -> bool {
-        const int pb = t & 1, s = t % kPfStages;
-        if (!mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((t / kPfStages) & 1))) return false;
+        const int pb = t & 1, s = t % kPfVStages;
+        if (!mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((t / kPfVStages) & 1))) return false;
         if (!mbar_wait(smem_addr(&p_full[pb]), static_cast<uint32_t>((t >> 1) & 1))) return false;
         tc_fence_after();
-        const uint32_t va = smem_addr(stage_ptr(s)) + 2 * kHalfTileBytes;
+        const uint32_t va = smem_addr(v_ptr(s));
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
           umma_bf16_ts(tmem + kTmemO, tmem + 64 * pb + 8 * k, sdesc_sw128(va + 2048 * k, kHalfTileBytes, 1024), kIdO,
@@ -387,11 +398,11 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
         return true;
       };
       for (int j = 0; j < nt && ok; ++j) {  // j counts the item's KV tiles
-        const int s = j % kPfStages, sb = j & 1;
-        ok = mbar_wait(smem_addr(&k_full[s]), static_cast<uint32_t>((j / kPfStages) & 1));
+        const int s = j % kPfKStages, sb = j & 1;
+        ok = mbar_wait(smem_addr(&k_full[s]), static_cast<uint32_t>((j / kPfKStages) & 1));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t ka = smem_addr(stage_ptr(s));
+        const uint32_t ka = smem_addr(k_ptr(s));
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k)
           umma_bf16(tmem + 64 * sb, sdesc_sw128(qa + (k >> 2) * (kPfRows * kHalfRowBytes) + 32 * (k & 3), 16, 1024),
@@ -506,10 +517,10 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       if (j == n - 1) {
         const int vz = kmax - j * kTile + 1;  // first row to clear
         if (vz < kTile) {
-          const int s = i % kPfStages;
-          (void)mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((i / kPfStages) & 1));
-          uint4 *v0 = reinterpret_cast<uint4 *>(stage_ptr(s) + 2 * kHalfTileBytes);
-          uint4 *v1 = reinterpret_cast<uint4 *>(stage_ptr(s) + 3 * kHalfTileBytes);
+          const int s = i % kPfVStages;
+          (void)mbar_wait(smem_addr(&v_full[s]), static_cast<uint32_t>((i / kPfVStages) & 1));
+          uint4 *v0 = reinterpret_cast<uint4 *>(v_ptr(s));
+          uint4 *v1 = reinterpret_cast<uint4 *>(v_ptr(s) + kHalfTileBytes);
           for (int c = vz * 8 + row; c < kTile * 8; c += kPfRows) {
             v0[c] = make_uint4(0, 0, 0, 0);
             v1[c] = make_uint4(0, 0, 0, 0);

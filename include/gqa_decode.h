@@ -96,6 +96,7 @@ typedef enum gqa_status {
 #define GQA_DEVERR_SEQLEN 0x2u    /* seq_lens[b] outside [1, max_seq_len] */
 #define GQA_DEVERR_PAGE 0x4u      /* a page-table entry outside [0, num_cache_blocks) */
 #define GQA_DEVERR_TIMEOUT 0x8u   /* a pipeline wait gave up (the kernel returned early) */
+#define GQA_DEVERR_LAUNCH 0x10u   /* a launch assumption did not hold (the kernel did no work) */
 
 /* Shapes and layout a plan is built for. */
 typedef struct gqa_plan_desc {
