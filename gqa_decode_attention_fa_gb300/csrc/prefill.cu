@@ -310,8 +310,9 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
 
   if (warp == kPfProducerWarp) {
     // ------------------------------------------------------------------ TMA producer
-    // Order: K_0, K_1, V_0, K_2, V_1, ... -- a K tile is released once S has used it, a V
-    // tile only after P V, so K runs one tile ahead.
+    // Order: K_0, V_0, K_1, V_1, ... -- each V tile goes out with its K tile, so that it has
+    // landed by the time its P is ready (the V ring is one stage deeper than the K ring,
+    // since a V tile is held until P V).
     if (lane == 0 && nt > 0) {
       const uint32_t qb_bytes = 2u * 64u * 2u * static_cast<uint32_t>(p.G * p.Tt);
       mbar_arrive_expect_tx(smem_addr(q_full), qb_bytes);
@@ -355,9 +356,8 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
       };
       for (int i = 0; i < nt && ok; ++i) {
         ok = load_k(i);
-        if (ok && i >= 1) ok = load_v(i - 1);
+        if (ok) ok = load_v(i);
       }
-      if (ok) ok = load_v(nt - 1);
       if (!ok) {
         atomicOr(p.err, GQA_DEVERR_TIMEOUT);
         // Do not leave while copies into this CTA's shared memory may still be in flight.
