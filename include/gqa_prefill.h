@@ -67,9 +67,12 @@ typedef struct gqa_prefill_desc {
  *                 (the caller owns and clears it); NULL discards them.  A chunk outside
  *                 [0, max_seq_len) (GQA_DEVERR_POSITION for s_b < 0, GQA_DEVERR_SEQLEN for
  *                 s_b + T > max_seq_len) appends nothing and gives zeros for its output; a
- *                 page id outside the pool appends nothing there and reads that page as zeros.
+ *                 page id outside the pool appends nothing there and reads that page as zeros;
+ *                 GQA_DEVERR_LAUNCH: the attention kernel's shared memory was not 1024-byte
+ *                 aligned, and it did no work (not expected on any supported device).
  *   stream     cudaStream_t as void*
- * Launches two kernels with programmatic stream serialization: the prologue kernel (one
+ * Launches two kernels (three when the last round of query tiles is cut into KV parts,
+ * the third merging their partials) with programmatic stream serialization: the prologue kernel (one
  * CTA per chunk token) reads q/k/v_new, q_start and the page table before it waits for the
  * preceding kernel in the stream, and writes `out` and the cache only after; so the kernel
  * launched immediately before the call must not write those inputs if it triggers
