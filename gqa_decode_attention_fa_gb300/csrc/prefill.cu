@@ -67,7 +67,7 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kPfKStages * kKvTileBytes;
 constexpr int kOffBar = kOffV + kPfVStages * kKvTileBytes;
-// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
+// barriers: q_full, k_full[2], k_empty[2], v_full[3], v_empty[3], s_full[2], p_full[2],
 // o_done, drain
 constexpr int kNumBars = 1 + 2 * kPfKStages + 2 * kPfVStages + 2 + 2 + 1 + 1;
 // The dynamic shared memory is declared 1024-byte aligned (the 128-byte swizzle needs it);
@@ -128,8 +128,8 @@ __device__ __forceinline__ long long cache_row_of(const PrefillParams &p, int b,
 // are contiguous in q/k/v_new, so one bulk copy each brings them into shared memory while
 // the CTA computes cos/sin of the token's position; then warp w rotates rows w, w + 8, ...
 // of the H_q query heads followed by the H_kv key heads (lane l holds dims 2l, 2l + 1,
-// 2l + 64, 2l + 65) from shared memory.  The inputs are read before the wait on the preceding kernel; `out` and the
-// cache are written after it.
+// 2l + 64, 2l + 65) from shared memory.  The inputs are read before the wait on the
+// preceding kernel; `out` and the cache are written after it.
 __global__ void __launch_bounds__(256, 6) prefill_rope_kernel(const PrefillParams p) {
   __shared__ float4 cs[kHeadDim / 2];  // (cos_hi, sin_hi, cos_lo, sin_lo) of pair i
   __shared__ __align__(8) uint64_t rows_bar;
