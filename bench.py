@@ -35,6 +35,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 HEADLINE = "qwen3-14b-40layer"
+# Steps of each by_config row's graph (whatever --steps is): enough that a short step's
+# first launches, which have no preceding step to overlap, weigh little in the mean.
+BY_CONFIG_STEPS = 50
 METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -531,9 +534,8 @@ Q4 = ("qwen3-14b-4k-q4", "qwen3-14b-ragged-q4")
 
 
 def run_q4(name: str, steps: int, warmup: int, local: int):
-    """The decode step over a 4-bit cache (gqa_decode_attn_q4: prologue, attention on the
-    index tiles, combine), K steps as one CUDA graph replay between CUDA events after
-    warm-up.  Caches
+    """The decode step over a 4-bit cache (gqa_decode_attn_q4), K steps as one CUDA graph
+    replayed between CUDA events after warm-up, the median of seven replays.  Caches
     smaller than twice L2 are replicated (> 3x L2 of copies, rotated across steps) so that
     every step reads from HBM.  Roofline: the cache bytes a step reads (64 index bytes + a
     4-byte scale per token, KV head and tensor) over the step's time."""
@@ -570,14 +572,17 @@ def run_q4(name: str, steps: int, warmup: int, local: int):
                 plan.run_q4(sets[k % len(sets)], out, stream)
         graph.replay()
         stream.synchronize()
-        a.record(stream)
-        graph.replay()
-        b.record(stream)
-        stream.synchronize()
+        reps = []
+        for _ in range(7):  # the median of seven timed replays
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            stream.synchronize()
+            reps.append(a.elapsed_time(b) * 1e3 / steps)
         del graph
     if plan.device_errors() != 0:
         raise SystemExit("bench: device error flags set during the 4-bit-cache steps")
-    us = a.elapsed_time(b) * 1e3 / steps
+    us = statistics.median(reps)
     peak, src = hbm_peak()
     gbs = kvb / (us * 1e-6) / 1e9
     single = plan.cluster_size > 0
@@ -714,10 +719,10 @@ def main():
             torch.cuda.empty_cache()
             continue
         if name in Q4:
-            by[name] = run_q4(name, min(args.steps, 50), args.warmup, local)
+            by[name] = run_q4(name, BY_CONFIG_STEPS, args.warmup, local)
             torch.cuda.empty_cache()
             continue
-        sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": min(args.steps, 50), "layers": 0})
+        sub = argparse.Namespace(**{**vars(args), "workload": name, "steps": BY_CONFIG_STEPS, "layers": 0})
         r, s = run_ours(sub, rank, world, local)
         del s
         torch.cuda.empty_cache()
