@@ -37,7 +37,7 @@ if ROOT not in sys.path:
 HEADLINE = "qwen3-14b-40layer"
 # Steps of each by_config row's graph (whatever --steps is): enough that a short step's
 # first launches, which have no preceding step to overlap, weigh little in the mean.
-BY_CONFIG_STEPS = 50
+BY_CONFIG_STEPS = 200
 METRIC = "GQA decode-attn µs/step and KV-read GB/s as fraction of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
