@@ -74,7 +74,7 @@ constexpr int kNumBars = 1 + 2 * kPfKStages + 2 * kPfVStages + 2 + 2 + 1 + 1;
 // the kernel checks it rather than reserving slack, so that two CTAs fit an SM.
 constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 16;
 constexpr int kPfMaxSlots = 320;                // split-tile partials the static scratch holds
-constexpr int kPfMaxSplit = 8;                  // KV parts of one split query tile
+constexpr int kPfMaxSplit = 6;                  // KV parts of one split query tile
 // A partial is column-major, [130][128 rows] floats: O columns, then m, then l, so that the
 // softmax warps (thread = row) write and read it in coalesced 128-byte lines.
 constexpr int kPartFloats = (kHeadDim + 2) * kPfRows;
