@@ -216,6 +216,22 @@ def test_rejects_bad_arguments():
     assert ex.value.status == binding.GQA_ERR_INVALID_ARG
 
 
+def test_two_sequences_with_tiles_cut_into_kv_parts():
+    """Two sequences of a 640-token chunk (416 query tiles of 25 tokens x 5 heads on a
+    152-SM GPU: 304 whole tiles, the last 112 cut into KV parts merged by the third
+    kernel), paged, at different cache offsets: every output row and appended row against
+    the oracle."""
+    w = wl.make_prefill(2, 40, 8, 640, [0, 200], paged=True, seed=16, max_seq=896, device="cuda", name="cut-b2")
+    k0, v0 = bits(w.k_cache), bits(w.v_cache)
+    ref = oracle_prefill(w)
+    assert ref["status"] == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, err)
+    assert int(err.item()) == 0
+    assert_out_close(out, ref["out"], "two sequences, cut tiles")
+    check_cache(w, k0, v0, ref)
+
+
 def test_full_size_workload_on_sampled_rows():
     """The benchmarked chunk (1024 tokens at positions 3072..4095 over a 4096-token cache):
     every appended k/v row against the oracle's prologue, and the output on 96 sampled
