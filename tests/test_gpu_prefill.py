@@ -176,6 +176,61 @@ def test_repeated_calls_are_bitwise_identical():
         assert torch.equal(r, runs[0])
 
 
+CHUNKS_300 = ((0, 128), (128, 256), (256, 300))
+
+
+def chunk_parts(w):
+    """The 300-token prompt's three calls: each chunk's q/k/v in tensors of its own."""
+    return [wl.PrefillWorkload(**{**w.__dict__, "T": e - a, "q_new": w.q_new[:, a:e].contiguous(),
+                                  "k_new": w.k_new[:, a:e].contiguous(), "v_new": w.v_new[:, a:e].contiguous(),
+                                  "q_start": torch.tensor([a], dtype=torch.int32, device="cuda")})
+            for a, e in CHUNKS_300]
+
+
+def test_calls_queued_back_to_back_and_replayed_from_a_graph():
+    """Each call's attention kernel reads what its own prologue wrote, and each call's
+    prologue waits for the previous call's readers of `out` and the cache.  The 300-token
+    prompt's three calls queued on one stream with no synchronisation between them; then the
+    same three calls captured in a CUDA graph and replayed on two other prompts (fresh
+    inputs and cache copied in before each replay), every output against the oracle's."""
+    w = wl.make_prefill(1, 40, 8, 300, [0], paged=True, seed=21, max_seq=320, device="cuda")
+    k0, v0 = w.k_cache.clone(), w.v_cache.clone()
+    ref = oracle_prefill(w)
+    parts = chunk_parts(w)
+    outs = [torch.full((1, e - a, 40, 128), float("nan"), dtype=torch.bfloat16, device="cuda") for a, e in CHUNKS_300]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for part, out in zip(parts, outs):
+        binding.prefill_attn_workload(part, out, device_errors=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_out_close(torch.cat(outs, dim=1), ref["out"], "queued calls")
+
+    w.k_cache.copy_(k0)
+    w.v_cache.copy_(v0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for part, out in zip(parts, outs):
+            binding.prefill_attn_workload(part, out, device_errors=err, stream=s)
+    for seed in (22, 23):
+        w2 = wl.make_prefill(1, 40, 8, 300, [0], paged=True, seed=seed, max_seq=320, device="cuda")
+        ref2 = oracle_prefill(w2)
+        for name in ("k_cache", "v_cache", "page_table", "q_norm_w", "k_norm_w"):
+            getattr(w, name).copy_(getattr(w2, name))
+        for (a, e), part in zip(CHUNKS_300, parts):
+            part.q_new.copy_(w2.q_new[:, a:e])
+            part.k_new.copy_(w2.k_new[:, a:e])
+            part.v_new.copy_(w2.v_new[:, a:e])
+        for out in outs:
+            out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_out_close(torch.cat(outs, dim=1), ref2["out"], f"graph replay, prompt {seed}")
+
+
 def test_out_of_range_chunks_give_zeros_and_flags():
     """Sequence 1's chunk runs past max_seq_len and sequence 2's starts before 0: both are
     flagged, write no cache row and output zeros; sequence 0 is unaffected."""
