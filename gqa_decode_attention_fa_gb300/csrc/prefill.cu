@@ -606,18 +606,23 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm)
 }
 
 // ------------------------------------------------------------------------------ merge
-// One CTA per (cut query tile r, 16 dims), four threads per row of the tile's 128-row M
-// tile (row = token-in-block * G + head, as in the attention kernel), four dims each.  It
-// waits for the attention kernel, weighs the non-empty parts of its row --
-// w_k = 2^(m_k - M) / L with M = max m_k, L = sum 2^(m_k - M) l_k -- and writes its dims of
-// the row in bf16.  A thread's loads of all parts are issued before the sums.
-constexpr int kPfMergeDims = 16;                     // dims a merge CTA covers
-constexpr int kPfMergeThreads = kPfRows * (kPfMergeDims / 4);
+// One CTA per (cut query tile r, 16 dims); a thread takes four consecutive rows of the
+// tile's 128-row M tile (row = token-in-block * G + head, as in the attention kernel) and
+// four dims, so that every partial it reads is a 16-byte vector of the column-major
+// partials (a warp reads 512 contiguous bytes).  It waits for the attention kernel, weighs
+// the non-empty parts of each row -- w_k = 2^(m_k - M) / L with M = max m_k,
+// L = sum 2^(m_k - M) l_k -- and writes its dims of the rows in bf16.  All of a thread's
+// loads are issued before the sums.
+constexpr int kPfMergeDims = 16;                                      // dims a merge CTA covers
+constexpr int kPfMergeThreads = (kPfRows / 4) * (kPfMergeDims / 4);  // 128
+__device__ __forceinline__ float f4_at(const float4 &v, int k) {
+  return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
 __global__ void __launch_bounds__(kPfMergeThreads) prefill_merge_kernel(const PrefillParams p) {
   griddep_wait();  // the attention kernel's partials
   const int r = static_cast<int>(blockIdx.x);
-  const int row = static_cast<int>(threadIdx.x) % kPfRows;
-  const int d0 = kPfMergeDims * static_cast<int>(blockIdx.y) + 4 * (static_cast<int>(threadIdx.x) / kPfRows);
+  const int r0 = 4 * (static_cast<int>(threadIdx.x) % (kPfRows / 4));  // rows r0 .. r0 + 3
+  const int d0 = kPfMergeDims * static_cast<int>(blockIdx.y) + 4 * (static_cast<int>(threadIdx.x) / (kPfRows / 4));
   const int tile = p.ndp + r;
   const int bk = p.B * p.Hkv;
   const int qb = p.nqb - 1 - tile / bk;
@@ -627,34 +632,43 @@ __global__ void __launch_bounds__(kPfMergeThreads) prefill_merge_kernel(const Pr
   const int s0 = p.q_start[b];
   if (!chunk_ok(p, s0)) return;  // the prologue wrote this chunk's zeros
   const int n = (s0 + t_end - 1) / kTile + 1;  // the tile's KV tiles, cut into ksplit parts
-  const int tl = row / p.G, g = row - tl * p.G, t = t0 + tl;
-  if (!(tl < p.Tt && t < t_end)) return;
   auto slot = [&](int pt) { return p.part + (static_cast<long long>(r) * p.ksplit + pt) * kPartFloats; };
-  float mv[kPfMaxSplit], lv[kPfMaxSplit], x[kPfMaxSplit][4];
+  float4 mv[kPfMaxSplit], lv[kPfMaxSplit], x[kPfMaxSplit][4];
+  const float4 none_m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int pt = 0; pt < kPfMaxSplit; ++pt) {  // every load first: (m, l) and the four dims
+  for (int pt = 0; pt < kPfMaxSplit; ++pt) {  // every load first: (m, l) and the four dims, four rows each
     const bool has = pt < p.ksplit && n * pt / p.ksplit < n * (pt + 1) / p.ksplit;
     const float *sp = slot(pt < p.ksplit ? pt : 0);
-    mv[pt] = has ? __ldcg(sp + kHeadDim * kPfRows + row) : -INFINITY;
-    lv[pt] = has ? __ldcg(sp + (kHeadDim + 1) * kPfRows + row) : 0.f;
+    mv[pt] = has ? __ldcg(reinterpret_cast<const float4 *>(sp + kHeadDim * kPfRows + r0)) : none_m;
+    lv[pt] = has ? __ldcg(reinterpret_cast<const float4 *>(sp + (kHeadDim + 1) * kPfRows + r0)) : zero;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) x[pt][e] = has ? __ldcg(sp + (d0 + e) * kPfRows + row) : 0.f;
+    for (int e = 0; e < 4; ++e)
+      x[pt][e] = has ? __ldcg(reinterpret_cast<const float4 *>(sp + (d0 + e) * kPfRows + r0)) : zero;
   }
-  float M = -INFINITY;
 #pragma unroll
-  for (int pt = 0; pt < kPfMaxSplit; ++pt)
-    if (lv[pt] > 0.f) M = fmaxf(M, mv[pt]);  // a part that saw none of the row's keys has l = 0
-  float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k = 0; k < 4; ++k) {  // row r0 + k
+    const int row = r0 + k;
+    const int tl = row / p.G, g = row - tl * p.G, t = t0 + tl;
+    float M = -INFINITY;
 #pragma unroll
-  for (int pt = 0; pt < kPfMaxSplit; ++pt) {
-    const float f = lv[pt] > 0.f ? fast_exp2(mv[pt] - M) : 0.f;
-    L += f * lv[pt];
+    for (int pt = 0; pt < kPfMaxSplit; ++pt)  // a part that saw none of the row's keys has l = 0
+      if (f4_at(lv[pt], k) > 0.f) M = fmaxf(M, f4_at(mv[pt], k));
+    float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = fmaf(f, x[pt][e], acc[e]);
+    for (int pt = 0; pt < kPfMaxSplit; ++pt) {
+      const float l = f4_at(lv[pt], k);
+      const float f = l > 0.f ? fast_exp2(f4_at(mv[pt], k) - M) : 0.f;
+      L += f * l;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = fmaf(f, f4_at(x[pt][e], k), acc[e]);
+    }
+    if (tl < p.Tt && t < t_end) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      uint16_t *dst = p.out + ((static_cast<long long>(b) * p.T + t) * p.Hq + kv * p.G + g) * kHeadDim + d0;
+      *reinterpret_cast<uint2 *>(dst) =
+          make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+    }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint16_t *dst = p.out + ((static_cast<long long>(b) * p.T + t) * p.Hq + kv * p.G + g) * kHeadDim + d0;
-  *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
 }
 
 // --------------------------------------------------------------------------- host side
