@@ -174,6 +174,31 @@ def test_new_token_mid_sequence_and_capacity_not_a_tile_multiple(form):
     full_check(w, what="positions < L-1, max_seq=150", cluster_size=form)
 
 
+def random_decode_geometry(seed):
+    """A seeded decode geometry: B in 1..6, H_kv in {1, 2, 4, 8}, G in {1, 2, 3, 5, 6, 7, 16},
+    lengths 1..700 (positions L_b - 1, or anywhere below L_b for some sequences), paged
+    or contiguous, with or without QK-norm, and a capacity that is not a tile multiple."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 7))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 5, 6, 7, 16]))
+    lens = [int(x) for x in rng.integers(1, 701, size=B)]
+    positions = [int(rng.integers(0, L)) if rng.integers(0, 3) == 0 else L - 1 for L in lens]
+    return dict(B=B, Hq=G * Hkv, Hkv=Hkv, lens=lens, positions=positions, paged=bool(rng.integers(0, 2)),
+                norm=bool(rng.integers(0, 2)), max_seq=max(lens) + int(rng.integers(0, 50)))
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("seed", range(6))
+def test_random_geometries(seed, form):
+    """Six seeded geometries (see random_decode_geometry) in both forms: output, cache and
+    rotated queries against the oracle."""
+    g = random_decode_geometry(2000 + seed)
+    w = wl.make(g["B"], g["Hq"], g["Hkv"], g["lens"], paged=g["paged"], seed=seed, qk_norm=g["norm"],
+                positions=g["positions"], max_seq=g["max_seq"], device="cuda", name=f"random-{seed}")
+    full_check(w, what=f"random geometry {g} form {form}", cluster_size=form)
+
+
 @pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 151, 1000])
 def test_worker_counts(workers):
     w = wl.make(5, 40, 8, [1, 700, 64, 3000, 129], paged=True, seed=8, device="cuda")

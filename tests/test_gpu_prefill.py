@@ -109,6 +109,38 @@ def test_prefill_parity(name):
     check_cache(w, k0, v0, ref)
 
 
+def random_geometry(seed):
+    """A seeded prefill geometry: B in 1..3, H_kv in {1, 2, 4, 8}, G in {1, 2, 3, 4, 6, 7, 12}
+    (query blocks of 128, 64, 42, 32, 21, 18 and 10 tokens), T in 1..200, chunk starts
+    anywhere (not tile-aligned), paged or contiguous, with or without QK-norm."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 4, 6, 7, 12]))
+    T = int(rng.integers(1, 201))
+    max_seq = int(rng.integers(T, T + 320))
+    starts = [int(x) for x in rng.integers(0, max_seq - T + 1, size=B)]
+    return dict(B=B, Hq=G * Hkv, Hkv=Hkv, T=T, starts=starts, max_seq=max_seq, paged=bool(rng.integers(0, 2)),
+                norm=bool(rng.integers(0, 2)))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_geometries(seed):
+    """Eight seeded geometries (see random_geometry): every output row and appended row
+    against the oracle, and no device error."""
+    g = random_geometry(1000 + seed)
+    w = wl.make_prefill(g["B"], g["Hq"], g["Hkv"], g["T"], g["starts"], paged=g["paged"], seed=seed,
+                        qk_norm=g["norm"], max_seq=g["max_seq"], device="cuda", name=f"random-{seed}")
+    k0, v0 = bits(w.k_cache), bits(w.v_cache)
+    ref = oracle_prefill(w)
+    assert ref["status"] == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = run_gpu(w, err)
+    assert int(err.item()) == 0, g
+    assert_out_close(out, ref["out"], f"random geometry {g}")
+    check_cache(w, k0, v0, ref)
+
+
 def test_v_values_far_from_unit_scale():
     """P V keeps V's bf16 range: KV head 2's values scaled by 2^-20 (every value far below
     fp16's normal range), KV head 5 holding 70000 in a cache row and -1e6 in a chunk row
