@@ -147,6 +147,45 @@ def test_q4_parity(name, form):
         assert_out_close(out, want, name)
 
 
+def random_q4_geometry(seed):
+    """A seeded 4-bit geometry: B in 1..5, H_kv in {1, 2, 4, 8}, G in {1, 2, 3, 5, 7, 16},
+    lengths 1..700, paged or contiguous, with or without QK-norm, a capacity that is not a
+    tile multiple."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 6))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 3, 5, 7, 16]))
+    lens = [int(x) for x in rng.integers(1, 701, size=B)]
+    return dict(B=B, Hq=G * Hkv, Hkv=Hkv, lens=lens, paged=bool(rng.integers(0, 2)), norm=bool(rng.integers(0, 2)),
+                max_seq=max(lens) + int(rng.integers(0, 50)))
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("seed", range(5))
+def test_q4_random_geometries(seed, form):
+    """Five seeded geometries (see random_q4_geometry) in both forms: every output and
+    appended row against the oracle."""
+    g = random_q4_geometry(3000 + seed)
+    w = wl.make_q4(g["B"], g["Hq"], g["Hkv"], g["lens"], paged=g["paged"], seed=seed, qk_norm=g["norm"],
+                   max_seq=g["max_seq"], device="cuda", name=f"random-{seed}")
+    k0, v0, ks0, vs0 = np_u8(w.k_idx), np_u8(w.v_idx), np_u8(w.k_scale), np_u8(w.v_scale)
+    ref = oracle_q4(w)
+    assert ref["status"] == 0
+    plan, out = run_gpu(w, cluster_size=form)
+    assert plan.device_errors() == 0
+    assert check_appended(w, k0, v0, ks0, vs0, ref) <= 2
+    want = oracle_out_on(w, ref)
+    what = f"random geometry {g} [C={plan.cluster_size}]"
+    if min(g["lens"]) <= 2:
+        # a context of one or two tokens returns (nearly) a dequantized v row, entries up to
+        # ~4, where one bf16 rounding can exceed 1e-2: allowed per element (2^-7 |ref|)
+        got = out.float().cpu().double().numpy()
+        assert np.all(np.abs(got - want) <= np.maximum(1e-2, 2.0 ** -7 * np.abs(want))), what
+        assert out_errors(out, want)[1] <= 2e-3, what
+    else:
+        assert_out_close(out, want, what)
+
+
 def test_q4_full_size_ragged_on_sampled_heads():
     """The benchmarked ragged batch (32 sequences, 512..8192 tokens, paged): every appended
     row, and 48 sampled (sequence, head) outputs against the oracle."""
